@@ -1,0 +1,176 @@
+"""CPU oracle for the FP8 scaled matrix multiply.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package. The product library
+(``fp8_scaled_gemm_gb300``) never imports it and shares no code with it.
+
+The arithmetic lives in ``fp8mm_oracle.c`` (plain C99 + OpenMP, fp64); this
+module only compiles it with gcc and marshals numpy arrays through ctypes.
+What it computes, with its sources on the pages:
+
+    out[i, j] = bf16_rne( sum_k dec(A[i, k]) * dec(Bt[j, k]) * S_ij + bias[j] )
+
+with ``S_ij = s_a * s_b`` (per-tensor) or ``s_a[i] * s_b[j]`` (row-wise):
+gist "matmul_fp8.py" (FP8 Matmul), ``matmul_fp8_kernel`` scale epilogue;
+PyTorch PR #125204 "fp8 row-scaling kernel for scaled_mm", Summary (row-wise
+scale lengths M and N, TN layout); PyTorch PR #142045, Summary (bias).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against values
+fixed by the pages or by mathematics (closed forms, exact rational brute
+force, torch's independent float8/bf16 conversions). No function is unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp8mm_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libfp8mm_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/libfp8mm_oracle.so`` with gcc."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    fresh = (os.path.exists(_LIB_PATH)
+             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC))
+    if fresh and not force:
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c99", "-O2", "-fopenmp", "-fPIC", "-shared",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        c_i64p = ctypes.POINTER(ctypes.c_int64)
+        lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_table.restype = None
+        lib.oracle_e4m3_table.argtypes = [ctypes.c_void_p]
+        lib.oracle_f64_to_bf16_rne.restype = ctypes.c_uint16
+        lib.oracle_f64_to_bf16_rne.argtypes = [ctypes.c_double]
+        lib.oracle_f64_to_bf16_array.restype = None
+        lib.oracle_f64_to_bf16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+        lib.oracle_bf16_to_f64.restype = ctypes.c_double
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_scaled_mm.restype = ctypes.c_int
+        lib.oracle_scaled_mm.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+            ctypes.c_void_p,
+            c_i64p, ctypes.c_int64, c_i64p, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int,
+        ]
+        _lib = lib
+        return lib
+
+
+def e4m3_table() -> np.ndarray:
+    """The 256 e4m3fn code values as fp64 (NaN at 0x7F and 0xFF)."""
+    t = np.empty(256, dtype=np.float64)
+    _load().oracle_e4m3_table(t.ctypes.data)
+    return t
+
+
+def e4m3_to_f64(code: int) -> float:
+    return float(_load().oracle_e4m3_to_f64(int(code)))
+
+
+def bf16_rne(x) -> np.ndarray:
+    """fp64 values -> bf16 bit patterns (uint16), one round-to-nearest-even."""
+    arr = np.asarray(x, dtype=np.float64)
+    xs = np.ascontiguousarray(arr.reshape(-1))
+    out = np.empty(xs.shape, dtype=np.uint16)
+    _load().oracle_f64_to_bf16_array(xs.ctypes.data, out.ctypes.data, xs.size)
+    return out.reshape(arr.shape)
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> fp64 values."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def scaled_mm(A, Bt, scale_a, scale_b, scale_mode: int, bias=None,
+              rows=None, cols=None, threads: int = 0):
+    """Oracle output on the grid ``rows x cols`` (all rows / columns if None).
+
+    A: uint8 [M, K] e4m3fn codes; Bt: uint8 [N, K] codes (B column-major);
+    scale_a / scale_b: float32 arrays of 1 value (scale_mode 0) or M / N
+    values (scale_mode 1); bias: uint16 bf16 patterns [N] or None.
+
+    Returns ``(out_bf16_bits uint16, ref64 float64, absum float64)``, each of
+    shape [len(rows), len(cols)]; ``absum`` is S_ij * sum_k |a_ik b_kj|.
+    """
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    Bt = np.ascontiguousarray(Bt, dtype=np.uint8)
+    if A.ndim != 2 or Bt.ndim != 2 or A.shape[1] != Bt.shape[1]:
+        raise ValueError("A must be [M,K] and Bt [N,K]")
+    M, K = A.shape
+    N = Bt.shape[0]
+    sa = np.ascontiguousarray(scale_a, dtype=np.float32).reshape(-1)
+    sb = np.ascontiguousarray(scale_b, dtype=np.float32).reshape(-1)
+    if scale_mode == 0:
+        if sa.size != 1 or sb.size != 1:
+            raise ValueError("per-tensor scales must hold one value each")
+    elif scale_mode == 1:
+        if sa.size != M or sb.size != N:
+            raise ValueError("row-wise scales must hold M and N values")
+    else:
+        raise ValueError("scale_mode must be 0 or 1")
+    bias_arr = None
+    if bias is not None:
+        bias_arr = np.ascontiguousarray(bias, dtype=np.uint16).reshape(-1)
+        if bias_arr.size != N:
+            raise ValueError("bias must hold N values")
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
+    nr = M if r is None else r.size
+    nc = N if c is None else c.size
+    out = np.zeros((nr, nc), dtype=np.uint16)
+    ref = np.zeros((nr, nc), dtype=np.float64)
+    mag = np.zeros((nr, nc), dtype=np.float64)
+    c_i64p = ctypes.POINTER(ctypes.c_int64)
+    rc = _load().oracle_scaled_mm(
+        A.ctypes.data, Bt.ctypes.data, M, N, K,
+        sa.ctypes.data, sb.ctypes.data, int(scale_mode),
+        None if bias_arr is None else bias_arr.ctypes.data,
+        None if r is None else r.ctypes.data_as(c_i64p), nr,
+        None if c is None else c.ctypes.data_as(c_i64p), nc,
+        out.ctypes.data, ref.ctypes.data, mag.ctypes.data, int(threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_scaled_mm failed with code {rc}")
+    return out, ref, mag
+
+
+def tolerance(ref_bits, absum) -> np.ndarray:
+    """Allowed |gpu - ref| per element: 2^-7 |ref| + 2^-20 absum.
+
+    ``ref`` is the bf16-rounded oracle value; the first term admits one bf16
+    ulp (a rounding boundary crossed by fp32 accumulation), the second the
+    fp32 accumulation error near cancellation.
+    """
+    ref = bf16_to_f64(ref_bits)
+    return np.abs(ref) * 2.0 ** -7 + np.asarray(absum) * 2.0 ** -20

@@ -1,0 +1,248 @@
+/*
+ * fp8mm_oracle.c -- plain CPU oracle for the FP8 scaled matrix multiply.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path links, loads or calls
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg use it. It shares no code, header, table or constant with the CUDA
+ * library (fp8_scaled_gemm_gb300/csrc).
+ *
+ * What it computes (one output element, i < M, j < N):
+ *
+ *   dot_ij = sum_k dec(A[i,k]) * dec(Bt[j,k])                      exact in fp64
+ *   S_ij   = s_a * s_b           (per-tensor)   or s_a[i] * s_b[j]  (row-wise)
+ *   ref_ij = dot_ij * S_ij + bias[j]            (bias optional)     in fp64
+ *   out_ij = bf16_rne(ref_ij)                   one rounding, fp64 -> bf16
+ *
+ * Sources:
+ *  - the product with scales applied after an fp32-or-better accumulation and
+ *    then a cast to the output type: gist "matmul_fp8.py" (FP8 Matmul),
+ *    `matmul_fp8_kernel`, the block that multiplies the accumulator by
+ *    `scale = scale_a[:, None] * scale_b[None, :]` (row-wise) or
+ *    `scale_a * scale_b` (per-tensor) and casts to `out_ptr`'s dtype;
+ *  - row-wise scale shapes (x's scale has length M, y's has length N, TN only):
+ *    PyTorch PR #125204 "fp8 row-scaling kernel for scaled_mm", Summary;
+ *  - B passed column-major (TN): gist "matmul_fp8.py", `benchmark()`, the
+ *    `b.to(dtype).t().contiguous().t()` step, so the oracle reads B as the
+ *    row-major matrix Bt[N,K];
+ *  - the bias epilogue: PyTorch PR #142045, Summary ("Limitations": scaled_mm
+ *    with bias values);
+ *  - the element type: torch.float8_e4m3fn / tl.float8e4nv, largest finite
+ *    value 448 (`torch.finfo(dtype).max`): gist "matmul_fp8.py", the dtype
+ *    map and `benchmark()`.
+ *
+ * Why fp64 is exact for the dot product: every e4m3fn value is an integer
+ * multiple of 2^-9 with magnitude <= 448, so each product is a multiple of
+ * 2^-18 with magnitude < 2^17.62; for K <= 2^14 every partial sum stays below
+ * 2^31.7 on the 2^-18 grid, i.e. needs at most 50 significand bits (< 53).
+ * The same holds for the sum of |products| used by the parity tolerance.
+ *
+ * e4m3fn encoding (OCP FP8 E4M3, "fn" = finite + NaN): 1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits; exponent field 0 encodes subnormals
+ * m * 2^-9; exponent 15 with mantissa 7 is NaN (codes 0x7F and 0xFF); there is
+ * no infinity.
+ *
+ * bf16: IEEE-754 binary32 truncated to its top 16 bits (8 exponent bits,
+ * 7 stored mantissa bits). The conversion here goes from fp64 to bf16 in a
+ * single round-to-nearest-even step, never through fp32 (which could round
+ * twice).
+ *
+ * Build: gcc -O2 -fopenmp -fPIC -shared (no -ffast-math: the rounding code
+ * relies on IEEE semantics and on nearbyint() in round-to-nearest-even mode).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* e4m3fn code -> value, from the bit-field definition above. */
+double oracle_e4m3_to_f64(uint8_t code)
+{
+    const int sign = (code >> 7) & 1;
+    const int expo = (code >> 3) & 0xF;
+    const int mant = code & 0x7;
+    double mag;
+    if (expo == 15 && mant == 7)
+        return NAN;
+    if (expo == 0)
+        mag = ldexp((double)mant, -9);            /* subnormal: m * 2^-9 */
+    else
+        mag = ldexp(8.0 + (double)mant, expo - 10); /* (1 + m/8) * 2^(e-7) */
+    return sign ? -mag : mag;
+}
+
+void oracle_e4m3_table(double table[256])
+{
+    for (int c = 0; c < 256; ++c)
+        table[c] = oracle_e4m3_to_f64((uint8_t)c);
+}
+
+/* bf16 bit pattern -> value (exact: bf16 is a subset of fp64). */
+double oracle_bf16_to_f64(uint16_t bits)
+{
+    uint32_t w = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/*
+ * fp64 -> bf16, round to nearest, ties to even, in one step.
+ * The value's quantum is 2^(e-7) for 2^e <= |x| < 2^(e+1), with e clamped at
+ * -126 below (bf16 subnormals share fp32's exponent range, quantum 2^-133).
+ * |x| / quantum is exact in fp64 (division by a power of two), nearbyint()
+ * rounds it half-to-even, and the result times the quantum is exact again.
+ * Results of 2^128 or more overflow to infinity. NaN maps to a quiet NaN
+ * with the input's sign.
+ */
+uint16_t oracle_f64_to_bf16_rne(double x)
+{
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double a, quantum, q, v;
+    int e;
+    float f;
+    uint32_t w;
+    if (isnan(x))
+        return (uint16_t)(sign | 0x7FC0u);
+    a = fabs(x);
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80u);
+    if (a == 0.0)
+        return sign;
+    (void)frexp(a, &e);       /* a = f * 2^e with 0.5 <= f < 1 */
+    e -= 1;                   /* 2^e <= a < 2^(e+1) */
+    if (e < -126)
+        e = -126;
+    quantum = ldexp(1.0, e - 7);
+    q = nearbyint(a / quantum);
+    v = q * quantum;
+    if (v >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80u);
+    f = (float)v;             /* exact: v is a bf16 value */
+    memcpy(&w, &f, sizeof w);
+    return (uint16_t)(sign | (uint16_t)(w >> 16));
+}
+
+/* Element-wise fp64 -> bf16 over an array (same rounding as above). */
+void oracle_f64_to_bf16_array(const double *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_f64_to_bf16_rne(x[i]);
+}
+
+/*
+ * The scaled matrix multiply on a grid of selected outputs.
+ *
+ *   A        e4m3fn codes, [M, K] row-major
+ *   Bt       e4m3fn codes, [N, K] row-major (B[K, N] column-major)
+ *   scale_a  1 value (scale_mode 0) or M values (scale_mode 1)
+ *   scale_b  1 value (scale_mode 0) or N values (scale_mode 1)
+ *   bias     bf16 bit patterns [N], or NULL
+ *   rows     n_rows row indices into [0, M), or NULL for all rows (n_rows = M)
+ *   cols     n_cols column indices into [0, N), or NULL for all (n_cols = N)
+ *   out      [n_rows, n_cols] bf16 bit patterns
+ *   ref64    [n_rows, n_cols] unrounded fp64 result, or NULL
+ *   absum    [n_rows, n_cols] S_ij * sum_k |a_ik * b_kj| (fp64), or NULL
+ *
+ * Returns 0, or -1 on a bad argument, -2 when out of memory.
+ */
+int oracle_scaled_mm(const uint8_t *A, const uint8_t *Bt,
+                     int64_t M, int64_t N, int64_t K,
+                     const float *scale_a, const float *scale_b, int scale_mode,
+                     const uint16_t *bias,
+                     const int64_t *rows, int64_t n_rows,
+                     const int64_t *cols, int64_t n_cols,
+                     uint16_t *out, double *ref64, double *absum,
+                     int n_threads)
+{
+    double table[256];
+    double *bdec;
+    int64_t r, c;
+    int bad = 0;
+
+    if (!A || !Bt || !scale_a || !scale_b || !out || M < 0 || N < 0 || K < 0)
+        return -1;
+    if (scale_mode != 0 && scale_mode != 1)
+        return -1;
+    if (!rows)
+        n_rows = M;
+    if (!cols)
+        n_cols = N;
+    for (r = 0; r < n_rows; ++r)
+        if (rows && (rows[r] < 0 || rows[r] >= M))
+            return -1;
+    for (c = 0; c < n_cols; ++c)
+        if (cols && (cols[c] < 0 || cols[c] >= N))
+            return -1;
+    if (n_rows == 0 || n_cols == 0)
+        return 0;
+
+    oracle_e4m3_table(table);
+
+    /* Decode the selected rows of Bt once. */
+    bdec = (double *)malloc((size_t)n_cols * (size_t)(K > 0 ? K : 1) * sizeof(double));
+    if (!bdec)
+        return -2;
+    for (c = 0; c < n_cols; ++c) {
+        const int64_t j = cols ? cols[c] : c;
+        for (int64_t k = 0; k < K; ++k)
+            bdec[c * K + k] = table[Bt[j * K + k]];
+    }
+
+#ifdef _OPENMP
+    if (n_threads > 0)
+        omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (r = 0; r < n_rows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        double *adec = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+        if (!adec) {
+            bad |= 1;
+            continue;
+        }
+        for (int64_t k = 0; k < K; ++k)
+            adec[k] = table[A[i * K + k]];
+        for (int64_t cc = 0; cc < n_cols; ++cc) {
+            const int64_t j = cols ? cols[cc] : cc;
+            const double *b = bdec + cc * K;
+            double dot = 0.0, mag = 0.0;
+            double S, ref;
+            for (int64_t k = 0; k < K; ++k) {
+                const double p = adec[k] * b[k];
+                dot += p;
+                mag += fabs(p);
+            }
+            if (scale_mode == 0)
+                S = (double)scale_a[0] * (double)scale_b[0];
+            else
+                S = (double)scale_a[i] * (double)scale_b[j];
+            ref = dot * S;
+            if (bias)
+                ref += oracle_bf16_to_f64(bias[j]);
+            out[r * n_cols + cc] = oracle_f64_to_bf16_rne(ref);
+            if (ref64)
+                ref64[r * n_cols + cc] = ref;
+            if (absum)
+                absum[r * n_cols + cc] = fabs(S) * mag;
+        }
+        free(adec);
+    }
+    free(bdec);
+    return bad ? -2 : 0;
+}
+
+/* Threads an OpenMP parallel region would use by default (for reports). */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
