@@ -1,0 +1,532 @@
+// fp8mm_api.cu -- the C ABI (include/fp8mm.h): argument checks, TMA
+// descriptor encoding, kernel choice and launch, split-K workspace, device
+// status word and the host-memory entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "fp8mm.h"
+#include "fp8mm_kernel.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutCycles = 4000000000ull;  // ~2 s at 2 GHz
+
+thread_local std::string t_last_error;
+thread_local std::string t_describe;
+
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    int *status = nullptr;               // in-kernel status word
+    float *ws = nullptr;                 // split-K partial tiles
+    size_t ws_bytes = 0;
+    unsigned int *counters = nullptr;    // split-K arrivals
+    size_t counter_count = 0;
+    void *stage[6] = {};                 // host entry point staging buffers
+    size_t stage_bytes[6] = {};
+};
+DeviceState g_dev[kMaxDevices];
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    t_last_error = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return FP8MM_ERR_CUDA;
+}
+
+// Per-device initialisation; returns FP8MM_OK and the state, or an error.
+int device_state(DeviceState **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        t_last_error = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return FP8MM_ERR_NODEV;
+    }
+    if (dev < 0 || dev >= kMaxDevices)
+        return FP8MM_ERR_NODEV;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetDeviceProperties");
+        d.sms = prop.multiProcessorCount;
+        d.cc_major = prop.major;
+        d.cc_minor = prop.minor;
+        if (!(d.cc_major == 10 && d.cc_minor == 3)) {
+            char buf[128];
+            snprintf(buf, sizeof buf, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                     d.cc_major, d.cc_minor);
+            t_last_error = buf;
+            return FP8MM_ERR_NODEV;
+        }
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+                t_last_error = "cuTensorMapEncodeTiled entry point not found";
+                return FP8MM_ERR_CUDA;
+            }
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        e = cudaMalloc(&d.status, sizeof(int));
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(status)");
+        e = cudaMemset(d.status, 0, sizeof(int));
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(status)");
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceSynchronize");
+        d.ready = true;
+    }
+    *out = &d;
+    return FP8MM_OK;
+}
+
+int grow_workspace(DeviceState &d, size_t ws_bytes, size_t counters)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (ws_bytes > d.ws_bytes) {
+        // The old buffer may still be in use by queued work on any stream.
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceSynchronize");
+        if (d.ws)
+            cudaFree(d.ws);
+        d.ws = nullptr;
+        d.ws_bytes = 0;
+        e = cudaMalloc(&d.ws, ws_bytes);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(workspace)");
+        d.ws_bytes = ws_bytes;
+    }
+    if (counters > d.counter_count) {
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceSynchronize");
+        if (d.counters)
+            cudaFree(d.counters);
+        d.counters = nullptr;
+        d.counter_count = 0;
+        e = cudaMalloc(&d.counters, counters * sizeof(unsigned int));
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(counters)");
+        e = cudaMemset(d.counters, 0, counters * sizeof(unsigned int));
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(counters)");
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceSynchronize");
+        d.counter_count = counters;
+    }
+    return FP8MM_OK;
+}
+
+// 2-D e4m3 tensor [rows, K] (K contiguous) read in boxes of
+// [box_rows, 128] with 128-byte swizzling; out-of-range elements read as 0.
+int encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t K, int box_rows)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(fp8mm::kBlockK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) rows=%lld K=%lld box_rows=%d",
+                 static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(K), box_rows);
+        t_last_error = buf;
+        return FP8MM_ERR_CUDA;
+    }
+    return FP8MM_OK;
+}
+
+struct Choice {
+    int variant;   // FP8MM_VARIANT_TILE or FP8MM_VARIANT_SWAP
+    int tile_n;
+    int split;
+    int tiles_p, tiles_q, kblocks, units, grid;
+};
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool tile_n_supported(int variant, int tile_n)
+{
+    if (variant == FP8MM_VARIANT_TILE)
+        return tile_n == 128 || tile_n == 256;
+    if (variant == FP8MM_VARIANT_SWAP)
+        return tile_n == 16 || tile_n == 32 || tile_n == 64 || tile_n == 128;
+    return false;
+}
+
+// Split factor that best fills the SMs: maximise units / (waves * sms),
+// keeping at least 4 K blocks per slice; ties go to the smaller split.
+int pick_split(int64_t tiles, int kblocks, int sms)
+{
+    if (tiles >= sms)
+        return 1;
+    int best = 1;
+    double best_eff = 0.0;
+    for (int s = 1; s <= 16; ++s) {
+        if (s > 1 && kblocks / s < 4)
+            break;
+        const int64_t units = tiles * s;
+        const int64_t waves = cdiv(units, sms);
+        const double eff = static_cast<double>(units) / static_cast<double>(waves * sms);
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = s;
+        }
+    }
+    return best;
+}
+
+int swap_tile_for(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+
+Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n, int split)
+{
+    Choice c{};
+    c.kblocks = static_cast<int>(cdiv(K, fp8mm::kBlockK));
+    if (variant == FP8MM_VARIANT_AUTO) {
+        if (M <= 128) {
+            variant = FP8MM_VARIANT_SWAP;
+            tile_n = swap_tile_for(M);
+        } else {
+            variant = FP8MM_VARIANT_TILE;
+            tile_n = 256;
+            if (cdiv(M, 128) * cdiv(N, 256) < sms)
+                tile_n = 128;
+        }
+        split = 0;
+    }
+    if (tile_n == 0)
+        tile_n = variant == FP8MM_VARIANT_TILE ? 256 : swap_tile_for(M);
+    c.variant = variant;
+    c.tile_n = tile_n;
+    const int64_t prow = variant == FP8MM_VARIANT_TILE ? M : N;
+    const int64_t qrow = variant == FP8MM_VARIANT_TILE ? N : M;
+    c.tiles_p = static_cast<int>(cdiv(prow, fp8mm::kTileP));
+    c.tiles_q = static_cast<int>(cdiv(qrow, tile_n));
+    const int64_t tiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q;
+    if (split <= 0)
+        split = pick_split(tiles, c.kblocks, sms);
+    split = std::max(1, std::min(split, c.kblocks));
+    c.split = split;
+    c.units = static_cast<int>(tiles * split);
+    c.grid = static_cast<int>(std::min<int64_t>(c.units, sms));
+    return c;
+}
+
+template <int BN, bool SWAP>
+int launch_kernel(const CUtensorMap &mp, const CUtensorMap &mq, const fp8mm::KernelParams &kp, int grid,
+                  cudaStream_t stream)
+{
+    using C = fp8mm::TileCfg<BN>;
+    auto kern = fp8mm::fp8mm_tc_kernel<BN, SWAP>;
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute");
+        attr_set[dev] = true;
+    }
+    kern<<<grid, fp8mm::kThreads, C::kSmemBytes, stream>>>(mp, mq, kp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "kernel launch");
+    return FP8MM_OK;
+}
+
+int dispatch(const Choice &c, const CUtensorMap &mp, const CUtensorMap &mq, const fp8mm::KernelParams &kp,
+             cudaStream_t stream)
+{
+    if (c.variant == FP8MM_VARIANT_TILE) {
+        switch (c.tile_n) {
+        case 128: return launch_kernel<128, false>(mp, mq, kp, c.grid, stream);
+        case 256: return launch_kernel<256, false>(mp, mq, kp, c.grid, stream);
+        }
+    } else {
+        switch (c.tile_n) {
+        case 16: return launch_kernel<16, true>(mp, mq, kp, c.grid, stream);
+        case 32: return launch_kernel<32, true>(mp, mq, kp, c.grid, stream);
+        case 64: return launch_kernel<64, true>(mp, mq, kp, c.grid, stream);
+        case 128: return launch_kernel<128, true>(mp, mq, kp, c.grid, stream);
+        }
+    }
+    return FP8MM_ERR_MODE;
+}
+
+int check_args(const void *A, const void *B, const float *sa, const float *sb, int scale_mode,
+               const void *bias, void *out, int64_t M, int64_t N, int64_t K)
+{
+    if (!A || !B || !sa || !sb || !out)
+        return FP8MM_ERR_NULL;
+    if (scale_mode != FP8MM_SCALE_TENSOR && scale_mode != FP8MM_SCALE_ROWWISE)
+        return FP8MM_ERR_MODE;
+    if (M < 0 || N < 0 || M > INT32_MAX || N > INT32_MAX)
+        return FP8MM_ERR_SHAPE;
+    if (K < 16 || (K % 16) != 0 || K > (int64_t(1) << 24))
+        return FP8MM_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
+        return FP8MM_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(sa) & 3) || (reinterpret_cast<uintptr_t>(sb) & 3) ||
+        (reinterpret_cast<uintptr_t>(out) & 3) || (reinterpret_cast<uintptr_t>(bias) & 1))
+        return FP8MM_ERR_ALIGN;
+    return FP8MM_OK;
+}
+
+int run(const void *A, const void *B, const float *sa, const float *sb, int scale_mode, const void *bias,
+        void *out, int64_t M, int64_t N, int64_t K, cudaStream_t stream, int variant, int tile_n, int split)
+{
+    int rc = check_args(A, B, sa, sb, scale_mode, bias, out, M, N, K);
+    if (rc != FP8MM_OK)
+        return rc;
+    if (variant != FP8MM_VARIANT_AUTO && variant != FP8MM_VARIANT_TILE && variant != FP8MM_VARIANT_SWAP)
+        return FP8MM_ERR_MODE;
+    if (variant != FP8MM_VARIANT_AUTO && tile_n != 0 && !tile_n_supported(variant, tile_n))
+        return FP8MM_ERR_MODE;
+    if (split < 0 || split > 16)
+        return FP8MM_ERR_MODE;
+    if (M == 0 || N == 0)
+        return FP8MM_OK;
+    DeviceState *d = nullptr;
+    rc = device_state(&d);
+    if (rc != FP8MM_OK)
+        return rc;
+
+    const Choice c = choose(M, N, K, d->sms, variant, tile_n, split);
+    fp8mm::KernelParams kp{};
+    kp.scale_a = sa;
+    kp.scale_b = sb;
+    kp.bias = static_cast<const __nv_bfloat16 *>(bias);
+    kp.out = static_cast<__nv_bfloat16 *>(out);
+    kp.status = d->status;
+    kp.M = static_cast<int>(M);
+    kp.N = static_cast<int>(N);
+    kp.K = static_cast<int>(K);
+    kp.tiles_p = c.tiles_p;
+    kp.tiles_q = c.tiles_q;
+    kp.splits = c.split;
+    kp.kblocks = c.kblocks;
+    kp.num_units = c.units;
+    kp.rowwise = scale_mode == FP8MM_SCALE_ROWWISE ? 1 : 0;
+    kp.group = 8;
+    kp.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % 8) == 0) ? 1 : 0;
+    kp.timeout_cycles = kDefaultTimeoutCycles;
+    if (c.split > 1) {
+        const int64_t tiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q;
+        const size_t ws = static_cast<size_t>(tiles) * c.split * fp8mm::kTileP * c.tile_n * sizeof(float);
+        rc = grow_workspace(*d, ws, static_cast<size_t>(tiles) * 4);
+        if (rc != FP8MM_OK)
+            return rc;
+        kp.ws = d->ws;
+        kp.counters = d->counters;
+    }
+
+    CUtensorMap mp, mq;
+    const bool swap = c.variant == FP8MM_VARIANT_SWAP;
+    // B column-major [K, N] is Bt[N, K] row-major.
+    rc = encode_operand_map(&mp, swap ? B : A, swap ? N : M, K, fp8mm::kTileP);
+    if (rc != FP8MM_OK)
+        return rc;
+    rc = encode_operand_map(&mq, swap ? A : B, swap ? M : N, K, c.tile_n);
+    if (rc != FP8MM_OK)
+        return rc;
+    return dispatch(c, mp, mq, kp, stream);
+}
+
+int grow_stage(DeviceState &d, int i, size_t bytes)
+{
+    if (bytes <= d.stage_bytes[i])
+        return FP8MM_OK;
+    if (d.stage[i]) {
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceSynchronize");
+        cudaFree(d.stage[i]);
+        d.stage[i] = nullptr;
+        d.stage_bytes[i] = 0;
+    }
+    cudaError_t e = cudaMalloc(&d.stage[i], bytes);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMalloc(staging)");
+    d.stage_bytes[i] = bytes;
+    return FP8MM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8_scaled_mm(const void *A, const void *B, const float *scale_a, const float *scale_b, int scale_mode,
+                  const void *bias, void *out, int64_t M, int64_t N, int64_t K, void *stream)
+{
+    return run(A, B, scale_a, scale_b, scale_mode, bias, out, M, N, K, static_cast<cudaStream_t>(stream),
+               FP8MM_VARIANT_AUTO, 0, 0);
+}
+
+int fp8_scaled_mm_config(const void *A, const void *B, const float *scale_a, const float *scale_b,
+                         int scale_mode, const void *bias, void *out, int64_t M, int64_t N, int64_t K,
+                         void *stream, int variant, int tile_n, int split_k)
+{
+    return run(A, B, scale_a, scale_b, scale_mode, bias, out, M, N, K, static_cast<cudaStream_t>(stream),
+               variant, tile_n, split_k);
+}
+
+int fp8_scaled_mm_host(const void *A, const void *B, const float *scale_a, const float *scale_b,
+                       int scale_mode, const void *bias, void *out, int64_t M, int64_t N, int64_t K,
+                       void *stream)
+{
+    int rc = check_args(A, B, scale_a, scale_b, scale_mode, bias, out, M, N, K);
+    if (rc != FP8MM_OK)
+        return rc;
+    if (M == 0 || N == 0)
+        return FP8MM_OK;
+    DeviceState *d = nullptr;
+    rc = device_state(&d);
+    if (rc != FP8MM_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t nsa = scale_mode == FP8MM_SCALE_ROWWISE ? static_cast<size_t>(M) : 1;
+    const size_t nsb = scale_mode == FP8MM_SCALE_ROWWISE ? static_cast<size_t>(N) : 1;
+    const size_t bytes[6] = {static_cast<size_t>(M) * K, static_cast<size_t>(N) * K, nsa * 4, nsb * 4,
+                             bias ? static_cast<size_t>(N) * 2 : 0, static_cast<size_t>(M) * N * 2};
+    const void *src[5] = {A, B, scale_a, scale_b, bias};
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        for (int i = 0; i < 6; ++i) {
+            if (bytes[i] == 0)
+                continue;
+            rc = grow_stage(*d, i, bytes[i]);
+            if (rc != FP8MM_OK)
+                return rc;
+        }
+    }
+    for (int i = 0; i < 5; ++i) {
+        if (bytes[i] == 0)
+            continue;
+        cudaError_t e = cudaMemcpyAsync(d->stage[i], src[i], bytes[i], cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyAsync(H2D)");
+    }
+    rc = run(d->stage[0], d->stage[1], static_cast<const float *>(d->stage[2]),
+             static_cast<const float *>(d->stage[3]), scale_mode, bias ? d->stage[4] : nullptr, d->stage[5], M,
+             N, K, s, FP8MM_VARIANT_AUTO, 0, 0);
+    if (rc != FP8MM_OK)
+        return rc;
+    cudaError_t e = cudaMemcpyAsync(out, d->stage[5], bytes[5], cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync(D2H)");
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    return FP8MM_OK;
+}
+
+int fp8mm_reserve_workspace(int64_t bytes)
+{
+    if (bytes < 0)
+        return FP8MM_ERR_SHAPE;
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc != FP8MM_OK)
+        return rc;
+    // Smallest partial tile is 128 x 16 fp32: bounds the tiles this can hold.
+    const size_t tiles = static_cast<size_t>(bytes) / (fp8mm::kTileP * 16 * sizeof(float)) + 1;
+    return grow_workspace(*d, static_cast<size_t>(bytes), tiles * 4);
+}
+
+int fp8mm_device_status(void *stream)
+{
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc != FP8MM_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamSynchronize");
+    int h = 0;
+    e = cudaMemcpy(&h, d->status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy(status)");
+    if (h == 0)
+        return FP8MM_OK;
+    e = cudaMemset(d->status, 0, sizeof(int));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemset(status)");
+    if (d->counters) {
+        e = cudaMemset(d->counters, 0, d->counter_count * sizeof(unsigned int));
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(counters)");
+    }
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceSynchronize");
+    char buf[96];
+    snprintf(buf, sizeof buf, "in-kernel wait ran out (site 0x%x)", h);
+    t_last_error = buf;
+    return FP8MM_ERR_TIMEOUT;
+}
+
+const char *fp8mm_status_string(int status)
+{
+    switch (status) {
+    case FP8MM_OK: return "ok";
+    case FP8MM_ERR_NULL: return "a required pointer is NULL";
+    case FP8MM_ERR_SHAPE: return "M, N or K out of range (K must be a positive multiple of 16)";
+    case FP8MM_ERR_ALIGN: return "pointer misaligned (A and B need 16 bytes)";
+    case FP8MM_ERR_MODE: return "unknown scale mode or unsupported kernel choice";
+    case FP8MM_ERR_CUDA: return "CUDA call failed";
+    case FP8MM_ERR_NODEV: return "no sm_103 CUDA device";
+    case FP8MM_ERR_TIMEOUT: return "an in-kernel wait ran out";
+    default: return "unknown status";
+    }
+}
+
+const char *fp8mm_last_error(void) { return t_last_error.c_str(); }
+
+const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mode)
+{
+    (void)scale_mode;
+    DeviceState *d = nullptr;
+    if (device_state(&d) != FP8MM_OK) {
+        t_describe = "no device";
+        return t_describe.c_str();
+    }
+    if (M <= 0 || N <= 0 || K < 16) {
+        t_describe = "no-op or invalid shape";
+        return t_describe.c_str();
+    }
+    const Choice c = choose(M, N, K, d->sms, FP8MM_VARIANT_AUTO, 0, 0);
+    char buf[160];
+    snprintf(buf, sizeof buf, "%s tile_n=%d split=%d tiles=%dx%d units=%d grid=%d",
+             c.variant == FP8MM_VARIANT_TILE ? "tile" : "swap", c.tile_n, c.split, c.tiles_p, c.tiles_q,
+             c.units, c.grid);
+    t_describe = buf;
+    return t_describe.c_str();
+}
+
+}  // extern "C"

@@ -1,0 +1,451 @@
+// fp8mm_kernel.cuh -- persistent, warp-specialised FP8 (e4m3) scaled GEMM for
+// sm_103a: TMA -> shared-memory ring -> tcgen05.mma (fp32 in tensor memory)
+// -> scale / bias / bf16 epilogue.
+//
+// What one output element is (the scaled_mm epilogue of the gist
+// "matmul_fp8.py", `matmul_fp8_kernel`; row-wise scales as in PyTorch PR
+// #125204, Summary; bias as in PyTorch PR #142045, Summary):
+//
+//     out[m, n] = bf16_rn( acc[m, n] * (s_a[m] * s_b[n]) + bias[n] )
+//     acc[m, n] = sum_k A[m, k] * Bt[n, k]   (exact products, fp32 sums)
+//
+// Roles in one 192-thread CTA (one CTA per SM, persistent over work units):
+//   warp 0      TMA producer: one thread streams 128-byte-wide K blocks of the
+//               two operands into a STAGES-deep ring (mbarrier full/empty).
+//   warp 1      MMA issuer: allocates tensor memory, one thread issues four
+//               K=32 tcgen05.mma per stage into one of two fp32 accumulators
+//               (128 lanes x BN columns each), commits stage-release and
+//               accumulator-ready barriers.
+//   warps 2-5   epilogue: each warp owns the 32 TMEM lanes its warp index
+//               allows (warp % 4), reads the accumulator with tcgen05.ld,
+//               applies scale and bias, rounds to bf16 and stores; it frees
+//               the accumulator so the MMA of tile t+2 can start while tile
+//               t+1 is still computing.
+//
+// Operand naming: "P" is the operand whose 128 rows become TMEM lanes, "Q"
+// the operand whose BN rows become TMEM columns. TILE variant: P = A (rows =
+// M), Q = Bt (rows = N). SWAP variant (skinny M): P = Bt, Q = A, so that N
+// fills the 128-lane dimension; the epilogue then writes the rows of out^T
+// as columns of out.
+//
+// Work units: (P tile, Q tile, K slice). P/Q tiles are visited in groups of
+// `group` P tiles that sweep all Q tiles (the GROUP_M rasterisation of the
+// gist's `matmul_fp8_kernel`); units are dealt to CTAs round-robin (the
+// persistent schedule of `matmul_fp8_persistent_kernel`). With split_k > 1
+// every slice writes an fp32 partial tile to a workspace; the last slice to
+// arrive (counted per 32-row quarter with an atomic) sums the partials in
+// slice order and runs the epilogue, so the result does not depend on
+// arrival order.
+//
+// Every mbarrier wait is bounded (clock64 budget). A wait that runs out sets
+// a CTA-wide abort flag and a device status word, every role leaves its loop,
+// the producer waits (bounded) for its own copies in flight, the MMA thread
+// waits (bounded) for its MMAs, and tensor memory is always released. No
+// wait depends on another CTA, and no named barrier is used inside a role.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fp8mm {
+
+constexpr int kTileP = 128;   // rows of the MMA A operand (TMEM lanes)
+constexpr int kBlockK = 128;  // K elements (= bytes) per ring stage: one 128-B swizzle row
+constexpr int kMmaK = 32;     // K per tcgen05.mma of kind::f8f6f4
+constexpr int kThreads = 192;
+
+// Device status codes (written once per launch, first writer wins).
+constexpr int kStatusTimeoutBase = 0x100;
+
+struct KernelParams {
+    const float *scale_a;           // 1 or M values
+    const float *scale_b;           // 1 or N values
+    const __nv_bfloat16 *bias;      // N values or nullptr
+    __nv_bfloat16 *out;             // [M, N] row-major
+    float *ws;                      // split-K partial tiles (splits > 1)
+    unsigned int *counters;         // split-K arrivals, 4 per output tile
+    int *status;                    // device status word
+    int M, N, K;
+    int tiles_p, tiles_q;           // ceil(P rows / 128), ceil(Q rows / BN)
+    int splits, kblocks;            // K slices per tile, ceil(K / 128)
+    int num_units;                  // tiles_p * tiles_q * splits
+    int rowwise;                    // 0 per-tensor, 1 row-wise scales
+    int group;                      // P tiles per rasterisation group
+    int vec_store;                  // 16-byte output stores allowed (TILE)
+    unsigned long long timeout_cycles;
+};
+
+template <int BN>
+struct TileCfg {
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is 16..256 step 16");
+    static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+    static constexpr int kPBytes = kTileP * kBlockK;
+    static constexpr int kQBytes = BN * kBlockK;
+    static constexpr int kStageBytes = kPBytes + kQBytes;
+    static constexpr int kTmemCols =
+        (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+    static constexpr int kChunk = BN < 32 ? BN : 32;   // TMEM columns per tcgen05.ld
+    static_assert(kQBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+    static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory");
+};
+
+// Bounded mbarrier waits.
+struct Waiter {
+    volatile int *abort_flag;
+    int *status;
+    unsigned long long limit;
+
+    // Returns false when the CTA is aborting (this wait ran out, or another
+    // role's did).
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, int where) const
+    {
+        if (ptx::mbar_try_wait(bar, parity))
+            return true;
+        const unsigned long long t0 = static_cast<unsigned long long>(clock64());
+        while (true) {
+            if (ptx::mbar_try_wait(bar, parity))
+                return true;
+            if (*abort_flag)
+                return false;
+            if (static_cast<unsigned long long>(clock64()) - t0 > limit) {
+                *abort_flag = 1;
+                atomicCAS(status, 0, kStatusTimeoutBase | where);
+                return false;
+            }
+        }
+    }
+
+    // Same budget, but ignores the abort flag: used to wait for this
+    // thread's own asynchronous work before leaving.
+    __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity, int where) const
+    {
+        const unsigned long long t0 = static_cast<unsigned long long>(clock64());
+        while (!ptx::mbar_try_wait(bar, parity)) {
+            if (static_cast<unsigned long long>(clock64()) - t0 > limit) {
+                *abort_flag = 1;
+                atomicCAS(status, 0, kStatusTimeoutBase | where);
+                return false;
+            }
+        }
+        return true;
+    }
+};
+
+struct Unit {
+    int tp, tq, split, tile, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const KernelParams &p)
+{
+    Unit w;
+    w.split = u % p.splits;
+    w.tile = u / p.splits;
+    const int in_group = p.group * p.tiles_q;
+    const int gid = w.tile / in_group;
+    const int first_p = gid * p.group;
+    const int gsize = min(p.tiles_p - first_p, p.group);
+    const int r = w.tile % in_group;
+    w.tp = first_p + r % gsize;
+    w.tq = r / gsize;
+    w.kb0 = static_cast<int>((static_cast<long long>(w.split) * p.kblocks) / p.splits);
+    w.kb1 = static_cast<int>((static_cast<long long>(w.split + 1) * p.kblocks) / p.splits);
+    return w;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Epilogue for CH accumulator columns held by one thread.
+// TILE: the thread owns output row m = pidx, columns n = qbase + j.
+// SWAP: the thread owns output column n = pidx, rows m = qbase + j.
+template <int CH, bool SWAP>
+__device__ __forceinline__ void store_chunk(const KernelParams &p, const float (&v)[CH], int pidx,
+                                            int qbase, float s_tensor)
+{
+    if (!SWAP) {
+        const int m = pidx;
+        if (m >= p.M)
+            return;
+        const float sa = p.rowwise ? __ldg(p.scale_a + m) : 0.0f;
+        float y[CH];
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const int n = qbase + j;
+            const bool in = n < p.N;
+            const float s = p.rowwise ? sa * (in ? __ldg(p.scale_b + n) : 0.0f) : s_tensor;
+            const float b = (p.bias != nullptr && in) ? __bfloat162float(p.bias[n]) : 0.0f;
+            y[j] = fmaf(v[j], s, b);
+        }
+        __nv_bfloat16 *orow = p.out + static_cast<size_t>(m) * p.N;
+        if (p.vec_store && qbase + CH <= p.N) {
+#pragma unroll
+            for (int j = 0; j < CH; j += 8) {
+                uint4 w;
+                w.x = pack_bf16x2(y[j + 0], y[j + 1]);
+                w.y = pack_bf16x2(y[j + 2], y[j + 3]);
+                w.z = pack_bf16x2(y[j + 4], y[j + 5]);
+                w.w = pack_bf16x2(y[j + 6], y[j + 7]);
+                *reinterpret_cast<uint4 *>(orow + qbase + j) = w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < CH; ++j)
+                if (qbase + j < p.N)
+                    orow[qbase + j] = __float2bfloat16_rn(y[j]);
+        }
+    } else {
+        const int n = pidx;
+        if (n >= p.N)
+            return;
+        const float sb = p.rowwise ? __ldg(p.scale_b + n) : 0.0f;
+        const float b = p.bias != nullptr ? __bfloat162float(p.bias[n]) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const int m = qbase + j;
+            if (m < p.M) {
+                const float s = p.rowwise ? __ldg(p.scale_a + m) * sb : s_tensor;
+                p.out[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(fmaf(v[j], s, b));
+            }
+        }
+    }
+}
+
+template <int CH>
+__device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[CH])
+{
+    if constexpr (CH == 32)
+        ptx::tmem_ld_32cols(taddr, v);
+    else
+        ptx::tmem_ld_16cols(taddr, v);
+}
+
+template <int BN, bool SWAP>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8mm_tc_kernel(const __grid_constant__ CUtensorMap tmap_p,
+                    const __grid_constant__ CUtensorMap tmap_q, const KernelParams p)
+{
+    using C = TileCfg<BN>;
+    constexpr int CH = C::kChunk;
+    constexpr int S = C::kStages;
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+
+    const uint32_t bar0 = sbase + S * C::kStageBytes;
+    // full[S] | empty[S] | tfull[2] | tempty[2] | done
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+    const uint32_t done_bar = bar0 + 8u * (2 * S + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S * C::kStageBytes + 8 * (2 * S + 5));
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(tfull_bar(a), 1);
+            ptx::mbar_init(tempty_bar(a), 128);
+        }
+        ptx::mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmap_p);
+        ptx::prefetch_tmap(&tmap_q);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const Waiter W{abort_flag, p.status, p.timeout_cycles};
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ---
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const Unit w = decode_unit(u, p);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!W.wait(empty_bar(stage), phase ^ 1u, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sp = sbase + stage * C::kStageBytes;
+                    ptx::mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
+                    ptx::tma_load_2d(sp, &tmap_p, full_bar(stage), kb * kBlockK, w.tp * kTileP);
+                    ptx::tma_load_2d(sp + C::kPBytes, &tmap_q, full_bar(stage), kb * kBlockK,
+                                     w.tq * BN);
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Own copies in flight must land before the CTA may exit.
+            const int n = issued < S ? issued : S;
+            int s = stage;
+            uint32_t ph = phase;
+            for (int i = 0; i < n; ++i) {
+                if (--s < 0) {
+                    s = S - 1;
+                    ph ^= 1u;
+                }
+                W.drain(full_bar(s), ph, 3);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // -------------------------------------------------- MMA issuer ---
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::idesc_e4m3_f32(kTileP, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const Unit w = decode_unit(u, p);
+                if (!W.wait(tempty_bar(acc), acc_phase ^ 1u, 1))
+                    break;
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!W.wait(full_bar(stage), phase, 2)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sp = sbase + stage * C::kStageBytes;
+                    const uint32_t sq = sp + C::kPBytes;
+#pragma unroll
+                    for (int k = 0; k < kBlockK / kMmaK; ++k) {
+                        ptx::mma_e4m3(d, ptx::sw128_kmajor_desc(sp + k * kMmaK),
+                                      ptx::sw128_kmajor_desc(sq + k * kMmaK), idesc,
+                                      (kb > w.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    ptx::mma_commit(empty_bar(stage));
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                ptx::mma_commit(tfull_bar(acc));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // Every MMA issued above must have completed before TMEM is freed.
+            ptx::mma_commit(done_bar);
+            W.drain(done_bar, 0, 4);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue ---
+        const int q = warp & 3;             // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;      // row within the 128-row P tile
+        const float s_tensor = p.rowwise ? 0.0f : __ldg(p.scale_a) * __ldg(p.scale_b);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            const Unit w = decode_unit(u, p);
+            if (!W.wait(tfull_bar(acc), acc_phase, 5))
+                break;
+            ptx::tc_fence_after();
+            const uint32_t trow =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            const int pidx = w.tp * kTileP + row;
+            if (p.splits == 1) {
+#pragma unroll 1
+                for (int c = 0; c < BN / CH; ++c) {
+                    float v[CH];
+                    tmem_load_chunk<CH>(trow + c * CH, v);
+                    store_chunk<CH, SWAP>(p, v, pidx, w.tq * BN + c * CH, s_tensor);
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(tempty_bar(acc));
+            } else {
+                const size_t tile_elems = static_cast<size_t>(kTileP) * BN;
+                float *mine = p.ws + (static_cast<size_t>(w.tile) * p.splits + w.split) * tile_elems;
+#pragma unroll 1
+                for (int c = 0; c < BN / CH; ++c) {
+                    float v[CH];
+                    tmem_load_chunk<CH>(trow + c * CH, v);
+#pragma unroll
+                    for (int j = 0; j < CH; ++j)
+                        __stcg(mine + static_cast<size_t>(c * CH + j) * kTileP + row, v[j]);
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(tempty_bar(acc));
+                __threadfence();
+                __syncwarp();
+                unsigned int old = 0;
+                unsigned int *cnt = p.counters + static_cast<size_t>(w.tile) * 4 + q;
+                if (lane == 0)
+                    old = atomicAdd(cnt, 1u);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                if (old == static_cast<unsigned int>(p.splits - 1)) {
+                    if (lane == 0)
+                        *cnt = 0u;   // ready for the next launch
+                    __threadfence();
+                    const float *base = p.ws + static_cast<size_t>(w.tile) * p.splits * tile_elems;
+#pragma unroll 1
+                    for (int c = 0; c < BN / CH; ++c) {
+                        float v[CH];
+#pragma unroll
+                        for (int j = 0; j < CH; ++j)
+                            v[j] = 0.0f;
+                        for (int s = 0; s < p.splits; ++s) {
+                            const float *part = base + static_cast<size_t>(s) * tile_elems;
+#pragma unroll
+                            for (int j = 0; j < CH; ++j)
+                                v[j] += __ldcg(part + static_cast<size_t>(c * CH + j) * kTileP + row);
+                        }
+                        store_chunk<CH, SWAP>(p, v, pidx, w.tq * BN + c * CH, s_tensor);
+                    }
+                }
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+}  // namespace fp8mm

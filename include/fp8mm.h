@@ -1,0 +1,155 @@
+/*
+ * fp8mm.h -- C ABI of the GB300 (sm_103a) FP8 scaled matrix multiply.
+ *
+ *   out[M,N] = bf16( (A[M,K] . B[K,N]) * (scale_a (x) scale_b) + bias[N] )
+ *
+ * A and B hold float8_e4m3fn codes; products are exact and accumulate in
+ * fp32 on the tensor cores (tcgen05, accumulators in tensor memory); the
+ * scale and the optional bias are applied to the fp32 sum, which is then
+ * rounded once to bf16 (round to nearest even).
+ *
+ * Operation sources:
+ *  - scaled_mm with per-tensor or row-wise scales, fp32 accumulation, output
+ *    cast: gist "matmul_fp8.py" (FP8 Matmul), `matmul_fp8_kernel` and its
+ *    scale epilogue; `torch._scaled_mm(a, b, scale_a, scale_b, out=...)` as
+ *    called in `torch_scaled_mm`.
+ *  - row-wise scales: x's scale of length M, y's of length N, TN layout only:
+ *    PyTorch PR #125204 "fp8 row-scaling kernel for scaled_mm", Summary.
+ *  - B column-major: gist "matmul_fp8.py", `benchmark()` (B is made
+ *    column-major "for cuBLAS compatibility").
+ *  - the bias epilogue: PyTorch PR #142045, Summary ("Limitations").
+ *  - 16-byte aligned, contiguous operands; K * itemsize a multiple of 16 with
+ *    out-of-range K zero-filled by TMA: PyTorch PR #142101, description and
+ *    the review reply on K not divisible by the K block.
+ *
+ * Layout (all row-major, no padding, leading dimension = row length):
+ *   A        e4m3fn [M, K], K contiguous.
+ *   B        e4m3fn [K, N] column-major, i.e. the bytes of Bt[N, K] row-major.
+ *   scale_a  fp32: 1 value (FP8MM_SCALE_TENSOR) or M values (FP8MM_SCALE_ROWWISE).
+ *   scale_b  fp32: 1 value (FP8MM_SCALE_TENSOR) or N values (FP8MM_SCALE_ROWWISE).
+ *   bias     bf16 [N], or NULL for none.
+ *   out      bf16 [M, N], N contiguous.
+ *
+ * Constraints: M >= 0, N >= 0, K >= 16 and K % 16 == 0 (the TMA row pitch
+ * of A and B must be a multiple of 16 bytes), A and B 16-byte aligned,
+ * scale_a / scale_b / out 4-byte aligned, bias 2-byte aligned. M == 0 or
+ * N == 0 is a no-op that returns FP8MM_OK. M, N <= 2^31 - 1, K <= 2^24.
+ *
+ * Ownership: the caller owns every buffer passed in; the library never keeps
+ * or frees them. The library owns a per-device split-K workspace (fp32
+ * partial tiles plus per-tile arrival counters) and the staging buffers of
+ * fp8_scaled_mm_host, both grown on demand and kept until the process exits.
+ *
+ * Threading: calls may come from any host thread. Calls that use the split-K
+ * workspace and run concurrently on different streams of one device race on
+ * it; issue them on one stream.
+ *
+ * Errors: argument errors are found on the host before anything is enqueued
+ * and come back as a negative fp8mm_status; nothing is launched then. A
+ * failing CUDA call returns FP8MM_ERR_CUDA and fp8mm_last_error() describes
+ * it. Kernels never trap: every wait inside them is bounded, and a wait that
+ * runs out records FP8MM_ERR_TIMEOUT in a per-device status word that
+ * fp8mm_device_status() reads.
+ */
+#ifndef FP8MM_H_
+#define FP8MM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fp8mm_scale_mode {
+    FP8MM_SCALE_TENSOR = 0,   /* one fp32 per operand                          */
+    FP8MM_SCALE_ROWWISE = 1   /* scale_a[M] per row of A, scale_b[N] per column of B */
+} fp8mm_scale_mode;
+
+typedef enum fp8mm_status {
+    FP8MM_OK = 0,
+    FP8MM_ERR_NULL = -1,      /* a required pointer is NULL                    */
+    FP8MM_ERR_SHAPE = -2,     /* M, N or K out of range, or K % 16 != 0        */
+    FP8MM_ERR_ALIGN = -3,     /* a pointer is not aligned as required          */
+    FP8MM_ERR_MODE = -4,      /* unknown scale_mode or kernel variant          */
+    FP8MM_ERR_CUDA = -5,      /* a CUDA call failed; see fp8mm_last_error()    */
+    FP8MM_ERR_NODEV = -6,     /* no CUDA device, or not an sm_103 device       */
+    FP8MM_ERR_TIMEOUT = -7    /* a bounded in-kernel wait ran out              */
+} fp8mm_status;
+
+/* Kernel variants (fp8_scaled_mm_config). */
+typedef enum fp8mm_variant {
+    FP8MM_VARIANT_AUTO = 0,   /* heuristic choice (what fp8_scaled_mm uses)     */
+    FP8MM_VARIANT_TILE = 1,   /* 128 x tile_n output tiles; tile rows over M    */
+    FP8MM_VARIANT_SWAP = 2    /* operands swapped: 128-row tiles over N, tile_n columns over M */
+} fp8mm_variant;
+
+/*
+ * out = bf16(A.B * (scale_a (x) scale_b) + bias), enqueued on `stream`
+ * (a cudaStream_t; NULL = the legacy default stream). All pointers are device
+ * pointers (or managed memory) of the current device. Asynchronous: returns
+ * once the work is enqueued; no host synchronisation.
+ */
+int fp8_scaled_mm(const void *A, const void *B,
+                  const float *scale_a, const float *scale_b, int scale_mode,
+                  const void *bias, void *out,
+                  int64_t M, int64_t N, int64_t K,
+                  void *stream);
+
+/*
+ * Same operation with an explicit kernel choice (tests, tuning, benchmarks).
+ *   variant   fp8mm_variant; AUTO ignores tile_n and split_k.
+ *   tile_n    TILE: 128 or 256. SWAP: 16, 32, 64 or 128 (M is covered by
+ *             ceil(M / tile_n) column tiles). 0 = heuristic.
+ *   split_k   1 .. 16 K-slices per output tile (reduced deterministically in
+ *             slice order by the last slice to arrive). 0 = heuristic.
+ * Returns FP8MM_ERR_MODE for an unsupported combination.
+ */
+int fp8_scaled_mm_config(const void *A, const void *B,
+                         const float *scale_a, const float *scale_b, int scale_mode,
+                         const void *bias, void *out,
+                         int64_t M, int64_t N, int64_t K,
+                         void *stream, int variant, int tile_n, int split_k);
+
+/*
+ * Host-memory entry point: A, B, scale_a, scale_b, bias and out are HOST
+ * pointers (pinned memory gives full copy bandwidth; pageable works). The
+ * call copies the inputs to device staging buffers owned by the library
+ * (grown on demand, kept per device), runs fp8_scaled_mm on `stream`, copies
+ * the result back into `out` and synchronises `stream` before returning.
+ * Same layouts and constraints as fp8_scaled_mm.
+ */
+int fp8_scaled_mm_host(const void *A, const void *B,
+                       const float *scale_a, const float *scale_b, int scale_mode,
+                       const void *bias, void *out,
+                       int64_t M, int64_t N, int64_t K,
+                       void *stream);
+
+/*
+ * Grow the current device's split-K workspace to at least `bytes` now, so
+ * that later calls do not allocate.
+ */
+int fp8mm_reserve_workspace(int64_t bytes);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's in-kernel
+ * status word. Returns FP8MM_OK, FP8MM_ERR_TIMEOUT (a bounded wait ran out;
+ * that launch's output is undefined, the split-K counters are reset here),
+ * or FP8MM_ERR_CUDA.
+ */
+int fp8mm_device_status(void *stream);
+
+/* Static description of a status code. */
+const char *fp8mm_status_string(int status);
+
+/* Detail of the last FP8MM_ERR_CUDA on this host thread ("" if none). */
+const char *fp8mm_last_error(void);
+
+/* The kernel fp8_scaled_mm would launch for this problem, as text
+ * ("tile tile_n=256 split=1 ..."); for logs and tests. */
+const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8MM_H_ */
