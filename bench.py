@@ -1,0 +1,397 @@
+"""Benchmark: FP8 scaled GEMM TFLOP/s at M = N = K = 8192 on GB300.
+
+One step = one FP8 scaled matrix multiply (the whole hot path: TMA loads,
+tcgen05 MMA, scale / bias / bf16 epilogue) over one batch of synthetic
+inputs made with the pages' quantisation recipe (bf16 randn, seed 42,
+scale = amax / 448, clamp, cast to e4m3fn, B column-major).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). With N > 1 (torchrun), every rank runs an
+independent replica on its own GPU (the output tiles are independent; there
+is no exchange step): value = all ranks' flops / max-over-ranks time.
+
+--impl reference times the CPU oracle (the plain fp64 C implementation the
+tests use) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 scaled-GEMM TFLOP/s at 8192³ (tensor/row-wise) and % of dense FP8 peak"
+UNIT = "TFLOP/s"
+M = N = K = 8192
+SEED = 42
+L2_BYTES = 129 * 1024 * 1024
+NOMINAL_FP8_PER_BF16 = 2.0      # dense fp8 : bf16 tensor rate on GB300 (4.5 / 2.25 PFLOP/s)
+FALLBACK_BF16_TFLOPS = 1900.0   # used only if the measured peaks file is absent
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=("tensor", "rowwise"), default="tensor",
+                    help="scaling of the headline line (the other is reported as a variant)")
+    ap.add_argument("--no-variant", action="store_true", help="skip the second scaling mode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "bf16_tflops_sustained": 1700.0,
+                "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------ clocks ---------
+
+REASON_BITS = {
+    0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+    0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+    0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+
+    def __init__(self, index: int, period_ms: int = 100):
+        self.index = index
+        self.period_ms = period_ms
+        self.samples = []       # (t, sm_mhz, max_mhz, reasons_mask)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--id={self.index}",
+               "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+               "--format=csv,noheader,nounits", f"-lms={self.period_ms}"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 3:
+                continue
+            try:
+                sm = float(parts[0])
+                mx = float(parts[1])
+                mask = int(parts[2], 16) if parts[2].startswith("0x") else int(parts[2])
+            except ValueError:
+                continue
+            self.samples.append((time.time(), sm, mx, mask))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed"
+        if not inside:
+            # a timed region shorter than the sampling period: use the samples
+            # nearest to it (the warm-up runs the same kernel)
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))
+            inside = near[:3]
+            window = "nearest"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "unavailable"}
+        mask = 0
+        for s in inside:
+            mask |= s[3]
+        reasons = [name for bit, name in REASON_BITS.items() if mask & bit and name != "gpu_idle"]
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------ GPU arm --------
+
+def make_device_sets(mode: int, device, n_sets: int):
+    """n_sets resident copies of the inputs (rotated per step) and outputs."""
+    import torch
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+
+    inp = make_inputs(M, N, K, mode, SEED, with_bias=False)
+    sets = []
+    for _ in range(n_sets):
+        sets.append({
+            "A": inp.a_q.to(device), "B": inp.bt_q.to(device).t(),
+            "sa": inp.scale_a.to(device), "sb": inp.scale_b.to(device),
+            "out": torch.empty((M, N), dtype=torch.bfloat16, device=device),
+        })
+    return inp, sets
+
+
+def time_device(mode: int, steps: int, warmup: int, device, sampler=None):
+    """Device-resident timing: inputs already in HBM; events on the launching stream."""
+    import torch
+    import fp8_scaled_gemm_gb300 as fm
+
+    per_set = M * K + N * K + 2 * M * N
+    n_sets = max(2, -(-3 * L2_BYTES // per_set))   # rotate > 3x L2 worth of operands
+    inp, sets = make_device_sets(mode, device, n_sets)
+    stream = torch.cuda.current_stream(device)
+
+    def step(i):
+        s = sets[i % n_sets]
+        fm.fp8_scaled_mm(s["A"], s["B"], s["sa"], s["sb"], mode, out=s["out"], stream=stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    if fm.fp8mm_device_status(stream) != 0:
+        raise RuntimeError("in-kernel wait ran out during warm-up: " + fm.fp8mm_last_error())
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    t0 = time.time()
+    for i in range(steps):
+        starts[i].record(stream)
+        step(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    t1 = time.time()
+    total_ms = starts[0].elapsed_time(ends[-1])
+    per_kernel = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if fm.fp8mm_device_status(stream) != 0:
+        raise RuntimeError("in-kernel wait ran out: " + fm.fp8mm_last_error())
+    return {
+        "total_ms": total_ms, "kernel_ms_mean": statistics.fmean(per_kernel),
+        "kernel_ms_p50": statistics.median(per_kernel),
+        "kernel_ms_p20": sorted(per_kernel)[int(0.2 * (steps - 1))],
+        "kernel_ms_p80": sorted(per_kernel)[int(0.8 * (steps - 1))],
+        "wall": (t0, t1), "n_sets": n_sets, "inp": inp,
+        "choice": fm.fp8mm_describe_choice(M, N, K, mode),
+    }
+
+
+def time_e2e(mode: int, steps: int, inp):
+    """End to end through the host-memory C entry point: every step copies the
+    inputs from pinned host memory, computes, and copies the result back."""
+    import torch
+    import fp8_scaled_gemm_gb300 as fm
+
+    A = inp.a_q.pin_memory()
+    Bt = inp.bt_q.pin_memory()
+    sa = inp.scale_a.pin_memory()
+    sb = inp.scale_b.pin_memory()
+    out = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        fm.fp8_scaled_mm_host(A, Bt.t(), sa, sb, mode, out=out)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        fm.fp8_scaled_mm_host(A, Bt.t(), sa, sb, mode, out=out)
+    dt = (time.perf_counter() - t0) / steps
+    h2d = A.numel() + Bt.numel() + 4 * (sa.numel() + sb.numel())
+    d2h = 2 * out.numel()
+    return {"value": round(2.0 * M * N * K / dt / 1e12, 2), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps, "ms_per_step": round(dt * 1e3, 4)}
+
+
+# ------------------------------------------------------------ CPU oracle -----
+
+def oracle_sample(inp, rows: int, threads: int = 0, cols: int = 0):
+    import numpy as np
+    import oracle
+
+    r = np.arange(rows, dtype=np.int64)
+    c = np.arange(cols, dtype=np.int64) if cols else None
+    t0 = time.perf_counter()
+    oracle.scaled_mm(inp.a_u8(), inp.bt_u8(), inp.sa_np(), inp.sb_np(), inp.scale_mode,
+                     bias=inp.bias_u16(), rows=r, cols=c, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp, target_s: float):
+    """The oracle (as it stands) on a bounded sample: the first R rows of the
+    output over all N columns and the full K, R sized to about target_s."""
+    import oracle
+
+    oracle.build()
+    cores = os.cpu_count() or 1
+    probe_rows = 8
+    t = oracle_sample(inp, probe_rows, cores)
+    rows = max(probe_rows, min(M, int(probe_rows * target_s / max(t, 1e-6))))
+    t = oracle_sample(inp, rows, cores)
+    flops = 2.0 * rows * N * K
+    return {"value": round(flops / t / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the {M}x{N}x{K} output, all columns, full K "
+                      f"({rows * N} outputs, {t:.1f} s, fp64 C + OpenMP)",
+            "seconds": round(t, 3)}
+
+
+# ------------------------------------------------------------ arms -----------
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import fp8_scaled_gemm_gb300 as fm
+    fm.load()
+
+    pk = peaks()
+    fp8_peak = pk["bf16_tflops"] * NOMINAL_FP8_PER_BF16
+    flops = 2.0 * M * N * K
+    head_mode = 0 if args.workload == "tensor" else 1
+
+    sampler = ClockSampler(torch.cuda.get_device_properties(device).index
+                           if hasattr(torch.cuda.get_device_properties(device), "index") else local)
+    sampler.start()
+    time.sleep(0.3)
+    res = time_device(head_mode, args.steps, args.warmup, device)
+    sampler.stop()
+    clocks = sampler.summary(*res["wall"])
+
+    total_ms = res["total_ms"]
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    achieved = flops / (res["kernel_ms_mean"] * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 inputs, fp32 accumulate, bf16 out", "data": "synthetic",
+        "pct_of_fp8_peak": round(100.0 * value / world / fp8_peak, 2),
+        "config": {"workload": f"scaled_mm M=N=K=8192 {'per-tensor' if head_mode == 0 else 'row-wise'} "
+                               "scaling, e4m3fn A row-major / B column-major, bf16 out, no bias",
+                   "M": M, "N": N, "K": K, "seed": SEED,
+                   "scale_mode": "per-tensor" if head_mode == 0 else "row-wise",
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "l2": f"inputs rotated over {res['n_sets']} resident copies "
+                         f"({res['n_sets'] * (M * K + N * K + 2 * M * N) / 2**20:.0f} MiB > L2)",
+                   "kernel": res["choice"]},
+        "kernel_ms": {"mean": round(res["kernel_ms_mean"], 5), "p50": round(res["kernel_ms_p50"], 5),
+                      "p20": round(res["kernel_ms_p20"], 5), "p80": round(res["kernel_ms_p80"], 5)},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4), "traffic": None,
+                     "peak_source": f"{pk['source']}: bf16 burst {pk['bf16_tflops']} TFLOP/s x "
+                                    f"{NOMINAL_FP8_PER_BF16} (nominal fp8:bf16 ratio)"},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+    }
+    if not args.no_variant:
+        other = 1 - head_mode
+        r2 = time_device(other, args.steps, args.warmup, device)
+        a2 = flops / (r2["kernel_ms_mean"] * 1e-3) / 1e12
+        line["variant"] = {
+            "scale_mode": "row-wise" if other == 1 else "per-tensor",
+            "value": round(flops * args.steps / (r2["total_ms"] * 1e-3) / 1e12, 2),
+            "kernel_ms_mean": round(r2["kernel_ms_mean"], 5), "achieved": round(a2, 2),
+            "frac": round(a2 / fp8_peak, 4), "kernel": r2["choice"]}
+        line["gpu_launches"] += args.steps
+    if not args.no_e2e:
+        line["e2e"] = time_e2e(head_mode, min(args.steps, 100), res["inp"])
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(res["inp"], args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+
+    oracle.build()
+    mode = 0 if args.workload == "tensor" else 1
+    inp = make_inputs(M, N, K, mode, SEED, with_bias=False)
+    cores = os.cpu_count() or 1
+    rows, cols = 8, 1024   # per step: an 8 x 1024 block of the output, full K
+    for _ in range(args.warmup):
+        oracle_sample(inp, rows, cores, cols)
+    t = 0.0
+    for _ in range(args.steps):
+        t += oracle_sample(inp, rows, cores, cols)
+    flops = 2.0 * rows * cols * K * args.steps
+    value = flops / t / 1e12
+    sample = (f"each step: rows 0..{rows - 1} x columns 0..{cols - 1} of the {M}x{N}x{K} "
+              "output, full K (the oracle decodes its operand rows on every call)")
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"scaled_mm M=N=K=8192 {'per-tensor' if mode == 0 else 'row-wise'} "
+                               "scaling (CPU oracle on a bounded row sample)",
+                   "M": M, "N": N, "K": K, "seed": SEED},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

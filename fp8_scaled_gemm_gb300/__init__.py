@@ -1,0 +1,196 @@
+"""GB300 (sm_103a) FP8 scaled matrix multiply.
+
+    out[M, N] = bf16( (A[M, K] . B[K, N]) * (scale_a (x) scale_b) + bias[N] )
+
+A thin ctypes binding over ``libfp8mm.so`` (``include/fp8mm.h``): each
+function has the name of the C entry point it calls and only checks and
+marshals arguments; every step of the computation runs in the CUDA kernels.
+There is no CPU fallback: if the library cannot be loaded, calls raise.
+
+Operation sources: gist "matmul_fp8.py" (FP8 Matmul), ``matmul_fp8_kernel``
+(scale epilogue) and ``benchmark()`` (B column-major); PyTorch PR #125204,
+Summary (row-wise scales of length M and N, TN layout); PyTorch PR #142045,
+Summary (bias).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import _build
+
+SCALE_TENSOR = 0
+SCALE_ROWWISE = 1
+VARIANT_AUTO = 0
+VARIANT_TILE = 1
+VARIANT_SWAP = 2
+
+STATUS = {
+    0: "FP8MM_OK", -1: "FP8MM_ERR_NULL", -2: "FP8MM_ERR_SHAPE", -3: "FP8MM_ERR_ALIGN",
+    -4: "FP8MM_ERR_MODE", -5: "FP8MM_ERR_CUDA", -6: "FP8MM_ERR_NODEV", -7: "FP8MM_ERR_TIMEOUT",
+}
+
+# Every symbol include/fp8mm.h declares.
+EXPORTS = (
+    "fp8_scaled_mm", "fp8_scaled_mm_config", "fp8_scaled_mm_host",
+    "fp8mm_reserve_workspace", "fp8mm_device_status", "fp8mm_status_string",
+    "fp8mm_last_error", "fp8mm_describe_choice",
+)
+
+_lib = None
+_lock = threading.Lock()
+
+
+class Fp8mmError(RuntimeError):
+    def __init__(self, status: int, detail: str = ""):
+        self.status = status
+        name = STATUS.get(status, str(status))
+        super().__init__(f"{name}: {detail}" if detail else name)
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load ``libfp8mm.so`` (built by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"CUDA library {path} is missing; build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        common = [vp, vp, vp, vp, i32, vp, vp, i64, i64, i64, vp]
+        lib.fp8_scaled_mm.argtypes = common
+        lib.fp8_scaled_mm.restype = i32
+        lib.fp8_scaled_mm_config.argtypes = common + [i32, i32, i32]
+        lib.fp8_scaled_mm_config.restype = i32
+        lib.fp8_scaled_mm_host.argtypes = common
+        lib.fp8_scaled_mm_host.restype = i32
+        lib.fp8mm_reserve_workspace.argtypes = [i64]
+        lib.fp8mm_reserve_workspace.restype = i32
+        lib.fp8mm_device_status.argtypes = [vp]
+        lib.fp8mm_device_status.restype = i32
+        lib.fp8mm_status_string.argtypes = [i32]
+        lib.fp8mm_status_string.restype = ctypes.c_char_p
+        lib.fp8mm_last_error.argtypes = []
+        lib.fp8mm_last_error.restype = ctypes.c_char_p
+        lib.fp8mm_describe_choice.argtypes = [i64, i64, i64, i32]
+        lib.fp8mm_describe_choice.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        detail = load().fp8mm_last_error().decode(errors="replace")
+        raise Fp8mmError(rc, detail)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def _validate(A, B, scale_a, scale_b, scale_mode, bias, out, device_side: bool):
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A must be [M, K] and B [K, N]")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
+    if A.dtype != torch.float8_e4m3fn or B.dtype != torch.float8_e4m3fn:
+        raise ValueError("A and B must be torch.float8_e4m3fn")
+    if A.stride() != (K, 1) and M > 1:
+        raise ValueError("A must be row-major contiguous [M, K]")
+    if B.stride() != (1, K) and N > 1:
+        raise ValueError("B must be column-major [K, N] (B.t() contiguous)")
+    if scale_mode not in (SCALE_TENSOR, SCALE_ROWWISE):
+        raise ValueError("scale_mode must be 0 (per-tensor) or 1 (row-wise)")
+    want_a = 1 if scale_mode == SCALE_TENSOR else M
+    want_b = 1 if scale_mode == SCALE_TENSOR else N
+    for name, s, n in (("scale_a", scale_a, want_a), ("scale_b", scale_b, want_b)):
+        if s.dtype != torch.float32 or s.numel() != n or not s.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 tensor of {n} values")
+    if bias is not None and (bias.dtype != torch.bfloat16 or bias.numel() != N
+                             or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous bfloat16 tensor of N values")
+    if out.dtype != torch.bfloat16 or tuple(out.shape) != (M, N) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bfloat16 [M, N] tensor")
+    tensors = [A, B, scale_a, scale_b, out] + ([bias] if bias is not None else [])
+    for t in tensors:
+        if device_side and not t.is_cuda:
+            raise ValueError("fp8_scaled_mm takes CUDA tensors (use fp8_scaled_mm_host for host memory)")
+        if not device_side and t.is_cuda:
+            raise ValueError("fp8_scaled_mm_host takes host (CPU) tensors")
+    return M, N, K
+
+
+def fp8_scaled_mm(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=None, stream=None):
+    """out = bf16(A.B * scale + bias) on the GPU. B is [K, N] column-major."""
+    if out is None:
+        out = torch.empty((A.shape[0], B.shape[1]), dtype=torch.bfloat16, device=A.device)
+    M, N, K = _validate(A, B, scale_a, scale_b, scale_mode, bias, out, True)
+    _check(load().fp8_scaled_mm(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), scale_mode,
+                                _ptr(bias), _ptr(out), M, N, K, _stream_handle(stream)))
+    return out
+
+
+def fp8_scaled_mm_config(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=None,
+                         stream=None, variant: int = VARIANT_AUTO, tile_n: int = 0,
+                         split_k: int = 0):
+    """fp8_scaled_mm with an explicit kernel choice (see include/fp8mm.h)."""
+    if out is None:
+        out = torch.empty((A.shape[0], B.shape[1]), dtype=torch.bfloat16, device=A.device)
+    M, N, K = _validate(A, B, scale_a, scale_b, scale_mode, bias, out, True)
+    _check(load().fp8_scaled_mm_config(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), scale_mode,
+                                       _ptr(bias), _ptr(out), M, N, K, _stream_handle(stream),
+                                       int(variant), int(tile_n), int(split_k)))
+    return out
+
+
+def fp8_scaled_mm_host(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=None, stream=None):
+    """Same operation on host (CPU) tensors: copies in, computes, copies out."""
+    if out is None:
+        out = torch.empty((A.shape[0], B.shape[1]), dtype=torch.bfloat16)
+    M, N, K = _validate(A, B, scale_a, scale_b, scale_mode, bias, out, False)
+    _check(load().fp8_scaled_mm_host(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), scale_mode,
+                                     _ptr(bias), _ptr(out), M, N, K, _stream_handle(stream)))
+    return out
+
+
+def fp8mm_reserve_workspace(nbytes: int) -> None:
+    _check(load().fp8mm_reserve_workspace(int(nbytes)))
+
+
+def fp8mm_device_status(stream=None) -> int:
+    """Synchronise and return the in-kernel status (0 = ok, -7 = a wait ran out)."""
+    return int(load().fp8mm_device_status(_stream_handle(stream)))
+
+
+def fp8mm_status_string(status: int) -> str:
+    return load().fp8mm_status_string(int(status)).decode()
+
+
+def fp8mm_last_error() -> str:
+    return load().fp8mm_last_error().decode(errors="replace")
+
+
+def fp8mm_describe_choice(M: int, N: int, K: int, scale_mode: int = SCALE_TENSOR) -> str:
+    return load().fp8mm_describe_choice(int(M), int(N), int(K), int(scale_mode)).decode()

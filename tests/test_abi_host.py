@@ -1,0 +1,118 @@
+"""Host-only checks of the C ABI (no GPU): the library builds and loads, it
+exports every function include/fp8mm.h declares, and argument errors come
+back as status codes before any CUDA call is made."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import fp8_scaled_gemm_gb300 as fm
+from fp8_scaled_gemm_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8mm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return fm.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_binding_exports():
+    assert header_functions() == sorted(fm.EXPORTS)
+
+
+def test_library_exports_every_header_function(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_status_strings(lib):
+    for code, name in fm.STATUS.items():
+        s = fm.fp8mm_status_string(code)
+        assert isinstance(s, str) and s
+    assert fm.fp8mm_status_string(0) == "ok"
+    assert fm.fp8mm_status_string(12345) == "unknown status"
+
+
+# Fake, never-dereferenced device addresses: argument checks must reject the
+# call before it touches CUDA.
+ALIGNED = 0x7F0000000000
+P = ctypes.c_void_p
+
+
+def call(lib, A=ALIGNED, B=ALIGNED, sa=ALIGNED, sb=ALIGNED, mode=0, bias=None, out=ALIGNED,
+         M=64, N=64, K=64):
+    return lib.fp8_scaled_mm(P(A) if A else None, P(B) if B else None, P(sa) if sa else None,
+                             P(sb) if sb else None, mode, P(bias) if bias else None,
+                             P(out) if out else None, M, N, K, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(A=0), -1), (dict(B=0), -1), (dict(sa=0), -1), (dict(sb=0), -1), (dict(out=0), -1),
+    (dict(mode=2), -4), (dict(mode=-1), -4),
+    (dict(K=0), -2), (dict(K=8), -2), (dict(K=24), -2), (dict(K=-16), -2), (dict(M=-1), -2),
+    (dict(N=-5), -2), (dict(M=2 ** 31), -2), (dict(K=2 ** 24 + 16), -2),
+    (dict(A=ALIGNED + 8), -3), (dict(B=ALIGNED + 1), -3), (dict(sa=ALIGNED + 2), -3),
+    (dict(out=ALIGNED + 2), -3), (dict(bias=ALIGNED + 1), -3),
+])
+def test_argument_errors_before_any_cuda_call(lib, kw, code):
+    assert call(lib, **kw) == code
+
+
+def test_empty_problem_is_a_noop(lib):
+    assert call(lib, M=0) == 0
+    assert call(lib, N=0) == 0
+
+
+def test_config_rejects_unsupported_choices(lib):
+    def cfg(variant, tile_n, split):
+        return lib.fp8_scaled_mm_config(P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), 0, None,
+                                        P(ALIGNED), 64, 64, 64, None, variant, tile_n, split)
+    assert cfg(3, 0, 0) == -4
+    assert cfg(1, 64, 0) == -4        # TILE takes 128 or 256
+    assert cfg(2, 256, 0) == -4       # SWAP takes 16..128
+    assert cfg(1, 128, 17) == -4
+    assert cfg(1, 128, -1) == -4
+
+
+def test_python_layer_validates_layouts():
+    M, N, K = 4, 8, 32
+    A = torch.zeros(M, K, dtype=torch.float8_e4m3fn)
+    Bt = torch.zeros(N, K, dtype=torch.float8_e4m3fn)
+    sa = torch.ones(1)
+    sb = torch.ones(1)
+    out = torch.empty(M, N, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="column-major"):
+        fm._validate(A, Bt.t().contiguous(), sa, sb, 0, None, out, False)
+    with pytest.raises(ValueError, match="float8"):
+        fm._validate(A.float(), Bt.t(), sa, sb, 0, None, out, False)
+    with pytest.raises(ValueError, match="scale_a"):
+        fm._validate(A, Bt.t(), torch.ones(M), sb, 0, None, out, False)
+    with pytest.raises(ValueError, match="scale_b"):
+        fm._validate(A, Bt.t(), torch.ones(M), torch.ones(1), 1, None, out, False)
+    with pytest.raises(ValueError, match="bias"):
+        fm._validate(A, Bt.t(), sa, sb, 0, torch.zeros(N), out, False)
+    with pytest.raises(ValueError, match="CUDA"):
+        fm._validate(A, Bt.t(), sa, sb, 0, None, out, True)
+    assert fm._validate(A, Bt.t(), sa, sb, 0, None, out, False) == (M, N, K)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(fm, "_lib", None)
+    monkeypatch.setattr(_build, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        fm.load()

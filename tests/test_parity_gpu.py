@@ -1,0 +1,127 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Small cases compare every output element; they span several tiles with a
+ragged tail in M, N and K. The configurations of the benchmark workloads are
+run at full size and compared on sampled rows and columns (every tile edge
+plus random indices), which the oracle computes one by one.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from tests._parity import bf16_bits, compare, run_and_compare, to_device
+
+pytestmark = pytest.mark.gpu
+
+TILE, SWAP = 1, 2
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _assert_ok(stats, label):
+    assert stats["violations"] == 0, f"{label}: {stats}"
+
+
+# ------------------------------------------------------------ small, full ---
+
+KERNELS = [(TILE, 128), (TILE, 256), (SWAP, 16), (SWAP, 32), (SWAP, 64), (SWAP, 128)]
+
+
+@pytest.mark.parametrize("variant,tile_n", KERNELS)
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("split", [1, 3])
+def test_every_kernel_on_a_ragged_shape(variant, tile_n, mode, split):
+    _need_gpu()
+    # M, N, K all ragged: 2+ tiles in each direction and a K tail of 16.
+    M, N, K = 300, 520, 400
+    stats, _, _ = run_and_compare(M, N, K, mode, seed=11, with_bias=(split == 3),
+                                  variant=variant, tile_n=tile_n, split_k=split)
+    _assert_ok(stats, f"v{variant} n{tile_n} mode{mode} split{split}")
+
+
+@pytest.mark.parametrize("shape", [
+    (256, 256, 256),            # the small per-tensor configuration (seed 0)
+    (1, 1, 16), (1, 7, 32), (7, 1, 48), (127, 129, 144), (129, 127, 16),
+    (255, 257, 128), (16, 77, 64),  # N odd: scalar stores
+    (64, 4096, 1024),
+])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_auto_choice_edge_shapes(shape, mode):
+    _need_gpu()
+    M, N, K = shape
+    stats, _, _ = run_and_compare(M, N, K, mode, seed=0, with_bias=(mode == 1))
+    _assert_ok(stats, f"{shape} mode{mode}")
+
+
+def test_empty_problems_leave_out_untouched():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    A = torch.zeros(0, 32, dtype=torch.float8_e4m3fn, device="cuda")
+    Bt = torch.zeros(8, 32, dtype=torch.float8_e4m3fn, device="cuda")
+    one = torch.ones(1, device="cuda")
+    out = torch.empty(0, 8, dtype=torch.bfloat16, device="cuda")
+    fm.fp8_scaled_mm(A, Bt.t(), one, one, 0, out=out)
+    torch.cuda.synchronize()
+
+
+def test_split_k_is_deterministic_and_workspace_is_reusable():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+    inp = make_inputs(48, 1000, 2048, 1, seed=5, with_bias=True)
+    A, Bt, sa, sb, bias = to_device(inp)
+    outs = []
+    for _ in range(3):
+        o = fm.fp8_scaled_mm_config(A, Bt.t(), sa, sb, 1, bias=bias, variant=SWAP, tile_n=64,
+                                    split_k=7)
+        outs.append(bf16_bits(o))
+    assert fm.fp8mm_device_status() == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    _assert_ok(compare(outs[0], inp), "split7")
+
+
+def test_host_entry_matches_device_entry():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+    inp = make_inputs(200, 333, 160, 1, seed=9, with_bias=True)
+    A, Bt, sa, sb, bias = to_device(inp)
+    dev = bf16_bits(fm.fp8_scaled_mm(A, Bt.t(), sa, sb, 1, bias=bias))
+    host = fm.fp8_scaled_mm_host(inp.a_q.pin_memory(), inp.bt_q.pin_memory().t(),
+                                 inp.scale_a, inp.scale_b, 1, bias=inp.bias)
+    assert np.array_equal(dev, bf16_bits(host))
+    _assert_ok(compare(dev, inp), "host/device")
+
+
+# ------------------------------------------------- full-size, sampled -------
+
+BENCH_SHAPES = [
+    (8192, 8192, 8192, 0, 42, False),   # per-tensor, the headline shape
+    (8192, 8192, 8192, 1, 42, False),   # row-wise, the headline shape
+    (3000, 5000, 4112, 1, 42, True),    # tails in M, N, K + bias
+    (16384, 8192, 1024, 1, 42, True),
+    (1, 8192, 8192, 1, 42, True),
+    (8191, 8193, 32, 1, 42, True),      # N odd, K = 32
+]
+
+SWEEP = [(m, n, k) for m in (16, 128, 1024, 4096, 16384)
+         for (n, k) in ((4096, 4096), (14336, 4096), (4096, 14336))]
+
+
+@pytest.mark.parametrize("M,N,K,mode,seed,bias", BENCH_SHAPES)
+def test_full_size_configs_sampled(M, N, K, mode, seed, bias):
+    _need_gpu()
+    stats, _, _ = run_and_compare(M, N, K, mode, seed, bias, sample=True)
+    _assert_ok(stats, f"{(M, N, K)} mode{mode}")
+
+
+@pytest.mark.parametrize("M,N,K", SWEEP)
+def test_rowwise_sweep_sampled(M, N, K):
+    _need_gpu()
+    stats, _, _ = run_and_compare(M, N, K, 1, 42, False, sample=True, n_random=32)
+    _assert_ok(stats, f"sweep {(M, N, K)}")
