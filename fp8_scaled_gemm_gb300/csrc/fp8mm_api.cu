@@ -281,14 +281,16 @@ int dispatch(const Choice &c, const CUtensorMap &mp, const CUtensorMap &mq, cons
 int check_args(const void *A, const void *B, const float *sa, const float *sb, int scale_mode,
                const void *bias, void *out, int64_t M, int64_t N, int64_t K)
 {
-    if (!A || !B || !sa || !sb || !out)
-        return FP8MM_ERR_NULL;
     if (scale_mode != FP8MM_SCALE_TENSOR && scale_mode != FP8MM_SCALE_ROWWISE)
         return FP8MM_ERR_MODE;
     if (M < 0 || N < 0 || M > INT32_MAX || N > INT32_MAX)
         return FP8MM_ERR_SHAPE;
     if (K < 16 || (K % 16) != 0 || K > (int64_t(1) << 24))
         return FP8MM_ERR_SHAPE;
+    if (M == 0 || N == 0)
+        return FP8MM_OK;   // empty output: nothing is read or written, pointers may be NULL
+    if (!A || !B || !sa || !sb || !out)
+        return FP8MM_ERR_NULL;
     if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
         return FP8MM_ERR_ALIGN;
     if ((reinterpret_cast<uintptr_t>(sa) & 3) || (reinterpret_cast<uintptr_t>(sb) & 3) ||

@@ -33,7 +33,8 @@
  * Constraints: M >= 0, N >= 0, K >= 16 and K % 16 == 0 (the TMA row pitch
  * of A and B must be a multiple of 16 bytes), A and B 16-byte aligned,
  * scale_a / scale_b / out 4-byte aligned, bias 2-byte aligned. M == 0 or
- * N == 0 is a no-op that returns FP8MM_OK. M, N <= 2^31 - 1, K <= 2^24.
+ * N == 0 is a no-op that returns FP8MM_OK (the pointers may then be NULL).
+ * M, N <= 2^31 - 1, K <= 2^24.
  *
  * Ownership: the caller owns every buffer passed in; the library never keeps
  * or frees them. The library owns a per-device split-K workspace (fp32
