@@ -36,7 +36,7 @@ STATUS = {
 
 # Every symbol include/fp8mm.h declares.
 EXPORTS = (
-    "fp8_scaled_mm", "fp8_scaled_mm_config", "fp8_scaled_mm_host",
+    "fp8_scaled_mm", "fp8_scaled_mm_config", "fp8_scaled_mm_host", "fp8_scaled_mm_noalloc",
     "fp8mm_reserve_workspace", "fp8mm_device_status", "fp8mm_status_string",
     "fp8mm_last_error", "fp8mm_describe_choice",
 )
@@ -78,6 +78,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fp8_scaled_mm_config.restype = i32
         lib.fp8_scaled_mm_host.argtypes = common
         lib.fp8_scaled_mm_host.restype = i32
+        lib.fp8_scaled_mm_noalloc.argtypes = common
+        lib.fp8_scaled_mm_noalloc.restype = i32
         lib.fp8mm_reserve_workspace.argtypes = [i64]
         lib.fp8mm_reserve_workspace.restype = i32
         lib.fp8mm_device_status.argtypes = [vp]
@@ -172,6 +174,22 @@ def fp8_scaled_mm_host(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=N
     M, N, K = _validate(A, B, scale_a, scale_b, scale_mode, bias, out, False)
     _check(load().fp8_scaled_mm_host(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), scale_mode,
                                      _ptr(bias), _ptr(out), M, N, K, _stream_handle(stream)))
+    return out
+
+
+def fp8_scaled_mm_noalloc(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=None, stream=None):
+    """fp8_scaled_mm for callers that cannot allocate device memory mid-run.
+
+    The library keeps its split-K scratch in a fixed array inside its device
+    image instead of allocating a workspace; problems that would need more
+    than that array holds raise Fp8mmError (FP8MM_ERR_SHAPE). ``out`` must be
+    given (allocating it here would defeat the purpose).
+    """
+    if out is None:
+        raise ValueError("fp8_scaled_mm_noalloc needs a preallocated out tensor")
+    M, N, K = _validate(A, B, scale_a, scale_b, scale_mode, bias, out, True)
+    _check(load().fp8_scaled_mm_noalloc(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), scale_mode,
+                                        _ptr(bias), _ptr(out), M, N, K, _stream_handle(stream)))
     return out
 
 

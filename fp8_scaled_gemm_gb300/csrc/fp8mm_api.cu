@@ -532,3 +532,157 @@ const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mod
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point (fp8_scaled_mm_noalloc).
+//
+// For callers that must not allocate device memory while they run: code that
+// executes inside a memory pool it does not own, or a runtime whose memory
+// was partitioned up front. Instead of the lazily grown split-K workspace it
+// uses one fixed scratch array that lives in the library's own device image,
+// so the memory is set aside when the module loads and never allocated later.
+//
+// Layout of the scratch array (every call on a device shares it; it keeps
+// the last call's contents):
+//   [0, 256)                      status word of the in-kernel bounded waits
+//   [256, 256 + 64 KiB)           split-K arrival counters (4 per output tile)
+//   [.., + 16 MiB)                fp32 split-K partial tiles
+// The status word and the counters a call uses are cleared on the caller's
+// stream before the kernel runs; the partial tiles are fully written before
+// they are read. Calls that overlap on the GPU (different streams, or
+// concurrent host threads on one device) race on the array.
+
+namespace {
+constexpr size_t kNoAllocStatusBytes = 256;
+constexpr size_t kNoAllocCounterBytes = size_t(64) * 1024;
+constexpr size_t kNoAllocPartialBytes = size_t(16) * 1024 * 1024;
+constexpr size_t kNoAllocScratchBytes = kNoAllocStatusBytes + kNoAllocCounterBytes + kNoAllocPartialBytes;
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+struct NoAllocDevice {
+    bool ready = false;
+    int sms = 0;
+    unsigned char *scratch = nullptr;   // device address of g_noalloc_scratch
+};
+NoAllocDevice g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: device checks, the tensor-map
+// encoder, and the device address of the scratch array (the array's name in
+// host code is only a host-side stand-in for it).
+int noalloc_setup(NoAllocDevice **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        t_last_error = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return FP8MM_ERR_NODEV;
+    }
+    if (dev < 0 || dev >= kMaxDevices)
+        return FP8MM_ERR_NODEV;
+    std::lock_guard<std::mutex> lock(g_mu);
+    NoAllocDevice &d = g_noalloc[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (!(major == 10 && minor == 3)) {
+            char buf[128];
+            snprintf(buf, sizeof buf, "device %d is sm_%d%d; this library is built for sm_103a", dev, major,
+                     minor);
+            t_last_error = buf;
+            return FP8MM_ERR_NODEV;
+        }
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+                t_last_error = "cuTensorMapEncodeTiled entry point not found";
+                return FP8MM_ERR_CUDA;
+            }
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+        d.scratch = static_cast<unsigned char *>(p);
+        d.sms = sms;
+        d.ready = true;
+    }
+    *out = &d;
+    return FP8MM_OK;
+}
+
+}  // namespace
+
+extern "C" int fp8_scaled_mm_noalloc(const void *A, const void *B, const float *scale_a,
+                                     const float *scale_b, int scale_mode, const void *bias, void *out,
+                                     int64_t M, int64_t N, int64_t K, void *stream)
+{
+    int rc = check_args(A, B, scale_a, scale_b, scale_mode, bias, out, M, N, K);
+    if (rc != FP8MM_OK)
+        return rc;
+    if (M == 0 || N == 0)
+        return FP8MM_OK;
+    NoAllocDevice *d = nullptr;
+    rc = noalloc_setup(&d);
+    if (rc != FP8MM_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    const Choice c = choose(M, N, K, d->sms, FP8MM_VARIANT_AUTO, 0, 0);
+    const size_t tiles = static_cast<size_t>(c.tiles_p) * c.tiles_q;
+    const size_t partial_bytes =
+        c.split > 1 ? tiles * c.split * fp8mm::kTileP * c.tile_n * sizeof(float) : 0;
+    const size_t counter_bytes = c.split > 1 ? tiles * 4 * sizeof(unsigned int) : 0;
+    if (partial_bytes > kNoAllocPartialBytes || counter_bytes > kNoAllocCounterBytes) {
+        char buf[256];
+        snprintf(buf, sizeof buf,
+                 "fp8_scaled_mm_noalloc: this problem needs %zu bytes of split-K partials and %zu bytes of "
+                 "counters; the static scratch holds %zu and %zu (use fp8_scaled_mm)",
+                 partial_bytes, counter_bytes, kNoAllocPartialBytes, kNoAllocCounterBytes);
+        t_last_error = buf;
+        return FP8MM_ERR_SHAPE;
+    }
+    cudaError_t e = cudaMemsetAsync(d->scratch, 0, kNoAllocStatusBytes + counter_bytes, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync(scratch)");
+
+    fp8mm::KernelParams kp{};
+    kp.scale_a = scale_a;
+    kp.scale_b = scale_b;
+    kp.bias = static_cast<const __nv_bfloat16 *>(bias);
+    kp.out = static_cast<__nv_bfloat16 *>(out);
+    kp.status = reinterpret_cast<int *>(d->scratch);
+    kp.counters = reinterpret_cast<unsigned int *>(d->scratch + kNoAllocStatusBytes);
+    kp.ws = reinterpret_cast<float *>(d->scratch + kNoAllocStatusBytes + kNoAllocCounterBytes);
+    kp.M = static_cast<int>(M);
+    kp.N = static_cast<int>(N);
+    kp.K = static_cast<int>(K);
+    kp.tiles_p = c.tiles_p;
+    kp.tiles_q = c.tiles_q;
+    kp.splits = c.split;
+    kp.kblocks = c.kblocks;
+    kp.num_units = c.units;
+    kp.rowwise = scale_mode == FP8MM_SCALE_ROWWISE ? 1 : 0;
+    kp.group = 8;
+    kp.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % 8) == 0) ? 1 : 0;
+    kp.timeout_cycles = kDefaultTimeoutCycles;
+
+    CUtensorMap mp, mq;
+    const bool swap = c.variant == FP8MM_VARIANT_SWAP;
+    rc = encode_operand_map(&mp, swap ? B : A, swap ? N : M, K, fp8mm::kTileP);
+    if (rc != FP8MM_OK)
+        return rc;
+    rc = encode_operand_map(&mq, swap ? A : B, swap ? M : N, K, c.tile_n);
+    if (rc != FP8MM_OK)
+        return rc;
+    return dispatch(c, mp, mq, kp, s);
+}

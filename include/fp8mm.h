@@ -126,6 +126,34 @@ int fp8_scaled_mm_host(const void *A, const void *B,
                        void *stream);
 
 /*
+ * Allocation-free variant of fp8_scaled_mm. The pages have no counterpart:
+ * this is an addition for callers that cannot allocate device memory while
+ * they run (for example code running inside a memory pool it does not own,
+ * or a runtime whose device memory was partitioned up front), because
+ * fp8_scaled_mm may cudaMalloc its split-K workspace on first use.
+ *
+ * Same arguments, layouts and result as fp8_scaled_mm. The split-K scratch
+ * is a fixed array inside the library's device image (about 16.1 MiB, held
+ * by every GPU that loads the library until the process exits): at most
+ * 16 MiB of fp32 partial tiles and 64 KiB of arrival counters. A problem
+ * whose kernel choice needs more is rejected with FP8MM_ERR_SHAPE and a
+ * message in fp8mm_last_error(); nothing is launched then. The call makes
+ * no cudaMalloc/cudaFree and uses no allocating library routine.
+ *
+ * The first call on a device does a one-time set-up (device checks and the
+ * scratch array's device address); make that first call before any stream
+ * capture. Every call on a device shares the scratch array and clears the
+ * parts it needs on `stream` first; calls that overlap on the GPU race on
+ * it. In-kernel wait timeouts of this entry point are not reported through
+ * fp8mm_device_status().
+ */
+int fp8_scaled_mm_noalloc(const void *A, const void *B,
+                          const float *scale_a, const float *scale_b, int scale_mode,
+                          const void *bias, void *out,
+                          int64_t M, int64_t N, int64_t K,
+                          void *stream);
+
+/*
  * Grow the current device's split-K workspace to at least `bytes` now, so
  * that later calls do not allocate.
  */

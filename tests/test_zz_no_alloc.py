@@ -1,0 +1,84 @@
+"""The allocation-free entry point, fp8_scaled_mm_noalloc, on the GPU.
+
+Some callers cannot allocate device memory while they run (code inside a
+memory pool it does not own, or a runtime whose memory was split up front),
+and fp8_scaled_mm may cudaMalloc its split-K workspace on first use. The
+allocation-free entry point keeps that scratch in a fixed array inside the
+library instead. These tests call it through the C ABI twice in a row on
+problems whose kernel choice uses split-K (so the scratch array is really
+used, and reused with the previous call's contents still in it) and compare
+its output with fp8_scaled_mm's within the parity tolerance of the other GPU
+tests. This file is collected last on purpose.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_scaled_gemm_gb300.inputs import make_inputs
+from tests._parity import bf16_bits, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@pytest.mark.parametrize("M,N,K,mode,with_bias", [
+    (16, 4096, 4096, 1, True),     # skinny: SWAP kernel with split-K
+    (100, 1000, 2048, 0, False),   # SWAP 128 with split-K, ragged N
+])
+def test_noalloc_matches_fp8_scaled_mm_on_two_calls(M, N, K, mode, with_bias):
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+
+    choice = fm.fp8mm_describe_choice(M, N, K, mode)
+    assert "split=1 " not in choice, f"expected a split-K choice, got {choice}"
+    inp = make_inputs(M, N, K, mode, seed=3, with_bias=with_bias)
+    A, Bt, sa, sb, bias = to_device(inp)
+    ref_out = fm.fp8_scaled_mm(A, Bt.t(), sa, sb, mode, bias=bias)
+    assert fm.fp8mm_device_status() == 0
+    ref_bits = bf16_bits(ref_out)
+    # the per-element tolerance of the parity tests, around the existing entry's output
+    _, _, absum = oracle.scaled_mm(inp.a_u8(), inp.bt_u8(), inp.sa_np(), inp.sb_np(), mode,
+                                   bias=inp.bias_u16())
+    tol = oracle.tolerance(ref_bits, absum)
+    ref = oracle.bf16_to_f64(ref_bits)
+
+    free_after = []
+    for call in range(2):
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        fm.fp8_scaled_mm_noalloc(A, Bt.t(), sa, sb, mode, bias=bias, out=out)
+        torch.cuda.synchronize()
+        free_after.append(torch.cuda.mem_get_info()[0])
+        got = oracle.bf16_to_f64(bf16_bits(out))
+        bad = int((~(np.abs(got - ref) <= tol)).sum())
+        assert bad == 0, f"call {call}: {bad} elements outside the tolerance"
+    # the second call found the array in place and took no device memory
+    assert free_after[1] == free_after[0]
+
+
+def test_noalloc_rejects_problems_beyond_the_static_scratch():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+
+    # M=128, N=8192, K=16384 on 152 SMs splits K 7 ways: 64 tiles x 7 slices x
+    # 128 x 128 fp32 partials = 28 MiB, more than the 16 MiB the array holds.
+    M, N, K = 128, 8192, 16384
+    A = torch.zeros(M, K, dtype=torch.float8_e4m3fn, device="cuda")
+    Bt = torch.zeros(N, K, dtype=torch.float8_e4m3fn, device="cuda")
+    sa = torch.ones(M, device="cuda")
+    sb = torch.ones(N, device="cuda")
+    out = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    if "split=1 " in fm.fp8mm_describe_choice(M, N, K, 1):
+        pytest.skip("this device's SM count gives no split-K choice for the probe shape")
+    with pytest.raises(fm.Fp8mmError) as ei:
+        fm.fp8_scaled_mm_noalloc(A, Bt.t(), sa, sb, 1, out=out)
+    assert ei.value.status == -2
+    assert "static scratch" in str(ei.value)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out).item() == 0   # nothing was launched
