@@ -15,6 +15,7 @@
 
 #include "fp8mm.h"
 #include "fp8mm_kernel.cuh"
+#include "fp8mm_kernel_pair.cuh"
 
 namespace {
 
@@ -162,7 +163,7 @@ int encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t
 }
 
 struct Choice {
-    int variant;   // FP8MM_VARIANT_TILE or FP8MM_VARIANT_SWAP
+    int variant;   // FP8MM_VARIANT_TILE, _SWAP or _PAIR
     int tile_n;
     int split;
     int tiles_p, tiles_q, kblocks, units, grid;
@@ -176,6 +177,8 @@ bool tile_n_supported(int variant, int tile_n)
         return tile_n == 128 || tile_n == 256;
     if (variant == FP8MM_VARIANT_SWAP)
         return tile_n == 16 || tile_n == 32 || tile_n == 64 || tile_n == 128;
+    if (variant == FP8MM_VARIANT_PAIR)
+        return tile_n == 128 || tile_n == 256;
     return false;
 }
 
@@ -208,21 +211,33 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
     Choice c{};
     c.kblocks = static_cast<int>(cdiv(K, fp8mm::kBlockK));
     if (variant == FP8MM_VARIANT_AUTO) {
+        split = 0;
         if (M <= 128) {
             variant = FP8MM_VARIANT_SWAP;
             tile_n = swap_tile_for(M);
+        } else if (cdiv(M, 256) * cdiv(N, 256) >= sms / 4) {
+            // enough 256 x 256 pair tiles to keep most SM pairs busy
+            variant = FP8MM_VARIANT_PAIR;
+            tile_n = 256;
         } else {
             variant = FP8MM_VARIANT_TILE;
             tile_n = 256;
             if (cdiv(M, 128) * cdiv(N, 256) < sms)
                 tile_n = 128;
         }
-        split = 0;
     }
     if (tile_n == 0)
-        tile_n = variant == FP8MM_VARIANT_TILE ? 256 : swap_tile_for(M);
+        tile_n = variant == FP8MM_VARIANT_SWAP ? swap_tile_for(M) : 256;
     c.variant = variant;
     c.tile_n = tile_n;
+    if (variant == FP8MM_VARIANT_PAIR) {
+        c.tiles_p = static_cast<int>(cdiv(M, 256));
+        c.tiles_q = static_cast<int>(cdiv(N, tile_n));
+        c.split = 1;
+        c.units = c.tiles_p * c.tiles_q;
+        c.grid = 2 * static_cast<int>(std::min<int64_t>(c.units, sms / 2));
+        return c;
+    }
     const int64_t prow = variant == FP8MM_VARIANT_TILE ? M : N;
     const int64_t qrow = variant == FP8MM_VARIANT_TILE ? N : M;
     c.tiles_p = static_cast<int>(cdiv(prow, fp8mm::kTileP));
@@ -259,10 +274,37 @@ int launch_kernel(const CUtensorMap &mp, const CUtensorMap &mq, const fp8mm::Ker
     return FP8MM_OK;
 }
 
+template <int BN>
+int launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const fp8mm::KernelParams &kp, int grid,
+                cudaStream_t stream)
+{
+    using C = fp8mm::PairCfg<BN>;
+    auto kern = fp8mm::fp8mm_pair_kernel<BN>;
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute");
+        attr_set[dev] = true;
+    }
+    kern<<<grid, fp8mm::kThreads, C::kSmemBytes, stream>>>(ma, mb, kp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "pair kernel launch");
+    return FP8MM_OK;
+}
+
 int dispatch(const Choice &c, const CUtensorMap &mp, const CUtensorMap &mq, const fp8mm::KernelParams &kp,
              cudaStream_t stream)
 {
-    if (c.variant == FP8MM_VARIANT_TILE) {
+    if (c.variant == FP8MM_VARIANT_PAIR) {
+        switch (c.tile_n) {
+        case 128: return launch_pair<128>(mp, mq, kp, c.grid, stream);
+        case 256: return launch_pair<256>(mp, mq, kp, c.grid, stream);
+        }
+    } else if (c.variant == FP8MM_VARIANT_TILE) {
         switch (c.tile_n) {
         case 128: return launch_kernel<128, false>(mp, mq, kp, c.grid, stream);
         case 256: return launch_kernel<256, false>(mp, mq, kp, c.grid, stream);
@@ -276,6 +318,25 @@ int dispatch(const Choice &c, const CUtensorMap &mp, const CUtensorMap &mq, cons
         }
     }
     return FP8MM_ERR_MODE;
+}
+
+// Tensor maps for the chosen kernel, then the launch. P is the operand whose
+// 128-row boxes feed the MMA's A side (A, or Bt for SWAP); Q's boxes are
+// tile_n rows (half of that per CTA for PAIR).
+int encode_and_dispatch(const Choice &c, const void *A, const void *B, int64_t M, int64_t N, int64_t K,
+                        const fp8mm::KernelParams &kp, cudaStream_t stream)
+{
+    CUtensorMap mp, mq;
+    const bool swap = c.variant == FP8MM_VARIANT_SWAP;
+    const int q_box = c.variant == FP8MM_VARIANT_PAIR ? c.tile_n / 2 : c.tile_n;
+    // B column-major [K, N] is Bt[N, K] row-major.
+    int rc = encode_operand_map(&mp, swap ? B : A, swap ? N : M, K, fp8mm::kTileP);
+    if (rc != FP8MM_OK)
+        return rc;
+    rc = encode_operand_map(&mq, swap ? A : B, swap ? M : N, K, q_box);
+    if (rc != FP8MM_OK)
+        return rc;
+    return dispatch(c, mp, mq, kp, stream);
 }
 
 int check_args(const void *A, const void *B, const float *sa, const float *sb, int scale_mode,
@@ -305,7 +366,10 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     int rc = check_args(A, B, sa, sb, scale_mode, bias, out, M, N, K);
     if (rc != FP8MM_OK)
         return rc;
-    if (variant != FP8MM_VARIANT_AUTO && variant != FP8MM_VARIANT_TILE && variant != FP8MM_VARIANT_SWAP)
+    if (variant != FP8MM_VARIANT_AUTO && variant != FP8MM_VARIANT_TILE && variant != FP8MM_VARIANT_SWAP &&
+        variant != FP8MM_VARIANT_PAIR)
+        return FP8MM_ERR_MODE;
+    if (variant == FP8MM_VARIANT_PAIR && split > 1)
         return FP8MM_ERR_MODE;
     if (variant != FP8MM_VARIANT_AUTO && tile_n != 0 && !tile_n_supported(variant, tile_n))
         return FP8MM_ERR_MODE;
@@ -347,16 +411,7 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
         kp.counters = d->counters;
     }
 
-    CUtensorMap mp, mq;
-    const bool swap = c.variant == FP8MM_VARIANT_SWAP;
-    // B column-major [K, N] is Bt[N, K] row-major.
-    rc = encode_operand_map(&mp, swap ? B : A, swap ? N : M, K, fp8mm::kTileP);
-    if (rc != FP8MM_OK)
-        return rc;
-    rc = encode_operand_map(&mq, swap ? A : B, swap ? M : N, K, c.tile_n);
-    if (rc != FP8MM_OK)
-        return rc;
-    return dispatch(c, mp, mq, kp, stream);
+    return encode_and_dispatch(c, A, B, M, N, K, kp, stream);
 }
 
 int grow_stage(DeviceState &d, int i, size_t bytes)
@@ -525,7 +580,7 @@ const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mod
     const Choice c = choose(M, N, K, d->sms, FP8MM_VARIANT_AUTO, 0, 0);
     char buf[160];
     snprintf(buf, sizeof buf, "%s tile_n=%d split=%d tiles=%dx%d units=%d grid=%d",
-             c.variant == FP8MM_VARIANT_TILE ? "tile" : "swap", c.tile_n, c.split, c.tiles_p, c.tiles_q,
+             c.variant == FP8MM_VARIANT_TILE ? "tile" : c.variant == FP8MM_VARIANT_PAIR ? "pair" : "swap", c.tile_n, c.split, c.tiles_p, c.tiles_q,
              c.units, c.grid);
     t_describe = buf;
     return t_describe.c_str();
@@ -676,13 +731,5 @@ extern "C" int fp8_scaled_mm_noalloc(const void *A, const void *B, const float *
     kp.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % 8) == 0) ? 1 : 0;
     kp.timeout_cycles = kDefaultTimeoutCycles;
 
-    CUtensorMap mp, mq;
-    const bool swap = c.variant == FP8MM_VARIANT_SWAP;
-    rc = encode_operand_map(&mp, swap ? B : A, swap ? N : M, K, fp8mm::kTileP);
-    if (rc != FP8MM_OK)
-        return rc;
-    rc = encode_operand_map(&mq, swap ? A : B, swap ? M : N, K, c.tile_n);
-    if (rc != FP8MM_OK)
-        return rc;
-    return dispatch(c, mp, mq, kp, s);
+    return encode_and_dispatch(c, A, B, M, N, K, kp, s);
 }

@@ -120,6 +120,25 @@ struct Waiter {
         }
     }
 
+    // As wait(), with cluster-scope acquire (arrivals released by the peer CTA).
+    __device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity, int where) const
+    {
+        if (ptx::mbar_try_wait_cluster(bar, parity))
+            return true;
+        const unsigned long long t0 = static_cast<unsigned long long>(clock64());
+        while (true) {
+            if (ptx::mbar_try_wait_cluster(bar, parity))
+                return true;
+            if (*abort_flag)
+                return false;
+            if (static_cast<unsigned long long>(clock64()) - t0 > limit) {
+                *abort_flag = 1;
+                atomicCAS(status, 0, kStatusTimeoutBase | where);
+                return false;
+            }
+        }
+    }
+
     // Same budget, but ignores the abort flag: used to wait for this
     // thread's own asynchronous work before leaving.
     __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity, int where) const
@@ -163,27 +182,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Epilogue for CH accumulator columns held by one thread.
+// Epilogue for CH accumulator columns held by one thread; the whole warp
+// calls it together (the per-column scale and bias are loaded once per lane
+// and broadcast with shuffles).
 // TILE: the thread owns output row m = pidx, columns n = qbase + j.
 // SWAP: the thread owns output column n = pidx, rows m = qbase + j.
 template <int CH, bool SWAP>
 __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (&v)[CH], int pidx,
-                                            int qbase, float s_tensor)
+                                            int qbase, float s_tensor, int lane)
 {
+    constexpr unsigned kAll = 0xffffffffu;
+    const int ql = qbase + (lane % CH);   // the Q index this lane loads for the warp
+    float y[CH];
     if (!SWAP) {
         const int m = pidx;
-        if (m >= p.M)
-            return;
-        const float sa = p.rowwise ? __ldg(p.scale_a + m) : 0.0f;
-        float y[CH];
+        const bool q_in = ql < p.N;
+        const float sbl = (p.rowwise && q_in) ? __ldg(p.scale_b + ql) : 0.0f;
+        const float bl = (p.bias != nullptr && q_in) ? __bfloat162float(p.bias[ql]) : 0.0f;
+        const float sa = (p.rowwise && m < p.M) ? __ldg(p.scale_a + m) : 0.0f;
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
-            const int n = qbase + j;
-            const bool in = n < p.N;
-            const float s = p.rowwise ? sa * (in ? __ldg(p.scale_b + n) : 0.0f) : s_tensor;
-            const float b = (p.bias != nullptr && in) ? __bfloat162float(p.bias[n]) : 0.0f;
-            y[j] = fmaf(v[j], s, b);
+            const float s = p.rowwise ? sa * __shfl_sync(kAll, sbl, j) : s_tensor;
+            y[j] = fmaf(v[j], s, __shfl_sync(kAll, bl, j));
         }
+        if (m >= p.M)
+            return;
         __nv_bfloat16 *orow = p.out + static_cast<size_t>(m) * p.N;
         if (p.vec_store && qbase + CH <= p.N) {
 #pragma unroll
@@ -203,17 +226,22 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
         }
     } else {
         const int n = pidx;
-        if (n >= p.N)
+        const bool n_in = n < p.N;
+        const float sal = (p.rowwise && ql < p.M) ? __ldg(p.scale_a + ql) : 0.0f;
+        const float sb = (p.rowwise && n_in) ? __ldg(p.scale_b + n) : 0.0f;
+        const float b = (p.bias != nullptr && n_in) ? __bfloat162float(p.bias[n]) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const float s = p.rowwise ? __shfl_sync(kAll, sal, j) * sb : s_tensor;
+            y[j] = fmaf(v[j], s, b);
+        }
+        if (!n_in)
             return;
-        const float sb = p.rowwise ? __ldg(p.scale_b + n) : 0.0f;
-        const float b = p.bias != nullptr ? __bfloat162float(p.bias[n]) : 0.0f;
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
             const int m = qbase + j;
-            if (m < p.M) {
-                const float s = p.rowwise ? __ldg(p.scale_a + m) * sb : s_tensor;
-                p.out[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(fmaf(v[j], s, b));
-            }
+            if (m < p.M)
+                p.out[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(y[j]);
         }
     }
 }
@@ -388,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < BN / CH; ++c) {
                     float v[CH];
                     tmem_load_chunk<CH>(trow + c * CH, v);
-                    store_chunk<CH, SWAP>(p, v, pidx, w.tq * BN + c * CH, s_tensor);
+                    store_chunk<CH, SWAP>(p, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
                 }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(tempty_bar(acc));
@@ -429,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int j = 0; j < CH; ++j)
                                 v[j] += __ldcg(part + static_cast<size_t>(c * CH + j) * kTileP + row);
                         }
-                        store_chunk<CH, SWAP>(p, v, pidx, w.tq * BN + c * CH, s_tensor);
+                        store_chunk<CH, SWAP>(p, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
                     }
                 }
             }

@@ -1,0 +1,235 @@
+// fp8mm_kernel_pair.cuh -- the same FP8 scaled GEMM with 2-SM MMAs: a cluster
+// of two CTAs computes one 256 x BN output tile with tcgen05.mma.cta_group::2.
+//
+// Each CTA of the pair loads half of every operand block into its own shared
+// memory: CTA r takes A rows [m0 + 128 r, +128) and Bt rows [n0 + BN/2 r,
+// +BN/2). The even CTA issues one 256 x BN x 32 MMA per K=32 slice; the
+// hardware reads the halves from both CTAs at the same shared-memory offsets
+// and writes D rows 0-127 into the even CTA's tensor memory, rows 128-255
+// into the odd CTA's. Per SM this moves (128 + BN/2) x 128 bytes of operands
+// per K block for 128 x BN outputs, 2/3 of what a 1-SM 128 x 256 tile moves,
+// which lets the ring be 6 stages deep.
+//
+// Synchronisation across the pair:
+//   full[s]   in the even CTA only: its producer arrives with expect_tx for
+//             both CTAs' bytes; both CTAs' TMA loads complete_tx on it.
+//   empty[s]  in both CTAs: released by a multicast tcgen05.commit.
+//   tfull[a]  in both CTAs: multicast commit after the last K block of a tile.
+//   tempty[a] in the even CTA: one arrival per epilogue warp of both CTAs (8).
+// Every wait is bounded as in fp8mm_kernel.cuh. The pair meets at a cluster
+// barrier after initialisation and before tensor memory is released, so no
+// CTA leaves while its peer may still signal it.
+#pragma once
+
+#include "fp8mm_kernel.cuh"
+
+namespace fp8mm {
+
+template <int BN>
+struct PairCfg {
+    static_assert(BN == 256 || BN == 128, "pair tile N");
+    static constexpr int kStages = 6;
+    static constexpr int kABytes = 128 * kBlockK;             // this CTA's A half
+    static constexpr int kBBytes = (BN / 2) * kBlockK;        // this CTA's Bt half
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kTmemCols = 2 * BN;                  // two fp32 accumulators
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+    static_assert(kBBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+    static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory");
+    static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
+};
+
+// Units: (256-row tile of M, BN-column tile of N); p.tiles_p counts 256-row
+// tiles, p.splits must be 1.
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    fp8mm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_b, const KernelParams p)
+{
+    using C = PairCfg<BN>;
+    constexpr int S = C::kStages;
+    constexpr int CH = 32;
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+
+    const uint32_t bar0 = sbase + S * C::kStageBytes;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+    const uint32_t done_bar = bar0 + 8u * (2 * S + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S * C::kStageBytes + 8 * (2 * S + 5));
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int cluster_id = static_cast<int>(blockIdx.x >> 1);
+    const int num_clusters = static_cast<int>(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(tfull_bar(a), 1);
+            ptx::mbar_init(tempty_bar(a), 8);
+        }
+        ptx::mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmap_a);
+        ptx::prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), C::kTmemCols);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    ptx::cluster_sync();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const Waiter W{abort_flag, p.status, p.timeout_cycles};
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ---
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+                const Unit w = decode_unit(u, p);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!W.wait(empty_bar(stage), phase ^ 1u, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = sbase + stage * C::kStageBytes;
+                    const uint32_t leader_full = ptx::mapa_shared(full_bar(stage), 0);
+                    if (rank == 0)
+                        ptx::mbar_arrive_expect_tx(full_bar(stage), 2u * C::kStageBytes);
+                    ptx::tma_load_2d_pair(sa, &tmap_a, leader_full, kb * kBlockK,
+                                          w.tp * 256 + static_cast<int>(rank) * 128);
+                    ptx::tma_load_2d_pair(sa + C::kABytes, &tmap_b, leader_full, kb * kBlockK,
+                                          w.tq * BN + static_cast<int>(rank) * (BN / 2));
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Own copies must land before the CTA may exit: the even CTA sees
+            // both CTAs' bytes on its full barriers; the odd CTA waits until
+            // its stages were consumed (released by the pair MMA).
+            const int n = issued < S ? issued : S;
+            int s = stage;
+            uint32_t ph = phase;
+            for (int i = 0; i < n; ++i) {
+                if (--s < 0) {
+                    s = S - 1;
+                    ph ^= 1u;
+                }
+                if (rank == 0)
+                    W.drain(full_bar(s), ph, 3);
+                else
+                    W.drain(empty_bar(s), ph, 6);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------- pair MMA (even CTA only) ---
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = ptx::idesc_e4m3_f32(256, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+                const Unit w = decode_unit(u, p);
+                if (!W.wait_cluster(tempty_bar(acc), acc_phase ^ 1u, 1))
+                    break;
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!W.wait(full_bar(stage), phase, 2)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = sbase + stage * C::kStageBytes;
+                    const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+                    for (int k = 0; k < kBlockK / kMmaK; ++k) {
+                        ptx::mma_e4m3_pair(d, ptx::sw128_kmajor_desc(sa + k * kMmaK),
+                                           ptx::sw128_kmajor_desc(sb + k * kMmaK), idesc,
+                                           (kb > w.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    ptx::mma_commit_pair_multicast(empty_bar(stage), 0x3);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                ptx::mma_commit_pair_multicast(tfull_bar(acc), 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            ptx::mma_commit_pair_multicast(done_bar, 0x1);
+            W.drain(done_bar, 0, 4);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue ---
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const float s_tensor = p.rowwise ? 0.0f : __ldg(p.scale_a) * __ldg(p.scale_b);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = cluster_id; u < p.num_units; u += num_clusters) {
+            const Unit w = decode_unit(u, p);
+            if (!W.wait(tfull_bar(acc), acc_phase, 5))
+                break;
+            ptx::tc_fence_after();
+            const uint32_t trow =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            const int m = w.tp * 256 + static_cast<int>(rank) * 128 + row;
+#pragma unroll 1
+            for (int c = 0; c < BN / CH; ++c) {
+                float v[CH];
+                tmem_load_chunk<CH>(trow + c * CH, v);
+                store_chunk<CH, false>(p, v, m, w.tq * BN + c * CH, s_tensor, lane);
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    ptx::cluster_sync();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    }
+}
+
+}  // namespace fp8mm

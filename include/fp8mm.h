@@ -81,7 +81,8 @@ typedef enum fp8mm_status {
 typedef enum fp8mm_variant {
     FP8MM_VARIANT_AUTO = 0,   /* heuristic choice (what fp8_scaled_mm uses)     */
     FP8MM_VARIANT_TILE = 1,   /* 128 x tile_n output tiles; tile rows over M    */
-    FP8MM_VARIANT_SWAP = 2    /* operands swapped: 128-row tiles over N, tile_n columns over M */
+    FP8MM_VARIANT_SWAP = 2,   /* operands swapped: 128-row tiles over N, tile_n columns over M */
+    FP8MM_VARIANT_PAIR = 3    /* 2-SM MMA: a CTA pair computes 256 x tile_n tiles (no split-K) */
 } fp8mm_variant;
 
 /*
@@ -100,9 +101,10 @@ int fp8_scaled_mm(const void *A, const void *B,
  * Same operation with an explicit kernel choice (tests, tuning, benchmarks).
  *   variant   fp8mm_variant; AUTO ignores tile_n and split_k.
  *   tile_n    TILE: 128 or 256. SWAP: 16, 32, 64 or 128 (M is covered by
- *             ceil(M / tile_n) column tiles). 0 = heuristic.
+ *             ceil(M / tile_n) column tiles). PAIR: 128 or 256. 0 = heuristic.
  *   split_k   1 .. 16 K-slices per output tile (reduced deterministically in
- *             slice order by the last slice to arrive). 0 = heuristic.
+ *             slice order by the last slice to arrive); PAIR takes 0 or 1.
+ *             0 = heuristic.
  * Returns FP8MM_ERR_MODE for an unsupported combination.
  */
 int fp8_scaled_mm_config(const void *A, const void *B,

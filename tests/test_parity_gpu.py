@@ -15,7 +15,7 @@ from tests._parity import bf16_bits, compare, run_and_compare, to_device
 
 pytestmark = pytest.mark.gpu
 
-TILE, SWAP = 1, 2
+TILE, SWAP, PAIR = 1, 2, 3
 
 
 def _need_gpu():
@@ -29,7 +29,8 @@ def _assert_ok(stats, label):
 
 # ------------------------------------------------------------ small, full ---
 
-KERNELS = [(TILE, 128), (TILE, 256), (SWAP, 16), (SWAP, 32), (SWAP, 64), (SWAP, 128)]
+KERNELS = [(TILE, 128), (TILE, 256), (SWAP, 16), (SWAP, 32), (SWAP, 64), (SWAP, 128),
+           (PAIR, 128), (PAIR, 256)]
 
 
 @pytest.mark.parametrize("variant,tile_n", KERNELS)
@@ -37,10 +38,13 @@ KERNELS = [(TILE, 128), (TILE, 256), (SWAP, 16), (SWAP, 32), (SWAP, 64), (SWAP, 
 @pytest.mark.parametrize("split", [1, 3])
 def test_every_kernel_on_a_ragged_shape(variant, tile_n, mode, split):
     _need_gpu()
-    # M, N, K all ragged: 2+ tiles in each direction and a K tail of 16.
+    # M, N, K all ragged: 2+ tiles in each direction and a K tail of 16. For
+    # PAIR the last 256-row tile leaves the odd CTA's rows entirely out of
+    # range, and the last column tile leaves the odd CTA's Bt half empty.
     M, N, K = 300, 520, 400
     stats, _, _ = run_and_compare(M, N, K, mode, seed=11, with_bias=(split == 3),
-                                  variant=variant, tile_n=tile_n, split_k=split)
+                                  variant=variant, tile_n=tile_n,
+                                  split_k=(1 if variant == PAIR else split))
     _assert_ok(stats, f"v{variant} n{tile_n} mode{mode} split{split}")
 
 
@@ -56,6 +60,16 @@ def test_auto_choice_edge_shapes(shape, mode):
     M, N, K = shape
     stats, _, _ = run_and_compare(M, N, K, mode, seed=0, with_bias=(mode == 1))
     _assert_ok(stats, f"{shape} mode{mode}")
+
+
+@pytest.mark.parametrize("shape", [(129, 300, 256), (512, 512, 1024), (1000, 777, 48)])
+def test_pair_kernel_shapes(shape):
+    _need_gpu()
+    M, N, K = shape
+    for tile_n in (128, 256):
+        stats, _, _ = run_and_compare(M, N, K, 1, seed=4, with_bias=True, variant=PAIR,
+                                      tile_n=tile_n, split_k=0)
+        _assert_ok(stats, f"pair{tile_n} {shape}")
 
 
 def test_empty_problems_leave_out_untouched():
