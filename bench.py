@@ -51,6 +51,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every benchmark shape instead (one JSON line per shape)")
+    ap.add_argument("--shapes", default="",
+                    help="with --sweep: comma list of MxNxK[:mode[:bias]] (default: all)")
     return ap.parse_args(argv)
 
 
@@ -291,6 +295,104 @@ def cpu_baseline(inp, target_s: float):
             "seconds": round(t, 3)}
 
 
+# ------------------------------------------------------------ sweep ----------
+
+SWEEP_SHAPES = (
+    [(m, n, k, 1, False) for m in (16, 128, 1024, 4096, 16384)
+     for (n, k) in ((4096, 4096), (14336, 4096), (4096, 14336))]
+    + [(3000, 5000, 4112, 1, True), (16384, 8192, 1024, 1, True), (1, 8192, 8192, 1, True),
+       (8191, 8193, 32, 1, True), (256, 256, 256, 0, False),
+       (8192, 8192, 8192, 0, False), (8192, 8192, 8192, 1, False)]
+)
+
+
+def algorithmic_bytes(M, N, K, mode, bias):
+    return M * K + N * K + 2 * M * N + (4 * (M + N) if mode == 1 else 8) + (2 * N if bias else 0)
+
+
+def time_shape(M, N, K, mode, bias, steps, warmup, device):
+    import torch
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+
+    inp = make_inputs(M, N, K, mode, SEED, with_bias=bias)
+    per_set = algorithmic_bytes(M, N, K, mode, bias)
+    n_sets = max(1, min(64, -(-3 * L2_BYTES // per_set)))
+    sets = []
+    for _ in range(n_sets):
+        sets.append((inp.a_q.to(device), inp.bt_q.to(device).t(), inp.scale_a.to(device),
+                     inp.scale_b.to(device), None if inp.bias is None else inp.bias.to(device),
+                     torch.empty((M, N), dtype=torch.bfloat16, device=device)))
+    stream = torch.cuda.current_stream(device)
+
+    def step(i):
+        A, B, sa, sb, b, o = sets[i % n_sets]
+        fm.fp8_scaled_mm(A, B, sa, sb, mode, bias=b, out=o)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    # The launches are captured in a CUDA graph so that host-side call
+    # overhead does not show up as kernel time for µs-scale problems.
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(steps):
+                step(i)
+    torch.cuda.synchronize(device)
+    graph.replay()
+    torch.cuda.synchronize(device)
+    per = []
+    for _ in range(5):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        per.append(e0.elapsed_time(e1) / steps)
+    if fm.fp8mm_device_status(stream) != 0:
+        raise RuntimeError("in-kernel wait ran out: " + fm.fp8mm_last_error())
+    del graph, sets
+    torch.cuda.empty_cache()
+    return statistics.median(per), min(per), n_sets, fm.fp8mm_describe_choice(M, N, K, mode)
+
+
+def run_sweep(args):
+    import torch
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    import fp8_scaled_gemm_gb300 as fm
+    fm.load()
+    pk = peaks()
+    fp8_peak = pk["bf16_tflops"] * NOMINAL_FP8_PER_BF16
+    shapes = SWEEP_SHAPES
+    if args.shapes:
+        shapes = []
+        for spec in args.shapes.split(","):
+            parts = spec.split(":")
+            M, N, K = (int(x) for x in parts[0].split("x"))
+            mode = int(parts[1]) if len(parts) > 1 else 1
+            bias = bool(int(parts[2])) if len(parts) > 2 else False
+            shapes.append((M, N, K, mode, bias))
+    for (M, N, K, mode, bias) in shapes:
+        mean, best, n_sets, choice = time_shape(M, N, K, mode, bias, args.steps, args.warmup, device)
+        flops = 2.0 * M * N * K
+        nbytes = algorithmic_bytes(M, N, K, mode, bias)
+        tflops = flops / (mean * 1e-3) / 1e12
+        gbs = nbytes / (mean * 1e-3) / 1e9
+        print(json.dumps({
+            "shape": [M, N, K], "scale_mode": "row-wise" if mode else "per-tensor", "bias": bias,
+            "kernel_us": round(mean * 1e3, 2), "kernel_us_best": round(best * 1e3, 2),
+            "timing": f"median of 5 CUDA-graph replays of {args.steps} launches",
+            "tflops": round(tflops, 1), "frac_fp8_peak": round(tflops / fp8_peak, 3),
+            "gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3),
+            "bound": "hbm" if flops / nbytes < fp8_peak * 1e12 / (pk["hbm_gbs"] * 1e9) else "tensor",
+            "rotated_sets": n_sets, "kernel": choice}), flush=True)
+
+
 # ------------------------------------------------------------ arms -----------
 
 def run_ours(args):
@@ -410,7 +512,9 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -162,6 +162,27 @@ int encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t
     return FP8MM_OK;
 }
 
+// bf16 output [M, N] (N contiguous) written in boxes of 32 rows x 64 columns
+// from a 128-byte-swizzled shared-memory stage.
+int encode_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[128];
+        snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled(out) failed (%d) M=%lld N=%lld", static_cast<int>(r),
+                 static_cast<long long>(M), static_cast<long long>(N));
+        t_last_error = buf;
+        return FP8MM_ERR_CUDA;
+    }
+    return FP8MM_OK;
+}
+
 struct Choice {
     int variant;   // FP8MM_VARIANT_TILE, _SWAP or _PAIR
     int tile_n;
@@ -182,22 +203,25 @@ bool tile_n_supported(int variant, int tile_n)
     return false;
 }
 
-// Split factor that best fills the SMs: maximise units / (waves * sms),
-// keeping at least 4 K blocks per slice; ties go to the smaller split.
-int pick_split(int64_t tiles, int kblocks, int sms)
+// Split-K factor from a small cost model, in units of one K block of one
+// tile: waves x (K blocks per slice + reduction), where a slice's reduction
+// (partial tile out through L2, counter, last slice reads all partials)
+// costs about as much as 5 K blocks for a 128 x 16..32 partial and grows
+// with the partial's size. Fitted to GB300 timings of the skinny shapes;
+// ties keep the smaller split.
+int pick_split(int64_t tiles, int kblocks, int sms, int tile_n)
 {
-    if (tiles >= sms)
-        return 1;
+    const double red = tile_n <= 32 ? 5.0 : tile_n <= 64 ? 10.0 : tile_n <= 128 ? 24.0 : 48.0;
     int best = 1;
-    double best_eff = 0.0;
+    double best_cost = 1e300;
     for (int s = 1; s <= 16; ++s) {
-        if (s > 1 && kblocks / s < 4)
+        if (s > 1 && kblocks / s < 2)
             break;
-        const int64_t units = tiles * s;
-        const int64_t waves = cdiv(units, sms);
-        const double eff = static_cast<double>(units) / static_cast<double>(waves * sms);
-        if (eff > best_eff + 1e-9) {
-            best_eff = eff;
+        const int64_t waves = cdiv(tiles * s, sms);
+        const double cost = static_cast<double>(waves) *
+                            (static_cast<double>(cdiv(kblocks, s)) + (s > 1 ? red : 0.0));
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
             best = s;
         }
     }
@@ -244,7 +268,7 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
     c.tiles_q = static_cast<int>(cdiv(qrow, tile_n));
     const int64_t tiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q;
     if (split <= 0)
-        split = pick_split(tiles, c.kblocks, sms);
+        split = pick_split(tiles, c.kblocks, sms, tile_n);
     split = std::max(1, std::min(split, c.kblocks));
     c.split = split;
     c.units = static_cast<int>(tiles * split);
@@ -253,10 +277,10 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
 }
 
 template <int BN, bool SWAP>
-int launch_kernel(const CUtensorMap &mp, const CUtensorMap &mq, const fp8mm::KernelParams &kp, int grid,
-                  cudaStream_t stream)
+int launch_kernel(const CUtensorMap &mp, const CUtensorMap &mq, const CUtensorMap &mo,
+                  const fp8mm::KernelParams &kp, int grid, cudaStream_t stream)
 {
-    using C = fp8mm::TileCfg<BN>;
+    using C = fp8mm::TileCfg<BN, SWAP>;
     auto kern = fp8mm::fp8mm_tc_kernel<BN, SWAP>;
     static bool attr_set[kMaxDevices] = {};
     int dev = 0;
@@ -267,7 +291,7 @@ int launch_kernel(const CUtensorMap &mp, const CUtensorMap &mq, const fp8mm::Ker
             return cuda_fail(e, "cudaFuncSetAttribute");
         attr_set[dev] = true;
     }
-    kern<<<grid, fp8mm::kThreads, C::kSmemBytes, stream>>>(mp, mq, kp);
+    kern<<<grid, fp8mm::kThreads, C::kSmemBytes, stream>>>(mp, mq, mo, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return cuda_fail(e, "kernel launch");
@@ -275,8 +299,8 @@ int launch_kernel(const CUtensorMap &mp, const CUtensorMap &mq, const fp8mm::Ker
 }
 
 template <int BN>
-int launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const fp8mm::KernelParams &kp, int grid,
-                cudaStream_t stream)
+int launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mo,
+                const fp8mm::KernelParams &kp, int grid, cudaStream_t stream)
 {
     using C = fp8mm::PairCfg<BN>;
     auto kern = fp8mm::fp8mm_pair_kernel<BN>;
@@ -289,32 +313,32 @@ int launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const fp8mm::Kerne
             return cuda_fail(e, "cudaFuncSetAttribute");
         attr_set[dev] = true;
     }
-    kern<<<grid, fp8mm::kThreads, C::kSmemBytes, stream>>>(ma, mb, kp);
+    kern<<<grid, fp8mm::kThreads, C::kSmemBytes, stream>>>(ma, mb, mo, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return cuda_fail(e, "pair kernel launch");
     return FP8MM_OK;
 }
 
-int dispatch(const Choice &c, const CUtensorMap &mp, const CUtensorMap &mq, const fp8mm::KernelParams &kp,
-             cudaStream_t stream)
+int dispatch(const Choice &c, const CUtensorMap &mp, const CUtensorMap &mq, const CUtensorMap &mo,
+             const fp8mm::KernelParams &kp, cudaStream_t stream)
 {
     if (c.variant == FP8MM_VARIANT_PAIR) {
         switch (c.tile_n) {
-        case 128: return launch_pair<128>(mp, mq, kp, c.grid, stream);
-        case 256: return launch_pair<256>(mp, mq, kp, c.grid, stream);
+        case 128: return launch_pair<128>(mp, mq, mo, kp, c.grid, stream);
+        case 256: return launch_pair<256>(mp, mq, mo, kp, c.grid, stream);
         }
     } else if (c.variant == FP8MM_VARIANT_TILE) {
         switch (c.tile_n) {
-        case 128: return launch_kernel<128, false>(mp, mq, kp, c.grid, stream);
-        case 256: return launch_kernel<256, false>(mp, mq, kp, c.grid, stream);
+        case 128: return launch_kernel<128, false>(mp, mq, mo, kp, c.grid, stream);
+        case 256: return launch_kernel<256, false>(mp, mq, mo, kp, c.grid, stream);
         }
     } else {
         switch (c.tile_n) {
-        case 16: return launch_kernel<16, true>(mp, mq, kp, c.grid, stream);
-        case 32: return launch_kernel<32, true>(mp, mq, kp, c.grid, stream);
-        case 64: return launch_kernel<64, true>(mp, mq, kp, c.grid, stream);
-        case 128: return launch_kernel<128, true>(mp, mq, kp, c.grid, stream);
+        case 16: return launch_kernel<16, true>(mp, mq, mo, kp, c.grid, stream);
+        case 32: return launch_kernel<32, true>(mp, mq, mo, kp, c.grid, stream);
+        case 64: return launch_kernel<64, true>(mp, mq, mo, kp, c.grid, stream);
+        case 128: return launch_kernel<128, true>(mp, mq, mo, kp, c.grid, stream);
         }
     }
     return FP8MM_ERR_MODE;
@@ -323,10 +347,21 @@ int dispatch(const Choice &c, const CUtensorMap &mp, const CUtensorMap &mq, cons
 // Tensor maps for the chosen kernel, then the launch. P is the operand whose
 // 128-row boxes feed the MMA's A side (A, or Bt for SWAP); Q's boxes are
 // tile_n rows (half of that per CTA for PAIR).
-int encode_and_dispatch(const Choice &c, const void *A, const void *B, int64_t M, int64_t N, int64_t K,
-                        const fp8mm::KernelParams &kp, cudaStream_t stream)
+int encode_and_dispatch(const Choice &c, const void *A, const void *B, void *out, int64_t M, int64_t N,
+                        int64_t K, fp8mm::KernelParams kp, cudaStream_t stream)
 {
-    CUtensorMap mp, mq;
+    CUtensorMap mp, mq, mo;
+    std::memset(&mo, 0, sizeof mo);
+    kp.out_tma = 0;
+    // Row-major epilogues store through TMA when the output rows are 16-byte
+    // aligned (TILE without split-K, PAIR); otherwise through plain stores.
+    if (c.variant != FP8MM_VARIANT_SWAP && c.split == 1 && (N % 8) == 0 &&
+        (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+        int rc = encode_out_map(&mo, out, M, N);
+        if (rc != FP8MM_OK)
+            return rc;
+        kp.out_tma = 1;
+    }
     const bool swap = c.variant == FP8MM_VARIANT_SWAP;
     const int q_box = c.variant == FP8MM_VARIANT_PAIR ? c.tile_n / 2 : c.tile_n;
     // B column-major [K, N] is Bt[N, K] row-major.
@@ -336,7 +371,7 @@ int encode_and_dispatch(const Choice &c, const void *A, const void *B, int64_t M
     rc = encode_operand_map(&mq, swap ? A : B, swap ? M : N, K, q_box);
     if (rc != FP8MM_OK)
         return rc;
-    return dispatch(c, mp, mq, kp, stream);
+    return dispatch(c, mp, mq, mo, kp, stream);
 }
 
 int check_args(const void *A, const void *B, const float *sa, const float *sb, int scale_mode,
@@ -411,7 +446,7 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
         kp.counters = d->counters;
     }
 
-    return encode_and_dispatch(c, A, B, M, N, K, kp, stream);
+    return encode_and_dispatch(c, A, B, out, M, N, K, kp, stream);
 }
 
 int grow_stage(DeviceState &d, int i, size_t bytes)
@@ -731,5 +766,5 @@ extern "C" int fp8_scaled_mm_noalloc(const void *A, const void *B, const float *
     kp.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % 8) == 0) ? 1 : 0;
     kp.timeout_cycles = kDefaultTimeoutCycles;
 
-    return encode_and_dispatch(c, A, B, M, N, K, kp, s);
+    return encode_and_dispatch(c, A, B, out, M, N, K, kp, s);
 }

@@ -75,20 +75,23 @@ struct KernelParams {
     int rowwise;                    // 0 per-tensor, 1 row-wise scales
     int group;                      // P tiles per rasterisation group
     int vec_store;                  // 16-byte output stores allowed (TILE)
+    int out_tma;                    // tmap_out is valid: rows leave through TMA stores
     unsigned long long timeout_cycles;
 };
 
-template <int BN>
+template <int BN, bool SWAP>
 struct TileCfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is 16..256 step 16");
+    static_assert(SWAP || BN % 64 == 0, "row epilogue works in 64-column blocks");
     static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
     static constexpr int kPBytes = kTileP * kBlockK;
     static constexpr int kQBytes = BN * kBlockK;
     static constexpr int kStageBytes = kPBytes + kQBytes;
+    static constexpr int kStagingBytes = SWAP ? 0 : 4 * 8192;   // 2 x 4 KB per epilogue warp
     static constexpr int kTmemCols =
         (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kBarBytes;
     static constexpr int kChunk = BN < 32 ? BN : 32;   // TMEM columns per tcgen05.ld
     static_assert(kQBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
     static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory");
@@ -246,6 +249,95 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
     }
 }
 
+// Row-major epilogue of one warp's 32 accumulator rows (TMEM lanes) x BN
+// columns, 64 columns at a time, through a 2 x 4 KB shared-memory stage per
+// warp. Each thread converts its row's 64 values to bf16 and writes them as
+// one 128-byte line of the stage, 16-byte chunks rotated by (row % 8) (the
+// 128-byte swizzle, so the eight threads of a quarter-warp hit distinct
+// banks). The block then leaves as one TMA tensor store of 32 rows x 64
+// columns (out-of-range rows and columns are clipped by the hardware), or,
+// when the output rows are not 16-byte aligned, as coalesced 4-byte row
+// segments. `chunks` counts the blocks this warp has staged so far, so the
+// two stage buffers alternate across tiles.
+template <int BN>
+__device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, const CUtensorMap *tmap_out,
+                                                     uint32_t trow, int m_row0, int n0, int lane,
+                                                     uint8_t *stage, uint32_t stage_smem, uint32_t &chunks,
+                                                     float s_tensor)
+{
+    constexpr unsigned kAll = 0xffffffffu;
+    const int m = m_row0 + lane;
+    const float sa = (p.rowwise && m < p.M) ? __ldg(p.scale_a + m) : 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+        const int nb = n0 + c * 64;
+        uint32_t w[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float v[32];
+            ptx::tmem_ld_32cols(trow + static_cast<uint32_t>(c * 64 + h * 32), v);
+            const int nl = nb + h * 32 + lane;
+            const bool in = nl < p.N;
+            const float sbl = (p.rowwise && in) ? __ldg(p.scale_b + nl) : 0.0f;
+            const float bl = (p.bias != nullptr && in) ? __bfloat162float(p.bias[nl]) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const float s0 = p.rowwise ? sa * __shfl_sync(kAll, sbl, j) : s_tensor;
+                const float s1 = p.rowwise ? sa * __shfl_sync(kAll, sbl, j + 1) : s_tensor;
+                const float y0 = fmaf(v[j], s0, __shfl_sync(kAll, bl, j));
+                const float y1 = fmaf(v[j + 1], s1, __shfl_sync(kAll, bl, j + 1));
+                w[h * 16 + j / 2] = pack_bf16x2(y0, y1);
+            }
+        }
+        const uint32_t buf = chunks & 1u;
+        if (p.out_tma && chunks >= 2) {
+            // the TMA store issued two blocks ago must have read this buffer
+            if (lane == 0)
+                ptx::bulk_wait_group_read<1>();
+            __syncwarp();
+        }
+        uint8_t *rowp = stage + buf * 4096u + lane * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+            uint4 val;
+            val.x = w[4 * cc + 0];
+            val.y = w[4 * cc + 1];
+            val.z = w[4 * cc + 2];
+            val.w = w[4 * cc + 3];
+            *reinterpret_cast<uint4 *>(rowp + ((cc ^ (lane & 7)) * 16)) = val;
+        }
+        if (p.out_tma) {
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::tma_store_2d(tmap_out, stage_smem + buf * 4096u, nb, m_row0);
+                ptx::bulk_commit_group();
+            }
+        } else {
+            __syncwarp();
+            const int col = nb + 2 * lane;
+#pragma unroll 4
+            for (int r = 0; r < 32; ++r) {
+                const int mm = m_row0 + r;
+                if (mm >= p.M)
+                    break;
+                const uint8_t *src =
+                    stage + buf * 4096u + r * 128 + ((((lane >> 2) ^ (r & 7)) & 7) * 16) + (lane & 3) * 4;
+                const uint32_t pr = *reinterpret_cast<const uint32_t *>(src);
+                __nv_bfloat16 *dst = p.out + static_cast<size_t>(mm) * p.N + col;
+                const unsigned short lo = static_cast<unsigned short>(pr & 0xFFFFu);
+                const unsigned short hi = static_cast<unsigned short>(pr >> 16);
+                if (col < p.N)
+                    dst[0] = __ushort_as_bfloat16(lo);
+                if (col + 1 < p.N)
+                    dst[1] = __ushort_as_bfloat16(hi);
+            }
+            __syncwarp();
+        }
+        ++chunks;
+    }
+}
+
 template <int CH>
 __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[CH])
 {
@@ -258,9 +350,10 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[CH])
 template <int BN, bool SWAP>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8mm_tc_kernel(const __grid_constant__ CUtensorMap tmap_p,
-                    const __grid_constant__ CUtensorMap tmap_q, const KernelParams p)
+                    const __grid_constant__ CUtensorMap tmap_q,
+                    const __grid_constant__ CUtensorMap tmap_out, const KernelParams p)
 {
-    using C = TileCfg<BN>;
+    using C = TileCfg<BN, SWAP>;
     constexpr int CH = C::kChunk;
     constexpr int S = C::kStages;
 
@@ -270,14 +363,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + pad;
     const uint32_t sbase = raw + pad;
 
-    const uint32_t bar0 = sbase + S * C::kStageBytes;
+    // stages[S] | epilogue stage (TILE) | barriers
+    const uint32_t staging0 = sbase + S * C::kStageBytes;
+    const uint32_t bar0 = staging0 + C::kStagingBytes;
     // full[S] | empty[S] | tfull[2] | tempty[2] | done
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
     const uint32_t done_bar = bar0 + 8u * (2 * S + 4);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S * C::kStageBytes + 8 * (2 * S + 5));
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + (bar0 - sbase) + 8 * (2 * S + 5));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -297,6 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmap_p);
         ptx::prefetch_tmap(&tmap_q);
+        if (!SWAP && p.out_tma)
+            ptx::prefetch_tmap(&tmap_out);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
@@ -401,6 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;             // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;      // row within the 128-row P tile
         const float s_tensor = p.rowwise ? 0.0f : __ldg(p.scale_a) * __ldg(p.scale_b);
+        const int ew = warp - 2;            // epilogue warp index: its stage buffers
+        uint8_t *stage = smem + (staging0 - sbase) + ew * 8192;
+        const uint32_t stage_smem = staging0 + static_cast<uint32_t>(ew * 8192);
+        uint32_t chunks = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
@@ -412,11 +513,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             const int pidx = w.tp * kTileP + row;
             if (p.splits == 1) {
+                if constexpr (!SWAP) {
+                    epilogue_rows_staged<BN>(p, &tmap_out, trow, w.tp * kTileP + q * 32, w.tq * BN, lane,
+                                             stage, stage_smem, chunks, s_tensor);
+                } else {
 #pragma unroll 1
-                for (int c = 0; c < BN / CH; ++c) {
-                    float v[CH];
-                    tmem_load_chunk<CH>(trow + c * CH, v);
-                    store_chunk<CH, SWAP>(p, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
+                    for (int c = 0; c < BN / CH; ++c) {
+                        float v[CH];
+                        tmem_load_chunk<CH>(trow + c * CH, v);
+                        store_chunk<CH, SWAP>(p, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
+                    }
                 }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(tempty_bar(acc));
@@ -466,6 +572,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
         }
+        // TMA stores must have finished reading the stage before the CTA exits
+        if (!SWAP && p.out_tma && lane == 0)
+            ptx::bulk_wait_group_all();
+        __syncwarp();
     }
 
     ptx::tc_fence_before();

@@ -33,8 +33,9 @@ struct PairCfg {
     static constexpr int kBBytes = (BN / 2) * kBlockK;        // this CTA's Bt half
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;                  // two fp32 accumulators
+    static constexpr int kStagingBytes = 4 * 8192;            // 2 x 4 KB per epilogue warp
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kBarBytes;
     static_assert(kBBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
     static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory");
     static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
@@ -45,11 +46,11 @@ struct PairCfg {
 template <int BN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fp8mm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                      const __grid_constant__ CUtensorMap tmap_b, const KernelParams p)
+                      const __grid_constant__ CUtensorMap tmap_b,
+                      const __grid_constant__ CUtensorMap tmap_out, const KernelParams p)
 {
     using C = PairCfg<BN>;
     constexpr int S = C::kStages;
-    constexpr int CH = 32;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -57,13 +58,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + pad;
     const uint32_t sbase = raw + pad;
 
-    const uint32_t bar0 = sbase + S * C::kStageBytes;
+    const uint32_t staging0 = sbase + S * C::kStageBytes;
+    const uint32_t bar0 = staging0 + C::kStagingBytes;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
     const uint32_t done_bar = bar0 + 8u * (2 * S + 4);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S * C::kStageBytes + 8 * (2 * S + 5));
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + (bar0 - sbase) + 8 * (2 * S + 5));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -86,6 +88,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmap_a);
         ptx::prefetch_tmap(&tmap_b);
+        if (p.out_tma)
+            ptx::prefetch_tmap(&tmap_out);
     }
     if (warp == 1) {
         ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), C::kTmemCols);
@@ -195,8 +199,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
         // ---------------------------------------------------- epilogue ---
         const int q = warp & 3;
-        const int row = q * 32 + lane;
         const float s_tensor = p.rowwise ? 0.0f : __ldg(p.scale_a) * __ldg(p.scale_b);
+        const int ew = warp - 2;
+        uint8_t *stage = smem + (staging0 - sbase) + ew * 8192;
+        const uint32_t stage_smem = staging0 + static_cast<uint32_t>(ew * 8192);
+        uint32_t chunks = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = cluster_id; u < p.num_units; u += num_clusters) {
@@ -206,13 +213,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const uint32_t trow =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            const int m = w.tp * 256 + static_cast<int>(rank) * 128 + row;
-#pragma unroll 1
-            for (int c = 0; c < BN / CH; ++c) {
-                float v[CH];
-                tmem_load_chunk<CH>(trow + c * CH, v);
-                store_chunk<CH, false>(p, v, m, w.tq * BN + c * CH, s_tensor, lane);
-            }
+            epilogue_rows_staged<BN>(p, &tmap_out, trow, w.tp * 256 + static_cast<int>(rank) * 128 + q * 32,
+                                     w.tq * BN, lane, stage, stage_smem, chunks, s_tensor);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0)
@@ -222,6 +224,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
         }
+        if (p.out_tma && lane == 0)
+            ptx::bulk_wait_group_all();
+        __syncwarp();
     }
 
     ptx::tc_fence_before();

@@ -30,7 +30,7 @@ def _need_gpu():
 
 @pytest.mark.parametrize("M,N,K,mode,with_bias", [
     (16, 4096, 4096, 1, True),     # skinny: SWAP kernel with split-K
-    (100, 1000, 2048, 0, False),   # SWAP 128 with split-K, ragged N
+    (40, 2000, 8192, 0, False),    # SWAP 64 with split-K, ragged M and N
 ])
 def test_noalloc_matches_fp8_scaled_mm_on_two_calls(M, N, K, mode, with_bias):
     _need_gpu()
@@ -62,20 +62,29 @@ def test_noalloc_matches_fp8_scaled_mm_on_two_calls(M, N, K, mode, with_bias):
     assert free_after[1] == free_after[0]
 
 
+def _scratch_bytes(choice: str) -> int:
+    """Split-K partial bytes of a kernel choice string ("swap tile_n=.. split=.. tiles=PxQ ...")."""
+    f = dict(kv.split("=") for kv in choice.split()[1:])
+    p, q = (int(x) for x in f["tiles"].split("x"))
+    split = int(f["split"])
+    return 0 if split == 1 else p * q * split * 128 * int(f["tile_n"]) * 4
+
+
 def test_noalloc_rejects_problems_beyond_the_static_scratch():
     _need_gpu()
     import fp8_scaled_gemm_gb300 as fm
 
-    # M=128, N=8192, K=16384 on 152 SMs splits K 7 ways: 64 tiles x 7 slices x
-    # 128 x 128 fp32 partials = 28 MiB, more than the 16 MiB the array holds.
-    M, N, K = 128, 8192, 16384
+    # Skinny and very deep: 100 tiles of 128 x 128 split 3 ways on 152 SMs,
+    # 300 fp32 partial tiles of 64 KiB = 18.75 MiB > the 16 MiB array.
+    M, N, K = 128, 12800, 65536
+    need = _scratch_bytes(fm.fp8mm_describe_choice(M, N, K, 1))
+    if need <= 16 * 2 ** 20:
+        pytest.skip("this device's SM count gives a smaller split for the probe shape")
     A = torch.zeros(M, K, dtype=torch.float8_e4m3fn, device="cuda")
     Bt = torch.zeros(N, K, dtype=torch.float8_e4m3fn, device="cuda")
     sa = torch.ones(M, device="cuda")
     sb = torch.ones(N, device="cuda")
     out = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
-    if "split=1 " in fm.fp8mm_describe_choice(M, N, K, 1):
-        pytest.skip("this device's SM count gives no split-K choice for the probe shape")
     with pytest.raises(fm.Fp8mmError) as ei:
         fm.fp8_scaled_mm_noalloc(A, Bt.t(), sa, sb, 1, out=out)
     assert ei.value.status == -2
