@@ -16,6 +16,7 @@
 #include "fp8mm.h"
 #include "fp8mm_kernel.cuh"
 #include "fp8mm_kernel_pair.cuh"
+#include "fp8mm_kernel_ck.cuh"
 
 namespace {
 
@@ -184,7 +185,7 @@ int encode_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N)
 }
 
 struct Choice {
-    int variant;   // FP8MM_VARIANT_TILE, _SWAP or _PAIR
+    int variant;   // FP8MM_VARIANT_TILE, _SWAP, _PAIR or _SWAPK
     int tile_n;
     int split;
     int tiles_p, tiles_q, kblocks, units, grid;
@@ -200,6 +201,8 @@ bool tile_n_supported(int variant, int tile_n)
         return tile_n == 16 || tile_n == 32 || tile_n == 64 || tile_n == 128;
     if (variant == FP8MM_VARIANT_PAIR)
         return tile_n == 128 || tile_n == 256;
+    if (variant == FP8MM_VARIANT_SWAPK)
+        return tile_n == 16 || tile_n == 32 || tile_n == 64 || tile_n == 128;
     return false;
 }
 
@@ -228,6 +231,88 @@ int pick_split(int64_t tiles, int kblocks, int sms, int tile_n)
     return best;
 }
 
+template <int BN, int CS>
+int launch_swapk(const CUtensorMap &mp, const CUtensorMap &mq, const fp8mm::KernelParams &kp, int grid,
+                 cudaStream_t stream)
+{
+    using C = fp8mm::ClusterKCfg<BN, CS>;
+    auto kern = fp8mm::fp8mm_swap_ck_kernel<BN, CS>;
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute");
+        attr_set[dev] = true;
+    }
+    kern<<<grid, fp8mm::kThreads, C::kSmemBytes, stream>>>(mp, mq, kp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cluster-K kernel launch");
+    return FP8MM_OK;
+}
+
+// Clusters of CS CTAs of the cluster-K kernel that fit on the device at once.
+template <int BN, int CS>
+int max_active_clusters_for()
+{
+    using C = fp8mm::ClusterKCfg<BN, CS>;
+    auto kern = fp8mm::fp8mm_swap_ck_kernel<BN, CS>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CS * 64, 1, 1);
+    cfg.blockDim = dim3(fp8mm::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = CS;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+int cs_index(int cs) { return cs == 2 ? 0 : cs == 4 ? 1 : 2; }
+int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : 3; }
+
+// Cached per device: [tile_n][cluster size] -> resident clusters.
+int max_active_clusters(int tile_n, int cs)
+{
+    static int cache[kMaxDevices][4][3];
+    static bool have[kMaxDevices][4][3];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int b = bn_index(tile_n), c = cs_index(cs);
+    if (!have[dev][b][c]) {
+        int n = 0;
+        switch (tile_n * 10 + cs) {
+        case 162: n = max_active_clusters_for<16, 2>(); break;
+        case 164: n = max_active_clusters_for<16, 4>(); break;
+        case 168: n = max_active_clusters_for<16, 8>(); break;
+        case 322: n = max_active_clusters_for<32, 2>(); break;
+        case 324: n = max_active_clusters_for<32, 4>(); break;
+        case 328: n = max_active_clusters_for<32, 8>(); break;
+        case 642: n = max_active_clusters_for<64, 2>(); break;
+        case 644: n = max_active_clusters_for<64, 4>(); break;
+        case 648: n = max_active_clusters_for<64, 8>(); break;
+        case 1282: n = max_active_clusters_for<128, 2>(); break;
+        case 1284: n = max_active_clusters_for<128, 4>(); break;
+        case 1288: n = max_active_clusters_for<128, 8>(); break;
+        }
+        cache[dev][b][c] = n;
+        have[dev][b][c] = true;
+    }
+    return cache[dev][b][c];
+}
+
 int swap_tile_for(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
 
 Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n, int split)
@@ -237,8 +322,31 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
     if (variant == FP8MM_VARIANT_AUTO) {
         split = 0;
         if (M <= 128) {
+            // Unsplit persistent SWAP kernel, or K spread over a cluster of
+            // 2/4/8 CTAs reduced through distributed shared memory: cost in K
+            // blocks of one tile = waves x (K blocks per CTA + reduction).
             variant = FP8MM_VARIANT_SWAP;
             tile_n = swap_tile_for(M);
+            const int64_t tiles = cdiv(N, fp8mm::kTileP) * cdiv(M, tile_n);
+            const int64_t kb = cdiv(K, fp8mm::kBlockK);
+            double best = static_cast<double>(cdiv(tiles, sms) * kb);
+            const double red = tile_n <= 32 ? 2.0 : tile_n <= 64 ? 3.0 : 4.0;
+            for (int cs : {2, 4, 8}) {
+                if (kb / cs < 2)
+                    break;
+                const int active = max_active_clusters(tile_n, cs);
+                if (active <= 0)
+                    continue;
+                const double cost = static_cast<double>(cdiv(tiles, active)) *
+                                    (static_cast<double>(cdiv(kb, cs)) + red);
+                if (cost < best - 1e-9) {
+                    best = cost;
+                    variant = FP8MM_VARIANT_SWAPK;
+                    split = cs;
+                }
+            }
+            if (variant == FP8MM_VARIANT_SWAP)
+                split = 1;
         } else if (cdiv(M, 256) * cdiv(N, 256) >= sms / 4) {
             // enough 256 x 256 pair tiles to keep most SM pairs busy
             variant = FP8MM_VARIANT_PAIR;
@@ -254,6 +362,18 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
         tile_n = variant == FP8MM_VARIANT_SWAP ? swap_tile_for(M) : 256;
     c.variant = variant;
     c.tile_n = tile_n;
+    if (variant == FP8MM_VARIANT_SWAPK) {
+        c.tiles_p = static_cast<int>(cdiv(N, fp8mm::kTileP));
+        c.tiles_q = static_cast<int>(cdiv(M, tile_n));
+        if (split != 2 && split != 4 && split != 8)
+            split = 4;
+        while (split > 2 && c.kblocks < split)
+            split /= 2;
+        c.split = split;    // cluster size: K slices per tile
+        c.units = c.tiles_p * c.tiles_q;
+        c.grid = c.units * split;
+        return c;
+    }
     if (variant == FP8MM_VARIANT_PAIR) {
         c.tiles_p = static_cast<int>(cdiv(M, 256));
         c.tiles_q = static_cast<int>(cdiv(N, tile_n));
@@ -323,6 +443,23 @@ int launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap 
 int dispatch(const Choice &c, const CUtensorMap &mp, const CUtensorMap &mq, const CUtensorMap &mo,
              const fp8mm::KernelParams &kp, cudaStream_t stream)
 {
+    if (c.variant == FP8MM_VARIANT_SWAPK) {
+        switch (c.tile_n * 10 + c.split) {
+        case 162: return launch_swapk<16, 2>(mp, mq, kp, c.grid, stream);
+        case 164: return launch_swapk<16, 4>(mp, mq, kp, c.grid, stream);
+        case 168: return launch_swapk<16, 8>(mp, mq, kp, c.grid, stream);
+        case 322: return launch_swapk<32, 2>(mp, mq, kp, c.grid, stream);
+        case 324: return launch_swapk<32, 4>(mp, mq, kp, c.grid, stream);
+        case 328: return launch_swapk<32, 8>(mp, mq, kp, c.grid, stream);
+        case 642: return launch_swapk<64, 2>(mp, mq, kp, c.grid, stream);
+        case 644: return launch_swapk<64, 4>(mp, mq, kp, c.grid, stream);
+        case 648: return launch_swapk<64, 8>(mp, mq, kp, c.grid, stream);
+        case 1282: return launch_swapk<128, 2>(mp, mq, kp, c.grid, stream);
+        case 1284: return launch_swapk<128, 4>(mp, mq, kp, c.grid, stream);
+        case 1288: return launch_swapk<128, 8>(mp, mq, kp, c.grid, stream);
+        }
+        return FP8MM_ERR_MODE;
+    }
     if (c.variant == FP8MM_VARIANT_PAIR) {
         switch (c.tile_n) {
         case 128: return launch_pair<128>(mp, mq, mo, kp, c.grid, stream);
@@ -353,16 +490,16 @@ int encode_and_dispatch(const Choice &c, const void *A, const void *B, void *out
     CUtensorMap mp, mq, mo;
     std::memset(&mo, 0, sizeof mo);
     kp.out_tma = 0;
+    const bool swap = c.variant == FP8MM_VARIANT_SWAP || c.variant == FP8MM_VARIANT_SWAPK;
     // Row-major epilogues store through TMA when the output rows are 16-byte
     // aligned (TILE without split-K, PAIR); otherwise through plain stores.
-    if (c.variant != FP8MM_VARIANT_SWAP && c.split == 1 && (N % 8) == 0 &&
+    if (!swap && c.split == 1 && (N % 8) == 0 &&
         (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
         int rc = encode_out_map(&mo, out, M, N);
         if (rc != FP8MM_OK)
             return rc;
         kp.out_tma = 1;
     }
-    const bool swap = c.variant == FP8MM_VARIANT_SWAP;
     const int q_box = c.variant == FP8MM_VARIANT_PAIR ? c.tile_n / 2 : c.tile_n;
     // B column-major [K, N] is Bt[N, K] row-major.
     int rc = encode_operand_map(&mp, swap ? B : A, swap ? N : M, K, fp8mm::kTileP);
@@ -402,7 +539,9 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     if (rc != FP8MM_OK)
         return rc;
     if (variant != FP8MM_VARIANT_AUTO && variant != FP8MM_VARIANT_TILE && variant != FP8MM_VARIANT_SWAP &&
-        variant != FP8MM_VARIANT_PAIR)
+        variant != FP8MM_VARIANT_PAIR && variant != FP8MM_VARIANT_SWAPK)
+        return FP8MM_ERR_MODE;
+    if (variant == FP8MM_VARIANT_SWAPK && split != 0 && split != 2 && split != 4 && split != 8)
         return FP8MM_ERR_MODE;
     if (variant == FP8MM_VARIANT_PAIR && split > 1)
         return FP8MM_ERR_MODE;
@@ -436,7 +575,7 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     kp.group = 8;
     kp.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % 8) == 0) ? 1 : 0;
     kp.timeout_cycles = kDefaultTimeoutCycles;
-    if (c.split > 1) {
+    if (c.split > 1 && c.variant != FP8MM_VARIANT_SWAPK) {
         const int64_t tiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q;
         const size_t ws = static_cast<size_t>(tiles) * c.split * fp8mm::kTileP * c.tile_n * sizeof(float);
         rc = grow_workspace(*d, ws, static_cast<size_t>(tiles) * 4);
@@ -615,7 +754,11 @@ const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mod
     const Choice c = choose(M, N, K, d->sms, FP8MM_VARIANT_AUTO, 0, 0);
     char buf[160];
     snprintf(buf, sizeof buf, "%s tile_n=%d split=%d tiles=%dx%d units=%d grid=%d",
-             c.variant == FP8MM_VARIANT_TILE ? "tile" : c.variant == FP8MM_VARIANT_PAIR ? "pair" : "swap", c.tile_n, c.split, c.tiles_p, c.tiles_q,
+             c.variant == FP8MM_VARIANT_TILE    ? "tile"
+             : c.variant == FP8MM_VARIANT_PAIR  ? "pair"
+             : c.variant == FP8MM_VARIANT_SWAPK ? "swapk"
+                                                : "swap",
+             c.tile_n, c.split, c.tiles_p, c.tiles_q,
              c.units, c.grid);
     t_describe = buf;
     return t_describe.c_str();
@@ -729,9 +872,10 @@ extern "C" int fp8_scaled_mm_noalloc(const void *A, const void *B, const float *
 
     const Choice c = choose(M, N, K, d->sms, FP8MM_VARIANT_AUTO, 0, 0);
     const size_t tiles = static_cast<size_t>(c.tiles_p) * c.tiles_q;
+    const bool global_split = c.split > 1 && c.variant != FP8MM_VARIANT_SWAPK;
     const size_t partial_bytes =
-        c.split > 1 ? tiles * c.split * fp8mm::kTileP * c.tile_n * sizeof(float) : 0;
-    const size_t counter_bytes = c.split > 1 ? tiles * 4 * sizeof(unsigned int) : 0;
+        global_split ? tiles * c.split * fp8mm::kTileP * c.tile_n * sizeof(float) : 0;
+    const size_t counter_bytes = global_split ? tiles * 4 * sizeof(unsigned int) : 0;
     if (partial_bytes > kNoAllocPartialBytes || counter_bytes > kNoAllocCounterBytes) {
         char buf[256];
         snprintf(buf, sizeof buf,

@@ -336,5 +336,14 @@ __device__ __forceinline__ void bulk_wait_group_all()
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+
+// Load a float from the shared memory of a CTA in the cluster (address from mapa).
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
 }  // namespace ptx
 }  // namespace fp8mm

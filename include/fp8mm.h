@@ -82,7 +82,9 @@ typedef enum fp8mm_variant {
     FP8MM_VARIANT_AUTO = 0,   /* heuristic choice (what fp8_scaled_mm uses)     */
     FP8MM_VARIANT_TILE = 1,   /* 128 x tile_n output tiles; tile rows over M    */
     FP8MM_VARIANT_SWAP = 2,   /* operands swapped: 128-row tiles over N, tile_n columns over M */
-    FP8MM_VARIANT_PAIR = 3    /* 2-SM MMA: a CTA pair computes 256 x tile_n tiles (no split-K) */
+    FP8MM_VARIANT_PAIR = 3,   /* 2-SM MMA: a CTA pair computes 256 x tile_n tiles (no split-K) */
+    FP8MM_VARIANT_SWAPK = 4   /* SWAP tiles with K spread over a cluster of split_k CTAs,
+                                 reduced through distributed shared memory (no workspace) */
 } fp8mm_variant;
 
 /*
@@ -101,10 +103,11 @@ int fp8_scaled_mm(const void *A, const void *B,
  * Same operation with an explicit kernel choice (tests, tuning, benchmarks).
  *   variant   fp8mm_variant; AUTO ignores tile_n and split_k.
  *   tile_n    TILE: 128 or 256. SWAP: 16, 32, 64 or 128 (M is covered by
- *             ceil(M / tile_n) column tiles). PAIR: 128 or 256. 0 = heuristic.
+ *             ceil(M / tile_n) column tiles). PAIR: 128 or 256. SWAPK: as
+ *             SWAP. 0 = heuristic.
  *   split_k   1 .. 16 K-slices per output tile (reduced deterministically in
- *             slice order by the last slice to arrive); PAIR takes 0 or 1.
- *             0 = heuristic.
+ *             slice order by the last slice to arrive); PAIR takes 0 or 1;
+ *             SWAPK takes the cluster size 2, 4 or 8 (0 = 4). 0 = heuristic.
  * Returns FP8MM_ERR_MODE for an unsupported combination.
  */
 int fp8_scaled_mm_config(const void *A, const void *B,

@@ -82,7 +82,8 @@ def test_config_rejects_unsupported_choices(lib):
     def cfg(variant, tile_n, split):
         return lib.fp8_scaled_mm_config(P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), 0, None,
                                         P(ALIGNED), 64, 64, 64, None, variant, tile_n, split)
-    assert cfg(4, 0, 0) == -4
+    assert cfg(5, 0, 0) == -4
+    assert cfg(4, 16, 3) == -4        # SWAPK cluster size is 2, 4 or 8
     assert cfg(3, 64, 0) == -4        # PAIR takes 128 or 256
     assert cfg(3, 256, 2) == -4       # PAIR has no split-K
     assert cfg(1, 64, 0) == -4        # TILE takes 128 or 256

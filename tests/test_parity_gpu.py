@@ -15,7 +15,7 @@ from tests._parity import bf16_bits, compare, run_and_compare, to_device
 
 pytestmark = pytest.mark.gpu
 
-TILE, SWAP, PAIR = 1, 2, 3
+TILE, SWAP, PAIR, SWAPK = 1, 2, 3, 4
 
 
 def _need_gpu():
@@ -70,6 +70,39 @@ def test_pair_kernel_shapes(shape):
         stats, _, _ = run_and_compare(M, N, K, 1, seed=4, with_bias=True, variant=PAIR,
                                       tile_n=tile_n, split_k=0)
         _assert_ok(stats, f"pair{tile_n} {shape}")
+
+
+@pytest.mark.parametrize("tile_n", [16, 32, 64, 128])
+@pytest.mark.parametrize("cs", [2, 4, 8])
+def test_cluster_k_kernel(tile_n, cs):
+    _need_gpu()
+    # ragged M, N and K; K blocks not divisible by the cluster size
+    M, N, K = min(tile_n, 100) - 3, 300, 1296
+    for mode, bias in ((0, False), (1, True)):
+        stats, _, _ = run_and_compare(M, N, K, mode, seed=21, with_bias=bias, variant=SWAPK,
+                                      tile_n=tile_n, split_k=cs)
+        _assert_ok(stats, f"swapk n{tile_n} cs{cs} mode{mode}")
+
+
+def test_cluster_k_with_fewer_k_blocks_than_ctas():
+    _need_gpu()
+    # K = 272 is 3 K blocks over a cluster of 8: five CTAs have no K block
+    stats, _, _ = run_and_compare(20, 260, 272, 1, seed=22, with_bias=True, variant=SWAPK,
+                                  tile_n=32, split_k=8)
+    _assert_ok(stats, "swapk empty slices")
+
+
+def test_cluster_k_is_deterministic():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+    inp = make_inputs(16, 4096, 4096, 1, seed=6, with_bias=True)
+    A, Bt, sa, sb, bias = to_device(inp)
+    outs = [bf16_bits(fm.fp8_scaled_mm_config(A, Bt.t(), sa, sb, 1, bias=bias, variant=SWAPK,
+                                              tile_n=16, split_k=8)) for _ in range(3)]
+    assert fm.fp8mm_device_status() == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    _assert_ok(compare(outs[0], inp), "swapk det")
 
 
 def test_empty_problems_leave_out_untouched():

@@ -29,8 +29,8 @@ def _need_gpu():
 
 
 @pytest.mark.parametrize("M,N,K,mode,with_bias", [
-    (16, 4096, 4096, 1, True),     # skinny: SWAP kernel with split-K
-    (40, 2000, 8192, 0, False),    # SWAP 64 with split-K, ragged M and N
+    (200, 2048, 16384, 1, True),   # few 128 x 128 tiles: split-K over 4 slices
+    (300, 1000, 8192, 0, False),   # split-K, ragged M and N
 ])
 def test_noalloc_matches_fp8_scaled_mm_on_two_calls(M, N, K, mode, with_bias):
     _need_gpu()
@@ -49,21 +49,26 @@ def test_noalloc_matches_fp8_scaled_mm_on_two_calls(M, N, K, mode, with_bias):
     tol = oracle.tolerance(ref_bits, absum)
     ref = oracle.bf16_to_f64(ref_bits)
 
-    free_after = []
-    for call in range(2):
-        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    # both outputs exist before the calls, so any change in free device
+    # memory across the two calls would come from the entry point itself
+    outs = [torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    for out in outs:
         fm.fp8_scaled_mm_noalloc(A, Bt.t(), sa, sb, mode, bias=bias, out=out)
-        torch.cuda.synchronize()
-        free_after.append(torch.cuda.mem_get_info()[0])
+    torch.cuda.synchronize()
+    free_after = torch.cuda.mem_get_info()[0]
+    for call, out in enumerate(outs):
         got = oracle.bf16_to_f64(bf16_bits(out))
         bad = int((~(np.abs(got - ref) <= tol)).sum())
         assert bad == 0, f"call {call}: {bad} elements outside the tolerance"
-    # the second call found the array in place and took no device memory
-    assert free_after[1] == free_after[0]
+    assert free_after == free_before
 
 
 def _scratch_bytes(choice: str) -> int:
     """Split-K partial bytes of a kernel choice string ("swap tile_n=.. split=.. tiles=PxQ ...")."""
+    if not choice.startswith(("tile", "swap ")):
+        return 0   # the pair and cluster kernels use no scratch
     f = dict(kv.split("=") for kv in choice.split()[1:])
     p, q = (int(x) for x in f["tiles"].split("x"))
     split = int(f["split"])
@@ -74,9 +79,9 @@ def test_noalloc_rejects_problems_beyond_the_static_scratch():
     _need_gpu()
     import fp8_scaled_gemm_gb300 as fm
 
-    # Skinny and very deep: 100 tiles of 128 x 128 split 3 ways on 152 SMs,
-    # 300 fp32 partial tiles of 64 KiB = 18.75 MiB > the 16 MiB array.
-    M, N, K = 128, 12800, 65536
+    # 100 tiles of 128 x 128 (TILE variant) and very deep K: split 3 ways on
+    # 152 SMs, 300 fp32 partial tiles of 64 KiB = 18.75 MiB > the 16 MiB array.
+    M, N, K = 640, 2560, 65536
     need = _scratch_bytes(fm.fp8mm_describe_choice(M, N, K, 1))
     if need <= 16 * 2 ** 20:
         pytest.skip("this device's SM count gives a smaller split for the probe shape")
@@ -85,6 +90,7 @@ def test_noalloc_rejects_problems_beyond_the_static_scratch():
     sa = torch.ones(M, device="cuda")
     sb = torch.ones(N, device="cuda")
     out = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    assert _scratch_bytes(fm.fp8mm_describe_choice(M, N, K, 1)) == need
     with pytest.raises(fm.Fp8mmError) as ei:
         fm.fp8_scaled_mm_noalloc(A, Bt.t(), sa, sb, 1, out=out)
     assert ei.value.status == -2
