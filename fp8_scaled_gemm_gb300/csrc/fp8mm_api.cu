@@ -411,7 +411,7 @@ int launch_kernel(const CUtensorMap &mp, const CUtensorMap &mq, const CUtensorMa
             return cuda_fail(e, "cudaFuncSetAttribute");
         attr_set[dev] = true;
     }
-    kern<<<grid, fp8mm::kThreads, C::kSmemBytes, stream>>>(mp, mq, mo, kp);
+    kern<<<grid, fp8mm::EpiShape<SWAP>::kThreads, C::kSmemBytes, stream>>>(mp, mq, mo, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return cuda_fail(e, "kernel launch");
@@ -433,7 +433,7 @@ int launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap 
             return cuda_fail(e, "cudaFuncSetAttribute");
         attr_set[dev] = true;
     }
-    kern<<<grid, fp8mm::kThreads, C::kSmemBytes, stream>>>(ma, mb, mo, kp);
+    kern<<<grid, fp8mm::EpiShape<false>::kThreads, C::kSmemBytes, stream>>>(ma, mb, mo, kp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return cuda_fail(e, "pair kernel launch");
@@ -578,7 +578,7 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     if (c.split > 1 && c.variant != FP8MM_VARIANT_SWAPK) {
         const int64_t tiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q;
         const size_t ws = static_cast<size_t>(tiles) * c.split * fp8mm::kTileP * c.tile_n * sizeof(float);
-        rc = grow_workspace(*d, ws, static_cast<size_t>(tiles) * 4);
+        rc = grow_workspace(*d, ws, static_cast<size_t>(tiles) * fp8mm::kCountersPerTile);
         if (rc != FP8MM_OK)
             return rc;
         kp.ws = d->ws;
@@ -686,7 +686,7 @@ int fp8mm_reserve_workspace(int64_t bytes)
         return rc;
     // Smallest partial tile is 128 x 16 fp32: bounds the tiles this can hold.
     const size_t tiles = static_cast<size_t>(bytes) / (fp8mm::kTileP * 16 * sizeof(float)) + 1;
-    return grow_workspace(*d, static_cast<size_t>(bytes), tiles * 4);
+    return grow_workspace(*d, static_cast<size_t>(bytes), tiles * fp8mm::kCountersPerTile);
 }
 
 int fp8mm_device_status(void *stream)
@@ -875,7 +875,7 @@ extern "C" int fp8_scaled_mm_noalloc(const void *A, const void *B, const float *
     const bool global_split = c.split > 1 && c.variant != FP8MM_VARIANT_SWAPK;
     const size_t partial_bytes =
         global_split ? tiles * c.split * fp8mm::kTileP * c.tile_n * sizeof(float) : 0;
-    const size_t counter_bytes = global_split ? tiles * 4 * sizeof(unsigned int) : 0;
+    const size_t counter_bytes = global_split ? tiles * fp8mm::kCountersPerTile * sizeof(unsigned int) : 0;
     if (partial_bytes > kNoAllocPartialBytes || counter_bytes > kNoAllocCounterBytes) {
         char buf[256];
         snprintf(buf, sizeof buf,

@@ -55,7 +55,18 @@ namespace fp8mm {
 constexpr int kTileP = 128;   // rows of the MMA A operand (TMEM lanes)
 constexpr int kBlockK = 128;  // K elements (= bytes) per ring stage: one 128-B swizzle row
 constexpr int kMmaK = 32;     // K per tcgen05.mma of kind::f8f6f4
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;          // SWAP kernels: TMA, MMA, 4 epilogue warps
+
+// Row-major (TILE / PAIR) kernels run 8 epilogue warps: two per TMEM lane
+// quarter, each taking half of the tile's columns.
+template <bool SWAP>
+struct EpiShape {
+    static constexpr int kWarps = SWAP ? 4 : 8;
+    static constexpr int kThreads = 64 + 32 * kWarps;
+};
+
+// Split-K arrival counters per output tile (one per epilogue warp, at most 8).
+constexpr int kCountersPerTile = 8;
 
 // Device status codes (written once per launch, first writer wins).
 constexpr int kStatusTimeoutBase = 0x100;
@@ -66,7 +77,7 @@ struct KernelParams {
     const __nv_bfloat16 *bias;      // N values or nullptr
     __nv_bfloat16 *out;             // [M, N] row-major
     float *ws;                      // split-K partial tiles (splits > 1)
-    unsigned int *counters;         // split-K arrivals, 4 per output tile
+    unsigned int *counters;         // split-K arrivals, kCountersPerTile per output tile
     int *status;                    // device status word
     int M, N, K;
     int tiles_p, tiles_q;           // ceil(P rows / 128), ceil(Q rows / BN)
@@ -87,7 +98,7 @@ struct TileCfg {
     static constexpr int kPBytes = kTileP * kBlockK;
     static constexpr int kQBytes = BN * kBlockK;
     static constexpr int kStageBytes = kPBytes + kQBytes;
-    static constexpr int kStagingBytes = SWAP ? 0 : 4 * 8192;   // 2 x 4 KB per epilogue warp
+    static constexpr int kStagingBytes = SWAP ? 0 : EpiShape<SWAP>::kWarps * 4096;   // 4 KB per epilogue warp
     static constexpr int kTmemCols =
         (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
     static constexpr int kBarBytes = 256;
@@ -250,15 +261,16 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
 }
 
 // Row-major epilogue of one warp's 32 accumulator rows (TMEM lanes) x BN
-// columns, 64 columns at a time, through a 2 x 4 KB shared-memory stage per
+// columns, 64 columns at a time, through a 4 KB shared-memory stage per
 // warp. Each thread converts its row's 64 values to bf16 and writes them as
 // one 128-byte line of the stage, 16-byte chunks rotated by (row % 8) (the
 // 128-byte swizzle, so the eight threads of a quarter-warp hit distinct
 // banks). The block then leaves as one TMA tensor store of 32 rows x 64
 // columns (out-of-range rows and columns are clipped by the hardware), or,
 // when the output rows are not 16-byte aligned, as coalesced 4-byte row
-// segments. `chunks` counts the blocks this warp has staged so far, so the
-// two stage buffers alternate across tiles.
+// segments. `chunks` counts the blocks this warp has staged so far; before
+// the stage is rewritten, the TMA store of the previous block must have read
+// it (that wait comes after the next block's TMEM loads and arithmetic).
 template <int BN>
 __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, const CUtensorMap *tmap_out,
                                                      uint32_t trow, int m_row0, int n0, int lane,
@@ -289,11 +301,11 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                 w[h * 16 + j / 2] = pack_bf16x2(y0, y1);
             }
         }
-        const uint32_t buf = chunks & 1u;
-        if (p.out_tma && chunks >= 2) {
-            // the TMA store issued two blocks ago must have read this buffer
+        const uint32_t buf = 0;
+        if (p.out_tma && chunks >= 1) {
+            // the TMA store of the previous block must have read the stage
             if (lane == 0)
-                ptx::bulk_wait_group_read<1>();
+                ptx::bulk_wait_group_read<0>();
             __syncwarp();
         }
         uint8_t *rowp = stage + buf * 4096u + lane * 128;
@@ -348,7 +360,7 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[CH])
 }
 
 template <int BN, bool SWAP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
     fp8mm_tc_kernel(const __grid_constant__ CUtensorMap tmap_p,
                     const __grid_constant__ CUtensorMap tmap_q,
                     const __grid_constant__ CUtensorMap tmap_out, const KernelParams p)
@@ -356,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = TileCfg<BN, SWAP>;
     constexpr int CH = C::kChunk;
     constexpr int S = C::kStages;
+    constexpr int kEpiWarps = EpiShape<SWAP>::kWarps;
+    constexpr int kWarpCols = BN / (kEpiWarps / 4);     // columns of one epilogue warp
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -385,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(tfull_bar(a), 1);
-            ptx::mbar_init(tempty_bar(a), 128);
+            ptx::mbar_init(tempty_bar(a), 32 * kEpiWarps);
         }
         ptx::mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -498,9 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;             // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;      // row within the 128-row P tile
         const float s_tensor = p.rowwise ? 0.0f : __ldg(p.scale_a) * __ldg(p.scale_b);
-        const int ew = warp - 2;            // epilogue warp index: its stage buffers
-        uint8_t *stage = smem + (staging0 - sbase) + ew * 8192;
-        const uint32_t stage_smem = staging0 + static_cast<uint32_t>(ew * 8192);
+        const int ew = warp - 2;            // epilogue warp index: its stage buffer
+        const int col0 = (ew / 4) * kWarpCols;  // this warp's first column of the tile
+        uint8_t *stage = smem + (staging0 - sbase) + ew * 4096;
+        const uint32_t stage_smem = staging0 + static_cast<uint32_t>(ew * 4096);
         uint32_t chunks = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -514,8 +529,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pidx = w.tp * kTileP + row;
             if (p.splits == 1) {
                 if constexpr (!SWAP) {
-                    epilogue_rows_staged<BN>(p, &tmap_out, trow, w.tp * kTileP + q * 32, w.tq * BN, lane,
-                                             stage, stage_smem, chunks, s_tensor);
+                    epilogue_rows_staged<kWarpCols>(p, &tmap_out, trow + col0, w.tp * kTileP + q * 32,
+                                                    w.tq * BN + col0, lane, stage, stage_smem, chunks,
+                                                    s_tensor);
                 } else {
 #pragma unroll 1
                     for (int c = 0; c < BN / CH; ++c) {
@@ -530,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const size_t tile_elems = static_cast<size_t>(kTileP) * BN;
                 float *mine = p.ws + (static_cast<size_t>(w.tile) * p.splits + w.split) * tile_elems;
 #pragma unroll 1
-                for (int c = 0; c < BN / CH; ++c) {
+                for (int c = col0 / CH; c < (col0 + kWarpCols) / CH; ++c) {
                     float v[CH];
                     tmem_load_chunk<CH>(trow + c * CH, v);
 #pragma unroll
@@ -542,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __threadfence();
                 __syncwarp();
                 unsigned int old = 0;
-                unsigned int *cnt = p.counters + static_cast<size_t>(w.tile) * 4 + q;
+                unsigned int *cnt = p.counters + static_cast<size_t>(w.tile) * kCountersPerTile + ew;
                 if (lane == 0)
                     old = atomicAdd(cnt, 1u);
                 old = __shfl_sync(0xffffffffu, old, 0);
@@ -552,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __threadfence();
                     const float *base = p.ws + static_cast<size_t>(w.tile) * p.splits * tile_elems;
 #pragma unroll 1
-                    for (int c = 0; c < BN / CH; ++c) {
+                    for (int c = col0 / CH; c < (col0 + kWarpCols) / CH; ++c) {
                         float v[CH];
 #pragma unroll
                         for (int j = 0; j < CH; ++j)

@@ -198,21 +198,35 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
         const float b = (p.bias != nullptr && n_in) ? __bfloat162float(p.bias[n]) : 0.0f;
         const float s_tensor = p.rowwise ? 0.0f : __ldg(p.scale_a) * __ldg(p.scale_b);
         const uint32_t local0 = ptx::smem_addr(partial);
+        // columns t / kRows, + CS, + 2 CS, ...: kItems per thread, processed
+        // kBatch at a time so that kBatch x CS remote loads are in flight
+        constexpr int kItems = BN / kColStep;
+        constexpr int kBatch = kItems < 8 ? kItems : 8;
+        static_assert(kItems % kBatch == 0, "column batches");
+        const int col0 = t / kRows;
 #pragma unroll 1
-        for (int col = t / kRows; col < BN; col += kColStep) {
-            const uint32_t off = static_cast<uint32_t>((col * kTileP + r) * 4);
-            float part[CS];
+        for (int i0 = 0; i0 < kItems; i0 += kBatch) {
+            float part[kBatch][CS];
 #pragma unroll
-            for (int s = 0; s < CS; ++s)
-                part[s] = ptx::ld_shared_cluster_f32(ptx::mapa_shared(local0 + off, static_cast<uint32_t>(s)));
-            float acc = part[0];
+            for (int i = 0; i < kBatch; ++i) {
+                const int col = col0 + (i0 + i) * kColStep;
+                const uint32_t off = static_cast<uint32_t>((col * kTileP + r) * 4);
 #pragma unroll
-            for (int s = 1; s < CS; ++s)
-                acc += part[s];
-            const int m = tq * BN + col;
-            if (n_in && m < p.M) {
-                const float sc = p.rowwise ? __ldg(p.scale_a + m) * sb : s_tensor;
-                p.out[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(fmaf(acc, sc, b));
+                for (int s = 0; s < CS; ++s)
+                    part[i][s] =
+                        ptx::ld_shared_cluster_f32(ptx::mapa_shared(local0 + off, static_cast<uint32_t>(s)));
+            }
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                float acc = part[i][0];
+#pragma unroll
+                for (int s = 1; s < CS; ++s)
+                    acc += part[i][s];
+                const int m = tq * BN + col0 + (i0 + i) * kColStep;
+                if (n_in && m < p.M) {
+                    const float sc = p.rowwise ? __ldg(p.scale_a + m) * sb : s_tensor;
+                    p.out[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(fmaf(acc, sc, b));
+                }
             }
         }
     }

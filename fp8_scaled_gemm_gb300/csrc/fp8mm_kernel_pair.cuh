@@ -15,7 +15,7 @@
 //             both CTAs' bytes; both CTAs' TMA loads complete_tx on it.
 //   empty[s]  in both CTAs: released by a multicast tcgen05.commit.
 //   tfull[a]  in both CTAs: multicast commit after the last K block of a tile.
-//   tempty[a] in the even CTA: one arrival per epilogue warp of both CTAs (8).
+//   tempty[a] in the even CTA: one arrival per epilogue warp of both CTAs (16).
 // Every wait is bounded as in fp8mm_kernel.cuh. The pair meets at a cluster
 // barrier after initialisation and before tensor memory is released, so no
 // CTA leaves while its peer may still signal it.
@@ -33,7 +33,8 @@ struct PairCfg {
     static constexpr int kBBytes = (BN / 2) * kBlockK;        // this CTA's Bt half
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;                  // two fp32 accumulators
-    static constexpr int kStagingBytes = 4 * 8192;            // 2 x 4 KB per epilogue warp
+    static constexpr int kEpiWarps = EpiShape<false>::kWarps;
+    static constexpr int kStagingBytes = kEpiWarps * 4096;    // 4 KB per epilogue warp
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kBarBytes;
     static_assert(kBBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
@@ -44,13 +45,14 @@ struct PairCfg {
 // Units: (256-row tile of M, BN-column tile of N); p.tiles_p counts 256-row
 // tiles, p.splits must be 1.
 template <int BN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<false>::kThreads, 1)
     fp8mm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_out, const KernelParams p)
 {
     using C = PairCfg<BN>;
     constexpr int S = C::kStages;
+    constexpr int kWarpCols = BN / (C::kEpiWarps / 4);   // columns of one epilogue warp
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -81,7 +83,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(tfull_bar(a), 1);
-            ptx::mbar_init(tempty_bar(a), 8);
+            ptx::mbar_init(tempty_bar(a), 2 * C::kEpiWarps);   // every epilogue warp of both CTAs
         }
         ptx::mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -201,8 +203,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const float s_tensor = p.rowwise ? 0.0f : __ldg(p.scale_a) * __ldg(p.scale_b);
         const int ew = warp - 2;
-        uint8_t *stage = smem + (staging0 - sbase) + ew * 8192;
-        const uint32_t stage_smem = staging0 + static_cast<uint32_t>(ew * 8192);
+        const int col0 = (ew / 4) * kWarpCols;
+        uint8_t *stage = smem + (staging0 - sbase) + ew * 4096;
+        const uint32_t stage_smem = staging0 + static_cast<uint32_t>(ew * 4096);
         uint32_t chunks = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -213,8 +216,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const uint32_t trow =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            epilogue_rows_staged<BN>(p, &tmap_out, trow, w.tp * 256 + static_cast<int>(rank) * 128 + q * 32,
-                                     w.tq * BN, lane, stage, stage_smem, chunks, s_tensor);
+            epilogue_rows_staged<kWarpCols>(p, &tmap_out, trow + col0,
+                                            w.tp * 256 + static_cast<int>(rank) * 128 + q * 32,
+                                            w.tq * BN + col0, lane, stage, stage_smem, chunks, s_tensor);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0)
