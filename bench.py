@@ -284,9 +284,13 @@ def cpu_baseline(inp, target_s: float):
 
     oracle.build()
     cores = os.cpu_count() or 1
-    probe_rows = 8
-    t = oracle_sample(inp, probe_rows, cores)
-    rows = max(probe_rows, min(M, int(probe_rows * target_s / max(t, 1e-6))))
+    # each call decodes all of Bt once (fixed cost) and then computes rows:
+    # fit t = fixed + rows * per_row from two probes and size the sample
+    t8 = oracle_sample(inp, 8, cores)
+    t64 = oracle_sample(inp, 64, cores)
+    per_row = max((t64 - t8) / 56.0, 1e-6)
+    fixed = max(t8 - 8 * per_row, 0.0)
+    rows = int(max(64, min(M, (target_s - fixed) / per_row)))
     t = oracle_sample(inp, rows, cores)
     flops = 2.0 * rows * N * K
     return {"value": round(flops / t / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
