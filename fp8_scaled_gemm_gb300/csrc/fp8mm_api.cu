@@ -231,6 +231,28 @@ int pick_split(int64_t tiles, int kblocks, int sms, int tile_n)
     return best;
 }
 
+// Launch with programmatic stream serialization: the kernel may start its
+// set-up while the previous kernel in the stream finishes; it calls
+// griddepcontrol.wait before touching global memory.
+template <typename Kern, typename... Args>
+int launch_pdl(Kern kern, int grid, int threads, int smem, cudaStream_t stream, const char *what, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (e != cudaSuccess)
+        return cuda_fail(e, what);
+    return FP8MM_OK;
+}
+
 template <int BN, int CS>
 int launch_swapk(const CUtensorMap &mp, const CUtensorMap &mq, const fp8mm::KernelParams &kp, int grid,
                  cudaStream_t stream)
@@ -246,11 +268,7 @@ int launch_swapk(const CUtensorMap &mp, const CUtensorMap &mq, const fp8mm::Kern
             return cuda_fail(e, "cudaFuncSetAttribute");
         attr_set[dev] = true;
     }
-    kern<<<grid, fp8mm::kThreads, C::kSmemBytes, stream>>>(mp, mq, kp);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return cuda_fail(e, "cluster-K kernel launch");
-    return FP8MM_OK;
+    return launch_pdl(kern, grid, fp8mm::kThreads, C::kSmemBytes, stream, "cluster-K kernel launch", mp, mq, kp);
 }
 
 // Clusters of CS CTAs of the cluster-K kernel that fit on the device at once.
@@ -334,7 +352,9 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
             for (int cs : {2, 4, 8}) {
                 if (kb / cs < 2)
                     break;
-                const int active = max_active_clusters(tile_n, cs);
+                // clusters that fit at once, counted in SMs: a second resident
+                // CTA on an SM adds no streaming bandwidth
+                const int active = std::min(max_active_clusters(tile_n, cs), sms / cs);
                 if (active <= 0)
                     continue;
                 const double cost = static_cast<double>(cdiv(tiles, active)) *
@@ -411,11 +431,8 @@ int launch_kernel(const CUtensorMap &mp, const CUtensorMap &mq, const CUtensorMa
             return cuda_fail(e, "cudaFuncSetAttribute");
         attr_set[dev] = true;
     }
-    kern<<<grid, fp8mm::EpiShape<SWAP>::kThreads, C::kSmemBytes, stream>>>(mp, mq, mo, kp);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return cuda_fail(e, "kernel launch");
-    return FP8MM_OK;
+    return launch_pdl(kern, grid, fp8mm::EpiShape<SWAP>::kThreads, C::kSmemBytes, stream, "kernel launch", mp, mq,
+                      mo, kp);
 }
 
 template <int BN>
@@ -433,11 +450,8 @@ int launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap 
             return cuda_fail(e, "cudaFuncSetAttribute");
         attr_set[dev] = true;
     }
-    kern<<<grid, fp8mm::EpiShape<false>::kThreads, C::kSmemBytes, stream>>>(ma, mb, mo, kp);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return cuda_fail(e, "pair kernel launch");
-    return FP8MM_OK;
+    return launch_pdl(kern, grid, fp8mm::EpiShape<false>::kThreads, C::kSmemBytes, stream, "pair kernel launch",
+                      ma, mb, mo, kp);
 }
 
 int dispatch(const Choice &c, const CUtensorMap &mp, const CUtensorMap &mq, const CUtensorMap &mo,

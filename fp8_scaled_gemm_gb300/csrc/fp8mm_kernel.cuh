@@ -94,7 +94,11 @@ template <int BN, bool SWAP>
 struct TileCfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is 16..256 step 16");
     static_assert(SWAP || BN % 64 == 0, "row epilogue works in 64-column blocks");
-    static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
+    // SWAP rings up to tile_n = 64 stay under ~110 KB so a CTA of the next
+    // launch can share the SM (programmatic dependent launch); the 128-wide
+    // SWAP and the TILE rings use the whole SM for depth.
+    static constexpr int kStages = SWAP ? (BN >= 128 ? 6 : BN >= 64 ? 4 : BN >= 32 ? 5 : 6)
+                                        : (BN >= 256 ? 4 : 6);
     static constexpr int kPBytes = kTileP * kBlockK;
     static constexpr int kQBytes = BN * kBlockK;
     static constexpr int kStageBytes = kPBytes + kQBytes;
@@ -417,6 +421,11 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+
+    // The set-up above touches no global memory; from here on everything may
+    // depend on the previous grid in the stream (programmatic dependent launch).
+    ptx::grid_launch_dependents();
+    ptx::grid_dependency_wait();
 
     const Waiter W{abort_flag, p.status, p.timeout_cycles};
 

@@ -94,6 +94,11 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    // The set-up above touches no global memory; from here on everything may
+    // depend on the previous grid in the stream (programmatic dependent launch).
+    ptx::grid_launch_dependents();
+    ptx::grid_dependency_wait();
+
     const Waiter W{abort_flag, p.status, p.timeout_cycles};
 
     if (warp == 0) {

@@ -345,5 +345,22 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
     return v;
 }
 
+
+// ------------------------------------------ programmatic dependent launch ---
+
+// Block until the previous grid in the stream has completed and its memory
+// is visible (no-op when the kernel was not launched as a dependent).
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next grid in the stream to start launching (its CTAs still wait
+// in grid_dependency_wait() for this grid to finish).
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace ptx
 }  // namespace fp8mm
