@@ -397,6 +397,24 @@ def run_sweep(args):
             "rotated_sets": n_sets, "kernel": choice}), flush=True)
 
 
+# ------------------------------------------------------------ ranks ----------
+
+def max_over_ranks(total_ms: float, device) -> float:
+    """The slowest rank's timed-region length (every rank runs a replica)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(total_ms)
+    t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, flops_per_step: float, steps: int, total_ms: float) -> float:
+    """Whole-job TFLOP/s: all ranks' flops over the slowest rank's time."""
+    return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------ arms -----------
 
 def run_ours(args):
@@ -423,13 +441,9 @@ def run_ours(args):
     sampler.stop()
     clocks = sampler.summary(*res["wall"])
 
-    total_ms = res["total_ms"]
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(res["total_ms"], device)
     ms_per_step = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_value(world, flops, args.steps, total_ms)
     achieved = flops / (res["kernel_ms_mean"] * 1e-3) / 1e12
 
     line = {
