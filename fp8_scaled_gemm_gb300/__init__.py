@@ -40,7 +40,7 @@ STATUS = {
 EXPORTS = (
     "fp8_scaled_mm", "fp8_scaled_mm_config", "fp8_scaled_mm_host", "fp8_scaled_mm_noalloc",
     "fp8mm_reserve_workspace", "fp8mm_device_status", "fp8mm_status_string",
-    "fp8mm_last_error", "fp8mm_describe_choice",
+    "fp8mm_last_error", "fp8mm_describe_choice", "fp8mm_debug_inject",
 )
 
 _lib = None
@@ -90,6 +90,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fp8mm_status_string.restype = ctypes.c_char_p
         lib.fp8mm_last_error.argtypes = []
         lib.fp8mm_last_error.restype = ctypes.c_char_p
+        lib.fp8mm_debug_inject.argtypes = [i64, i64]
+        lib.fp8mm_debug_inject.restype = i32
         lib.fp8mm_describe_choice.argtypes = [i64, i64, i64, i32]
         lib.fp8mm_describe_choice.restype = ctypes.c_char_p
         _lib = lib
@@ -210,6 +212,12 @@ def fp8mm_status_string(status: int) -> str:
 
 def fp8mm_last_error() -> str:
     return load().fp8mm_last_error().decode(errors="replace")
+
+
+def fp8mm_debug_inject(stop_after_kblocks: int = -1, wait_limit_cycles: int = 0) -> None:
+    """Test hook: make CTA 0's producer stop early so a bounded wait runs out
+    (see include/fp8mm.h). fp8mm_debug_inject() restores normal operation."""
+    _check(load().fp8mm_debug_inject(int(stop_after_kblocks), int(wait_limit_cycles)))
 
 
 def fp8mm_describe_choice(M: int, N: int, K: int, scale_mode: int = SCALE_TENSOR) -> str:

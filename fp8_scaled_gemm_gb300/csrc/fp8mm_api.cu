@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -24,6 +25,15 @@ constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutCycles = 4000000000ull;  // ~2 s at 2 GHz
 
 thread_local std::string t_last_error;
+
+// Test hooks (fp8mm_debug_inject): apply to every launch until reset.
+std::atomic<long long> g_inject_stop_after{-1};
+std::atomic<unsigned long long> g_wait_limit{0};
+
+unsigned long long wait_limit() {
+    const unsigned long long v = g_wait_limit.load();
+    return v ? v : kDefaultTimeoutCycles;
+}
 thread_local std::string t_describe;
 
 std::mutex g_mu;
@@ -588,7 +598,8 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     kp.rowwise = scale_mode == FP8MM_SCALE_ROWWISE ? 1 : 0;
     kp.group = 8;
     kp.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % 8) == 0) ? 1 : 0;
-    kp.timeout_cycles = kDefaultTimeoutCycles;
+    kp.timeout_cycles = wait_limit();
+    kp.inject_stop_after = static_cast<int>(g_inject_stop_after.load());
     if (c.split > 1 && c.variant != FP8MM_VARIANT_SWAPK) {
         const int64_t tiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q;
         const size_t ws = static_cast<size_t>(tiles) * c.split * fp8mm::kTileP * c.tile_n * sizeof(float);
@@ -734,6 +745,15 @@ int fp8mm_device_status(void *stream)
     snprintf(buf, sizeof buf, "in-kernel wait ran out (site 0x%x)", h);
     t_last_error = buf;
     return FP8MM_ERR_TIMEOUT;
+}
+
+int fp8mm_debug_inject(int64_t stop_after_kblocks, int64_t wait_limit_cycles)
+{
+    if (stop_after_kblocks < -1 || stop_after_kblocks > INT32_MAX || wait_limit_cycles < 0)
+        return FP8MM_ERR_SHAPE;
+    g_inject_stop_after.store(stop_after_kblocks);
+    g_wait_limit.store(static_cast<unsigned long long>(wait_limit_cycles));
+    return FP8MM_OK;
 }
 
 const char *fp8mm_status_string(int status)
@@ -922,7 +942,8 @@ extern "C" int fp8_scaled_mm_noalloc(const void *A, const void *B, const float *
     kp.rowwise = scale_mode == FP8MM_SCALE_ROWWISE ? 1 : 0;
     kp.group = 8;
     kp.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % 8) == 0) ? 1 : 0;
-    kp.timeout_cycles = kDefaultTimeoutCycles;
+    kp.timeout_cycles = wait_limit();
+    kp.inject_stop_after = static_cast<int>(g_inject_stop_after.load());
 
     return encode_and_dispatch(c, A, B, out, M, N, K, kp, s);
 }

@@ -87,6 +87,7 @@ struct KernelParams {
     int group;                      // P tiles per rasterisation group
     int vec_store;                  // 16-byte output stores allowed (TILE)
     int out_tma;                    // tmap_out is valid: rows leave through TMA stores
+    int inject_stop_after;          // test hook: CTA 0's producer stops after this many K blocks (-1: off)
     unsigned long long timeout_cycles;
 };
 
@@ -439,6 +440,10 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
             for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
                 const Unit w = decode_unit(u, p);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (p.inject_stop_after >= 0 && blockIdx.x == 0 && issued >= p.inject_stop_after) {
+                        ok = false;   // test hook: the MMA's wait for the next block runs out
+                        break;
+                    }
                     if (!W.wait(empty_bar(stage), phase ^ 1u, 0)) {
                         ok = false;
                         break;

@@ -172,6 +172,19 @@ int fp8mm_reserve_workspace(int64_t bytes);
  */
 int fp8mm_device_status(void *stream);
 
+/*
+ * Test hook for the bounded in-kernel waits (failure detection without a GPU
+ * fault). From the next launch on, in the 128-row kernels (TILE, SWAP), the
+ * TMA producer of CTA 0 stops after `stop_after_kblocks` K blocks, so the
+ * MMA thread's wait for the next block runs out: the kernel records
+ * FP8MM_ERR_TIMEOUT in the device status word, releases its tensor memory
+ * and returns; that launch's output is undefined. `wait_limit_cycles` > 0
+ * replaces the wait budget of every kernel (default 4e9 clock64 cycles).
+ * fp8mm_debug_inject(-1, 0) restores normal operation. Returns
+ * FP8MM_ERR_SHAPE for out-of-range arguments. Not for production use.
+ */
+int fp8mm_debug_inject(int64_t stop_after_kblocks, int64_t wait_limit_cycles);
+
 /* Static description of a status code. */
 const char *fp8mm_status_string(int status);
 

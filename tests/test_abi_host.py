@@ -92,6 +92,14 @@ def test_config_rejects_unsupported_choices(lib):
     assert cfg(1, 128, -1) == -4
 
 
+def test_debug_inject_validates_arguments(lib):
+    assert lib.fp8mm_debug_inject(-2, 0) == -2
+    assert lib.fp8mm_debug_inject(5, -1) == -2
+    assert lib.fp8mm_debug_inject(2 ** 31, 0) == -2
+    assert lib.fp8mm_debug_inject(3, 1 << 22) == 0
+    assert lib.fp8mm_debug_inject(-1, 0) == 0      # back to normal
+
+
 def test_python_layer_validates_layouts():
     M, N, K = 4, 8, 32
     A = torch.zeros(M, K, dtype=torch.float8_e4m3fn)
