@@ -30,6 +30,7 @@ VARIANT_TILE = 1
 VARIANT_SWAP = 2
 VARIANT_PAIR = 3
 VARIANT_SWAPK = 4
+VARIANT_SWAPPAIR = 5
 
 STATUS = {
     0: "FP8MM_OK", -1: "FP8MM_ERR_NULL", -2: "FP8MM_ERR_SHAPE", -3: "FP8MM_ERR_ALIGN",

@@ -98,12 +98,16 @@ struct TileCfg {
     // SWAP rings up to tile_n = 64 stay under ~110 KB so a CTA of the next
     // launch can share the SM (programmatic dependent launch); the 128-wide
     // SWAP and the TILE rings use the whole SM for depth.
+    // TILE-256 is chosen for K <= 1024 (the pair kernel takes deeper K), where
+    // the epilogue dominates: 3 stages leave room for two stage buffers per
+    // epilogue warp.
     static constexpr int kStages = SWAP ? (BN >= 128 ? 6 : BN >= 64 ? 4 : BN >= 32 ? 5 : 6)
-                                        : (BN >= 256 ? 4 : 6);
+                                        : (BN >= 256 ? 3 : 6);
+    static constexpr int kStageBufs = (!SWAP && BN >= 256) ? 2 : 1;   // 4 KB epilogue stages per warp
     static constexpr int kPBytes = kTileP * kBlockK;
     static constexpr int kQBytes = BN * kBlockK;
     static constexpr int kStageBytes = kPBytes + kQBytes;
-    static constexpr int kStagingBytes = SWAP ? 0 : EpiShape<SWAP>::kWarps * 4096;   // 4 KB per epilogue warp
+    static constexpr int kStagingBytes = SWAP ? 0 : EpiShape<SWAP>::kWarps * 4096 * kStageBufs;
     static constexpr int kTmemCols =
         (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
     static constexpr int kBarBytes = 256;
@@ -276,7 +280,7 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
 // segments. `chunks` counts the blocks this warp has staged so far; before
 // the stage is rewritten, the TMA store of the previous block must have read
 // it (that wait comes after the next block's TMEM loads and arithmetic).
-template <int BN>
+template <int BN, int NBUF>
 __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, const CUtensorMap *tmap_out,
                                                      uint32_t trow, int m_row0, int n0, int lane,
                                                      uint8_t *stage, uint32_t stage_smem, uint32_t &chunks,
@@ -297,20 +301,23 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
             const bool in = nl < p.N;
             const float sbl = (p.rowwise && in) ? __ldg(p.scale_b + nl) : 0.0f;
             const float bl = (p.bias != nullptr && in) ? __bfloat162float(p.bias[nl]) : 0.0f;
+            const bool has_bias = p.bias != nullptr;
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
                 const float s0 = p.rowwise ? sa * __shfl_sync(kAll, sbl, j) : s_tensor;
                 const float s1 = p.rowwise ? sa * __shfl_sync(kAll, sbl, j + 1) : s_tensor;
-                const float y0 = fmaf(v[j], s0, __shfl_sync(kAll, bl, j));
-                const float y1 = fmaf(v[j + 1], s1, __shfl_sync(kAll, bl, j + 1));
+                const float b0 = has_bias ? __shfl_sync(kAll, bl, j) : 0.0f;
+                const float b1 = has_bias ? __shfl_sync(kAll, bl, j + 1) : 0.0f;
+                const float y0 = fmaf(v[j], s0, b0);
+                const float y1 = fmaf(v[j + 1], s1, b1);
                 w[h * 16 + j / 2] = pack_bf16x2(y0, y1);
             }
         }
-        const uint32_t buf = 0;
-        if (p.out_tma && chunks >= 1) {
-            // the TMA store of the previous block must have read the stage
+        const uint32_t buf = NBUF == 1 ? 0u : (chunks & 1u);
+        if (p.out_tma && chunks >= NBUF) {
+            // the TMA store issued NBUF blocks ago must have read this stage
             if (lane == 0)
-                ptx::bulk_wait_group_read<0>();
+                ptx::bulk_wait_group_read<NBUF - 1>();
             __syncwarp();
         }
         uint8_t *rowp = stage + buf * 4096u + lane * 128;
@@ -528,8 +535,8 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
         const float s_tensor = p.rowwise ? 0.0f : __ldg(p.scale_a) * __ldg(p.scale_b);
         const int ew = warp - 2;            // epilogue warp index: its stage buffer
         const int col0 = (ew / 4) * kWarpCols;  // this warp's first column of the tile
-        uint8_t *stage = smem + (staging0 - sbase) + ew * 4096;
-        const uint32_t stage_smem = staging0 + static_cast<uint32_t>(ew * 4096);
+        uint8_t *stage = smem + (staging0 - sbase) + ew * 4096 * C::kStageBufs;
+        const uint32_t stage_smem = staging0 + static_cast<uint32_t>(ew * 4096 * C::kStageBufs);
         uint32_t chunks = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -543,7 +550,7 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
             const int pidx = w.tp * kTileP + row;
             if (p.splits == 1) {
                 if constexpr (!SWAP) {
-                    epilogue_rows_staged<kWarpCols>(p, &tmap_out, trow + col0, w.tp * kTileP + q * 32,
+                    epilogue_rows_staged<kWarpCols, C::kStageBufs>(p, &tmap_out, trow + col0, w.tp * kTileP + q * 32,
                                                     w.tq * BN + col0, lane, stage, stage_smem, chunks,
                                                     s_tensor);
                 } else {

@@ -10,6 +10,11 @@
 // per K block for 128 x BN outputs, 2/3 of what a 1-SM 128 x 256 tile moves,
 // which lets the ring be 6 stages deep.
 //
+// SWAP form (skinny M): the same pair mechanics with the operand roles of
+// the SWAP variant: P = Bt (256 rows of N per pair tile, 128 per CTA) and
+// Q = A (BN rows of M, BN/2 per CTA); D rows are columns of out. Per CTA this
+// loads half of A per K block instead of all of it.
+//
 // Synchronisation across the pair:
 //   full[s]   in the even CTA only: its producer arrives with expect_tx for
 //             both CTAs' bytes; both CTAs' TMA loads complete_tx on it.
@@ -25,34 +30,36 @@
 
 namespace fp8mm {
 
-template <int BN>
+template <int BN, bool SWAP>
 struct PairCfg {
-    static_assert(BN == 256 || BN == 128, "pair tile N");
-    static constexpr int kStages = 6;
-    static constexpr int kABytes = 128 * kBlockK;             // this CTA's A half
-    static constexpr int kBBytes = (BN / 2) * kBlockK;        // this CTA's Bt half
+    static_assert(SWAP ? (BN == 16 || BN == 32 || BN == 64 || BN == 128) : (BN == 256 || BN == 128),
+                  "pair tile N");
+    static constexpr int kABytes = 128 * kBlockK;             // this CTA's half of the P block
+    static constexpr int kBBytes = (BN / 2) * kBlockK;        // this CTA's half of the Q block
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kTmemCols = 2 * BN;                  // two fp32 accumulators
-    static constexpr int kEpiWarps = EpiShape<false>::kWarps;
-    static constexpr int kStagingBytes = kEpiWarps * 4096;    // 4 KB per epilogue warp
-    static constexpr int kBarBytes = 256;
+    static constexpr int kStages = SWAP ? 196608 / kStageBytes : 6;
+    static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;   // two fp32 accumulators
+    static constexpr int kEpiWarps = EpiShape<SWAP>::kWarps;
+    static constexpr int kStagingBytes = SWAP ? 0 : kEpiWarps * 4096;   // 4 KB per row-epilogue warp
+    static constexpr int kBarBytes = 512;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kBarBytes;
     static_assert(kBBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
     static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory");
     static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
 };
 
-// Units: (256-row tile of M, BN-column tile of N); p.tiles_p counts 256-row
+// Units: (256-row tile of P, BN-row tile of Q); p.tiles_p counts 256-row
 // tiles, p.splits must be 1.
-template <int BN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<false>::kThreads, 1)
+template <int BN, bool SWAP>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
     fp8mm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_out, const KernelParams p)
 {
-    using C = PairCfg<BN>;
+    using C = PairCfg<BN, SWAP>;
     constexpr int S = C::kStages;
     constexpr int kWarpCols = BN / (C::kEpiWarps / 4);   // columns of one epilogue warp
+    constexpr int CH = BN < 32 ? BN : 32;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -90,7 +97,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<false>::kTh
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmap_a);
         ptx::prefetch_tmap(&tmap_b);
-        if (p.out_tma)
+        if (!SWAP && p.out_tma)
             ptx::prefetch_tmap(&tmap_out);
     }
     if (warp == 1) {
@@ -221,9 +228,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<false>::kTh
             ptx::tc_fence_after();
             const uint32_t trow =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            epilogue_rows_staged<kWarpCols>(p, &tmap_out, trow + col0,
-                                            w.tp * 256 + static_cast<int>(rank) * 128 + q * 32,
-                                            w.tq * BN + col0, lane, stage, stage_smem, chunks, s_tensor);
+            if constexpr (!SWAP) {
+                epilogue_rows_staged<kWarpCols, 1>(p, &tmap_out, trow + col0,
+                                                w.tp * 256 + static_cast<int>(rank) * 128 + q * 32,
+                                                w.tq * BN + col0, lane, stage, stage_smem, chunks, s_tensor);
+            } else {
+                const int pidx = w.tp * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
+#pragma unroll 1
+                for (int c = 0; c < BN / CH; ++c) {
+                    float v[CH];
+                    tmem_load_chunk<CH>(trow + c * CH, v);
+                    store_chunk<CH, true>(p, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
+                }
+            }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0)
@@ -233,7 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<false>::kTh
                 acc_phase ^= 1u;
             }
         }
-        if (p.out_tma && lane == 0)
+        if (!SWAP && p.out_tma && lane == 0)
             ptx::bulk_wait_group_all();
         __syncwarp();
     }

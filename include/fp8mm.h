@@ -83,8 +83,10 @@ typedef enum fp8mm_variant {
     FP8MM_VARIANT_TILE = 1,   /* 128 x tile_n output tiles; tile rows over M    */
     FP8MM_VARIANT_SWAP = 2,   /* operands swapped: 128-row tiles over N, tile_n columns over M */
     FP8MM_VARIANT_PAIR = 3,   /* 2-SM MMA: a CTA pair computes 256 x tile_n tiles (no split-K) */
-    FP8MM_VARIANT_SWAPK = 4   /* SWAP tiles with K spread over a cluster of split_k CTAs,
+    FP8MM_VARIANT_SWAPK = 4,  /* SWAP tiles with K spread over a cluster of split_k CTAs,
                                  reduced through distributed shared memory (no workspace) */
+    FP8MM_VARIANT_SWAPPAIR = 5 /* SWAP with 2-SM MMA: a CTA pair covers 256 rows of N and
+                                  shares the tile_n rows of A (no split-K) */
 } fp8mm_variant;
 
 /*
@@ -104,9 +106,10 @@ int fp8_scaled_mm(const void *A, const void *B,
  *   variant   fp8mm_variant; AUTO ignores tile_n and split_k.
  *   tile_n    TILE: 128 or 256. SWAP: 16, 32, 64 or 128 (M is covered by
  *             ceil(M / tile_n) column tiles). PAIR: 128 or 256. SWAPK: as
- *             SWAP. 0 = heuristic.
+ *             SWAP. SWAPPAIR: 16, 32, 64 or 128. 0 = heuristic.
  *   split_k   1 .. 16 K-slices per output tile (reduced deterministically in
- *             slice order by the last slice to arrive); PAIR takes 0 or 1;
+ *             slice order by the last slice to arrive); PAIR and SWAPPAIR
+ *             take 0 or 1;
  *             SWAPK takes the cluster size 2, 4 or 8 (0 = 4). 0 = heuristic.
  * Returns FP8MM_ERR_MODE for an unsupported combination.
  */
