@@ -640,6 +640,42 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     return encode_and_dispatch(c, A, B, out, M, N, K, kp, stream);
 }
 
+// Streams and events of the host-memory entry point (one set per device).
+constexpr int kHostChunks = 8;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, mm = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t a_ready[kHostChunks] = {}, mm_done[kHostChunks] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+
+// Called with g_mu held.
+int host_pipe(HostPipe **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    HostPipe &hp = g_pipe[dev];
+    if (!hp.ready) {
+        if ((e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&hp.mm, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "host pipeline set-up");
+        for (int i = 0; i < kHostChunks; ++i) {
+            if ((e = cudaEventCreateWithFlags(&hp.a_ready[i], cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&hp.mm_done[i], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e, "host pipeline set-up");
+        }
+        hp.ready = true;
+    }
+    *out = &hp;
+    return FP8MM_OK;
+}
+
 int grow_stage(DeviceState &d, int i, size_t bytes)
 {
     if (bytes <= d.stage_bytes[i])
@@ -696,7 +732,7 @@ int fp8_scaled_mm_host(const void *A, const void *B, const float *scale_a, const
     const size_t nsb = scale_mode == FP8MM_SCALE_ROWWISE ? static_cast<size_t>(N) : 1;
     const size_t bytes[6] = {static_cast<size_t>(M) * K, static_cast<size_t>(N) * K, nsa * 4, nsb * 4,
                              bias ? static_cast<size_t>(N) * 2 : 0, static_cast<size_t>(M) * N * 2};
-    const void *src[5] = {A, B, scale_a, scale_b, bias};
+    HostPipe *hp = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         for (int i = 0; i < 6; ++i) {
@@ -706,25 +742,54 @@ int fp8_scaled_mm_host(const void *A, const void *B, const float *scale_a, const
             if (rc != FP8MM_OK)
                 return rc;
         }
+        rc = host_pipe(&hp);
+        if (rc != FP8MM_OK)
+            return rc;
     }
-    for (int i = 0; i < 5; ++i) {
-        if (bytes[i] == 0)
-            continue;
-        cudaError_t e = cudaMemcpyAsync(d->stage[i], src[i], bytes[i], cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "cudaMemcpyAsync(H2D)");
+    uint8_t *dA = static_cast<uint8_t *>(d->stage[0]);
+    uint8_t *dB = static_cast<uint8_t *>(d->stage[1]);
+    float *dsa = static_cast<float *>(d->stage[2]);
+    float *dsb = static_cast<float *>(d->stage[3]);
+    void *dbias = bias ? d->stage[4] : nullptr;
+    uint8_t *dout = static_cast<uint8_t *>(d->stage[5]);
+
+    // Rows of A and out are cut into chunks: chunk i's GEMM starts as soon
+    // as its rows of A have arrived (after the scales, bias and all of B),
+    // and its rows of out leave while later chunks copy in and compute.
+    const int64_t rows = std::max<int64_t>(1024, ((cdiv(M, kHostChunks) + 255) / 256) * 256);
+    const int chunks = static_cast<int>(cdiv(M, rows));
+    cudaError_t e;
+#define FP8MM_TRY(call, what)      \
+    if ((e = (call)) != cudaSuccess) \
+        return cuda_fail(e, what);
+    FP8MM_TRY(cudaEventRecord(hp->start, s), "cudaEventRecord");
+    FP8MM_TRY(cudaStreamWaitEvent(hp->in, hp->start, 0), "cudaStreamWaitEvent");
+    FP8MM_TRY(cudaMemcpyAsync(dsa, scale_a, bytes[2], cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync(H2D)");
+    FP8MM_TRY(cudaMemcpyAsync(dsb, scale_b, bytes[3], cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync(H2D)");
+    if (bias)
+        FP8MM_TRY(cudaMemcpyAsync(dbias, bias, bytes[4], cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync(H2D)");
+    FP8MM_TRY(cudaMemcpyAsync(dB, B, bytes[1], cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync(H2D)");
+    for (int i = 0; i < chunks; ++i) {
+        const int64_t r0 = i * rows, mi = std::min<int64_t>(rows, M - r0);
+        FP8MM_TRY(cudaMemcpyAsync(dA + r0 * K, static_cast<const uint8_t *>(A) + r0 * K,
+                                  static_cast<size_t>(mi * K), cudaMemcpyHostToDevice, hp->in),
+                  "cudaMemcpyAsync(H2D)");
+        FP8MM_TRY(cudaEventRecord(hp->a_ready[i], hp->in), "cudaEventRecord");
+        FP8MM_TRY(cudaStreamWaitEvent(hp->mm, hp->a_ready[i], 0), "cudaStreamWaitEvent");
+        rc = run(dA + r0 * K, dB, scale_mode == FP8MM_SCALE_ROWWISE ? dsa + r0 : dsa, dsb, scale_mode, dbias,
+                 dout + r0 * N * 2, mi, N, K, hp->mm, FP8MM_VARIANT_AUTO, 0, 0);
+        if (rc != FP8MM_OK)
+            return rc;
+        FP8MM_TRY(cudaEventRecord(hp->mm_done[i], hp->mm), "cudaEventRecord");
+        FP8MM_TRY(cudaStreamWaitEvent(hp->out, hp->mm_done[i], 0), "cudaStreamWaitEvent");
+        FP8MM_TRY(cudaMemcpyAsync(static_cast<uint8_t *>(out) + r0 * N * 2, dout + r0 * N * 2,
+                                  static_cast<size_t>(mi * N * 2), cudaMemcpyDeviceToHost, hp->out),
+                  "cudaMemcpyAsync(D2H)");
     }
-    rc = run(d->stage[0], d->stage[1], static_cast<const float *>(d->stage[2]),
-             static_cast<const float *>(d->stage[3]), scale_mode, bias ? d->stage[4] : nullptr, d->stage[5], M,
-             N, K, s, FP8MM_VARIANT_AUTO, 0, 0);
-    if (rc != FP8MM_OK)
-        return rc;
-    cudaError_t e = cudaMemcpyAsync(out, d->stage[5], bytes[5], cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "cudaMemcpyAsync(D2H)");
-    e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "cudaStreamSynchronize");
+    FP8MM_TRY(cudaEventRecord(hp->done, hp->out), "cudaEventRecord");
+    FP8MM_TRY(cudaStreamWaitEvent(s, hp->done, 0), "cudaStreamWaitEvent");
+    FP8MM_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+#undef FP8MM_TRY
     return FP8MM_OK;
 }
 

@@ -123,9 +123,13 @@ int fp8_scaled_mm_config(const void *A, const void *B,
  * Host-memory entry point: A, B, scale_a, scale_b, bias and out are HOST
  * pointers (pinned memory gives full copy bandwidth; pageable works). The
  * call copies the inputs to device staging buffers owned by the library
- * (grown on demand, kept per device), runs fp8_scaled_mm on `stream`, copies
- * the result back into `out` and synchronises `stream` before returning.
- * Same layouts and constraints as fp8_scaled_mm.
+ * (grown on demand, kept per device), computes, copies the result back into
+ * `out` and synchronises `stream` before returning. Internally the rows of A
+ * and out are cut into up to 8 chunks on three library streams, so that
+ * chunk i computes while later rows of A arrive and earlier rows of out
+ * leave; the work is ordered after everything already queued on `stream`.
+ * Same layouts, constraints and result as fp8_scaled_mm (the chunks run the
+ * same kernels as fp8_scaled_mm would for their row counts).
  */
 int fp8_scaled_mm_host(const void *A, const void *B,
                        const float *scale_a, const float *scale_b, int scale_mode,

@@ -82,7 +82,9 @@ def test_config_rejects_unsupported_choices(lib):
     def cfg(variant, tile_n, split):
         return lib.fp8_scaled_mm_config(P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), 0, None,
                                         P(ALIGNED), 64, 64, 64, None, variant, tile_n, split)
-    assert cfg(5, 0, 0) == -4
+    assert cfg(6, 0, 0) == -4
+    assert cfg(5, 256, 0) == -4       # SWAPPAIR takes 16..128
+    assert cfg(5, 64, 2) == -4        # SWAPPAIR has no split-K
     assert cfg(4, 16, 3) == -4        # SWAPK cluster size is 2, 4 or 8
     assert cfg(3, 64, 0) == -4        # PAIR takes 128 or 256
     assert cfg(3, 256, 2) == -4       # PAIR has no split-K

@@ -15,7 +15,7 @@ from tests._parity import bf16_bits, compare, run_and_compare, to_device
 
 pytestmark = pytest.mark.gpu
 
-TILE, SWAP, PAIR, SWAPK = 1, 2, 3, 4
+TILE, SWAP, PAIR, SWAPK, SWAPPAIR = 1, 2, 3, 4, 5
 
 
 def _need_gpu():
@@ -30,7 +30,7 @@ def _assert_ok(stats, label):
 # ------------------------------------------------------------ small, full ---
 
 KERNELS = [(TILE, 128), (TILE, 256), (SWAP, 16), (SWAP, 32), (SWAP, 64), (SWAP, 128),
-           (PAIR, 128), (PAIR, 256)]
+           (PAIR, 128), (PAIR, 256), (SWAPPAIR, 16), (SWAPPAIR, 32), (SWAPPAIR, 64), (SWAPPAIR, 128)]
 
 
 @pytest.mark.parametrize("variant,tile_n", KERNELS)
@@ -44,7 +44,7 @@ def test_every_kernel_on_a_ragged_shape(variant, tile_n, mode, split):
     M, N, K = 300, 520, 400
     stats, _, _ = run_and_compare(M, N, K, mode, seed=11, with_bias=(split == 3),
                                   variant=variant, tile_n=tile_n,
-                                  split_k=(1 if variant == PAIR else split))
+                                  split_k=(1 if variant in (PAIR, SWAPPAIR) else split))
     _assert_ok(stats, f"v{variant} n{tile_n} mode{mode} split{split}")
 
 
@@ -82,6 +82,18 @@ def test_cluster_k_kernel(tile_n, cs):
         stats, _, _ = run_and_compare(M, N, K, mode, seed=21, with_bias=bias, variant=SWAPK,
                                       tile_n=tile_n, split_k=cs)
         _assert_ok(stats, f"swapk n{tile_n} cs{cs} mode{mode}")
+
+
+@pytest.mark.parametrize("tile_n", [16, 32, 64, 128])
+def test_swap_pair_kernel(tile_n):
+    _need_gpu()
+    # ragged M and N: the last 256-row pair tile leaves the odd CTA with
+    # N rows 384..511 out of range; K tail of 16
+    M, N, K = max(1, tile_n - 5), 600, 784
+    for mode, bias in ((0, False), (1, True)):
+        stats, _, _ = run_and_compare(M, N, K, mode, seed=23, with_bias=bias, variant=SWAPPAIR,
+                                      tile_n=tile_n, split_k=0)
+        _assert_ok(stats, f"swappair n{tile_n} mode{mode}")
 
 
 def test_cluster_k_with_fewer_k_blocks_than_ctas():
@@ -143,6 +155,21 @@ def test_host_entry_matches_device_entry():
                                  inp.scale_a, inp.scale_b, 1, bias=inp.bias)
     assert np.array_equal(dev, bf16_bits(host))
     _assert_ok(compare(dev, inp), "host/device")
+
+
+def test_host_entry_in_several_chunks():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+    # 3000 rows: three 1024-row chunks (the last one ragged), row-wise + bias
+    inp = make_inputs(3000, 1000, 528, 1, seed=12, with_bias=True)
+    host = fm.fp8_scaled_mm_host(inp.a_q.pin_memory(), inp.bt_q.pin_memory().t(),
+                                 inp.scale_a.pin_memory(), inp.scale_b.pin_memory(), 1,
+                                 bias=inp.bias.pin_memory())
+    _assert_ok(compare(bf16_bits(host), inp), "host chunks")
+    # a second call reuses the staging buffers and the pipeline
+    host2 = fm.fp8_scaled_mm_host(inp.a_q, inp.bt_q.t(), inp.scale_a, inp.scale_b, 1, bias=inp.bias)
+    assert np.array_equal(bf16_bits(host), bf16_bits(host2))
 
 
 # ------------------------------------------------- full-size, sampled -------
