@@ -8,7 +8,9 @@ The arithmetic lives in ``fp8mm_oracle.c`` (plain C99 + OpenMP, fp64); this
 module only compiles it with gcc and marshals numpy arrays through ctypes.
 What it computes, with its sources on the pages:
 
-    out[i, j] = bf16_rne( sum_k dec(A[i, k]) * dec(Bt[j, k]) * S_ij + bias[j] )
+    out[i, j] = round( sum_k dec(A[i, k]) * dec(Bt[j, k]) * S_ij + bias[j] )
+
+(dec: e4m3fn or e5m2 codes; round: fp64 -> bf16 or fp16, one RNE step)
 
 with ``S_ij = s_a * s_b`` (per-tensor) or ``s_a[i] * s_b[j]`` (row-wise):
 gist "matmul_fp8.py" (FP8 Matmul), ``matmul_fp8_kernel`` scale epilogue;
@@ -69,6 +71,22 @@ def _load():
         lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
+        lib.oracle_e5m2_table.restype = None
+        lib.oracle_e5m2_table.argtypes = [ctypes.c_void_p]
+        lib.oracle_f64_to_f16_array.restype = None
+        lib.oracle_f64_to_f16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+        lib.oracle_f16_to_f64.restype = ctypes.c_double
+        lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_scaled_mm_typed.restype = ctypes.c_int
+        lib.oracle_scaled_mm_typed.argtypes = [
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_int,
+            c_i64p, ctypes.c_int64, c_i64p, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int,
+        ]
         lib.oracle_scaled_mm.restype = ctypes.c_int
         lib.oracle_scaled_mm.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p,
@@ -103,6 +121,35 @@ def bf16_rne(x) -> np.ndarray:
     return out.reshape(arr.shape)
 
 
+E4M3, E5M2 = 0, 1
+BF16, F16 = 0, 1
+
+
+def e5m2_table() -> np.ndarray:
+    """The 256 e5m2 code values as fp64 (+-inf at 0x7C / 0xFC, NaN at 0x7D-0x7F, 0xFD-0xFF)."""
+    t = np.empty(256, dtype=np.float64)
+    _load().oracle_e5m2_table(t.ctypes.data)
+    return t
+
+
+def f16_rne(x) -> np.ndarray:
+    """fp64 values -> IEEE binary16 bit patterns (uint16), one round-to-nearest-even."""
+    arr = np.asarray(x, dtype=np.float64)
+    xs = np.ascontiguousarray(arr.reshape(-1))
+    out = np.empty(xs.shape, dtype=np.uint16)
+    _load().oracle_f64_to_f16_array(xs.ctypes.data, out.ctypes.data, xs.size)
+    return out.reshape(arr.shape)
+
+
+def f16_to_f64(bits) -> np.ndarray:
+    """binary16 bit patterns (uint16) -> fp64 values."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def out_to_f64(bits, out_type: int) -> np.ndarray:
+    return bf16_to_f64(bits) if out_type == BF16 else f16_to_f64(bits)
+
+
 def bf16_to_f64(bits) -> np.ndarray:
     """bf16 bit patterns (uint16) -> fp64 values."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
@@ -114,14 +161,17 @@ def max_threads() -> int:
 
 
 def scaled_mm(A, Bt, scale_a, scale_b, scale_mode: int, bias=None,
-              rows=None, cols=None, threads: int = 0):
+              rows=None, cols=None, threads: int = 0,
+              a_type: int = E4M3, b_type: int = E4M3, out_type: int = BF16):
     """Oracle output on the grid ``rows x cols`` (all rows / columns if None).
 
-    A: uint8 [M, K] e4m3fn codes; Bt: uint8 [N, K] codes (B column-major);
-    scale_a / scale_b: float32 arrays of 1 value (scale_mode 0) or M / N
-    values (scale_mode 1); bias: uint16 bf16 patterns [N] or None.
+    A: uint8 [M, K] fp8 codes (a_type 0 e4m3fn, 1 e5m2); Bt: uint8 [N, K]
+    codes (B column-major, b_type likewise); scale_a / scale_b: float32
+    arrays of 1 value (scale_mode 0) or M / N values (scale_mode 1); bias:
+    uint16 bit patterns [N] of the output type or None; out_type 0 bf16,
+    1 fp16.
 
-    Returns ``(out_bf16_bits uint16, ref64 float64, absum float64)``, each of
+    Returns ``(out_bits uint16, ref64 float64, absum float64)``, each of
     shape [len(rows), len(cols)]; ``absum`` is S_ij * sum_k |a_ik b_kj|.
     """
     A = np.ascontiguousarray(A, dtype=np.uint8)
@@ -153,10 +203,10 @@ def scaled_mm(A, Bt, scale_a, scale_b, scale_mode: int, bias=None,
     ref = np.zeros((nr, nc), dtype=np.float64)
     mag = np.zeros((nr, nc), dtype=np.float64)
     c_i64p = ctypes.POINTER(ctypes.c_int64)
-    rc = _load().oracle_scaled_mm(
-        A.ctypes.data, Bt.ctypes.data, M, N, K,
+    rc = _load().oracle_scaled_mm_typed(
+        A.ctypes.data, int(a_type), Bt.ctypes.data, int(b_type), M, N, K,
         sa.ctypes.data, sb.ctypes.data, int(scale_mode),
-        None if bias_arr is None else bias_arr.ctypes.data,
+        None if bias_arr is None else bias_arr.ctypes.data, int(out_type),
         None if r is None else r.ctypes.data_as(c_i64p), nr,
         None if c is None else c.ctypes.data_as(c_i64p), nc,
         out.ctypes.data, ref.ctypes.data, mag.ctypes.data, int(threads))
@@ -165,12 +215,16 @@ def scaled_mm(A, Bt, scale_a, scale_b, scale_mode: int, bias=None,
     return out, ref, mag
 
 
-def tolerance(ref_bits, absum) -> np.ndarray:
-    """Allowed |gpu - ref| per element: 2^-7 |ref| + 2^-20 absum.
+def tolerance(ref_bits, absum, out_type: int = BF16) -> np.ndarray:
+    """Allowed |gpu - ref| per element: ulp_rel |ref| + 2^-20 absum.
 
-    ``ref`` is the bf16-rounded oracle value; the first term admits one bf16
-    ulp (a rounding boundary crossed by fp32 accumulation), the second the
-    fp32 accumulation error near cancellation.
+    ``ref`` is the rounded oracle value; the first term admits one unit in
+    the last place of the output type (2^-7 relative for bf16, 2^-10 for
+    fp16; a rounding boundary crossed by fp32 accumulation), the second the
+    fp32 accumulation error near cancellation. For fp16 outputs one quantum
+    of the subnormal range (2^-24) is also admitted.
     """
-    ref = bf16_to_f64(ref_bits)
-    return np.abs(ref) * 2.0 ** -7 + np.asarray(absum) * 2.0 ** -20
+    ref = out_to_f64(ref_bits, out_type)
+    if out_type == BF16:
+        return np.abs(ref) * 2.0 ** -7 + np.asarray(absum) * 2.0 ** -20
+    return np.abs(ref) * 2.0 ** -10 + np.asarray(absum) * 2.0 ** -20 + 2.0 ** -24

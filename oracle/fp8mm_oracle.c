@@ -79,6 +79,89 @@ void oracle_e4m3_table(double table[256])
         table[c] = oracle_e4m3_to_f64((uint8_t)c);
 }
 
+/* e5m2 code -> value (OCP FP8 E5M2: 1 sign bit, 5 exponent bits with bias
+ * 15, 2 mantissa bits, IEEE-style: exponent 0 encodes subnormals m * 2^-16,
+ * exponent 31 encodes infinity (m = 0) and NaN (m != 0)). The gist
+ * "matmul_fp8.py", `benchmark()`, names torch.float8_e5m2 beside e4m3fn. */
+double oracle_e5m2_to_f64(uint8_t code)
+{
+    const int sign = (code >> 7) & 1;
+    const int expo = (code >> 2) & 0x1F;
+    const int mant = code & 0x3;
+    double mag;
+    if (expo == 31)
+        mag = mant ? NAN : INFINITY;
+    else if (expo == 0)
+        mag = ldexp((double)mant, -16);              /* subnormal: m * 2^-16 */
+    else
+        mag = ldexp(4.0 + (double)mant, expo - 17);  /* (1 + m/4) * 2^(e-15) */
+    return sign ? -mag : mag;
+}
+
+void oracle_e5m2_table(double table[256])
+{
+    for (int c = 0; c < 256; ++c)
+        table[c] = oracle_e5m2_to_f64((uint8_t)c);
+}
+
+/*
+ * fp64 -> IEEE binary16 bit pattern, round to nearest, ties to even, in one
+ * step: quantum 2^(e-10) for 2^e <= |x| < 2^(e+1), e clamped at -14 below
+ * (subnormal quantum 2^-24); results of 65520 (= 2^16 - 2^4, the tie above
+ * the largest finite 65504) or more overflow to infinity.
+ */
+uint16_t oracle_f64_to_f16_rne(double x)
+{
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double a, quantum, q;
+    int e;
+    if (isnan(x))
+        return (uint16_t)(sign | 0x7E00u);
+    a = fabs(x);
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7C00u);
+    if (a == 0.0)
+        return sign;
+    (void)frexp(a, &e);
+    e -= 1;
+    if (e < -14)
+        e = -14;
+    quantum = ldexp(1.0, e - 10);
+    q = nearbyint(a / quantum);          /* integer significand count */
+    if (q * quantum >= 65520.0)
+        return (uint16_t)(sign | 0x7C00u);
+    /* encode: subnormal (e == -14 and q < 1024) or normal */
+    if (q < 1024.0)
+        return (uint16_t)(sign | (uint16_t)q);           /* exponent field 0 */
+    if (q >= 2048.0) {                    /* rounding carried into the next binade */
+        q /= 2.0;
+        e += 1;
+    }
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)((int)q - 1024));
+}
+
+void oracle_f64_to_f16_array(const double *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_f64_to_f16_rne(x[i]);
+}
+
+/* binary16 bit pattern -> value (exact). */
+double oracle_f16_to_f64(uint16_t bits)
+{
+    const int sign = (bits >> 15) & 1;
+    const int expo = (bits >> 10) & 0x1F;
+    const int mant = bits & 0x3FF;
+    double mag;
+    if (expo == 31)
+        mag = mant ? NAN : INFINITY;
+    else if (expo == 0)
+        mag = ldexp((double)mant, -24);
+    else
+        mag = ldexp(1024.0 + (double)mant, expo - 25);
+    return sign ? -mag : mag;
+}
+
 /* bf16 bit pattern -> value (exact: bf16 is a subset of fp64). */
 double oracle_bf16_to_f64(uint16_t bits)
 {
@@ -135,29 +218,35 @@ void oracle_f64_to_bf16_array(const double *x, uint16_t *out, int64_t n)
 /*
  * The scaled matrix multiply on a grid of selected outputs.
  *
- *   A        e4m3fn codes, [M, K] row-major
- *   Bt       e4m3fn codes, [N, K] row-major (B[K, N] column-major)
+ *   A        fp8 codes, [M, K] row-major; a_type 0 = e4m3fn, 1 = e5m2
+ *   Bt       fp8 codes, [N, K] row-major (B[K, N] column-major); b_type likewise
  *   scale_a  1 value (scale_mode 0) or M values (scale_mode 1)
  *   scale_b  1 value (scale_mode 0) or N values (scale_mode 1)
- *   bias     bf16 bit patterns [N], or NULL
+ *   bias     [N] bit patterns of the output type, or NULL
+ *   out_type 0 = bf16, 1 = fp16 (IEEE binary16)
  *   rows     n_rows row indices into [0, M), or NULL for all rows (n_rows = M)
  *   cols     n_cols column indices into [0, N), or NULL for all (n_cols = N)
- *   out      [n_rows, n_cols] bf16 bit patterns
+ *   out      [n_rows, n_cols] bit patterns of the output type
  *   ref64    [n_rows, n_cols] unrounded fp64 result, or NULL
  *   absum    [n_rows, n_cols] S_ij * sum_k |a_ik * b_kj| (fp64), or NULL
  *
+ * The fp64 dot product is exact when both operands are e4m3fn (see the file
+ * header). With e5m2 operands (values are multiples of 2^-16 up to 57344)
+ * a sum can need more than 53 bits; it is then rounded in fp64, an error
+ * below K * 2^-53 * absum, far inside any fp32-accumulation tolerance.
+ *
  * Returns 0, or -1 on a bad argument, -2 when out of memory.
  */
-int oracle_scaled_mm(const uint8_t *A, const uint8_t *Bt,
-                     int64_t M, int64_t N, int64_t K,
-                     const float *scale_a, const float *scale_b, int scale_mode,
-                     const uint16_t *bias,
-                     const int64_t *rows, int64_t n_rows,
-                     const int64_t *cols, int64_t n_cols,
-                     uint16_t *out, double *ref64, double *absum,
-                     int n_threads)
+int oracle_scaled_mm_typed(const uint8_t *A, int a_type, const uint8_t *Bt, int b_type,
+                           int64_t M, int64_t N, int64_t K,
+                           const float *scale_a, const float *scale_b, int scale_mode,
+                           const uint16_t *bias, int out_type,
+                           const int64_t *rows, int64_t n_rows,
+                           const int64_t *cols, int64_t n_cols,
+                           uint16_t *out, double *ref64, double *absum,
+                           int n_threads)
 {
-    double table[256];
+    double table_a[256], table_b[256];
     double *bdec;
     int64_t r, c;
     int bad = 0;
@@ -165,6 +254,8 @@ int oracle_scaled_mm(const uint8_t *A, const uint8_t *Bt,
     if (!A || !Bt || !scale_a || !scale_b || !out || M < 0 || N < 0 || K < 0)
         return -1;
     if (scale_mode != 0 && scale_mode != 1)
+        return -1;
+    if ((a_type != 0 && a_type != 1) || (b_type != 0 && b_type != 1) || (out_type != 0 && out_type != 1))
         return -1;
     if (!rows)
         n_rows = M;
@@ -179,7 +270,14 @@ int oracle_scaled_mm(const uint8_t *A, const uint8_t *Bt,
     if (n_rows == 0 || n_cols == 0)
         return 0;
 
-    oracle_e4m3_table(table);
+    if (a_type == 0)
+        oracle_e4m3_table(table_a);
+    else
+        oracle_e5m2_table(table_a);
+    if (b_type == 0)
+        oracle_e4m3_table(table_b);
+    else
+        oracle_e5m2_table(table_b);
 
     /* Decode the selected rows of Bt once. */
     bdec = (double *)malloc((size_t)n_cols * (size_t)(K > 0 ? K : 1) * sizeof(double));
@@ -188,7 +286,7 @@ int oracle_scaled_mm(const uint8_t *A, const uint8_t *Bt,
     for (c = 0; c < n_cols; ++c) {
         const int64_t j = cols ? cols[c] : c;
         for (int64_t k = 0; k < K; ++k)
-            bdec[c * K + k] = table[Bt[j * K + k]];
+            bdec[c * K + k] = table_b[Bt[j * K + k]];
     }
 
 #ifdef _OPENMP
@@ -207,7 +305,7 @@ int oracle_scaled_mm(const uint8_t *A, const uint8_t *Bt,
             continue;
         }
         for (int64_t k = 0; k < K; ++k)
-            adec[k] = table[A[i * K + k]];
+            adec[k] = table_a[A[i * K + k]];
         for (int64_t cc = 0; cc < n_cols; ++cc) {
             const int64_t j = cols ? cols[cc] : cc;
             const double *b = bdec + cc * K;
@@ -224,8 +322,8 @@ int oracle_scaled_mm(const uint8_t *A, const uint8_t *Bt,
                 S = (double)scale_a[i] * (double)scale_b[j];
             ref = dot * S;
             if (bias)
-                ref += oracle_bf16_to_f64(bias[j]);
-            out[r * n_cols + cc] = oracle_f64_to_bf16_rne(ref);
+                ref += out_type == 0 ? oracle_bf16_to_f64(bias[j]) : oracle_f16_to_f64(bias[j]);
+            out[r * n_cols + cc] = out_type == 0 ? oracle_f64_to_bf16_rne(ref) : oracle_f64_to_f16_rne(ref);
             if (ref64)
                 ref64[r * n_cols + cc] = ref;
             if (absum)
@@ -235,6 +333,20 @@ int oracle_scaled_mm(const uint8_t *A, const uint8_t *Bt,
     }
     free(bdec);
     return bad ? -2 : 0;
+}
+
+/* The e4m3fn x e4m3fn -> bf16 case (the benchmark path). */
+int oracle_scaled_mm(const uint8_t *A, const uint8_t *Bt,
+                     int64_t M, int64_t N, int64_t K,
+                     const float *scale_a, const float *scale_b, int scale_mode,
+                     const uint16_t *bias,
+                     const int64_t *rows, int64_t n_rows,
+                     const int64_t *cols, int64_t n_cols,
+                     uint16_t *out, double *ref64, double *absum,
+                     int n_threads)
+{
+    return oracle_scaled_mm_typed(A, 0, Bt, 0, M, N, K, scale_a, scale_b, scale_mode, bias, 0, rows, n_rows,
+                                  cols, n_cols, out, ref64, absum, n_threads);
 }
 
 /* Threads an OpenMP parallel region would use by default (for reports). */

@@ -381,3 +381,145 @@ def test_pins_catch_planted_mistakes():
     }
     for name, fn in planted.items():
         assert not np.array_equal(fn(), truth), name
+
+
+# ------------------------------------------------ other dtypes (e5m2, fp16) --
+
+def torch_e5m2_decode(codes) -> np.ndarray:
+    t = torch.as_tensor(np.asarray(codes, dtype=np.uint8)).view(torch.float8_e5m2)
+    return t.to(torch.float64).numpy()
+
+
+def frac_round(x: Fraction, p: int, emin: int) -> Fraction:
+    """Exact RNE of a rational to p significand bits, exponent floor emin."""
+    if x == 0:
+        return Fraction(0)
+    sign = -1 if x < 0 else 1
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, emin)
+    quantum = Fraction(2) ** (e - (p - 1))
+    q = a / quantum
+    n = q.numerator // q.denominator
+    rem = q - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return sign * n * quantum
+
+
+def frac_to_f16_bits(x: Fraction) -> int:
+    v = frac_round(x, 11, -14)
+    if abs(v) >= 65520:
+        return (0x8000 if x < 0 else 0) | 0x7C00
+    h = np.array([float(v)], dtype=np.float16)
+    assert Fraction(float(h[0])) == v
+    return int(h.view(np.uint16)[0]) | (0x8000 if (x < 0 and v == 0) else 0)
+
+
+def test_e5m2_all_256_codes_match_torch():
+    ours = oracle.e5m2_table()
+    theirs = torch_e5m2_decode(np.arange(256))
+    nan = np.isnan(ours)
+    assert np.array_equal(nan, np.isnan(theirs))
+    assert np.array_equal(ours[~nan], theirs[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(theirs[~nan]))
+
+
+def test_e5m2_landmarks():
+    t = oracle.e5m2_table()
+    assert t[0x7B] == 57344.0 == torch.finfo(torch.float8_e5m2).max
+    assert t[0x7C] == float("inf") and t[0xFC] == float("-inf")
+    assert list(np.flatnonzero(np.isnan(t))) == [0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF]
+    assert t[0x3C] == 1.0
+    assert t[0x01] == 2.0 ** -16 and t[0x04] == 2.0 ** -14
+    fin = t[np.isfinite(t)]
+    assert np.all(fin * 2 ** 16 == np.round(fin * 2 ** 16))
+
+
+def test_f16_rne_matches_torch_on_fp32_values():
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 2 ** 32, size=300_000, dtype=np.uint64).astype(np.uint32)
+    f32 = bits.view(np.float32)
+    f32 = f32[~np.isnan(f32)]
+    ours = oracle.f16_rne(f32.astype(np.float64))
+    theirs = torch.from_numpy(f32.copy()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, theirs)
+
+
+def test_f16_rne_vs_exact_rational_random_fp64():
+    rng = np.random.default_rng(12)
+    mant = rng.random(3000) + 1.0
+    expo = rng.integers(-27, 17, size=3000)
+    sign = np.where(rng.random(3000) < 0.5, -1.0, 1.0)
+    xs = sign * np.ldexp(mant, expo)
+    ours = oracle.f16_rne(xs)
+    for x, o in zip(xs, ours):
+        assert int(o) == frac_to_f16_bits(Fraction(float(x))), x
+
+
+def test_f16_rne_specials():
+    assert int(oracle.f16_rne(65504.0)) == 0x7BFF
+    assert int(oracle.f16_rne(65519.99)) == 0x7BFF
+    assert int(oracle.f16_rne(65520.0)) == 0x7C00          # tie above max -> inf
+    assert int(oracle.f16_rne(-70000.0)) == 0xFC00
+    assert int(oracle.f16_rne(2.0 ** -24)) == 0x0001        # min subnormal
+    assert int(oracle.f16_rne(2.0 ** -25)) == 0x0000        # tie -> even (0)
+    assert int(oracle.f16_rne(3 * 2.0 ** -25)) == 0x0002    # tie -> even (2)
+    assert int(oracle.f16_rne(2.0 ** -14 * (1 - 2 ** -12))) == 0x0400   # rounds up into the normals
+    assert int(oracle.f16_rne(1 + 2 ** -11)) == 0x3C00      # tie -> even
+    assert int(oracle.f16_rne(1 + 2 ** -11 + 2 ** -40)) == 0x3C01   # single rounding from fp64
+    assert int(oracle.f16_rne(-0.0)) == 0x8000
+
+
+def exact_typed(A, Bt, at, bt, sa, sb, mode, bias_bits, out_type):
+    dec = {0: torch_e4m3_decode, 1: torch_e5m2_decode}
+    Ad, Bd = dec[at](A), dec[bt](Bt)
+    M, K = Ad.shape
+    N = Bd.shape[0]
+    out = np.zeros((M, N), dtype=np.uint16)
+    bv = None
+    if bias_bits is not None:
+        bv = oracle.out_to_f64(bias_bits, out_type)
+    for i in range(M):
+        for j in range(N):
+            dot = sum((Fraction(float(Ad[i, k])) * Fraction(float(Bd[j, k])) for k in range(K)),
+                      Fraction(0))
+            S = Fraction(float(sa[0 if mode == 0 else i])) * Fraction(float(sb[0 if mode == 0 else j]))
+            v = dot * S + (Fraction(float(bv[j])) if bv is not None else 0)
+            out[i, j] = frac_to_bf16_bits(v) if out_type == 0 else frac_to_f16_bits(v)
+    return out
+
+
+def finite_e5m2(rng, shape):
+    c = rng.integers(0, 256, size=shape, dtype=np.int64)
+    c = np.where((c & 0x7C) == 0x7C, c & 0xF3, c)     # no inf / NaN exponent
+    return c.astype(np.uint8)
+
+
+@pytest.mark.parametrize("at,bt", [(1, 1), (0, 1), (1, 0)])
+@pytest.mark.parametrize("out_type", [0, 1])
+def test_brute_force_other_dtypes(at, bt, out_type):
+    rng = np.random.default_rng(100 * at + 10 * bt + out_type)
+    M, N, K = 4, 5, 9
+    gen = {0: lambda s: finite_codes(rng, s), 1: lambda s: finite_e5m2(rng, s)}
+    A, Bt = gen[at]((M, K)), gen[bt]((N, K))
+    # scales keep fp16 results in range for e5m2 magnitudes
+    sa = (rng.random(M) * 2 ** -12 + 2 ** -14).astype(np.float32)
+    sb = (rng.random(N) * 2 ** -12 + 2 ** -14).astype(np.float32)
+    bias = (torch.randn(N) * 0.1).to(torch.bfloat16 if out_type == 0 else torch.float16) \
+        .view(torch.int16).numpy().view(np.uint16)
+    out, _, _ = oracle.scaled_mm(A, Bt, sa, sb, 1, bias=bias, a_type=at, b_type=bt, out_type=out_type)
+    assert np.array_equal(out, exact_typed(A, Bt, at, bt, sa, sb, 1, bias, out_type))
+
+
+def test_fp16_output_bias_only():
+    rng = np.random.default_rng(13)
+    A = np.zeros((3, 16), np.uint8)
+    Bt = finite_e5m2(rng, (7, 16))
+    bias = (torch.randn(7) * 3).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    out, _, _ = oracle.scaled_mm(A, Bt, [2.0], [3.0], 0, bias=bias, b_type=1, out_type=1)
+    assert np.array_equal(out, np.broadcast_to(bias, (3, 7)))
