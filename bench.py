@@ -54,7 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="time every benchmark shape instead (one JSON line per shape)")
     ap.add_argument("--shapes", default="",
-                    help="with --sweep: comma list of MxNxK[:mode[:bias]] (default: all)")
+                    help="with --sweep: comma list of MxNxK[:mode[:bias[:a_dtype:b_dtype:out_dtype]]] "
+                         "(default: all benchmark shapes; dtypes e4m3|e5m2 and bf16|fp16)")
     return ap.parse_args(argv)
 
 
@@ -311,27 +312,34 @@ SWEEP_SHAPES = (
 
 
 def algorithmic_bytes(M, N, K, mode, bias):
+    # fp8 operands (1 byte), 16-bit output and bias, fp32 scales
     return M * K + N * K + 2 * M * N + (4 * (M + N) if mode == 1 else 8) + (2 * N if bias else 0)
 
 
-def time_shape(M, N, K, mode, bias, steps, warmup, device):
+def time_shape(M, N, K, mode, bias, steps, warmup, device, types=("e4m3", "e4m3", "bf16")):
     import torch
     import fp8_scaled_gemm_gb300 as fm
     from fp8_scaled_gemm_gb300.inputs import make_inputs
 
-    inp = make_inputs(M, N, K, mode, SEED, with_bias=bias)
+    inp = make_inputs(M, N, K, mode, SEED, with_bias=bias, a_dtype=types[0], b_dtype=types[1],
+                      out_dtype=types[2])
+    odt = torch.bfloat16 if types[2] == "bf16" else torch.float16
+    typed = tuple(types) != ("e4m3", "e4m3", "bf16")
     per_set = algorithmic_bytes(M, N, K, mode, bias)
     n_sets = max(1, min(64, -(-3 * L2_BYTES // per_set)))
     sets = []
     for _ in range(n_sets):
         sets.append((inp.a_q.to(device), inp.bt_q.to(device).t(), inp.scale_a.to(device),
                      inp.scale_b.to(device), None if inp.bias is None else inp.bias.to(device),
-                     torch.empty((M, N), dtype=torch.bfloat16, device=device)))
+                     torch.empty((M, N), dtype=odt, device=device)))
     stream = torch.cuda.current_stream(device)
 
     def step(i):
         A, B, sa, sb, b, o = sets[i % n_sets]
-        fm.fp8_scaled_mm(A, B, sa, sb, mode, bias=b, out=o)
+        if typed:
+            fm.fp8_scaled_mm_ex(A, B, sa, sb, mode, bias=b, out=o)
+        else:
+            fm.fp8_scaled_mm(A, B, sa, sb, mode, bias=b, out=o)
 
     for i in range(warmup):
         step(i)
@@ -372,7 +380,7 @@ def run_sweep(args):
     fm.load()
     pk = peaks()
     fp8_peak = pk["bf16_tflops"] * NOMINAL_FP8_PER_BF16
-    shapes = SWEEP_SHAPES
+    shapes = [s + (("e4m3", "e4m3", "bf16"),) for s in SWEEP_SHAPES]
     if args.shapes:
         shapes = []
         for spec in args.shapes.split(","):
@@ -380,15 +388,18 @@ def run_sweep(args):
             M, N, K = (int(x) for x in parts[0].split("x"))
             mode = int(parts[1]) if len(parts) > 1 else 1
             bias = bool(int(parts[2])) if len(parts) > 2 else False
-            shapes.append((M, N, K, mode, bias))
-    for (M, N, K, mode, bias) in shapes:
-        mean, best, n_sets, choice = time_shape(M, N, K, mode, bias, args.steps, args.warmup, device)
+            types = tuple(parts[3:6]) if len(parts) >= 6 else ("e4m3", "e4m3", "bf16")
+            shapes.append((M, N, K, mode, bias, types))
+    for (M, N, K, mode, bias, types) in shapes:
+        mean, best, n_sets, choice = time_shape(M, N, K, mode, bias, args.steps, args.warmup, device,
+                                                types)
         flops = 2.0 * M * N * K
         nbytes = algorithmic_bytes(M, N, K, mode, bias)
         tflops = flops / (mean * 1e-3) / 1e12
         gbs = nbytes / (mean * 1e-3) / 1e9
         print(json.dumps({
             "shape": [M, N, K], "scale_mode": "row-wise" if mode else "per-tensor", "bias": bias,
+            "types": list(types),
             "kernel_us": round(mean * 1e3, 2), "kernel_us_best": round(best * 1e3, 2),
             "timing": f"median of 5 CUDA-graph replays of {args.steps} launches",
             "tflops": round(tflops, 1), "frac_fp8_peak": round(tflops / fp8_peak, 3),

@@ -32,6 +32,18 @@ VARIANT_PAIR = 3
 VARIANT_SWAPK = 4
 VARIANT_SWAPPAIR = 5
 
+TYPE_E4M3, TYPE_E5M2 = 0, 1
+OUT_BF16, OUT_F16 = 0, 1
+_FP8 = {torch.float8_e4m3fn: TYPE_E4M3, torch.float8_e5m2: TYPE_E5M2}
+_OUT = {torch.bfloat16: OUT_BF16, torch.float16: OUT_F16}
+
+
+class Options(ctypes.Structure):
+    """fp8mm_options of include/fp8mm.h."""
+    _fields_ = [("a_type", ctypes.c_int), ("b_type", ctypes.c_int), ("out_type", ctypes.c_int),
+                ("variant", ctypes.c_int), ("tile_n", ctypes.c_int), ("split_k", ctypes.c_int)]
+
+
 STATUS = {
     0: "FP8MM_OK", -1: "FP8MM_ERR_NULL", -2: "FP8MM_ERR_SHAPE", -3: "FP8MM_ERR_ALIGN",
     -4: "FP8MM_ERR_MODE", -5: "FP8MM_ERR_CUDA", -6: "FP8MM_ERR_NODEV", -7: "FP8MM_ERR_TIMEOUT",
@@ -39,7 +51,8 @@ STATUS = {
 
 # Every symbol include/fp8mm.h declares.
 EXPORTS = (
-    "fp8_scaled_mm", "fp8_scaled_mm_config", "fp8_scaled_mm_host", "fp8_scaled_mm_noalloc",
+    "fp8_scaled_mm", "fp8_scaled_mm_config", "fp8_scaled_mm_ex", "fp8_scaled_mm_host",
+    "fp8_scaled_mm_noalloc",
     "fp8mm_reserve_workspace", "fp8mm_device_status", "fp8mm_status_string",
     "fp8mm_last_error", "fp8mm_describe_choice", "fp8mm_debug_inject",
 )
@@ -79,6 +92,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fp8_scaled_mm.restype = i32
         lib.fp8_scaled_mm_config.argtypes = common + [i32, i32, i32]
         lib.fp8_scaled_mm_config.restype = i32
+        lib.fp8_scaled_mm_ex.argtypes = common + [ctypes.POINTER(Options)]
+        lib.fp8_scaled_mm_ex.restype = i32
         lib.fp8_scaled_mm_host.argtypes = common
         lib.fp8_scaled_mm_host.restype = i32
         lib.fp8_scaled_mm_noalloc.argtypes = common
@@ -115,15 +130,16 @@ def _stream_handle(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(int(stream.cuda_stream))
 
 
-def _validate(A, B, scale_a, scale_b, scale_mode, bias, out, device_side: bool):
+def _validate(A, B, scale_a, scale_b, scale_mode, bias, out, device_side: bool, typed: bool = False):
     if A.dim() != 2 or B.dim() != 2:
         raise ValueError("A must be [M, K] and B [K, N]")
     M, K = A.shape
     K2, N = B.shape
     if K2 != K:
         raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
-    if A.dtype != torch.float8_e4m3fn or B.dtype != torch.float8_e4m3fn:
-        raise ValueError("A and B must be torch.float8_e4m3fn")
+    fp8 = tuple(_FP8) if typed else (torch.float8_e4m3fn,)
+    if A.dtype not in fp8 or B.dtype not in fp8:
+        raise ValueError("A and B must be torch.float8_e4m3fn" + (" or float8_e5m2" if typed else ""))
     if A.stride() != (K, 1) and M > 1:
         raise ValueError("A must be row-major contiguous [M, K]")
     if B.stride() != (1, K) and N > 1:
@@ -135,11 +151,12 @@ def _validate(A, B, scale_a, scale_b, scale_mode, bias, out, device_side: bool):
     for name, s, n in (("scale_a", scale_a, want_a), ("scale_b", scale_b, want_b)):
         if s.dtype != torch.float32 or s.numel() != n or not s.is_contiguous():
             raise ValueError(f"{name} must be a contiguous float32 tensor of {n} values")
-    if bias is not None and (bias.dtype != torch.bfloat16 or bias.numel() != N
-                             or not bias.is_contiguous()):
-        raise ValueError("bias must be a contiguous bfloat16 tensor of N values")
-    if out.dtype != torch.bfloat16 or tuple(out.shape) != (M, N) or not out.is_contiguous():
-        raise ValueError("out must be a contiguous bfloat16 [M, N] tensor")
+    outs = tuple(_OUT) if typed else (torch.bfloat16,)
+    if out.dtype not in outs or tuple(out.shape) != (M, N) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, N] tensor of " +
+                         ("bfloat16 or float16" if typed else "bfloat16"))
+    if bias is not None and (bias.dtype != out.dtype or bias.numel() != N or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous tensor of N values with out's dtype")
     tensors = [A, B, scale_a, scale_b, out] + ([bias] if bias is not None else [])
     for t in tensors:
         if device_side and not t.is_cuda:
@@ -169,6 +186,21 @@ def fp8_scaled_mm_config(A, B, scale_a, scale_b, scale_mode: int, bias=None, out
     _check(load().fp8_scaled_mm_config(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), scale_mode,
                                        _ptr(bias), _ptr(out), M, N, K, _stream_handle(stream),
                                        int(variant), int(tile_n), int(split_k)))
+    return out
+
+
+def fp8_scaled_mm_ex(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=None, stream=None,
+                     out_dtype=torch.bfloat16, variant: int = VARIANT_AUTO, tile_n: int = 0,
+                     split_k: int = 0):
+    """The operation with e4m3fn / e5m2 operands and a bf16 / fp16 output
+    (types taken from the tensors; bias has out's dtype)."""
+    if out is None:
+        out = torch.empty((A.shape[0], B.shape[1]), dtype=out_dtype, device=A.device)
+    M, N, K = _validate(A, B, scale_a, scale_b, scale_mode, bias, out, True, typed=True)
+    opt = Options(_FP8[A.dtype], _FP8[B.dtype], _OUT[out.dtype], int(variant), int(tile_n), int(split_k))
+    _check(load().fp8_scaled_mm_ex(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), scale_mode,
+                                   _ptr(bias), _ptr(out), M, N, K, _stream_handle(stream),
+                                   ctypes.byref(opt)))
     return out
 
 

@@ -175,13 +175,14 @@ int encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t
 
 // bf16 output [M, N] (N contiguous) written in boxes of 32 rows x 64 columns
 // from a 128-byte-swizzled shared-memory stage.
-int encode_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N)
+int encode_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N, bool f16)
 {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
     cuuint32_t box[2] = {64, 32};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims, strides, box, estr,
+    CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out,
+                          dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -543,7 +544,7 @@ int encode_and_dispatch(const Choice &c, const void *A, const void *B, void *out
     // aligned (TILE without split-K, PAIR); otherwise through plain stores.
     if (!swap && c.split == 1 && (N % 8) == 0 &&
         (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
-        int rc = encode_out_map(&mo, out, M, N);
+        int rc = encode_out_map(&mo, out, M, N, kp.out_f16 != 0);
         if (rc != FP8MM_OK)
             return rc;
         kp.out_tma = 1;
@@ -581,8 +582,12 @@ int check_args(const void *A, const void *B, const float *sa, const float *sb, i
     return FP8MM_OK;
 }
 
+// Format codes of the MMA instruction descriptor for the operand types.
+uint32_t fmt_code(int t) { return t == FP8MM_TYPE_E5M2 ? 1u : 0u; }
+
 int run(const void *A, const void *B, const float *sa, const float *sb, int scale_mode, const void *bias,
-        void *out, int64_t M, int64_t N, int64_t K, cudaStream_t stream, int variant, int tile_n, int split)
+        void *out, int64_t M, int64_t N, int64_t K, cudaStream_t stream, int variant, int tile_n, int split,
+        int a_type = FP8MM_TYPE_E4M3, int b_type = FP8MM_TYPE_E4M3, int out_type = FP8MM_OUT_BF16)
 {
     int rc = check_args(A, B, sa, sb, scale_mode, bias, out, M, N, K);
     if (rc != FP8MM_OK)
@@ -600,6 +605,10 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
         return FP8MM_ERR_MODE;
     if (split < 0 || split > 16)
         return FP8MM_ERR_MODE;
+    if ((a_type != FP8MM_TYPE_E4M3 && a_type != FP8MM_TYPE_E5M2) ||
+        (b_type != FP8MM_TYPE_E4M3 && b_type != FP8MM_TYPE_E5M2) ||
+        (out_type != FP8MM_OUT_BF16 && out_type != FP8MM_OUT_F16))
+        return FP8MM_ERR_MODE;
     if (M == 0 || N == 0)
         return FP8MM_OK;
     DeviceState *d = nullptr;
@@ -611,9 +620,17 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     fp8mm::KernelParams kp{};
     kp.scale_a = sa;
     kp.scale_b = sb;
-    kp.bias = static_cast<const __nv_bfloat16 *>(bias);
-    kp.out = static_cast<__nv_bfloat16 *>(out);
+    kp.bias = static_cast<const unsigned short *>(bias);
+    kp.out = static_cast<unsigned short *>(out);
     kp.status = d->status;
+    {
+        // The MMA's A side is the P operand: A for TILE / PAIR, Bt for the SWAP kinds.
+        const bool swap = c.variant == FP8MM_VARIANT_SWAP || c.variant == FP8MM_VARIANT_SWAPK ||
+                          c.variant == FP8MM_VARIANT_SWAPPAIR;
+        const uint32_t fp = fmt_code(swap ? b_type : a_type), fq = fmt_code(swap ? a_type : b_type);
+        kp.idesc_fmt = (fp << 7) | (fq << 10);
+        kp.out_f16 = out_type == FP8MM_OUT_F16 ? 1 : 0;
+    }
     kp.M = static_cast<int>(M);
     kp.N = static_cast<int>(N);
     kp.K = static_cast<int>(K);
@@ -712,6 +729,17 @@ int fp8_scaled_mm_config(const void *A, const void *B, const float *scale_a, con
 {
     return run(A, B, scale_a, scale_b, scale_mode, bias, out, M, N, K, static_cast<cudaStream_t>(stream),
                variant, tile_n, split_k);
+}
+
+int fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, const float *scale_b, int scale_mode,
+                     const void *bias, void *out, int64_t M, int64_t N, int64_t K, void *stream,
+                     const fp8mm_options *options)
+{
+    if (!options)
+        return FP8MM_ERR_NULL;
+    return run(A, B, scale_a, scale_b, scale_mode, bias, out, M, N, K, static_cast<cudaStream_t>(stream),
+               options->variant, options->tile_n, options->split_k, options->a_type, options->b_type,
+               options->out_type);
 }
 
 int fp8_scaled_mm_host(const void *A, const void *B, const float *scale_a, const float *scale_b,
@@ -1019,8 +1047,8 @@ extern "C" int fp8_scaled_mm_noalloc(const void *A, const void *B, const float *
     fp8mm::KernelParams kp{};
     kp.scale_a = scale_a;
     kp.scale_b = scale_b;
-    kp.bias = static_cast<const __nv_bfloat16 *>(bias);
-    kp.out = static_cast<__nv_bfloat16 *>(out);
+    kp.bias = static_cast<const unsigned short *>(bias);
+    kp.out = static_cast<unsigned short *>(out);
     kp.status = reinterpret_cast<int *>(d->scratch);
     kp.counters = reinterpret_cast<unsigned int *>(d->scratch + kNoAllocStatusBytes);
     kp.ws = reinterpret_cast<float *>(d->scratch + kNoAllocStatusBytes + kNoAllocCounterBytes);

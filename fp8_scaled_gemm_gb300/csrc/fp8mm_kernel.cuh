@@ -47,6 +47,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "sm103_ptx.cuh"
 
@@ -74,8 +75,8 @@ constexpr int kStatusTimeoutBase = 0x100;
 struct KernelParams {
     const float *scale_a;           // 1 or M values
     const float *scale_b;           // 1 or N values
-    const __nv_bfloat16 *bias;      // N values or nullptr
-    __nv_bfloat16 *out;             // [M, N] row-major
+    const unsigned short *bias;     // N values (output type) or nullptr
+    unsigned short *out;            // [M, N] row-major, bf16 or fp16 bit patterns
     float *ws;                      // split-K partial tiles (splits > 1)
     unsigned int *counters;         // split-K arrivals, kCountersPerTile per output tile
     int *status;                    // device status word
@@ -88,6 +89,8 @@ struct KernelParams {
     int vec_store;                  // 16-byte output stores allowed (TILE)
     int out_tma;                    // tmap_out is valid: rows leave through TMA stores
     int inject_stop_after;          // test hook: CTA 0's producer stops after this many K blocks (-1: off)
+    uint32_t idesc_fmt;             // operand format bits of the MMA instruction descriptor
+    int out_f16;                    // 1: fp16 output and bias, 0: bf16
     unsigned long long timeout_cycles;
 };
 
@@ -199,10 +202,26 @@ __device__ __forceinline__ Unit decode_unit(int u, const KernelParams &p)
     return w;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+// Output conversions (round to nearest even) for bf16 or fp16.
+__device__ __forceinline__ uint32_t pack_out2(float lo, float hi, int f16)
 {
+    if (f16) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ unsigned short to_out(float y, int f16)
+{
+    return f16 ? __half_as_ushort(__float2half_rn(y)) : __bfloat16_as_ushort(__float2bfloat16_rn(y));
+}
+
+__device__ __forceinline__ float bias_value(const KernelParams &p, int n)
+{
+    const unsigned short b = p.bias[n];
+    return p.out_f16 ? __half2float(__ushort_as_half(b)) : __bfloat162float(__ushort_as_bfloat16(b));
 }
 
 // Epilogue for CH accumulator columns held by one thread; the whole warp
@@ -221,7 +240,7 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
         const int m = pidx;
         const bool q_in = ql < p.N;
         const float sbl = (p.rowwise && q_in) ? __ldg(p.scale_b + ql) : 0.0f;
-        const float bl = (p.bias != nullptr && q_in) ? __bfloat162float(p.bias[ql]) : 0.0f;
+        const float bl = (p.bias != nullptr && q_in) ? bias_value(p, ql) : 0.0f;
         const float sa = (p.rowwise && m < p.M) ? __ldg(p.scale_a + m) : 0.0f;
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
@@ -230,29 +249,29 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
         }
         if (m >= p.M)
             return;
-        __nv_bfloat16 *orow = p.out + static_cast<size_t>(m) * p.N;
+        unsigned short *orow = p.out + static_cast<size_t>(m) * p.N;
         if (p.vec_store && qbase + CH <= p.N) {
 #pragma unroll
             for (int j = 0; j < CH; j += 8) {
                 uint4 w;
-                w.x = pack_bf16x2(y[j + 0], y[j + 1]);
-                w.y = pack_bf16x2(y[j + 2], y[j + 3]);
-                w.z = pack_bf16x2(y[j + 4], y[j + 5]);
-                w.w = pack_bf16x2(y[j + 6], y[j + 7]);
+                w.x = pack_out2(y[j + 0], y[j + 1], p.out_f16);
+                w.y = pack_out2(y[j + 2], y[j + 3], p.out_f16);
+                w.z = pack_out2(y[j + 4], y[j + 5], p.out_f16);
+                w.w = pack_out2(y[j + 6], y[j + 7], p.out_f16);
                 *reinterpret_cast<uint4 *>(orow + qbase + j) = w;
             }
         } else {
 #pragma unroll
             for (int j = 0; j < CH; ++j)
                 if (qbase + j < p.N)
-                    orow[qbase + j] = __float2bfloat16_rn(y[j]);
+                    orow[qbase + j] = to_out(y[j], p.out_f16);
         }
     } else {
         const int n = pidx;
         const bool n_in = n < p.N;
         const float sal = (p.rowwise && ql < p.M) ? __ldg(p.scale_a + ql) : 0.0f;
         const float sb = (p.rowwise && n_in) ? __ldg(p.scale_b + n) : 0.0f;
-        const float b = (p.bias != nullptr && n_in) ? __bfloat162float(p.bias[n]) : 0.0f;
+        const float b = (p.bias != nullptr && n_in) ? bias_value(p, n) : 0.0f;
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
             const float s = p.rowwise ? __shfl_sync(kAll, sal, j) * sb : s_tensor;
@@ -264,7 +283,7 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
         for (int j = 0; j < CH; ++j) {
             const int m = qbase + j;
             if (m < p.M)
-                p.out[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(y[j]);
+                p.out[static_cast<size_t>(m) * p.N + n] = to_out(y[j], p.out_f16);
         }
     }
 }
@@ -300,7 +319,7 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
             const int nl = nb + h * 32 + lane;
             const bool in = nl < p.N;
             const float sbl = (p.rowwise && in) ? __ldg(p.scale_b + nl) : 0.0f;
-            const float bl = (p.bias != nullptr && in) ? __bfloat162float(p.bias[nl]) : 0.0f;
+            const float bl = (p.bias != nullptr && in) ? bias_value(p, nl) : 0.0f;
             const bool has_bias = p.bias != nullptr;
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
@@ -310,7 +329,7 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                 const float b1 = has_bias ? __shfl_sync(kAll, bl, j + 1) : 0.0f;
                 const float y0 = fmaf(v[j], s0, b0);
                 const float y1 = fmaf(v[j + 1], s1, b1);
-                w[h * 16 + j / 2] = pack_bf16x2(y0, y1);
+                w[h * 16 + j / 2] = pack_out2(y0, y1, p.out_f16);
             }
         }
         const uint32_t buf = NBUF == 1 ? 0u : (chunks & 1u);
@@ -348,13 +367,11 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                 const uint8_t *src =
                     stage + buf * 4096u + r * 128 + ((((lane >> 2) ^ (r & 7)) & 7) * 16) + (lane & 3) * 4;
                 const uint32_t pr = *reinterpret_cast<const uint32_t *>(src);
-                __nv_bfloat16 *dst = p.out + static_cast<size_t>(mm) * p.N + col;
-                const unsigned short lo = static_cast<unsigned short>(pr & 0xFFFFu);
-                const unsigned short hi = static_cast<unsigned short>(pr >> 16);
+                unsigned short *dst = p.out + static_cast<size_t>(mm) * p.N + col;
                 if (col < p.N)
-                    dst[0] = __ushort_as_bfloat16(lo);
+                    dst[0] = static_cast<unsigned short>(pr & 0xFFFFu);
                 if (col + 1 < p.N)
-                    dst[1] = __ushort_as_bfloat16(hi);
+                    dst[1] = static_cast<unsigned short>(pr >> 16);
             }
             __syncwarp();
         }
@@ -483,7 +500,7 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
     } else if (warp == 1) {
         // -------------------------------------------------- MMA issuer ---
         if (lane == 0) {
-            constexpr uint32_t idesc = ptx::idesc_e4m3_f32(kTileP, BN);
+            const uint32_t idesc = ptx::idesc_e4m3_f32(kTileP, BN) | p.idesc_fmt;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;

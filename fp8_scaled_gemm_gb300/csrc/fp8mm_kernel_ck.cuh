@@ -135,7 +135,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // -------------------------------------------------- MMA issuer ---
         if (lane == 0) {
-            constexpr uint32_t idesc = ptx::idesc_e4m3_f32(kTileP, BN);
+            const uint32_t idesc = ptx::idesc_e4m3_f32(kTileP, BN) | p.idesc_fmt;
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -200,7 +200,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
         const int n = tp * kTileP + r;
         const bool n_in = n < p.N;
         const float sb = (p.rowwise && n_in) ? __ldg(p.scale_b + n) : 0.0f;
-        const float b = (p.bias != nullptr && n_in) ? __bfloat162float(p.bias[n]) : 0.0f;
+        const float b = (p.bias != nullptr && n_in) ? bias_value(p, n) : 0.0f;
         const float s_tensor = p.rowwise ? 0.0f : __ldg(p.scale_a) * __ldg(p.scale_b);
         const uint32_t local0 = ptx::smem_addr(partial);
         // columns t / kRows, + CS, + 2 CS, ...: kItems per thread, processed
@@ -230,7 +230,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
                 const int m = tq * BN + col0 + (i0 + i) * kColStep;
                 if (n_in && m < p.M) {
                     const float sc = p.rowwise ? __ldg(p.scale_a + m) * sb : s_tensor;
-                    p.out[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(fmaf(acc, sc, b));
+                    p.out[static_cast<size_t>(m) * p.N + n] = to_out(fmaf(acc, sc, b), p.out_f16);
                 }
             }
         }

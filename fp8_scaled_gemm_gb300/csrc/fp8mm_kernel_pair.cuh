@@ -166,7 +166,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
     } else if (warp == 1) {
         // ------------------------------------- pair MMA (even CTA only) ---
         if (lane == 0 && rank == 0) {
-            constexpr uint32_t idesc = ptx::idesc_e4m3_f32(256, BN);
+            const uint32_t idesc = ptx::idesc_e4m3_f32(256, BN) | p.idesc_fmt;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;

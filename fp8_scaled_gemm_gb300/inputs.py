@@ -26,6 +26,7 @@ from typing import Optional
 import torch
 
 E4M3_MAX = 448.0  # torch.finfo(torch.float8_e4m3fn).max
+FP8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 
 
 @dataclass
@@ -38,7 +39,10 @@ class ScaledMMInputs:
     bt_q: torch.Tensor              # float8_e4m3fn [N, K] row-major (B column-major)
     scale_a: torch.Tensor           # float32 [1] or [M]
     scale_b: torch.Tensor           # float32 [1] or [N]
-    bias: Optional[torch.Tensor]    # bfloat16 [N] or None
+    bias: Optional[torch.Tensor]    # bfloat16 / float16 [N] or None
+    a_type: int = 0                 # 0 e4m3fn, 1 e5m2
+    b_type: int = 0
+    out_type: int = 0               # 0 bf16, 1 fp16
 
     # numpy views for the oracle (uint8 codes, float32 scales, uint16 bias bits)
     def a_u8(self):
@@ -58,6 +62,10 @@ class ScaledMMInputs:
             return None
         return self.bias.view(torch.int16).numpy().view("uint16")
 
+    def oracle_types(self):
+        """Keyword arguments of oracle.scaled_mm for this input set's types."""
+        return {"a_type": self.a_type, "b_type": self.b_type, "out_type": self.out_type}
+
     @property
     def b_colmajor(self) -> torch.Tensor:
         """B[K, N] as the column-major view of ``bt_q``."""
@@ -65,7 +73,10 @@ class ScaledMMInputs:
 
 
 def make_inputs(M: int, N: int, K: int, scale_mode: int, seed: int,
-                with_bias: bool = False) -> ScaledMMInputs:
+                with_bias: bool = False, a_dtype: str = "e4m3", b_dtype: str = "e4m3",
+                out_dtype: str = "bf16") -> ScaledMMInputs:
+    """The recipe above; ``a_dtype`` / ``b_dtype`` pick e4m3fn or e5m2 (scale
+    = amax / finfo(dtype).max), ``out_dtype`` the bias dtype (bf16 or fp16)."""
     if scale_mode not in (0, 1):
         raise ValueError("scale_mode must be 0 (per-tensor) or 1 (row-wise)")
     g = torch.Generator(device="cpu")
@@ -75,7 +86,10 @@ def make_inputs(M: int, N: int, K: int, scale_mode: int, seed: int,
     bias = None
     if with_bias:
         bias = (torch.randn(N, dtype=torch.bfloat16, generator=g) * 0.1).contiguous()
-    qmax = E4M3_MAX
+        if out_dtype == "fp16":
+            bias = bias.to(torch.float16)
+    ta, tb = FP8[a_dtype], FP8[b_dtype]
+    qa, qb = torch.finfo(ta).max, torch.finfo(tb).max
     if scale_mode == 0:
         sa = a.abs().max().to(torch.float32).view(1, 1)
         sb = b.t().abs().max().to(torch.float32).view(1, 1)
@@ -83,16 +97,17 @@ def make_inputs(M: int, N: int, K: int, scale_mode: int, seed: int,
         sa = a.abs().amax(dim=1, keepdim=True).to(torch.float32)           # [M, 1]
         sb = b.t().abs().amax(dim=1, keepdim=True).to(torch.float32)       # [N, 1]
         sb = sb.t().contiguous()                                           # [1, N]
-    sa = sa / qmax
-    sb = sb / qmax
-    a_q = (a / sa).clamp(-qmax, qmax).to(torch.float8_e4m3fn)
-    b_q = (b / sb).clamp(-qmax, qmax).to(torch.float8_e4m3fn)
+    sa = sa / qa
+    sb = sb / qb
+    a_q = (a / sa).clamp(-qa, qa).to(ta)
+    b_q = (b / sb).clamp(-qb, qb).to(tb)
     bt_q = b_q.t().contiguous()
     return ScaledMMInputs(
         M=M, N=N, K=K, scale_mode=scale_mode,
         a_q=a_q.contiguous(), bt_q=bt_q,
         scale_a=sa.reshape(-1).contiguous(), scale_b=sb.reshape(-1).contiguous(),
-        bias=bias)
+        bias=bias, a_type=0 if a_dtype == "e4m3" else 1, b_type=0 if b_dtype == "e4m3" else 1,
+        out_type=0 if out_dtype == "bf16" else 1)
 
 
 def from_codes(A_u8, Bt_u8, scale_a, scale_b, scale_mode: int,

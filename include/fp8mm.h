@@ -119,6 +119,42 @@ int fp8_scaled_mm_config(const void *A, const void *B,
                          int64_t M, int64_t N, int64_t K,
                          void *stream, int variant, int tile_n, int split_k);
 
+/* Element types of fp8_scaled_mm_ex. */
+typedef enum fp8mm_type {
+    FP8MM_TYPE_E4M3 = 0,      /* float8_e4m3fn operand                          */
+    FP8MM_TYPE_E5M2 = 1       /* float8_e5m2 operand                            */
+} fp8mm_type;
+
+typedef enum fp8mm_out_type {
+    FP8MM_OUT_BF16 = 0,       /* bf16 output and bias                           */
+    FP8MM_OUT_F16 = 1         /* IEEE fp16 output and bias                      */
+} fp8mm_out_type;
+
+typedef struct fp8mm_options {
+    int a_type;               /* fp8mm_type of A                                */
+    int b_type;               /* fp8mm_type of B                                */
+    int out_type;             /* fp8mm_out_type of out and bias                 */
+    int variant;              /* fp8mm_variant (0 = heuristic)                  */
+    int tile_n;               /* as in fp8_scaled_mm_config (0 = heuristic)     */
+    int split_k;              /* as in fp8_scaled_mm_config (0 = heuristic)     */
+} fp8mm_options;
+
+/*
+ * The operation with other element types: A and B each e4m3fn or e5m2
+ * (mixed allowed; the tensor cores multiply them exactly and sum in fp32),
+ * out and bias bf16 or fp16 (one round-to-nearest-even of the fp32 result).
+ * Sources: the gist "matmul_fp8.py", `benchmark()`, quantises to
+ * float8_e4m3fn or float8_e5m2 and casts the accumulator to the output's
+ * dtype (`matmul_fp8_kernel`, fp16 output when SPLIT_K is used). Layouts,
+ * alignment and the other arguments as fp8_scaled_mm / _config; unknown
+ * type codes return FP8MM_ERR_MODE; options == NULL returns FP8MM_ERR_NULL.
+ */
+int fp8_scaled_mm_ex(const void *A, const void *B,
+                     const float *scale_a, const float *scale_b, int scale_mode,
+                     const void *bias, void *out,
+                     int64_t M, int64_t N, int64_t K,
+                     void *stream, const fp8mm_options *options);
+
 /*
  * Host-memory entry point: A, B, scale_a, scale_b, bias and out are HOST
  * pointers (pinned memory gives full copy bandwidth; pageable works). The

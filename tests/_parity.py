@@ -41,13 +41,13 @@ def to_device(inp: ScaledMMInputs, device="cuda"):
 
 
 def compare(gpu_bits: np.ndarray, inp: ScaledMMInputs, rows=None, cols=None, threads: int = 0):
-    """Compare GPU bf16 bits (already restricted to rows x cols) with the oracle."""
+    """Compare GPU output bits (already restricted to rows x cols) with the oracle."""
     ref_bits, _, absum = oracle.scaled_mm(
         inp.a_u8(), inp.bt_u8(), inp.sa_np(), inp.sb_np(), inp.scale_mode,
-        bias=inp.bias_u16(), rows=rows, cols=cols, threads=threads)
-    gpu = oracle.bf16_to_f64(gpu_bits)
-    ref = oracle.bf16_to_f64(ref_bits)
-    tol = oracle.tolerance(ref_bits, absum)
+        bias=inp.bias_u16(), rows=rows, cols=cols, threads=threads, **inp.oracle_types())
+    gpu = oracle.out_to_f64(gpu_bits, inp.out_type)
+    ref = oracle.out_to_f64(ref_bits, inp.out_type)
+    tol = oracle.tolerance(ref_bits, absum, inp.out_type)
     err = np.abs(gpu - ref)
     bad = ~(err <= tol)          # NaN in gpu counts as bad
     ratio = np.where(tol > 0, err / np.where(tol > 0, tol, 1), np.where(err > 0, np.inf, 0))
@@ -62,13 +62,20 @@ def compare(gpu_bits: np.ndarray, inp: ScaledMMInputs, rows=None, cols=None, thr
 
 
 def run_and_compare(M, N, K, mode, seed, with_bias, variant=0, tile_n=0, split_k=0,
-                    sample=False, n_random=64, inp=None):
+                    sample=False, n_random=64, inp=None, a_dtype="e4m3", b_dtype="e4m3",
+                    out_dtype="bf16"):
     import fp8_scaled_gemm_gb300 as fm
     if inp is None:
-        inp = make_inputs(M, N, K, mode, seed, with_bias=with_bias)
+        inp = make_inputs(M, N, K, mode, seed, with_bias=with_bias, a_dtype=a_dtype,
+                          b_dtype=b_dtype, out_dtype=out_dtype)
     A, Bt, sa, sb, bias = to_device(inp)
-    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    fm.fp8_scaled_mm_config(A, Bt.t(), sa, sb, mode, bias=bias, out=out,
+    odt = torch.bfloat16 if inp.out_type == 0 else torch.float16
+    out = torch.full((M, N), float("nan"), dtype=odt, device="cuda")
+    if (inp.a_type, inp.b_type, inp.out_type) == (0, 0, 0):
+        fm.fp8_scaled_mm_config(A, Bt.t(), sa, sb, mode, bias=bias, out=out,
+                                variant=variant, tile_n=tile_n, split_k=split_k)
+    else:
+        fm.fp8_scaled_mm_ex(A, Bt.t(), sa, sb, mode, bias=bias, out=out,
                             variant=variant, tile_n=tile_n, split_k=split_k)
     status = fm.fp8mm_device_status()
     assert status == 0, f"device status {status}: {fm.fp8mm_last_error()}"

@@ -94,6 +94,18 @@ def test_config_rejects_unsupported_choices(lib):
     assert cfg(1, 128, -1) == -4
 
 
+def test_ex_rejects_unknown_types(lib):
+    def ex(at, bt, ot):
+        opt = fm.Options(at, bt, ot, 0, 0, 0)
+        return lib.fp8_scaled_mm_ex(P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), 0, None, P(ALIGNED),
+                                    64, 64, 64, None, ctypes.byref(opt))
+    assert ex(2, 0, 0) == -4
+    assert ex(0, -1, 0) == -4
+    assert ex(0, 0, 2) == -4
+    assert lib.fp8_scaled_mm_ex(P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), 0, None, P(ALIGNED),
+                                64, 64, 64, None, None) == -1
+
+
 def test_debug_inject_validates_arguments(lib):
     assert lib.fp8mm_debug_inject(-2, 0) == -2
     assert lib.fp8mm_debug_inject(5, -1) == -2
@@ -119,6 +131,10 @@ def test_python_layer_validates_layouts():
         fm._validate(A, Bt.t(), torch.ones(M), torch.ones(1), 1, None, out, False)
     with pytest.raises(ValueError, match="bias"):
         fm._validate(A, Bt.t(), sa, sb, 0, torch.zeros(N), out, False)
+    with pytest.raises(ValueError, match="float8"):      # e5m2 only through the typed entry
+        fm._validate(A.view(torch.float8_e5m2), Bt.t(), sa, sb, 0, None, out, False)
+    assert fm._validate(A.view(torch.float8_e5m2), Bt.t(), sa, sb, 0, None, out.half(), False,
+                        typed=True) == (M, N, K)
     with pytest.raises(ValueError, match="CUDA"):
         fm._validate(A, Bt.t(), sa, sb, 0, None, out, True)
     assert fm._validate(A, Bt.t(), sa, sb, 0, None, out, False) == (M, N, K)

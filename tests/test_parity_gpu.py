@@ -172,6 +172,36 @@ def test_host_entry_in_several_chunks():
     assert np.array_equal(bf16_bits(host), bf16_bits(host2))
 
 
+# ------------------------------------------------- other element types ------
+
+TYPES = [("e5m2", "e5m2", "bf16"), ("e4m3", "e5m2", "fp16"), ("e5m2", "e4m3", "fp16")]
+
+
+@pytest.mark.parametrize("variant,tile_n,split", [
+    (TILE, 128, 1), (TILE, 256, 2), (SWAP, 16, 1), (SWAP, 64, 3), (PAIR, 256, 0),
+    (SWAPK, 16, 4), (SWAPK, 128, 2), (SWAPPAIR, 32, 0)])
+@pytest.mark.parametrize("types", TYPES)
+def test_other_element_types_every_kernel(variant, tile_n, split, types):
+    _need_gpu()
+    at, bt, ot = types
+    M = 300 if variant in (TILE, PAIR) else min(tile_n, 100) - 3
+    stats, _, _ = run_and_compare(M, 520, 400, 1, seed=41, with_bias=True, variant=variant,
+                                  tile_n=tile_n, split_k=split, a_dtype=at, b_dtype=bt, out_dtype=ot)
+    _assert_ok(stats, f"v{variant} n{tile_n} {types}")
+
+
+@pytest.mark.parametrize("types", TYPES)
+def test_other_element_types_auto_full_size_sampled(types):
+    _need_gpu()
+    at, bt, ot = types
+    stats, _, _ = run_and_compare(8192, 8192, 8192, 0, 42, False, sample=True, n_random=32,
+                                  a_dtype=at, b_dtype=bt, out_dtype=ot)
+    _assert_ok(stats, f"8192^3 {types}")
+    stats, _, _ = run_and_compare(16, 4096, 4096, 1, 42, True, sample=True, n_random=32,
+                                  a_dtype=at, b_dtype=bt, out_dtype=ot)
+    _assert_ok(stats, f"16x4096x4096 {types}")
+
+
 # ------------------------------------------------- full-size, sampled -------
 
 BENCH_SHAPES = [
