@@ -87,6 +87,13 @@ def _load():
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_int,
         ]
+        lib.oracle_encode_e4m3.restype = ctypes.c_uint8
+        lib.oracle_encode_e4m3.argtypes = [ctypes.c_float]
+        lib.oracle_encode_e5m2.restype = ctypes.c_uint8
+        lib.oracle_encode_e5m2.argtypes = [ctypes.c_float]
+        lib.oracle_quantize.restype = ctypes.c_int
+        lib.oracle_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         lib.oracle_scaled_mm.restype = ctypes.c_int
         lib.oracle_scaled_mm.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p,
@@ -213,6 +220,34 @@ def scaled_mm(A, Bt, scale_a, scale_b, scale_mode: int, bias=None,
     if rc != 0:
         raise RuntimeError(f"oracle_scaled_mm failed with code {rc}")
     return out, ref, mag
+
+
+def encode(values, q_type: int = E4M3) -> np.ndarray:
+    """fp32 values -> fp8 codes (round to nearest even); NaN -> 0x7F | sign."""
+    lib = _load()
+    f = lib.oracle_encode_e4m3 if q_type == E4M3 else lib.oracle_encode_e5m2
+    v = np.asarray(values, dtype=np.float32).reshape(-1)
+    return np.fromiter((f(float(x)) for x in v), dtype=np.uint8, count=v.size)
+
+
+def quantize(x_bf16_bits, scale_mode: int, q_type: int = E4M3, threads: int = 0):
+    """bf16 bit patterns [R, C] -> (fp8 codes uint8 [R, C], fp32 scales [1] or [R]).
+
+    The quantisation recipe of the gist "matmul_fp8.py" (`get_scale`,
+    `benchmark()`): amax over the tensor or each row, scale = amax / qmax,
+    codes = encode(clamp(x / scale, -qmax, qmax)), all in fp32.
+    """
+    x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)
+    if x.ndim != 2:
+        raise ValueError("x must be [R, C]")
+    R, C = x.shape
+    q = np.zeros((R, C), dtype=np.uint8)
+    scale = np.zeros(1 if scale_mode == 0 else R, dtype=np.float32)
+    rc = _load().oracle_quantize(x.ctypes.data, R, C, int(scale_mode), int(q_type), q.ctypes.data,
+                                 scale.ctypes.data, int(threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_quantize failed with code {rc}")
+    return q, scale
 
 
 def tolerance(ref_bits, absum, out_type: int = BF16) -> np.ndarray:

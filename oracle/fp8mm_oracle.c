@@ -349,6 +349,137 @@ int oracle_scaled_mm(const uint8_t *A, const uint8_t *Bt,
                                   cols, n_cols, out, ref64, absum, n_threads);
 }
 
+/*
+ * Quantisation of bf16 data to fp8 codes, the step before the matmul in the
+ * gist "matmul_fp8.py", `get_scale` and `benchmark()`:
+ *
+ *   amax  = max |x|                 over the tensor (mode 0) or each row (mode 1)
+ *   scale = fp32(amax) / qmax       fp32 division; qmax = 448 (e4m3fn), 57344 (e5m2)
+ *   v     = fp32(x) / scale         fp32 division, one correctly rounded step
+ *   v     = clamp(v, -qmax, qmax)   NaN stays NaN
+ *   q     = encode(v)               round to nearest, ties to even mantissa
+ *
+ * Two cases the recipe leaves open, read this way: a zero scale (every
+ * element of the tensor or row is +-0) gives the codes of +-0 rather than
+ * the NaN of 0/0, and every NaN becomes the code 0x7F.
+ *
+ * The divisions are IEEE binary32 operations (C float arithmetic compiled
+ * without contraction or fast-math), the precision the pages compute in
+ * (a bf16 tensor divided by an fp32 scale promotes to fp32).
+ */
+uint8_t oracle_encode_e4m3(float v)
+{
+    const uint8_t sign = signbit(v) ? 0x80u : 0u;
+    double a, q;
+    int e;
+    if (isnan(v))
+        return 0x7Fu;                     /* one NaN code for every NaN */
+    a = fabs((double)v);
+    if (a == 0.0)
+        return sign;
+    (void)frexp(a, &e);
+    e -= 1;                               /* 2^e <= a < 2^(e+1) */
+    if (e < -6) {                         /* subnormal range: quantum 2^-9 */
+        q = nearbyint(a / ldexp(1.0, -9));
+        if (q >= 8.0)                     /* rounded up to the smallest normal */
+            return (uint8_t)(sign | 0x08u);
+        return (uint8_t)(sign | (uint8_t)q);
+    }
+    q = nearbyint(a / ldexp(1.0, e - 3)); /* significand in eighths: 8..16 */
+    if (q >= 16.0) {
+        q /= 2.0;
+        e += 1;
+    }
+    if (e > 8 || (e == 8 && q > 14.0))    /* beyond 448: not reached after the clamp */
+        return (uint8_t)(sign | 0x7Eu);
+    return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)((int)q - 8));
+}
+
+uint8_t oracle_encode_e5m2(float v)
+{
+    const uint8_t sign = signbit(v) ? 0x80u : 0u;
+    double a, q;
+    int e;
+    if (isnan(v))
+        return 0x7Fu;
+    a = fabs((double)v);
+    if (isinf(a))
+        return (uint8_t)(sign | 0x7Cu);
+    if (a == 0.0)
+        return sign;
+    (void)frexp(a, &e);
+    e -= 1;
+    if (e < -14) {                        /* subnormal range: quantum 2^-16 */
+        q = nearbyint(a / ldexp(1.0, -16));
+        if (q >= 4.0)
+            return (uint8_t)(sign | 0x04u);
+        return (uint8_t)(sign | (uint8_t)q);
+    }
+    q = nearbyint(a / ldexp(1.0, e - 2)); /* significand in quarters: 4..8 */
+    if (q >= 8.0) {
+        q /= 2.0;
+        e += 1;
+    }
+    if (e > 15)                           /* beyond 57344: not reached after the clamp */
+        return (uint8_t)(sign | 0x7Bu);
+    return (uint8_t)(sign | (uint8_t)((e + 15) << 2) | (uint8_t)((int)q - 4));
+}
+
+/*
+ * x: bf16 bit patterns [R, C] row-major; mode 0 per-tensor, 1 per-row;
+ * q_type 0 e4m3fn, 1 e5m2; q: [R, C] codes; scale: 1 (mode 0) or R values.
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_quantize(const uint16_t *x, int64_t R, int64_t C, int mode, int q_type, uint8_t *q, float *scale,
+                    int n_threads)
+{
+    const float qmax = q_type == 0 ? 448.0f : 57344.0f;
+    int64_t r;
+    if (!x || !q || !scale || R < 0 || C < 0 || (mode != 0 && mode != 1) || (q_type != 0 && q_type != 1))
+        return -1;
+#ifdef _OPENMP
+    if (n_threads > 0)
+        omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    if (mode == 0) {
+        float amax = 0.0f;
+        for (int64_t i = 0; i < R * C; ++i) {
+            const float a = fabsf((float)oracle_bf16_to_f64(x[i]));
+            if (a > amax || isnan(a))
+                amax = isnan(amax) ? amax : a;
+        }
+        scale[0] = amax / qmax;
+    }
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < R; ++r) {
+        float s;
+        if (mode == 1) {
+            float amax = 0.0f;
+            for (int64_t c = 0; c < C; ++c) {
+                const float a = fabsf((float)oracle_bf16_to_f64(x[r * C + c]));
+                if (a > amax || isnan(a))
+                    amax = isnan(amax) ? amax : a;
+            }
+            scale[r] = amax / qmax;
+            s = scale[r];
+        } else {
+            s = scale[0];
+        }
+        for (int64_t c = 0; c < C; ++c) {
+            const float xv = (float)oracle_bf16_to_f64(x[r * C + c]);
+            float v = s == 0.0f ? xv : xv / s;
+            if (v < -qmax)
+                v = -qmax;
+            else if (v > qmax)
+                v = qmax;
+            q[r * C + c] = q_type == 0 ? oracle_encode_e4m3(v) : oracle_encode_e5m2(v);
+        }
+    }
+    return 0;
+}
+
 /* Threads an OpenMP parallel region would use by default (for reports). */
 int oracle_max_threads(void)
 {
