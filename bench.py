@@ -53,6 +53,9 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--sweep", action="store_true",
                     help="time every benchmark shape instead (one JSON line per shape)")
+    ap.add_argument("--quant", action="store_true",
+                    help="time the bf16 -> fp8 quantisation step instead (one JSON line per shape; "
+                         "--shapes takes RxC[:mode[:e4m3|e5m2]])")
     ap.add_argument("--shapes", default="",
                     help="with --sweep: comma list of MxNxK[:mode[:bias[:a_dtype:b_dtype:out_dtype]]] "
                          "(default: all benchmark shapes; dtypes e4m3|e5m2 and bf16|fp16)")
@@ -408,6 +411,88 @@ def run_sweep(args):
             "rotated_sets": n_sets, "kernel": choice}), flush=True)
 
 
+QUANT_SHAPES = [(8192, 8192, 0), (8192, 8192, 1), (16384, 8192, 1), (4096, 14336, 1), (14336, 4096, 1),
+                (16, 4096, 1), (128, 4096, 1), (16384, 1024, 0)]
+
+
+def quant_bytes(R, C, mode):
+    # bf16 in, fp8 codes out, fp32 scales out
+    return 3 * R * C + 4 * (R if mode == 1 else 1)
+
+
+def time_quant(R, C, mode, q_dtype, steps, warmup, device):
+    import torch
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import bf16_matrix
+
+    x = bf16_matrix(R, C, SEED).to(device)
+    per_set = quant_bytes(R, C, mode)
+    n_sets = max(1, min(64, -(-3 * L2_BYTES // per_set)))
+    sets = []
+    for i in range(n_sets):
+        xi = x if i == 0 else torch.roll(x, shifts=i, dims=1).contiguous()
+        sets.append((xi, torch.empty((R, C), dtype=q_dtype, device=device),
+                     torch.empty(R if mode else 1, dtype=torch.float32, device=device)))
+    stream = torch.cuda.current_stream(device)
+
+    def step(i):
+        xi, q, s = sets[i % n_sets]
+        fm.fp8_quantize(xi, mode, q_dtype, out=q, scale=s)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(steps):
+                step(i)
+    torch.cuda.synchronize(device)
+    graph.replay()
+    torch.cuda.synchronize(device)
+    per = []
+    for _ in range(5):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        per.append(e0.elapsed_time(e1) / steps)
+    del graph, sets
+    torch.cuda.empty_cache()
+    return statistics.median(per), min(per), n_sets
+
+
+def run_quant(args):
+    import torch
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    import fp8_scaled_gemm_gb300 as fm
+    fm.load()
+    pk = peaks()
+    dts = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+    shapes = [(R, C, mode, "e4m3") for (R, C, mode) in QUANT_SHAPES]
+    if args.shapes:
+        shapes = []
+        for spec in args.shapes.split(","):
+            parts = spec.split(":")
+            R, C = (int(v) for v in parts[0].split("x"))
+            shapes.append((R, C, int(parts[1]) if len(parts) > 1 else 1, parts[2] if len(parts) > 2 else "e4m3"))
+    for (R, C, mode, qt) in shapes:
+        mean, best, n_sets = time_quant(R, C, mode, dts[qt], args.steps, args.warmup, device)
+        nbytes = quant_bytes(R, C, mode)
+        gbs = nbytes / (mean * 1e-3) / 1e9
+        print(json.dumps({
+            "op": "fp8_quantize", "shape": [R, C], "scale_mode": "row-wise" if mode else "per-tensor",
+            "type": qt, "kernel_us": round(mean * 1e3, 2), "kernel_us_best": round(best * 1e3, 2),
+            "timing": f"median of 5 CUDA-graph replays of {args.steps} calls",
+            "gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3), "bound": "hbm",
+            "launches_per_call": 2 if mode == 0 else 1, "rotated_sets": n_sets}), flush=True)
+
+
 # ------------------------------------------------------------ ranks ----------
 
 def max_over_ranks(total_ms: float, device) -> float:
@@ -541,6 +626,8 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.quant:
+        return run_quant(args)
     if args.sweep:
         run_sweep(args)
     elif args.impl == "reference":

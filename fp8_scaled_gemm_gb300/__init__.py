@@ -52,7 +52,7 @@ STATUS = {
 # Every symbol include/fp8mm.h declares.
 EXPORTS = (
     "fp8_scaled_mm", "fp8_scaled_mm_config", "fp8_scaled_mm_ex", "fp8_scaled_mm_host",
-    "fp8_scaled_mm_noalloc",
+    "fp8_scaled_mm_noalloc", "fp8_quantize", "fp8_scaled_mm_bf16",
     "fp8mm_reserve_workspace", "fp8mm_device_status", "fp8mm_status_string",
     "fp8mm_last_error", "fp8mm_describe_choice", "fp8mm_debug_inject",
 )
@@ -98,6 +98,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fp8_scaled_mm_host.restype = i32
         lib.fp8_scaled_mm_noalloc.argtypes = common
         lib.fp8_scaled_mm_noalloc.restype = i32
+        lib.fp8_quantize.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp]
+        lib.fp8_quantize.restype = i32
+        lib.fp8_scaled_mm_bf16.argtypes = [vp, vp, i32, vp, vp, i64, i64, i64, vp, vp, vp, vp, vp,
+                                           ctypes.POINTER(Options)]
+        lib.fp8_scaled_mm_bf16.restype = i32
         lib.fp8mm_reserve_workspace.argtypes = [i64]
         lib.fp8mm_reserve_workspace.restype = i32
         lib.fp8mm_device_status.argtypes = [vp]
@@ -227,6 +232,75 @@ def fp8_scaled_mm_noalloc(A, B, scale_a, scale_b, scale_mode: int, bias=None, ou
     M, N, K = _validate(A, B, scale_a, scale_b, scale_mode, bias, out, True)
     _check(load().fp8_scaled_mm_noalloc(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), scale_mode,
                                         _ptr(bias), _ptr(out), M, N, K, _stream_handle(stream)))
+    return out
+
+
+def _validate_bf16_rows(name, x, device_side=True):
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D bfloat16 tensor")
+    if x.shape[1] % 8 != 0:
+        raise ValueError(f"{name}'s row length must be a multiple of 8")
+    if device_side and not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def fp8_quantize(x, scale_mode: int, dtype=torch.float8_e4m3fn, out=None, scale=None, stream=None):
+    """bf16 x [R, C] -> (fp8 codes [R, C], fp32 scales [1] or [R]) on the GPU.
+
+    amax over the tensor (scale_mode 0) or each row (1), scale = amax / qmax,
+    codes = fp8(clamp(x / scale, -qmax, qmax)): the recipe of the gist
+    "matmul_fp8.py" (``get_scale``, ``benchmark()``). For B pass ``B.t()``
+    of a column-major B, i.e. Bt [N, K].
+    """
+    _validate_bf16_rows("x", x)
+    if dtype not in _FP8:
+        raise ValueError("dtype must be torch.float8_e4m3fn or torch.float8_e5m2")
+    if scale_mode not in (SCALE_TENSOR, SCALE_ROWWISE):
+        raise ValueError("scale_mode must be 0 (per-tensor) or 1 (row-wise)")
+    R, C = x.shape
+    if out is None:
+        out = torch.empty((R, C), dtype=dtype, device=x.device)
+    if scale is None:
+        scale = torch.empty(1 if scale_mode == SCALE_TENSOR else R, dtype=torch.float32, device=x.device)
+    if out.dtype != dtype or tuple(out.shape) != (R, C) or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA [R, C] tensor of the requested fp8 dtype")
+    n_scale = 1 if scale_mode == SCALE_TENSOR else R
+    if scale.dtype != torch.float32 or scale.numel() != n_scale or not scale.is_contiguous() or not scale.is_cuda:
+        raise ValueError(f"scale must be a contiguous CUDA float32 tensor of {n_scale} values")
+    _check(load().fp8_quantize(_ptr(x), R, C, int(scale_mode), _FP8[dtype], _ptr(out), _ptr(scale),
+                               _stream_handle(stream)))
+    return out, scale
+
+
+def fp8_scaled_mm_bf16(A, B, scale_mode: int, bias=None, out=None, stream=None,
+                       out_dtype=torch.bfloat16, a_dtype=torch.float8_e4m3fn, b_dtype=torch.float8_e4m3fn,
+                       variant: int = VARIANT_AUTO, tile_n: int = 0, split_k: int = 0,
+                       return_quantized: bool = False):
+    """The whole path from bf16 operands: quantise A [M, K] and B [K, N]
+    (column-major) with ``scale_mode``, then the scaled matmul. Returns out,
+    or (out, A_q, B_q, scale_a, scale_b) with ``return_quantized``."""
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError("A must be [M, K] and B [K, N]")
+    Bt = B.t()
+    _validate_bf16_rows("A", A)
+    _validate_bf16_rows("B.t()", Bt)
+    M, K = A.shape
+    N = B.shape[1]
+    dev = A.device
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=dev)
+    a_q = torch.empty((M, K), dtype=a_dtype, device=dev)
+    bt_q = torch.empty((N, K), dtype=b_dtype, device=dev)
+    ns_a, ns_b = (1, 1) if scale_mode == SCALE_TENSOR else (M, N)
+    scale_a = torch.empty(ns_a, dtype=torch.float32, device=dev)
+    scale_b = torch.empty(ns_b, dtype=torch.float32, device=dev)
+    _validate(a_q, bt_q.t(), scale_a, scale_b, scale_mode, bias, out, True, typed=True)
+    opt = Options(_FP8[a_dtype], _FP8[b_dtype], _OUT[out.dtype], int(variant), int(tile_n), int(split_k))
+    _check(load().fp8_scaled_mm_bf16(_ptr(A), _ptr(Bt), int(scale_mode), _ptr(bias), _ptr(out), M, N, K,
+                                     _ptr(a_q), _ptr(bt_q), _ptr(scale_a), _ptr(scale_b),
+                                     _stream_handle(stream), ctypes.byref(opt)))
+    if return_quantized:
+        return out, a_q, bt_q.t(), scale_a, scale_b
     return out
 
 

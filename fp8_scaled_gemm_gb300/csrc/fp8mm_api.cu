@@ -18,6 +18,7 @@
 #include "fp8mm_kernel.cuh"
 #include "fp8mm_kernel_pair.cuh"
 #include "fp8mm_kernel_ck.cuh"
+#include "fp8mm_quant.cuh"
 
 namespace {
 
@@ -44,6 +45,7 @@ struct DeviceState {
     int sms = 0;
     int cc_major = 0, cc_minor = 0;
     int *status = nullptr;               // in-kernel status word
+    unsigned int *qscratch = nullptr;    // per-tensor quantisation: per-CTA maxima + counter
     float *ws = nullptr;                 // split-K partial tiles
     size_t ws_bytes = 0;
     unsigned int *counters = nullptr;    // split-K arrivals
@@ -104,6 +106,13 @@ int device_state(DeviceState **out)
         e = cudaMemset(d.status, 0, sizeof(int));
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaMemset(status)");
+        const size_t qbytes = (fp8q::kMaxPartials + 1) * sizeof(unsigned int);
+        e = cudaMalloc(&d.qscratch, qbytes);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(quantisation scratch)");
+        e = cudaMemset(d.qscratch, 0, qbytes);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(quantisation scratch)");
         e = cudaDeviceSynchronize();
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaDeviceSynchronize");
@@ -657,6 +666,89 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     return encode_and_dispatch(c, A, B, out, M, N, K, kp, stream);
 }
 
+// ------------------------------------------------------ quantisation ---
+
+int check_quant_args(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, const void *q,
+                     const float *scale)
+{
+    if (R < 0 || C < 0 || C % 8 != 0 || R > (int64_t(1) << 40) / (C > 0 ? C : 1))
+        return FP8MM_ERR_SHAPE;
+    if (scale_mode != FP8MM_SCALE_TENSOR && scale_mode != FP8MM_SCALE_ROWWISE)
+        return FP8MM_ERR_MODE;
+    if (q_type != FP8MM_TYPE_E4M3 && q_type != FP8MM_TYPE_E5M2)
+        return FP8MM_ERR_MODE;
+    if (R == 0 || C == 0)
+        return FP8MM_OK;
+    if (!x || !q || !scale)
+        return FP8MM_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(q) & 7) ||
+        (reinterpret_cast<uintptr_t>(scale) & 3))
+        return FP8MM_ERR_ALIGN;
+    return FP8MM_OK;
+}
+
+template <int L, int W, int CH>
+int launch_quant_rows(const fp8q::QuantParams &p, int sms, cudaStream_t stream)
+{
+    constexpr int teams = fp8q::kThreads / (L * W);
+    const int64_t ctas = cdiv(p.R, teams);
+    const int grid = static_cast<int>(std::min<int64_t>(ctas, static_cast<int64_t>(sms) * 64));
+    return launch_pdl(fp8q::quant_rows_kernel<L, W, CH>, grid, fp8q::kThreads, 0, stream,
+                      "quantisation launch", p);
+}
+
+// Enqueues the quantisation of x [R, C]; arguments already checked, R, C > 0.
+int quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, void *q, float *scale,
+             cudaStream_t stream, const DeviceState &d)
+{
+    fp8q::QuantParams p{};
+    p.x = static_cast<const uint4 *>(x);
+    p.q = static_cast<uint2 *>(q);
+    p.scale = scale;
+    p.partial = d.qscratch;
+    p.R = R;
+    p.groups = C / 8;
+    p.total = R * (C / 8);
+    p.q_type = q_type;
+    if (scale_mode == FP8MM_SCALE_TENSOR) {
+        const int g1 = static_cast<int>(std::max<int64_t>(
+            1, std::min<int64_t>({cdiv(p.total, fp8q::kThreads * fp8q::kUnroll * 2),
+                                  static_cast<int64_t>(d.sms) * 4, fp8q::kMaxPartials})));
+        int rc = launch_pdl(fp8q::quant_amax_kernel, g1, fp8q::kThreads, 0, stream, "amax launch", p);
+        if (rc != FP8MM_OK)
+            return rc;
+        const int g2 = static_cast<int>(std::max<int64_t>(
+            1, std::min<int64_t>(cdiv(p.total, fp8q::kThreads * fp8q::kUnroll), static_cast<int64_t>(d.sms) * 8)));
+        return launch_pdl(fp8q::quant_convert_kernel, g2, fp8q::kThreads, 0, stream, "quantisation launch", p);
+    }
+    const int64_t g = p.groups;
+    const int sms = d.sms;
+    if (g <= 4)
+        return launch_quant_rows<4, 1, 1>(p, sms, stream);
+    if (g <= 8)
+        return launch_quant_rows<8, 1, 1>(p, sms, stream);
+    if (g <= 16)
+        return launch_quant_rows<16, 1, 1>(p, sms, stream);
+    if (g <= 32)
+        return launch_quant_rows<32, 1, 1>(p, sms, stream);
+    if (g <= 64)
+        return launch_quant_rows<32, 1, 2>(p, sms, stream);
+    if (g <= 128)
+        return launch_quant_rows<32, 1, 4>(p, sms, stream);
+    if (g <= 256)
+        return launch_quant_rows<32, 2, 4>(p, sms, stream);
+    if (g <= 512)
+        return launch_quant_rows<32, 4, 4>(p, sms, stream);
+    if (g <= 1024)
+        return launch_quant_rows<32, 8, 4>(p, sms, stream);
+    if (g <= 2048)
+        return launch_quant_rows<32, 8, 8>(p, sms, stream);
+    if (g <= 4096)
+        return launch_quant_rows<32, 8, 16>(p, sms, stream);
+    const int grid = static_cast<int>(std::min<int64_t>(R, static_cast<int64_t>(sms) * 8));
+    return launch_pdl(fp8q::quant_rows_long_kernel, grid, fp8q::kThreads, 0, stream, "quantisation launch", p);
+}
+
 // Streams and events of the host-memory entry point (one set per device).
 constexpr int kHostChunks = 8;
 struct HostPipe {
@@ -740,6 +832,47 @@ int fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, const f
     return run(A, B, scale_a, scale_b, scale_mode, bias, out, M, N, K, static_cast<cudaStream_t>(stream),
                options->variant, options->tile_n, options->split_k, options->a_type, options->b_type,
                options->out_type);
+}
+
+int fp8_quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, void *q, float *scale,
+                 void *stream)
+{
+    int rc = check_quant_args(x, R, C, scale_mode, q_type, q, scale);
+    if (rc != FP8MM_OK || R == 0 || C == 0)
+        return rc;
+    DeviceState *d = nullptr;
+    rc = device_state(&d);
+    if (rc != FP8MM_OK)
+        return rc;
+    return quantize(x, R, C, scale_mode, q_type, q, scale, static_cast<cudaStream_t>(stream), *d);
+}
+
+int fp8_scaled_mm_bf16(const void *A, const void *B, int scale_mode, const void *bias, void *out, int64_t M,
+                       int64_t N, int64_t K, void *A_q, void *B_q, float *scale_a, float *scale_b, void *stream,
+                       const fp8mm_options *options)
+{
+    fp8mm_options o = {FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16, FP8MM_VARIANT_AUTO, 0, 0};
+    if (options)
+        o = *options;
+    // the GEMM's own checks first (its operands are the quantised copies)
+    int rc = check_args(A_q, B_q, scale_a, scale_b, scale_mode, bias, out, M, N, K);
+    if (rc != FP8MM_OK)
+        return rc;
+    if (M == 0 || N == 0)
+        return FP8MM_OK;
+    if ((rc = check_quant_args(A, M, K, scale_mode, o.a_type, A_q, scale_a)) != FP8MM_OK ||
+        (rc = check_quant_args(B, N, K, scale_mode, o.b_type, B_q, scale_b)) != FP8MM_OK)
+        return rc;
+    DeviceState *d = nullptr;
+    rc = device_state(&d);
+    if (rc != FP8MM_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((rc = quantize(A, M, K, scale_mode, o.a_type, A_q, scale_a, s, *d)) != FP8MM_OK ||
+        (rc = quantize(B, N, K, scale_mode, o.b_type, B_q, scale_b, s, *d)) != FP8MM_OK)
+        return rc;
+    return run(A_q, B_q, scale_a, scale_b, scale_mode, bias, out, M, N, K, s, o.variant, o.tile_n, o.split_k,
+               o.a_type, o.b_type, o.out_type);
 }
 
 int fp8_scaled_mm_host(const void *A, const void *B, const float *scale_a, const float *scale_b,

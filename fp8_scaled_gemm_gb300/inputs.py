@@ -123,3 +123,69 @@ def from_codes(A_u8, Bt_u8, scale_a, scale_b, scale_mode: int,
         bias = torch.from_numpy(np.ascontiguousarray(bias_u16, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
     return ScaledMMInputs(M=A.shape[0], N=Bt.shape[0], K=A.shape[1], scale_mode=scale_mode,
                           a_q=A, bt_q=Bt, scale_a=sa, scale_b=sb, bias=bias)
+
+
+# ------------------------------------------------ bf16 data to quantise ---
+# Plain bf16 matrices for the quantisation step (no quantisation arithmetic
+# here: the values are drawn or listed, then stored as bf16).
+
+def bf16_matrix(R: int, C: int, seed: int, kind: str = "randn") -> torch.Tensor:
+    """bf16 [R, C] on the CPU.
+
+    ``randn``: the pages' operand data (``torch.randn`` in bf16).
+    ``wide``: randn times a per-row power of two in [2^-40, 2^40] and a
+    per-element power of two in [2^-12, 1], so rows differ in range and hold
+    values far below their maximum.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    if kind == "randn":
+        return torch.randn(R, C, dtype=torch.bfloat16, generator=g)
+    if kind == "wide":
+        x = torch.randn(R, C, dtype=torch.float32, generator=g)
+        x = x * torch.exp2(torch.randint(-40, 41, (R, 1), generator=g).float())
+        x = x * torch.exp2(torch.randint(-12, 1, (R, C), generator=g).float())
+        return x.to(torch.bfloat16)
+    raise ValueError(f"unknown kind {kind!r}")
+
+
+def bf16_significand_rows(amax_exps=(0,)) -> torch.Tensor:
+    """One row per (bf16 significand m, exponent e in amax_exps): the row's
+    largest magnitude is (1 + m/128) 2^e, and it also holds every bf16 value
+    (1 + k/128) 2^(e-d) below that, d = 0..24, with both signs; rows are
+    zero-padded to a common length that is a multiple of 16."""
+    rows = []
+    for e in amax_exps:
+        for m in range(128):
+            amax = (1 + m / 128) * 2.0 ** e
+            vals = [amax] + [(1 + k / 128) * 2.0 ** (e - d) for d in range(25) for k in range(128)]
+            vals = [v for v in vals if v <= amax]
+            rows.append(vals + [-v for v in vals])
+    C = (max(len(r) for r in rows) + 15) // 16 * 16
+    out = torch.zeros(len(rows), C, dtype=torch.float64)
+    for i, r in enumerate(rows):
+        out[i, :len(r)] = torch.tensor(r, dtype=torch.float64)
+    return out.to(torch.float32).to(torch.bfloat16)
+
+
+def bf16_special_rows(C: int = 64) -> torch.Tensor:
+    """Rows for the degenerate cases: all +0; one NaN; +inf with finite
+    values; all -0; -inf; bf16 subnormals only; values near the bf16
+    maximum; values near the smallest normal; a randn row."""
+    inf, nan = float("inf"), float("nan")
+    x = torch.zeros(9, C, dtype=torch.float32)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(1234)
+    base = torch.randn(C, generator=g)
+    x[1] = base
+    x[1, C // 3] = nan
+    x[2] = base
+    x[2, 5] = inf
+    x[3] = -0.0
+    x[4] = base
+    x[4, 7] = -inf
+    x[5] = base * 2.0 ** -128          # bf16 subnormals
+    x[6] = base.sign() * (3.0e38 - base.abs() * 1e37)
+    x[7] = base * 2.0 ** -124
+    x[8] = base
+    return x.to(torch.bfloat16)

@@ -174,6 +174,64 @@ int fp8_scaled_mm_host(const void *A, const void *B,
                        void *stream);
 
 /*
+ * Quantise bf16 data to fp8 codes with fp32 scales: the step that makes the
+ * operands of fp8_scaled_mm (gist "matmul_fp8.py", `get_scale` and
+ * `benchmark()`):
+ *
+ *   amax  = max |x|  over all of x (FP8MM_SCALE_TENSOR) or over each row
+ *           (FP8MM_SCALE_ROWWISE)
+ *   scale = amax / qmax, in fp32; qmax = 448 (e4m3fn) or 57344 (e5m2), the
+ *           format's largest finite value (torch.finfo(dtype).max)
+ *   q     = fp8(clamp(x / scale, -qmax, qmax)): fp32 division, correctly
+ *           rounded; conversion rounds to nearest, ties to even
+ *
+ * For B pass Bt, i.e. B [K, N] column-major as the row-major [N, K] array:
+ * its row-wise scales are then B's per-column scales, the layout
+ * fp8_scaled_mm takes.
+ *
+ *   x      device bf16 [R, C], row-major, C contiguous; 16-byte aligned.
+ *   R, C   R >= 0, C >= 0, C % 8 == 0. R == 0 or C == 0 is a no-op.
+ *   scale_mode  FP8MM_SCALE_TENSOR or FP8MM_SCALE_ROWWISE.
+ *   q_type FP8MM_TYPE_E4M3 or FP8MM_TYPE_E5M2.
+ *   q      device fp8 [R, C] (output), 8-byte aligned.
+ *   scale  device fp32 (output): 1 value, or R values (row-wise); 4-byte aligned.
+ *
+ * Cases the recipe leaves open: a zero scale (all elements +-0) gives the
+ * codes of +-0 instead of the NaN of 0/0; every NaN encodes as 0x7F; a NaN
+ * anywhere in the tensor (row) makes its scale NaN and all its codes NaN;
+ * an infinity makes the scale inf, finite elements then encode as +-0.
+ *
+ * Asynchronous on `stream`. Row-wise is one kernel launch; per-tensor is two
+ * (amax, then conversion) and uses a small per-device scratch (1024 maxima
+ * and a counter) owned by the library, so per-tensor calls that overlap on
+ * the GPU on different streams of one device race on it.
+ */
+int fp8_quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type,
+                 void *q, float *scale, void *stream);
+
+/*
+ * The whole path from bf16 operands: quantise A [M, K] and B (column-major
+ * [K, N], i.e. Bt [N, K] row-major) as fp8_quantize does, with scale_mode
+ * for both, then out = fp8_scaled_mm_ex(A_q, B_q, scale_a, scale_b, ...).
+ * The launches are chained on `stream` (programmatic dependent launch).
+ *
+ *   A, B      device bf16, 16-byte aligned; K % 16 == 0 as for fp8_scaled_mm.
+ *   A_q, B_q  device fp8 outputs, [M, K] and Bt [N, K], 16-byte aligned;
+ *             their element types are options->a_type / b_type.
+ *   scale_a, scale_b  device fp32 outputs, 1 or M / N values.
+ *   bias, out as fp8_scaled_mm_ex (out type options->out_type).
+ *   options   may be NULL: e4m3 operands, bf16 out, automatic kernel choice.
+ *
+ * The caller owns A_q, B_q and the scales, which hold the quantised
+ * operands afterwards (reusable as fp8_scaled_mm inputs).
+ */
+int fp8_scaled_mm_bf16(const void *A, const void *B, int scale_mode,
+                       const void *bias, void *out,
+                       int64_t M, int64_t N, int64_t K,
+                       void *A_q, void *B_q, float *scale_a, float *scale_b,
+                       void *stream, const fp8mm_options *options);
+
+/*
  * Allocation-free variant of fp8_scaled_mm. The pages have no counterpart:
  * this is an addition for callers that cannot allocate device memory while
  * they run (for example code running inside a memory pool it does not own,

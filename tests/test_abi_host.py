@@ -145,3 +145,44 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_build, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         fm.load()
+
+
+def qcall(lib, x=ALIGNED, R=64, C=64, mode=0, q_type=0, q=ALIGNED, scale=ALIGNED):
+    return lib.fp8_quantize(P(x) if x else None, R, C, mode, q_type, P(q) if q else None,
+                            P(scale) if scale else None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(C=12), -2), (dict(C=-8), -2), (dict(R=-1), -2), (dict(R=2 ** 40, C=64), -2),
+    (dict(mode=2), -4), (dict(q_type=2), -4), (dict(q_type=-1), -4),
+    (dict(x=0), -1), (dict(q=0), -1), (dict(scale=0), -1),
+    (dict(x=ALIGNED + 8), -3), (dict(q=ALIGNED + 4), -3), (dict(scale=ALIGNED + 2), -3),
+    (dict(R=0, x=0, q=0, scale=0), 0), (dict(C=0, x=0, q=0, scale=0), 0),
+])
+def test_quantize_argument_errors_before_any_cuda_call(lib, kw, code):
+    assert qcall(lib, **kw) == code
+
+
+def test_bf16_path_argument_errors(lib):
+    def bf(A=ALIGNED, B=ALIGNED, M=64, N=64, K=64, aq=ALIGNED, bq=ALIGNED, opt=None, mode=0):
+        return lib.fp8_scaled_mm_bf16(P(A) if A else None, P(B) if B else None, mode, None, P(ALIGNED),
+                                      M, N, K, P(aq) if aq else None, P(bq) if bq else None,
+                                      P(ALIGNED), P(ALIGNED), None,
+                                      ctypes.byref(opt) if opt is not None else None)
+    assert bf(aq=0) == -1
+    assert bf(A=0) == -1
+    assert bf(K=24) == -2
+    assert bf(mode=3) == -4
+    assert bf(opt=fm.Options(3, 0, 0, 0, 0, 0)) == -4
+    assert bf(A=ALIGNED + 8) == -3
+    assert bf(M=0, A=0, B=0, aq=0, bq=0) == 0
+
+
+def test_python_quantize_validation():
+    x = torch.zeros(4, 16, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        fm.fp8_quantize(x, 0)
+    with pytest.raises(ValueError, match="multiple of 8"):
+        fm.fp8_quantize(torch.zeros(4, 12, dtype=torch.bfloat16), 0)
+    with pytest.raises(ValueError, match="bfloat16"):
+        fm.fp8_quantize(x.float(), 0)

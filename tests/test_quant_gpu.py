@@ -1,0 +1,188 @@
+"""GPU parity of the quantisation step (bf16 -> fp8 codes + fp32 scales)
+through the C ABI, against the oracle: codes and scales bit for bit.
+
+The codes are integers decided by fp32 arithmetic (one division and one
+rounding per element), so both sides take the same fp32 steps and must agree
+exactly; NaN scales compare as NaN.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_scaled_gemm_gb300.inputs import (bf16_matrix, bf16_significand_rows, bf16_special_rows,
+                                          make_inputs)
+from tests._parity import bf16_bits, compare
+
+pytestmark = pytest.mark.gpu
+
+DT = {0: torch.float8_e4m3fn, 1: torch.float8_e5m2}
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _bits(x: torch.Tensor) -> np.ndarray:
+    return x.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _same_scales(got: np.ndarray, want: np.ndarray) -> bool:
+    both_nan = np.isnan(got) & np.isnan(want)
+    return bool(np.all(both_nan | (got.view(np.uint32) == want.view(np.uint32))))
+
+
+def quantize_and_compare(x_cpu: torch.Tensor, mode: int, q_type: int):
+    import fp8_scaled_gemm_gb300 as fm
+    q, s = fm.fp8_quantize(x_cpu.cuda(), mode, DT[q_type])
+    torch.cuda.synchronize()
+    q_gpu = q.view(torch.uint8).cpu().numpy()
+    s_gpu = s.cpu().numpy()
+    q_ref, s_ref = oracle.quantize(_bits(x_cpu), mode, q_type)
+    bad = np.argwhere(q_gpu != q_ref)
+    assert _same_scales(s_gpu, s_ref), f"scales differ: {np.nonzero(s_gpu.view(np.uint32) != s_ref.view(np.uint32))}"
+    assert bad.size == 0, (f"{len(bad)} codes differ; first {bad[:5].tolist()}: gpu "
+                           f"{[int(q_gpu[tuple(i)]) for i in bad[:5]]} oracle {[int(q_ref[tuple(i)]) for i in bad[:5]]}")
+    return q, s
+
+
+# Row lengths that reach every team shape of the row-wise kernel (4, 8, 16,
+# 32 lanes; 1, 2, 4, 8 warps; 1 to 16 groups per thread) and the two-pass
+# kernel for rows longer than 32768.
+ROW_LENGTHS = [8, 40, 64, 120, 256, 264, 512, 1000, 1024, 2048, 2056, 4096, 8192, 12288, 16384, 24576,
+               32768, 32776, 65536]
+
+
+@pytest.mark.parametrize("C", ROW_LENGTHS)
+@pytest.mark.parametrize("mode", [0, 1])
+def test_quantize_every_row_length(C, mode):
+    _need_gpu()
+    R = 37 if C >= 4096 else 301
+    for q_type in (0, 1):
+        quantize_and_compare(bf16_matrix(R, C, seed=C + mode, kind="wide"), mode, q_type)
+
+
+@pytest.mark.parametrize("q_type", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_quantize_every_reachable_significand_pair(q_type, mode):
+    _need_gpu()
+    # every bf16 row maximum (128 significands at 2^0, 2^-100, 2^-130 and
+    # 2^120) against every bf16 value below it: all the (x, scale) pairs the
+    # recipe can produce, up to powers of two, plus subnormal scales
+    x = bf16_significand_rows((0, -100, -130, 120))
+    quantize_and_compare(x, mode, q_type)
+
+
+@pytest.mark.parametrize("q_type", [0, 1])
+def test_quantize_degenerate_rows(q_type):
+    _need_gpu()
+    x = bf16_special_rows(64)
+    q, s = quantize_and_compare(x, 1, q_type)
+    s = s.cpu().numpy()
+    assert s[0] == 0 and np.isnan(s[1]) and np.isinf(s[2]) and s[3] == 0 and np.isinf(s[4])
+    # each degenerate row alone, per tensor
+    for r in range(x.shape[0]):
+        quantize_and_compare(x[r:r + 1].contiguous(), 0, q_type)
+
+
+def test_quantize_many_rows_grid_stride():
+    _need_gpu()
+    # more rows than the grid has teams: 4-lane teams, 64 rows per CTA pass
+    quantize_and_compare(bf16_matrix(700_000, 8, seed=3), 1, 0)
+    # one-row-per-CTA teams with more rows than CTAs
+    quantize_and_compare(bf16_matrix(10_000, 8192, seed=4), 1, 0)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("q_type", [0, 1])
+def test_quantize_full_size_operand(mode, q_type):
+    _need_gpu()
+    # the benchmark's operand: bf16 randn 8192 x 8192, compared in full
+    quantize_and_compare(bf16_matrix(8192, 8192, seed=42), mode, q_type)
+
+
+def test_per_tensor_back_to_back_calls_reuse_the_scratch():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    xs = [bf16_matrix(999, 1024, seed=s, kind="wide") for s in range(4)]
+    dev = [x.cuda() for x in xs]
+    outs = [fm.fp8_quantize(d, 0) for d in dev]     # queued back to back on one stream
+    torch.cuda.synchronize()
+    for x, (q, s) in zip(xs, outs):
+        q_ref, s_ref = oracle.quantize(_bits(x), 0, 0)
+        assert np.array_equal(q.view(torch.uint8).cpu().numpy(), q_ref)
+        assert _same_scales(s.cpu().numpy(), s_ref)
+
+
+def test_quantize_matches_the_input_recipe_of_the_benchmark():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    # the GEMM tests' operands come from the same recipe in PyTorch CPU ops
+    inp = make_inputs(300, 520, 400, 1, seed=5)
+    g = torch.Generator().manual_seed(5)
+    a = torch.randn(300, 400, dtype=torch.bfloat16, generator=g)
+    b = torch.randn(400, 520, dtype=torch.bfloat16, generator=g)
+    qa, sa = fm.fp8_quantize(a.cuda(), 1)
+    qb, sb = fm.fp8_quantize(b.t().contiguous().cuda(), 1)
+    assert torch.equal(qa.cpu().view(torch.uint8), inp.a_q.view(torch.uint8))
+    assert torch.equal(qb.cpu().view(torch.uint8), inp.bt_q.view(torch.uint8))
+    assert torch.equal(sa.cpu(), inp.scale_a) and torch.equal(sb.cpu(), inp.scale_b)
+
+
+# ------------------------------------------------- bf16 -> GEMM, end to end ---
+
+def _bf16_path(M, N, K, mode, seed, bias, a_dtype=torch.float8_e4m3fn, b_dtype=torch.float8_e4m3fn,
+               out_dtype=torch.bfloat16, sample=False):
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import from_codes
+    from tests._parity import sample_indices
+    a = bf16_matrix(M, K, seed)
+    bt = bf16_matrix(N, K, seed + 1)
+    bias_t = None
+    if bias:
+        bias_t = (bf16_matrix(1, N, seed + 2).reshape(-1) * 0.1).to(out_dtype)
+    out, a_q, b_q, s_a, s_b = fm.fp8_scaled_mm_bf16(
+        a.cuda(), bt.cuda().t(), mode, bias=None if bias_t is None else bias_t.cuda(),
+        out_dtype=out_dtype, a_dtype=a_dtype, b_dtype=b_dtype, return_quantized=True)
+    assert fm.fp8mm_device_status() == 0
+    at, bt_type = {torch.float8_e4m3fn: 0, torch.float8_e5m2: 1}[a_dtype], \
+        {torch.float8_e4m3fn: 0, torch.float8_e5m2: 1}[b_dtype]
+    qa_ref, sa_ref = oracle.quantize(_bits(a), mode, at)
+    qb_ref, sb_ref = oracle.quantize(_bits(bt), mode, bt_type)
+    assert np.array_equal(a_q.view(torch.uint8).cpu().numpy(), qa_ref)
+    assert np.array_equal(b_q.t().contiguous().view(torch.uint8).cpu().numpy(), qb_ref)
+    assert _same_scales(s_a.cpu().numpy(), sa_ref) and _same_scales(s_b.cpu().numpy(), sb_ref)
+    inp = from_codes(qa_ref, qb_ref, sa_ref, sb_ref, mode,
+                     None if bias_t is None else _bits(bias_t))
+    inp.a_type, inp.b_type = at, bt_type
+    inp.out_type = 0 if out_dtype == torch.bfloat16 else 1
+    bits = bf16_bits(out)
+    rows = cols = None
+    if sample:
+        rows = sample_indices(M, 128, 32, seed + 3)
+        cols = sample_indices(N, 128, 32, seed + 4)
+        bits = bits[np.ix_(rows, cols)]
+    stats = compare(bits, inp, rows, cols)
+    assert stats["violations"] == 0, stats
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("shape", [(300, 520, 400), (1, 4096, 1024), (16, 14336, 4096), (129, 257, 16)])
+def test_bf16_path_small(mode, shape):
+    _need_gpu()
+    _bf16_path(*shape, mode, seed=31, bias=(mode == 1))
+
+
+def test_bf16_path_other_types():
+    _need_gpu()
+    _bf16_path(300, 520, 400, 1, 33, True, a_dtype=torch.float8_e5m2, out_dtype=torch.float16)
+    _bf16_path(300, 520, 400, 0, 34, False, b_dtype=torch.float8_e5m2)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_bf16_path_full_size_sampled(mode):
+    _need_gpu()
+    _bf16_path(8192, 8192, 8192, mode, seed=42, bias=False, sample=True)
