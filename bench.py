@@ -82,25 +82,31 @@ def peaks():
                 "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+GEMM_KERNEL_SOURCES = ("fp8mm_kernel.cuh", "fp8mm_kernel_pair.cuh", "fp8mm_kernel_ck.cuh", "sm103_ptx.cuh")
+
+
 def kernel_src_sha() -> str:
-    """Hash of the CUDA sources; a stored ncu traffic figure is used only for this hash."""
+    """Hash of the GEMM kernels' CUDA sources; a stored ncu traffic figure is
+    used only while this hash and the launch configuration both match."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "fp8_scaled_gemm_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in GEMM_KERNEL_SOURCES:
         h.update(f.encode())
         with open(os.path.join(d, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(key: str):
+def measured_traffic(key: str, kernel: str):
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)[key]
     except (OSError, KeyError, ValueError):
         return None
-    return t["bytes"] if t.get("kernel_src_sha") == kernel_src_sha() else None
+    if t.get("kernel_src_sha") != kernel_src_sha() or t.get("kernel") != kernel:
+        return None
+    return t["bytes"]
 
 
 # ------------------------------------------------------------ clocks ---------
@@ -560,7 +566,7 @@ def run_ours(args):
                       "p20": round(res["kernel_ms_p20"], 5), "p80": round(res["kernel_ms_p80"], 5)},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(fp8_peak, 1),
                      "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
-                     "traffic": measured_traffic("tensor" if head_mode == 0 else "rowwise"),
+                     "traffic": measured_traffic("tensor" if head_mode == 0 else "rowwise", res["choice"]),
                      "traffic_unit": "bytes per launch (ncu dram read+write)",
                      "peak_source": f"{pk['source']}: bf16 burst {pk['bf16_tflops']} TFLOP/s x "
                                     f"{NOMINAL_FP8_PER_BF16} (nominal fp8:bf16 ratio)"},

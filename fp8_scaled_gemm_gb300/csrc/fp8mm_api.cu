@@ -711,14 +711,29 @@ int quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, vo
     p.total = R * (C / 8);
     p.q_type = q_type;
     if (scale_mode == FP8MM_SCALE_TENSOR) {
+        // amax: half of what the SMs hold at once streams best (a pure read);
+        // convert: one full wave
+        static int occ_amax[kMaxDevices] = {}, occ_conv[kMaxDevices] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (!occ_amax[dev]) {
+            int a = 0, c = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, fp8q::quant_amax_kernel, fp8q::kThreads, 0);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, fp8q::quant_convert_kernel, fp8q::kThreads, 0);
+            occ_amax[dev] = std::max(1, a);
+            occ_conv[dev] = std::max(1, c);
+        }
+        p.keep = std::min<int64_t>(p.total, (int64_t(64) << 20) / 16);
         const int g1 = static_cast<int>(std::max<int64_t>(
-            1, std::min<int64_t>({cdiv(p.total, fp8q::kThreads * fp8q::kUnroll * 2),
-                                  static_cast<int64_t>(d.sms) * 4, fp8q::kMaxPartials})));
+            1, std::min<int64_t>({cdiv(p.total, fp8q::kThreads * fp8q::kUnroll),
+                                  static_cast<int64_t>(d.sms) * std::max(1, occ_amax[dev] / 2),
+                                  fp8q::kMaxPartials})));
         int rc = launch_pdl(fp8q::quant_amax_kernel, g1, fp8q::kThreads, 0, stream, "amax launch", p);
         if (rc != FP8MM_OK)
             return rc;
         const int g2 = static_cast<int>(std::max<int64_t>(
-            1, std::min<int64_t>(cdiv(p.total, fp8q::kThreads * fp8q::kUnroll), static_cast<int64_t>(d.sms) * 8)));
+            1, std::min<int64_t>(cdiv(p.total, fp8q::kThreads * fp8q::kUnroll),
+                                 static_cast<int64_t>(d.sms) * occ_conv[dev])));
         return launch_pdl(fp8q::quant_convert_kernel, g2, fp8q::kThreads, 0, stream, "quantisation launch", p);
     }
     const int64_t g = p.groups;

@@ -14,7 +14,8 @@
 // registers. Per-tensor scaling needs the global amax before any division:
 // an amax kernel (the last CTA to finish turns the per-CTA maxima into the
 // scale) and a convert kernel that walks the tensor in reverse, so that the
-// part the amax pass read last is still in L2.
+// part the amax pass read last is still in L2 (the amax pass marks the last
+// 64 MB it reads evict-last, everything else evict-first).
 //
 // amax runs on the bf16 bit patterns: |x| is the pattern with the sign bit
 // cleared, and unsigned order on those patterns is the order of |x| with NaN
@@ -22,13 +23,18 @@
 // gives amax, and a NaN anywhere makes the scale NaN as a float max would.
 //
 // Division: x / scale must be the correctly rounded fp32 quotient, because
-// the quotient decides an fp8 code. With the scale normalised to s1 in [1, 2)
-// by a power of two p (x1 = x p, exact), r1 = RN(1/s1), q0 = RN(x1 r1) and
-// one correction q1 = RN(q0 + (x1 - q0 s1) r1) (two FMAs) give RN(x / scale)
-// for every bf16 x and every scale of this recipe (Markstein's division
-// correction, P. Markstein, "Computation of elementary functions on the IBM
-// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990). Scales outside
-// [2^-120, 2^120), zero, inf or NaN take the IEEE division __fdiv_rn.
+// the quotient decides an fp8 code. For scales in [2^-80, 2^100) the kernels
+// use r = RN(1/scale), q0 = RN(x r), e = RN(q0 scale - x) (one FMA, exact)
+// and q1 = RN(q0 - e r) (one FMA): Markstein's correction of a quotient by
+// its residual (P. Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990), which gives
+// RN(x / scale) for every bf16 x and every scale this recipe produces while
+// the residual stays a normal number, i.e. for |x| >= 2^-100. Smaller |x|
+// have |x / scale| < 2^-20, below half the smallest fp8 subnormal, and q1
+// is then within a few fp32 ulps of the quotient: the code is +-0 either
+// way. The signs of the FMA operands are chosen so that x = -0 gives -0.
+// Scales outside that range, zero, inf or NaN take the IEEE division
+// __fdiv_rn.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -50,6 +56,7 @@ struct QuantParams {
     long long groups;        // groups of 8 per row (C / 8)
     long long total;         // R * groups
     int q_type;              // 0 e4m3fn, 1 e5m2
+    long long keep;          // per-tensor: groups at the end of x that the amax pass marks evict-last in L2
 };
 
 __device__ __forceinline__ float qmax_of(int q_type) { return q_type == 0 ? 448.0f : 57344.0f; }
@@ -66,22 +73,19 @@ __device__ __forceinline__ uint32_t amax_acc(uint32_t acc, const uint4 &v)
 __device__ __forceinline__ uint32_t fold_halves(uint32_t acc) { return max(acc & 0xFFFFu, acc >> 16); }
 
 struct Divider {
-    float s, s1, r1, p;
-    int mode;   // 0: zero scale, 1: normalised reciprocal + correction, 2: IEEE division
+    float s, r;
+    int mode;   // 0: zero scale, 1: reciprocal + one correction, 2: IEEE division
 };
 
 __device__ __forceinline__ Divider make_divider(float s)
 {
     Divider d;
     d.s = s;
-    d.s1 = d.r1 = d.p = 0.0f;
+    d.r = 0.0f;
     if (s == 0.0f) {
         d.mode = 0;
-    } else if (s >= 0x1p-120f && s < 0x1p120f) {
-        const int e = static_cast<int>((__float_as_uint(s) >> 23) & 0xFFu) - 127;  // s normal here
-        d.p = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-        d.s1 = __fmul_rn(s, d.p);                           // in [1, 2), exact
-        d.r1 = __frcp_rn(d.s1);
+    } else if (s >= 0x1p-80f && s < 0x1p100f) {
+        d.r = __frcp_rn(s);
         d.mode = 1;
     } else {
         d.mode = 2;
@@ -89,14 +93,12 @@ __device__ __forceinline__ Divider make_divider(float s)
     return d;
 }
 
-// x / scale for the normalised-reciprocal path (mode 1); x is finite there.
+// x / scale for the reciprocal path (mode 1); x is finite there.
 __device__ __forceinline__ float div_fast(const Divider &d, float x)
 {
-    const float x1 = __fmul_rn(x, d.p);
-    const float q0 = __fmul_rn(x1, d.r1);
-    const float res = __fmaf_rn(-q0, d.s1, x1);
-    const float q1 = __fmaf_rn(res, d.r1, q0);
-    return copysignf(q1, x);                                // keeps the sign of a zero quotient
+    const float q0 = __fmul_rn(x, d.r);
+    const float e = __fmaf_rn(q0, d.s, -x);
+    return __fmaf_rn(-e, d.r, q0);
 }
 
 // x / scale for the other modes.
@@ -151,6 +153,32 @@ __device__ __forceinline__ uint2 convert_group(const Divider &d, const uint4 &v,
     return r;
 }
 
+// L2 eviction-priority policies for the per-tensor passes.
+__device__ __forceinline__ uint64_t l2_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint4 load_group(const uint4 *p, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void store_group(uint2 *p, uint2 v, uint64_t pol)
+{
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "l"(pol) : "memory");
+}
 __device__ __forceinline__ uint4 load_group(const uint4 *p)
 {
     uint4 v;
@@ -285,19 +313,23 @@ __global__ void __launch_bounds__(kThreads) quant_amax_kernel(const QuantParams 
     fp8mm::ptx::grid_launch_dependents();
     fp8mm::ptx::grid_dependency_wait();
     const long long stride = static_cast<long long>(gridDim.x) * kThreads;
+    // The convert pass reads the tensor from its end: the last `keep` groups
+    // are asked to stay in L2, the rest to leave first.
+    const uint64_t keep_pol = l2_evict_last(), pass_pol = l2_evict_first();
+    const long long keep_from = p.total - p.keep;
     uint32_t acc = 0;
     long long g = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
     for (; g + (kUnroll - 1) * stride < p.total; g += kUnroll * stride) {
         uint4 v[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
-            v[u] = load_group(p.x + g + u * stride);
+            v[u] = load_group(p.x + g + u * stride, g + u * stride >= keep_from ? keep_pol : pass_pol);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
             acc = amax_acc(acc, v[u]);
     }
     for (; g < p.total; g += stride)
-        acc = amax_acc(acc, load_group(p.x + g));
+        acc = amax_acc(acc, load_group(p.x + g, g >= keep_from ? keep_pol : pass_pol));
     acc = fold_halves(acc);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
@@ -341,18 +373,20 @@ template <bool FAST>
 __device__ __forceinline__ void convert_tensor(const QuantParams &p, const Divider &d)
 {
     const long long stride = static_cast<long long>(gridDim.x) * kThreads;
+    const uint64_t pol = l2_evict_first();      // neither x nor the codes are read again here
     long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
     for (; i + (kUnroll - 1) * stride < p.total; i += kUnroll * stride) {
         uint4 v[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
-            v[u] = load_group(p.x + (p.total - 1 - (i + u * stride)));
+            v[u] = load_group(p.x + (p.total - 1 - (i + u * stride)), pol);
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
-            p.q[p.total - 1 - (i + u * stride)] = convert_group<FAST>(d, v[u], p.q_type);
+            store_group(p.q + (p.total - 1 - (i + u * stride)), convert_group<FAST>(d, v[u], p.q_type), pol);
     }
     for (; i < p.total; i += stride)
-        p.q[p.total - 1 - i] = convert_group<FAST>(d, load_group(p.x + (p.total - 1 - i)), p.q_type);
+        store_group(p.q + (p.total - 1 - i), convert_group<FAST>(d, load_group(p.x + (p.total - 1 - i), pol), p.q_type),
+                    pol);
 }
 
 __global__ void __launch_bounds__(kThreads) quant_convert_kernel(const QuantParams p)

@@ -149,16 +149,16 @@ def bf16_matrix(R: int, C: int, seed: int, kind: str = "randn") -> torch.Tensor:
     raise ValueError(f"unknown kind {kind!r}")
 
 
-def bf16_significand_rows(amax_exps=(0,)) -> torch.Tensor:
+def bf16_significand_rows(amax_exps=(0,), depth: int = 25) -> torch.Tensor:
     """One row per (bf16 significand m, exponent e in amax_exps): the row's
     largest magnitude is (1 + m/128) 2^e, and it also holds every bf16 value
-    (1 + k/128) 2^(e-d) below that, d = 0..24, with both signs; rows are
+    (1 + k/128) 2^(e-d) below that, d = 0..depth-1, with both signs; rows are
     zero-padded to a common length that is a multiple of 16."""
     rows = []
     for e in amax_exps:
         for m in range(128):
             amax = (1 + m / 128) * 2.0 ** e
-            vals = [amax] + [(1 + k / 128) * 2.0 ** (e - d) for d in range(25) for k in range(128)]
+            vals = [amax] + [(1 + k / 128) * 2.0 ** (e - d) for d in range(depth) for k in range(128)]
             vals = [v for v in vals if v <= amax]
             rows.append(vals + [-v for v in vals])
     C = (max(len(r) for r in rows) + 15) // 16 * 16

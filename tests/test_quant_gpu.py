@@ -77,6 +77,16 @@ def test_quantize_every_reachable_significand_pair(q_type, mode):
 
 
 @pytest.mark.parametrize("q_type", [0, 1])
+def test_quantize_edges_of_the_reciprocal_path(q_type):
+    _need_gpu()
+    # row maxima whose scales sit just inside and just outside the range the
+    # reciprocal path takes ([2^-80, 2^100)), with values 60 binades below
+    # the maximum, where that path's residual leaves the normal range
+    x = bf16_significand_rows((-72, -71, -70, 107, 108), depth=60)
+    quantize_and_compare(x, 1, q_type)
+
+
+@pytest.mark.parametrize("q_type", [0, 1])
 def test_quantize_degenerate_rows(q_type):
     _need_gpu()
     x = bf16_special_rows(64)
