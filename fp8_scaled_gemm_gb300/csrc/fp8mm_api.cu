@@ -711,8 +711,7 @@ int quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, vo
     p.total = R * (C / 8);
     p.q_type = q_type;
     if (scale_mode == FP8MM_SCALE_TENSOR) {
-        // amax: half of what the SMs hold at once streams best (a pure read);
-        // convert: one full wave
+        // one wave of each kernel: at most what the SMs hold at once
         static int occ_amax[kMaxDevices] = {}, occ_conv[kMaxDevices] = {};
         int dev = 0;
         cudaGetDevice(&dev);
@@ -726,8 +725,7 @@ int quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, vo
         p.keep = std::min<int64_t>(p.total, (int64_t(64) << 20) / 16);
         const int g1 = static_cast<int>(std::max<int64_t>(
             1, std::min<int64_t>({cdiv(p.total, fp8q::kThreads * fp8q::kUnroll),
-                                  static_cast<int64_t>(d.sms) * std::max(1, occ_amax[dev] / 2),
-                                  fp8q::kMaxPartials})));
+                                  static_cast<int64_t>(d.sms) * occ_amax[dev], fp8q::kMaxPartials})));
         int rc = launch_pdl(fp8q::quant_amax_kernel, g1, fp8q::kThreads, 0, stream, "amax launch", p);
         if (rc != FP8MM_OK)
             return rc;
