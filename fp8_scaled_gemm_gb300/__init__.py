@@ -52,7 +52,7 @@ STATUS = {
 # Every symbol include/fp8mm.h declares.
 EXPORTS = (
     "fp8_scaled_mm", "fp8_scaled_mm_config", "fp8_scaled_mm_ex", "fp8_scaled_mm_host",
-    "fp8_scaled_mm_noalloc", "fp8_quantize", "fp8_scaled_mm_bf16",
+    "fp8_scaled_mm_noalloc", "fp8_quantize", "fp8_scaled_mm_bf16", "fp8_scaled_bmm",
     "fp8mm_reserve_workspace", "fp8mm_device_status", "fp8mm_status_string",
     "fp8mm_last_error", "fp8mm_describe_choice", "fp8mm_debug_inject",
 )
@@ -98,6 +98,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fp8_scaled_mm_host.restype = i32
         lib.fp8_scaled_mm_noalloc.argtypes = common
         lib.fp8_scaled_mm_noalloc.restype = i32
+        lib.fp8_scaled_bmm.argtypes = [vp, vp, vp, vp, i32, vp, vp, i64, i64, i64, i64, vp,
+                                       ctypes.POINTER(Options)]
+        lib.fp8_scaled_bmm.restype = i32
         lib.fp8_quantize.argtypes = [vp, i64, i64, i32, i32, vp, vp, vp]
         lib.fp8_quantize.restype = i32
         lib.fp8_scaled_mm_bf16.argtypes = [vp, vp, i32, vp, vp, i64, i64, i64, vp, vp, vp, vp, vp,
@@ -206,6 +209,46 @@ def fp8_scaled_mm_ex(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=Non
     _check(load().fp8_scaled_mm_ex(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), scale_mode,
                                    _ptr(bias), _ptr(out), M, N, K, _stream_handle(stream),
                                    ctypes.byref(opt)))
+    return out
+
+
+def fp8_scaled_bmm(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=None, stream=None,
+                   out_dtype=torch.bfloat16, variant: int = VARIANT_AUTO, tile_n: int = 0, split_k: int = 0):
+    """Batched scaled matmul: out[b] = A[b] . B[b] * scale + bias for every b.
+
+    A is [batch, M, K] contiguous; B is [batch, K, N] with every item
+    column-major (``B.transpose(1, 2)`` contiguous); scale_a is [batch] or
+    [batch, M], scale_b [batch] or [batch, N]; bias [N] is shared; out is
+    [batch, M, N]. Element types as for fp8_scaled_mm_ex.
+    """
+    if A.dim() != 3 or B.dim() != 3 or A.shape[0] != B.shape[0] or A.shape[2] != B.shape[1]:
+        raise ValueError("A must be [batch, M, K] and B [batch, K, N]")
+    nb, M, K = A.shape
+    N = B.shape[2]
+    if out is None:
+        out = torch.empty((nb, M, N), dtype=out_dtype, device=A.device)
+    if A.dtype not in _FP8 or B.dtype not in _FP8:
+        raise ValueError("A and B must be torch.float8_e4m3fn or float8_e5m2")
+    if not A.is_contiguous():
+        raise ValueError("A must be contiguous [batch, M, K]")
+    if not B.transpose(1, 2).is_contiguous():
+        raise ValueError("every item of B must be column-major (B.transpose(1, 2) contiguous)")
+    if scale_mode not in (SCALE_TENSOR, SCALE_ROWWISE):
+        raise ValueError("scale_mode must be 0 (per-tensor) or 1 (row-wise)")
+    for name, s, n in (("scale_a", scale_a, nb * (1 if scale_mode == SCALE_TENSOR else M)),
+                       ("scale_b", scale_b, nb * (1 if scale_mode == SCALE_TENSOR else N))):
+        if s.dtype != torch.float32 or s.numel() != n or not s.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 tensor of {n} values")
+    if out.dtype not in _OUT or tuple(out.shape) != (nb, M, N) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [batch, M, N] bfloat16 or float16 tensor")
+    if bias is not None and (bias.dtype != out.dtype or bias.numel() != N or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous tensor of N values with out's dtype")
+    for t in [A, B, scale_a, scale_b, out] + ([bias] if bias is not None else []):
+        if not t.is_cuda:
+            raise ValueError("fp8_scaled_bmm takes CUDA tensors")
+    opt = Options(_FP8[A.dtype], _FP8[B.dtype], _OUT[out.dtype], int(variant), int(tile_n), int(split_k))
+    _check(load().fp8_scaled_bmm(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), scale_mode, _ptr(bias),
+                                 _ptr(out), nb, M, N, K, _stream_handle(stream), ctypes.byref(opt)))
     return out
 
 

@@ -161,15 +161,18 @@ int grow_workspace(DeviceState &d, size_t ws_bytes, size_t counters)
     return FP8MM_OK;
 }
 
-// 2-D e4m3 tensor [rows, K] (K contiguous) read in boxes of
-// [box_rows, 128] with 128-byte swizzling; out-of-range elements read as 0.
-int encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t K, int box_rows)
+// 3-D fp8 tensor [batch, rows, K] (K contiguous, items back to back) read in
+// boxes of [1, box_rows, 128] with 128-byte swizzling; out-of-range elements
+// (rows or K beyond the item's extent) read as 0.
+int encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t K, int box_rows,
+                       int64_t batch = 1)
 {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(fp8mm::kBlockK), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides,
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(K) * static_cast<cuuint64_t>(rows)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(fp8mm::kBlockK), static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -182,15 +185,15 @@ int encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t
     return FP8MM_OK;
 }
 
-// bf16 output [M, N] (N contiguous) written in boxes of 32 rows x 64 columns
-// from a 128-byte-swizzled shared-memory stage.
-int encode_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N, bool f16)
+// 16-bit output [batch, M, N] (N contiguous) written in boxes of 32 rows x
+// 64 columns of one item from a 128-byte-swizzled shared-memory stage.
+int encode_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N, bool f16, int64_t batch = 1)
 {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
-    cuuint32_t box[2] = {64, 32};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out,
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(N) * 2 * static_cast<cuuint64_t>(M)};
+    cuuint32_t box[3] = {64, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out,
                           dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -353,7 +356,7 @@ int max_active_clusters(int tile_n, int cs)
 
 int swap_tile_for(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
 
-Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n, int split)
+Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n, int split, int64_t batch = 1)
 {
     Choice c{};
     c.kblocks = static_cast<int>(cdiv(K, fp8mm::kBlockK));
@@ -365,7 +368,7 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
             // blocks of one tile = waves x (K blocks per CTA + reduction).
             variant = FP8MM_VARIANT_SWAP;
             tile_n = swap_tile_for(M);
-            const int64_t tiles = cdiv(N, fp8mm::kTileP) * cdiv(M, tile_n);
+            const int64_t tiles = cdiv(N, fp8mm::kTileP) * cdiv(M, tile_n) * batch;
             const int64_t kb = cdiv(K, fp8mm::kBlockK);
             double best = static_cast<double>(cdiv(tiles, sms) * kb);
             const double red = tile_n <= 32 ? 2.0 : tile_n <= 64 ? 3.0 : 4.0;
@@ -390,19 +393,19 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
             // fixed per-launch costs. It stays available as an explicit choice.)
             if (variant == FP8MM_VARIANT_SWAP)
                 split = 1;
-        } else if (K <= 1024 && cdiv(M, 128) * cdiv(N, 256) >= sms) {
+        } else if (K <= 1024 && cdiv(M, 128) * cdiv(N, 256) * batch >= sms) {
             // shallow K: the epilogue dominates; the 1-SM kernel with two
             // stage buffers per epilogue warp measured 7-15 % faster
             variant = FP8MM_VARIANT_TILE;
             tile_n = 256;
-        } else if (cdiv(M, 256) * cdiv(N, 256) >= sms / 4) {
+        } else if (cdiv(M, 256) * cdiv(N, 256) * batch >= sms / 4) {
             // enough 256 x 256 pair tiles to keep most SM pairs busy
             variant = FP8MM_VARIANT_PAIR;
             tile_n = 256;
         } else {
             variant = FP8MM_VARIANT_TILE;
             tile_n = 256;
-            if (cdiv(M, 128) * cdiv(N, 256) < sms)
+            if (cdiv(M, 128) * cdiv(N, 256) * batch < sms)
                 tile_n = 128;
         }
     }
@@ -418,7 +421,7 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
         while (split > 2 && c.kblocks < split)
             split /= 2;
         c.split = split;    // cluster size: K slices per tile
-        c.units = c.tiles_p * c.tiles_q;
+        c.units = static_cast<int>(static_cast<int64_t>(c.tiles_p) * c.tiles_q * batch);
         c.grid = c.units * split;
         return c;
     }
@@ -426,7 +429,7 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
         c.tiles_p = static_cast<int>(cdiv(N, 256));
         c.tiles_q = static_cast<int>(cdiv(M, tile_n));
         c.split = 1;
-        c.units = c.tiles_p * c.tiles_q;
+        c.units = static_cast<int>(static_cast<int64_t>(c.tiles_p) * c.tiles_q * batch);
         c.grid = 2 * static_cast<int>(std::min<int64_t>(c.units, sms / 2));
         return c;
     }
@@ -434,7 +437,7 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
         c.tiles_p = static_cast<int>(cdiv(M, 256));
         c.tiles_q = static_cast<int>(cdiv(N, tile_n));
         c.split = 1;
-        c.units = c.tiles_p * c.tiles_q;
+        c.units = static_cast<int>(static_cast<int64_t>(c.tiles_p) * c.tiles_q * batch);
         c.grid = 2 * static_cast<int>(std::min<int64_t>(c.units, sms / 2));
         return c;
     }
@@ -442,7 +445,7 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
     const int64_t qrow = variant == FP8MM_VARIANT_TILE ? N : M;
     c.tiles_p = static_cast<int>(cdiv(prow, fp8mm::kTileP));
     c.tiles_q = static_cast<int>(cdiv(qrow, tile_n));
-    const int64_t tiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q;
+    const int64_t tiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q * batch;
     if (split <= 0)
         split = pick_split(tiles, c.kblocks, sms, tile_n);
     split = std::max(1, std::min(split, c.kblocks));
@@ -542,7 +545,7 @@ int dispatch(const Choice &c, const CUtensorMap &mp, const CUtensorMap &mq, cons
 // 128-row boxes feed the MMA's A side (A, or Bt for SWAP); Q's boxes are
 // tile_n rows (half of that per CTA for PAIR).
 int encode_and_dispatch(const Choice &c, const void *A, const void *B, void *out, int64_t M, int64_t N,
-                        int64_t K, fp8mm::KernelParams kp, cudaStream_t stream)
+                        int64_t K, fp8mm::KernelParams kp, cudaStream_t stream, int64_t batch = 1)
 {
     CUtensorMap mp, mq, mo;
     std::memset(&mo, 0, sizeof mo);
@@ -553,7 +556,7 @@ int encode_and_dispatch(const Choice &c, const void *A, const void *B, void *out
     // aligned (TILE without split-K, PAIR); otherwise through plain stores.
     if (!swap && c.split == 1 && (N % 8) == 0 &&
         (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
-        int rc = encode_out_map(&mo, out, M, N, kp.out_f16 != 0);
+        int rc = encode_out_map(&mo, out, M, N, kp.out_f16 != 0, batch);
         if (rc != FP8MM_OK)
             return rc;
         kp.out_tma = 1;
@@ -561,10 +564,10 @@ int encode_and_dispatch(const Choice &c, const void *A, const void *B, void *out
     const bool pair = c.variant == FP8MM_VARIANT_PAIR || c.variant == FP8MM_VARIANT_SWAPPAIR;
     const int q_box = pair ? c.tile_n / 2 : c.tile_n;
     // B column-major [K, N] is Bt[N, K] row-major.
-    int rc = encode_operand_map(&mp, swap ? B : A, swap ? N : M, K, fp8mm::kTileP);
+    int rc = encode_operand_map(&mp, swap ? B : A, swap ? N : M, K, fp8mm::kTileP, batch);
     if (rc != FP8MM_OK)
         return rc;
-    rc = encode_operand_map(&mq, swap ? A : B, swap ? M : N, K, q_box);
+    rc = encode_operand_map(&mq, swap ? A : B, swap ? M : N, K, q_box, batch);
     if (rc != FP8MM_OK)
         return rc;
     return dispatch(c, mp, mq, mo, kp, stream);
@@ -596,7 +599,8 @@ uint32_t fmt_code(int t) { return t == FP8MM_TYPE_E5M2 ? 1u : 0u; }
 
 int run(const void *A, const void *B, const float *sa, const float *sb, int scale_mode, const void *bias,
         void *out, int64_t M, int64_t N, int64_t K, cudaStream_t stream, int variant, int tile_n, int split,
-        int a_type = FP8MM_TYPE_E4M3, int b_type = FP8MM_TYPE_E4M3, int out_type = FP8MM_OUT_BF16)
+        int a_type = FP8MM_TYPE_E4M3, int b_type = FP8MM_TYPE_E4M3, int out_type = FP8MM_OUT_BF16,
+        int64_t batch = 1)
 {
     int rc = check_args(A, B, sa, sb, scale_mode, bias, out, M, N, K);
     if (rc != FP8MM_OK)
@@ -618,14 +622,19 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
         (b_type != FP8MM_TYPE_E4M3 && b_type != FP8MM_TYPE_E5M2) ||
         (out_type != FP8MM_OUT_BF16 && out_type != FP8MM_OUT_F16))
         return FP8MM_ERR_MODE;
-    if (M == 0 || N == 0)
+    if (batch < 0)
+        return FP8MM_ERR_SHAPE;
+    if (M == 0 || N == 0 || batch == 0)
         return FP8MM_OK;
+    // work units (tiles x K slices of the whole batch) are counted in int
+    if (batch * cdiv(M, 16) * cdiv(N, 128) * 16 > INT32_MAX)
+        return FP8MM_ERR_SHAPE;
     DeviceState *d = nullptr;
     rc = device_state(&d);
     if (rc != FP8MM_OK)
         return rc;
 
-    const Choice c = choose(M, N, K, d->sms, variant, tile_n, split);
+    const Choice c = choose(M, N, K, d->sms, variant, tile_n, split, batch);
     fp8mm::KernelParams kp{};
     kp.scale_a = sa;
     kp.scale_b = sb;
@@ -647,6 +656,7 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     kp.tiles_q = c.tiles_q;
     kp.splits = c.split;
     kp.kblocks = c.kblocks;
+    kp.batch = static_cast<int>(batch);
     kp.num_units = c.units;
     kp.rowwise = scale_mode == FP8MM_SCALE_ROWWISE ? 1 : 0;
     kp.group = 8;
@@ -654,7 +664,7 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     kp.timeout_cycles = wait_limit();
     kp.inject_stop_after = static_cast<int>(g_inject_stop_after.load());
     if (c.split > 1 && c.variant != FP8MM_VARIANT_SWAPK) {
-        const int64_t tiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q;
+        const int64_t tiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q * batch;
         const size_t ws = static_cast<size_t>(tiles) * c.split * fp8mm::kTileP * c.tile_n * sizeof(float);
         rc = grow_workspace(*d, ws, static_cast<size_t>(tiles) * fp8mm::kCountersPerTile);
         if (rc != FP8MM_OK)
@@ -663,7 +673,7 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
         kp.counters = d->counters;
     }
 
-    return encode_and_dispatch(c, A, B, out, M, N, K, kp, stream);
+    return encode_and_dispatch(c, A, B, out, M, N, K, kp, stream, batch);
 }
 
 // ------------------------------------------------------ quantisation ---
@@ -886,6 +896,21 @@ int fp8_scaled_mm_bf16(const void *A, const void *B, int scale_mode, const void 
         return rc;
     return run(A_q, B_q, scale_a, scale_b, scale_mode, bias, out, M, N, K, s, o.variant, o.tile_n, o.split_k,
                o.a_type, o.b_type, o.out_type);
+}
+
+int fp8_scaled_bmm(const void *A, const void *B, const float *scale_a, const float *scale_b, int scale_mode,
+                   const void *bias, void *out, int64_t batch, int64_t M, int64_t N, int64_t K, void *stream,
+                   const fp8mm_options *options)
+{
+    fp8mm_options o = {FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16, FP8MM_VARIANT_AUTO, 0, 0};
+    if (options)
+        o = *options;
+    if (batch < 0)
+        return FP8MM_ERR_SHAPE;
+    // an empty batch is an empty problem: nothing is read or written, pointers may be NULL
+    return run(A, B, scale_a, scale_b, scale_mode, bias, out, batch == 0 ? 0 : M, N, K,
+               static_cast<cudaStream_t>(stream), o.variant, o.tile_n, o.split_k, o.a_type, o.b_type, o.out_type,
+               batch);
 }
 
 int fp8_scaled_mm_host(const void *A, const void *B, const float *scale_a, const float *scale_b,
@@ -1205,6 +1230,7 @@ extern "C" int fp8_scaled_mm_noalloc(const void *A, const void *B, const float *
     kp.tiles_q = c.tiles_q;
     kp.splits = c.split;
     kp.kblocks = c.kblocks;
+    kp.batch = 1;
     kp.num_units = c.units;
     kp.rowwise = scale_mode == FP8MM_SCALE_ROWWISE ? 1 : 0;
     kp.group = 8;

@@ -72,18 +72,23 @@ constexpr int kCountersPerTile = 8;
 // Device status codes (written once per launch, first writer wins).
 constexpr int kStatusTimeoutBase = 0x100;
 
+// A batch of `batch` independent problems of one shape: operand tensor maps
+// are 3-D ({K, rows, batch}); item b has its own scales (scale_a + b, or
+// + b M row-wise; likewise scale_b) and output (out + b M N); the bias is
+// shared by every item.
 struct KernelParams {
-    const float *scale_a;           // 1 or M values
-    const float *scale_b;           // 1 or N values
+    const float *scale_a;           // batch x (1 or M) values
+    const float *scale_b;           // batch x (1 or N) values
     const unsigned short *bias;     // N values (output type) or nullptr
-    unsigned short *out;            // [M, N] row-major, bf16 or fp16 bit patterns
+    unsigned short *out;            // [batch, M, N] row-major, bf16 or fp16 bit patterns
     float *ws;                      // split-K partial tiles (splits > 1)
     unsigned int *counters;         // split-K arrivals, kCountersPerTile per output tile
     int *status;                    // device status word
     int M, N, K;
     int tiles_p, tiles_q;           // ceil(P rows / 128), ceil(Q rows / BN)
     int splits, kblocks;            // K slices per tile, ceil(K / 128)
-    int num_units;                  // tiles_p * tiles_q * splits
+    int batch;                      // problems in the batch (1: a single matrix product)
+    int num_units;                  // batch * tiles_p * tiles_q * splits
     int rowwise;                    // 0 per-tensor, 1 row-wise scales
     int group;                      // P tiles per rasterisation group
     int vec_store;                  // 16-byte output stores allowed (TILE)
@@ -182,7 +187,7 @@ struct Waiter {
 };
 
 struct Unit {
-    int tp, tq, split, tile, kb0, kb1;
+    int b, tp, tq, split, tile, kb0, kb1;   // tile: index over the whole batch (workspace, counters)
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const KernelParams &p)
@@ -190,16 +195,34 @@ __device__ __forceinline__ Unit decode_unit(int u, const KernelParams &p)
     Unit w;
     w.split = u % p.splits;
     w.tile = u / p.splits;
+    const int per_item = p.tiles_p * p.tiles_q;
+    w.b = w.tile / per_item;
+    const int t = w.tile - w.b * per_item;
     const int in_group = p.group * p.tiles_q;
-    const int gid = w.tile / in_group;
+    const int gid = t / in_group;
     const int first_p = gid * p.group;
     const int gsize = min(p.tiles_p - first_p, p.group);
-    const int r = w.tile % in_group;
+    const int r = t % in_group;
     w.tp = first_p + r % gsize;
     w.tq = r / gsize;
     w.kb0 = static_cast<int>((static_cast<long long>(w.split) * p.kblocks) / p.splits);
     w.kb1 = static_cast<int>((static_cast<long long>(w.split + 1) * p.kblocks) / p.splits);
     return w;
+}
+
+// The parameters of batch item b: its scales and its output matrix.
+__device__ __forceinline__ KernelParams for_item(const KernelParams &p, int b)
+{
+    KernelParams q = p;
+    q.scale_a += p.rowwise ? static_cast<size_t>(b) * p.M : static_cast<size_t>(b);
+    q.scale_b += p.rowwise ? static_cast<size_t>(b) * p.N : static_cast<size_t>(b);
+    q.out += static_cast<size_t>(b) * p.M * p.N;
+    return q;
+}
+
+__device__ __forceinline__ float tensor_scale(const KernelParams &q)
+{
+    return q.rowwise ? 0.0f : __ldg(q.scale_a) * __ldg(q.scale_b);
 }
 
 // Output conversions (round to nearest even) for bf16 or fp16.
@@ -303,7 +326,7 @@ template <int BN, int NBUF>
 __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, const CUtensorMap *tmap_out,
                                                      uint32_t trow, int m_row0, int n0, int lane,
                                                      uint8_t *stage, uint32_t stage_smem, uint32_t &chunks,
-                                                     float s_tensor)
+                                                     float s_tensor, int item)
 {
     constexpr unsigned kAll = 0xffffffffu;
     const int m = m_row0 + lane;
@@ -353,7 +376,7 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                ptx::tma_store_2d(tmap_out, stage_smem + buf * 4096u, nb, m_row0);
+                ptx::tma_store_3d(tmap_out, stage_smem + buf * 4096u, nb, m_row0, item);
                 ptx::bulk_commit_group();
             }
         } else {
@@ -474,9 +497,9 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
                     }
                     const uint32_t sp = sbase + stage * C::kStageBytes;
                     ptx::mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
-                    ptx::tma_load_2d(sp, &tmap_p, full_bar(stage), kb * kBlockK, w.tp * kTileP);
-                    ptx::tma_load_2d(sp + C::kPBytes, &tmap_q, full_bar(stage), kb * kBlockK,
-                                     w.tq * BN);
+                    ptx::tma_load_3d(sp, &tmap_p, full_bar(stage), kb * kBlockK, w.tp * kTileP, w.b);
+                    ptx::tma_load_3d(sp + C::kPBytes, &tmap_q, full_bar(stage), kb * kBlockK,
+                                     w.tq * BN, w.b);
                     ++issued;
                     if (++stage == S) {
                         stage = 0;
@@ -549,7 +572,6 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
         // ---------------------------------------------------- epilogue ---
         const int q = warp & 3;             // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;      // row within the 128-row P tile
-        const float s_tensor = p.rowwise ? 0.0f : __ldg(p.scale_a) * __ldg(p.scale_b);
         const int ew = warp - 2;            // epilogue warp index: its stage buffer
         const int col0 = (ew / 4) * kWarpCols;  // this warp's first column of the tile
         uint8_t *stage = smem + (staging0 - sbase) + ew * 4096 * C::kStageBufs;
@@ -559,6 +581,8 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
             const Unit w = decode_unit(u, p);
+            const KernelParams pb = for_item(p, w.b);
+            const float s_tensor = tensor_scale(pb);
             if (!W.wait(tfull_bar(acc), acc_phase, 5))
                 break;
             ptx::tc_fence_after();
@@ -567,15 +591,15 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
             const int pidx = w.tp * kTileP + row;
             if (p.splits == 1) {
                 if constexpr (!SWAP) {
-                    epilogue_rows_staged<kWarpCols, C::kStageBufs>(p, &tmap_out, trow + col0, w.tp * kTileP + q * 32,
+                    epilogue_rows_staged<kWarpCols, C::kStageBufs>(pb, &tmap_out, trow + col0, w.tp * kTileP + q * 32,
                                                     w.tq * BN + col0, lane, stage, stage_smem, chunks,
-                                                    s_tensor);
+                                                    s_tensor, w.b);
                 } else {
 #pragma unroll 1
                     for (int c = 0; c < BN / CH; ++c) {
                         float v[CH];
                         tmem_load_chunk<CH>(trow + c * CH, v);
-                        store_chunk<CH, SWAP>(p, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
+                        store_chunk<CH, SWAP>(pb, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
                     }
                 }
                 ptx::tc_fence_before();
@@ -617,7 +641,7 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
                             for (int j = 0; j < CH; ++j)
                                 v[j] += __ldcg(part + static_cast<size_t>(c * CH + j) * kTileP + row);
                         }
-                        store_chunk<CH, SWAP>(p, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
+                        store_chunk<CH, SWAP>(pb, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
                     }
                 }
             }

@@ -12,7 +12,7 @@
 // in slice order 0..CS-1 (reading its peers' shared memory with
 // ld.shared::cluster), applies scale and bias, rounds to bf16 and stores.
 // A second cluster barrier keeps every CTA alive until its peers have read
-// its partial. There is no global workspace, no atomic and no memory fence,
+// its partial. With a batch, cluster c / (tiles_p tiles_q) picks the item. There is no global workspace, no atomic and no memory fence,
 // and the result does not depend on timing.
 //
 // One tile per cluster (no persistence): every thread executes exactly two
@@ -67,7 +67,9 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rank = static_cast<int>(ptx::cluster_ctarank());
-    const int tile = static_cast<int>(blockIdx.x) / CS;
+    const int tile_g = static_cast<int>(blockIdx.x) / CS;     // over the whole batch
+    const int item = tile_g / (p.tiles_p * p.tiles_q);
+    const int tile = tile_g - item * (p.tiles_p * p.tiles_q);
     const int tp = tile % p.tiles_p;
     const int tq = tile / p.tiles_p;
     const int kb0 = static_cast<int>((static_cast<long long>(rank) * p.kblocks) / CS);
@@ -112,8 +114,8 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 const uint32_t sp = sbase + stage * C::kStageBytes;
                 ptx::mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
-                ptx::tma_load_2d(sp, &tmap_p, full_bar(stage), kb * kBlockK, tp * kTileP);
-                ptx::tma_load_2d(sp + C::kPBytes, &tmap_q, full_bar(stage), kb * kBlockK, tq * BN);
+                ptx::tma_load_3d(sp, &tmap_p, full_bar(stage), kb * kBlockK, tp * kTileP, item);
+                ptx::tma_load_3d(sp + C::kPBytes, &tmap_q, full_bar(stage), kb * kBlockK, tq * BN, item);
                 ++issued;
                 if (++stage == S) {
                     stage = 0;
@@ -193,15 +195,16 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (warp >= 2 && !*abort_flag) {
         // ------------------------- reduce rows [rank * 128/CS, +128/CS) ---
+        const KernelParams pb = for_item(p, item);
         constexpr int kRows = kTileP / CS;
         constexpr int kColStep = 128 / kRows;               // = CS
         const int t = threadIdx.x - 64;                     // 0..127
         const int r = rank * kRows + t % kRows;             // row of the tile (a column n of out)
         const int n = tp * kTileP + r;
         const bool n_in = n < p.N;
-        const float sb = (p.rowwise && n_in) ? __ldg(p.scale_b + n) : 0.0f;
-        const float b = (p.bias != nullptr && n_in) ? bias_value(p, n) : 0.0f;
-        const float s_tensor = p.rowwise ? 0.0f : __ldg(p.scale_a) * __ldg(p.scale_b);
+        const float sb = (pb.rowwise && n_in) ? __ldg(pb.scale_b + n) : 0.0f;
+        const float b = (pb.bias != nullptr && n_in) ? bias_value(pb, n) : 0.0f;
+        const float s_tensor = tensor_scale(pb);
         const uint32_t local0 = ptx::smem_addr(partial);
         // columns t / kRows, + CS, + 2 CS, ...: kItems per thread, processed
         // kBatch at a time so that kBatch x CS remote loads are in flight
@@ -229,8 +232,8 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
                     acc += part[i][s];
                 const int m = tq * BN + col0 + (i0 + i) * kColStep;
                 if (n_in && m < p.M) {
-                    const float sc = p.rowwise ? __ldg(p.scale_a + m) * sb : s_tensor;
-                    p.out[static_cast<size_t>(m) * p.N + n] = to_out(fmaf(acc, sc, b), p.out_f16);
+                    const float sc = pb.rowwise ? __ldg(pb.scale_a + m) * sb : s_tensor;
+                    pb.out[static_cast<size_t>(m) * pb.N + n] = to_out(fmaf(acc, sc, b), pb.out_f16);
                 }
             }
         }

@@ -134,10 +134,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
                     const uint32_t leader_full = ptx::mapa_shared(full_bar(stage), 0);
                     if (rank == 0)
                         ptx::mbar_arrive_expect_tx(full_bar(stage), 2u * C::kStageBytes);
-                    ptx::tma_load_2d_pair(sa, &tmap_a, leader_full, kb * kBlockK,
-                                          w.tp * 256 + static_cast<int>(rank) * 128);
-                    ptx::tma_load_2d_pair(sa + C::kABytes, &tmap_b, leader_full, kb * kBlockK,
-                                          w.tq * BN + static_cast<int>(rank) * (BN / 2));
+                    ptx::tma_load_3d_pair(sa, &tmap_a, leader_full, kb * kBlockK,
+                                          w.tp * 256 + static_cast<int>(rank) * 128, w.b);
+                    ptx::tma_load_3d_pair(sa + C::kABytes, &tmap_b, leader_full, kb * kBlockK,
+                                          w.tq * BN + static_cast<int>(rank) * (BN / 2), w.b);
                     ++issued;
                     if (++stage == S) {
                         stage = 0;
@@ -213,7 +213,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
     } else {
         // ---------------------------------------------------- epilogue ---
         const int q = warp & 3;
-        const float s_tensor = p.rowwise ? 0.0f : __ldg(p.scale_a) * __ldg(p.scale_b);
         const int ew = warp - 2;
         const int col0 = (ew / 4) * kWarpCols;
         uint8_t *stage = smem + (staging0 - sbase) + ew * 4096;
@@ -223,22 +222,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
         uint32_t acc_phase = 0;
         for (int u = cluster_id; u < p.num_units; u += num_clusters) {
             const Unit w = decode_unit(u, p);
+            const KernelParams pb = for_item(p, w.b);
+            const float s_tensor = tensor_scale(pb);
             if (!W.wait(tfull_bar(acc), acc_phase, 5))
                 break;
             ptx::tc_fence_after();
             const uint32_t trow =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             if constexpr (!SWAP) {
-                epilogue_rows_staged<kWarpCols, 1>(p, &tmap_out, trow + col0,
+                epilogue_rows_staged<kWarpCols, 1>(pb, &tmap_out, trow + col0,
                                                 w.tp * 256 + static_cast<int>(rank) * 128 + q * 32,
-                                                w.tq * BN + col0, lane, stage, stage_smem, chunks, s_tensor);
+                                                w.tq * BN + col0, lane, stage, stage_smem, chunks, s_tensor,
+                                                w.b);
             } else {
                 const int pidx = w.tp * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
 #pragma unroll 1
                 for (int c = 0; c < BN / CH; ++c) {
                     float v[CH];
                     tmem_load_chunk<CH>(trow + c * CH, v);
-                    store_chunk<CH, true>(p, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
+                    store_chunk<CH, true>(pb, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
                 }
             }
             ptx::tc_fence_before();

@@ -174,6 +174,36 @@ int fp8_scaled_mm_host(const void *A, const void *B,
                        void *stream);
 
 /*
+ * Batched form: `batch` independent products of one shape,
+ *
+ *   out[b] = cast( (A[b] . B[b]) * (scale_a[b] (x) scale_b[b]) + bias )
+ *
+ * for b < batch, in one launch (the operands are read through 3-D TMA
+ * tensor maps [batch, rows, K]). The pages name this case as the one that
+ * 2-D-only TMA descriptors block (PyTorch PR #142101, "Additional notes",
+ * the note on torch.bmm); each item follows fp8_scaled_mm exactly.
+ *
+ *   A        fp8 [batch, M, K]: items back to back, each row-major.
+ *   B        fp8 [batch, K, N] with every item column-major, i.e. the bytes
+ *            of Bt [batch, N, K] row-major.
+ *   scale_a  fp32: batch values (FP8MM_SCALE_TENSOR, one per item) or
+ *            batch * M values (ROWWISE, item b's at b * M).
+ *   scale_b  fp32: batch or batch * N values, likewise.
+ *   bias     [N] of the output type shared by every item, or NULL.
+ *   out      [batch, M, N], items back to back, each row-major.
+ *   options  element types and kernel choice as for fp8_scaled_mm_ex; NULL
+ *            for e4m3 operands, bf16 output, automatic choice.
+ *
+ * Constraints as fp8_scaled_mm, plus batch >= 0 (0 is a no-op) and
+ * batch * ceil(M/16) * ceil(N/128) * 16 < 2^31 (FP8MM_ERR_SHAPE otherwise).
+ */
+int fp8_scaled_bmm(const void *A, const void *B,
+                   const float *scale_a, const float *scale_b, int scale_mode,
+                   const void *bias, void *out,
+                   int64_t batch, int64_t M, int64_t N, int64_t K,
+                   void *stream, const fp8mm_options *options);
+
+/*
  * Quantise bf16 data to fp8 codes with fp32 scales: the step that makes the
  * operands of fp8_scaled_mm (gist "matmul_fp8.py", `get_scale` and
  * `benchmark()`):

@@ -186,3 +186,16 @@ def test_python_quantize_validation():
         fm.fp8_quantize(torch.zeros(4, 12, dtype=torch.bfloat16), 0)
     with pytest.raises(ValueError, match="bfloat16"):
         fm.fp8_quantize(x.float(), 0)
+
+
+def test_bmm_argument_errors(lib):
+    def bmm(batch=2, M=64, N=64, K=64, opt=None, A=ALIGNED):
+        return lib.fp8_scaled_bmm(P(A) if A else None, P(ALIGNED), P(ALIGNED), P(ALIGNED), 0, None, P(ALIGNED),
+                                  batch, M, N, K, None, ctypes.byref(opt) if opt is not None else None)
+    assert bmm(batch=-1) == -2
+    assert bmm(batch=0, A=0) == 0                  # empty batch: no-op before the pointer checks
+    assert bmm(batch=2 ** 30, M=4096, N=4096) == -2  # work units would overflow
+    assert bmm(K=24) == -2
+    assert bmm(A=0) == -1
+    assert bmm(opt=fm.Options(0, 5, 0, 0, 0, 0)) == -4
+    assert bmm(opt=fm.Options(0, 0, 0, 9, 0, 0)) == -4
