@@ -57,8 +57,9 @@ def parse_args(argv=None):
                     help="time the bf16 -> fp8 quantisation step instead (one JSON line per shape; "
                          "--shapes takes RxC[:mode[:e4m3|e5m2]])")
     ap.add_argument("--shapes", default="",
-                    help="with --sweep: comma list of MxNxK[:mode[:bias[:a_dtype:b_dtype:out_dtype]]] "
-                         "(default: all benchmark shapes; dtypes e4m3|e5m2 and bf16|fp16)")
+                    help="with --sweep: comma list of [B@]MxNxK[:mode[:bias[:a_dtype:b_dtype:out_dtype]]] "
+                         "(default: all benchmark shapes; B@ = a batch of B products, fp8_scaled_bmm; "
+                         "dtypes e4m3|e5m2 and bf16|fp16)")
     return ap.parse_args(argv)
 
 
@@ -320,12 +321,12 @@ SWEEP_SHAPES = (
 )
 
 
-def algorithmic_bytes(M, N, K, mode, bias):
+def algorithmic_bytes(M, N, K, mode, bias, batch=1):
     # fp8 operands (1 byte), 16-bit output and bias, fp32 scales
-    return M * K + N * K + 2 * M * N + (4 * (M + N) if mode == 1 else 8) + (2 * N if bias else 0)
+    return batch * (M * K + N * K + 2 * M * N + (4 * (M + N) if mode == 1 else 8)) + (2 * N if bias else 0)
 
 
-def time_shape(M, N, K, mode, bias, steps, warmup, device, types=("e4m3", "e4m3", "bf16")):
+def time_shape(M, N, K, mode, bias, steps, warmup, device, types=("e4m3", "e4m3", "bf16"), batch=1):
     import torch
     import fp8_scaled_gemm_gb300 as fm
     from fp8_scaled_gemm_gb300.inputs import make_inputs
@@ -334,18 +335,28 @@ def time_shape(M, N, K, mode, bias, steps, warmup, device, types=("e4m3", "e4m3"
                       out_dtype=types[2])
     odt = torch.bfloat16 if types[2] == "bf16" else torch.float16
     typed = tuple(types) != ("e4m3", "e4m3", "bf16")
-    per_set = algorithmic_bytes(M, N, K, mode, bias)
+    per_set = algorithmic_bytes(M, N, K, mode, bias, batch)
     n_sets = max(1, min(64, -(-3 * L2_BYTES // per_set)))
     sets = []
     for _ in range(n_sets):
-        sets.append((inp.a_q.to(device), inp.bt_q.to(device).t(), inp.scale_a.to(device),
-                     inp.scale_b.to(device), None if inp.bias is None else inp.bias.to(device),
-                     torch.empty((M, N), dtype=odt, device=device)))
+        if batch == 1:
+            sets.append((inp.a_q.to(device), inp.bt_q.to(device).t(), inp.scale_a.to(device),
+                         inp.scale_b.to(device), None if inp.bias is None else inp.bias.to(device),
+                         torch.empty((M, N), dtype=odt, device=device)))
+        else:
+            # every item of the batch holds the same operands (the timing does not depend on values)
+            a = inp.a_q.to(device).unsqueeze(0).expand(batch, M, K).contiguous()
+            bt = inp.bt_q.to(device).unsqueeze(0).expand(batch, N, K).contiguous()
+            sets.append((a, bt.transpose(1, 2), inp.scale_a.to(device).repeat(batch),
+                         inp.scale_b.to(device).repeat(batch), None if inp.bias is None else inp.bias.to(device),
+                         torch.empty((batch, M, N), dtype=odt, device=device)))
     stream = torch.cuda.current_stream(device)
 
     def step(i):
         A, B, sa, sb, b, o = sets[i % n_sets]
-        if typed:
+        if batch > 1:
+            fm.fp8_scaled_bmm(A, B, sa, sb, mode, bias=b, out=o)
+        elif typed:
             fm.fp8_scaled_mm_ex(A, B, sa, sb, mode, bias=b, out=o)
         else:
             fm.fp8_scaled_mm(A, B, sa, sb, mode, bias=b, out=o)
@@ -377,7 +388,7 @@ def time_shape(M, N, K, mode, bias, steps, warmup, device, types=("e4m3", "e4m3"
         raise RuntimeError("in-kernel wait ran out: " + fm.fp8mm_last_error())
     del graph, sets
     torch.cuda.empty_cache()
-    return statistics.median(per), min(per), n_sets, fm.fp8mm_describe_choice(M, N, K, mode)
+    return statistics.median(per), min(per), n_sets, fm.fp8mm_describe_bmm_choice(batch, M, N, K, mode)
 
 
 def run_sweep(args):
@@ -389,25 +400,30 @@ def run_sweep(args):
     fm.load()
     pk = peaks()
     fp8_peak = pk["bf16_tflops"] * NOMINAL_FP8_PER_BF16
-    shapes = [s + (("e4m3", "e4m3", "bf16"),) for s in SWEEP_SHAPES]
+    shapes = [s + (("e4m3", "e4m3", "bf16"), 1) for s in SWEEP_SHAPES]
     if args.shapes:
         shapes = []
         for spec in args.shapes.split(","):
             parts = spec.split(":")
-            M, N, K = (int(x) for x in parts[0].split("x"))
+            batch = 1
+            dims = parts[0]
+            if "@" in dims:
+                b, dims = dims.split("@")
+                batch = int(b)
+            M, N, K = (int(x) for x in dims.split("x"))
             mode = int(parts[1]) if len(parts) > 1 else 1
             bias = bool(int(parts[2])) if len(parts) > 2 else False
             types = tuple(parts[3:6]) if len(parts) >= 6 else ("e4m3", "e4m3", "bf16")
-            shapes.append((M, N, K, mode, bias, types))
-    for (M, N, K, mode, bias, types) in shapes:
+            shapes.append((M, N, K, mode, bias, types, batch))
+    for (M, N, K, mode, bias, types, batch) in shapes:
         mean, best, n_sets, choice = time_shape(M, N, K, mode, bias, args.steps, args.warmup, device,
-                                                types)
-        flops = 2.0 * M * N * K
-        nbytes = algorithmic_bytes(M, N, K, mode, bias)
+                                                types, batch)
+        flops = 2.0 * M * N * K * batch
+        nbytes = algorithmic_bytes(M, N, K, mode, bias, batch)
         tflops = flops / (mean * 1e-3) / 1e12
         gbs = nbytes / (mean * 1e-3) / 1e9
         print(json.dumps({
-            "shape": [M, N, K], "scale_mode": "row-wise" if mode else "per-tensor", "bias": bias,
+            "shape": [M, N, K], "batch": batch, "scale_mode": "row-wise" if mode else "per-tensor", "bias": bias,
             "types": list(types),
             "kernel_us": round(mean * 1e3, 2), "kernel_us_best": round(best * 1e3, 2),
             "timing": f"median of 5 CUDA-graph replays of {args.steps} launches",

@@ -33,6 +33,7 @@ VARIANT_SWAPK = 4
 VARIANT_SWAPPAIR = 5
 
 TYPE_E4M3, TYPE_E5M2 = 0, 1
+MAJOR_K, MAJOR_MN = 0, 1
 OUT_BF16, OUT_F16 = 0, 1
 _FP8 = {torch.float8_e4m3fn: TYPE_E4M3, torch.float8_e5m2: TYPE_E5M2}
 _OUT = {torch.bfloat16: OUT_BF16, torch.float16: OUT_F16}
@@ -53,8 +54,9 @@ STATUS = {
 EXPORTS = (
     "fp8_scaled_mm", "fp8_scaled_mm_config", "fp8_scaled_mm_ex", "fp8_scaled_mm_host",
     "fp8_scaled_mm_noalloc", "fp8_quantize", "fp8_scaled_mm_bf16", "fp8_scaled_bmm",
+    "fp8_scaled_mm_layout",
     "fp8mm_reserve_workspace", "fp8mm_device_status", "fp8mm_status_string",
-    "fp8mm_last_error", "fp8mm_describe_choice", "fp8mm_debug_inject",
+    "fp8mm_last_error", "fp8mm_describe_choice", "fp8mm_describe_bmm_choice", "fp8mm_debug_inject",
 )
 
 _lib = None
@@ -98,6 +100,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fp8_scaled_mm_host.restype = i32
         lib.fp8_scaled_mm_noalloc.argtypes = common
         lib.fp8_scaled_mm_noalloc.restype = i32
+        lib.fp8_scaled_mm_layout.argtypes = [vp, i32, vp, i32, vp, vp, i32, vp, vp, i64, i64, i64, vp,
+                                             ctypes.POINTER(Options)]
+        lib.fp8_scaled_mm_layout.restype = i32
         lib.fp8_scaled_bmm.argtypes = [vp, vp, vp, vp, i32, vp, vp, i64, i64, i64, i64, vp,
                                        ctypes.POINTER(Options)]
         lib.fp8_scaled_bmm.restype = i32
@@ -118,6 +123,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fp8mm_debug_inject.restype = i32
         lib.fp8mm_describe_choice.argtypes = [i64, i64, i64, i32]
         lib.fp8mm_describe_choice.restype = ctypes.c_char_p
+        lib.fp8mm_describe_bmm_choice.argtypes = [i64, i64, i64, i64, i32]
+        lib.fp8mm_describe_bmm_choice.restype = ctypes.c_char_p
         _lib = lib
         return lib
 
@@ -209,6 +216,53 @@ def fp8_scaled_mm_ex(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=Non
     _check(load().fp8_scaled_mm_ex(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), scale_mode,
                                    _ptr(bias), _ptr(out), M, N, K, _stream_handle(stream),
                                    ctypes.byref(opt)))
+    return out
+
+
+def _major(t, k_stride_dim: int) -> int:
+    """MAJOR_K if the operand's K dimension (dim k_stride_dim) is contiguous,
+    MAJOR_MN if the other one is; raises otherwise."""
+    other = 1 - k_stride_dim
+    if t.stride(k_stride_dim) == 1 and t.stride(other) == t.shape[k_stride_dim]:
+        return MAJOR_K
+    if t.stride(other) == 1 and t.stride(k_stride_dim) == t.shape[other]:
+        return MAJOR_MN
+    raise ValueError("operands must be contiguous in one of their two dimensions")
+
+
+def fp8_scaled_mm_layout(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=None, stream=None,
+                         out_dtype=torch.bfloat16, variant: int = VARIANT_AUTO, tile_n: int = 0,
+                         split_k: int = 0):
+    """The operation with A [M, K] and B [K, N] in any of the four layouts
+    (each operand row- or column-major, read from its strides). An operand
+    whose K dimension is not contiguous is transposed on the GPU first."""
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError("A must be [M, K] and B [K, N]")
+    M, K = A.shape
+    N = B.shape[1]
+    a_major = _major(A, 1)
+    b_major = _major(B, 0)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    if A.dtype not in _FP8 or B.dtype not in _FP8:
+        raise ValueError("A and B must be torch.float8_e4m3fn or float8_e5m2")
+    if scale_mode not in (SCALE_TENSOR, SCALE_ROWWISE):
+        raise ValueError("scale_mode must be 0 (per-tensor) or 1 (row-wise)")
+    for name, s, n in (("scale_a", scale_a, 1 if scale_mode == SCALE_TENSOR else M),
+                       ("scale_b", scale_b, 1 if scale_mode == SCALE_TENSOR else N)):
+        if s.dtype != torch.float32 or s.numel() != n or not s.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 tensor of {n} values")
+    if out.dtype not in _OUT or tuple(out.shape) != (M, N) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, N] bfloat16 or float16 tensor")
+    if bias is not None and (bias.dtype != out.dtype or bias.numel() != N or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous tensor of N values with out's dtype")
+    for t in [A, B, scale_a, scale_b, out] + ([bias] if bias is not None else []):
+        if not t.is_cuda:
+            raise ValueError("fp8_scaled_mm_layout takes CUDA tensors")
+    opt = Options(_FP8[A.dtype], _FP8[B.dtype], _OUT[out.dtype], int(variant), int(tile_n), int(split_k))
+    _check(load().fp8_scaled_mm_layout(_ptr(A), a_major, _ptr(B), b_major, _ptr(scale_a), _ptr(scale_b),
+                                       scale_mode, _ptr(bias), _ptr(out), M, N, K, _stream_handle(stream),
+                                       ctypes.byref(opt)))
     return out
 
 
@@ -372,3 +426,7 @@ def fp8mm_debug_inject(stop_after_kblocks: int = -1, wait_limit_cycles: int = 0)
 
 def fp8mm_describe_choice(M: int, N: int, K: int, scale_mode: int = SCALE_TENSOR) -> str:
     return load().fp8mm_describe_choice(int(M), int(N), int(K), int(scale_mode)).decode()
+
+
+def fp8mm_describe_bmm_choice(batch: int, M: int, N: int, K: int, scale_mode: int = SCALE_TENSOR) -> str:
+    return load().fp8mm_describe_bmm_choice(int(batch), int(M), int(N), int(K), int(scale_mode)).decode()

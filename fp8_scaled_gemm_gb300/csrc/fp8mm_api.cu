@@ -19,6 +19,7 @@
 #include "fp8mm_kernel_pair.cuh"
 #include "fp8mm_kernel_ck.cuh"
 #include "fp8mm_quant.cuh"
+#include "fp8mm_transpose.cuh"
 
 namespace {
 
@@ -50,8 +51,8 @@ struct DeviceState {
     size_t ws_bytes = 0;
     unsigned int *counters = nullptr;    // split-K arrivals
     size_t counter_count = 0;
-    void *stage[6] = {};                 // host entry point staging buffers
-    size_t stage_bytes[6] = {};
+    void *stage[8] = {};                 // staging: host entry point [0..5], K-major operand copies [6..7]
+    size_t stage_bytes[8] = {};
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -772,6 +773,24 @@ int quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, vo
     return launch_pdl(fp8q::quant_rows_long_kernel, grid, fp8q::kThreads, 0, stream, "quantisation launch", p);
 }
 
+// ------------------------------------------------------- transposition ---
+
+// Enqueues out[C, R] = in[R, C]^T (bytes).
+int transpose_bytes(const void *in, void *out, int64_t R, int64_t C, cudaStream_t stream, int sms)
+{
+    fp8t::TransposeParams tp{};
+    tp.in = static_cast<const uint8_t *>(in);
+    tp.out = static_cast<uint8_t *>(out);
+    tp.R = R;
+    tp.C = C;
+    tp.tiles_r = cdiv(R, fp8t::kTile);
+    tp.tiles_c = cdiv(C, fp8t::kTile);
+    tp.vec_in = (C % 16 == 0 && (reinterpret_cast<uintptr_t>(in) & 15) == 0) ? 1 : 0;
+    tp.vec_out = (R % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) ? 1 : 0;
+    const int grid = static_cast<int>(std::min<int64_t>(tp.tiles_r * tp.tiles_c, static_cast<int64_t>(sms) * 8));
+    return launch_pdl(fp8t::transpose_u8_kernel, grid, fp8t::kThreads, 0, stream, "transpose launch", tp);
+}
+
 // Streams and events of the host-memory entry point (one set per device).
 constexpr int kHostChunks = 8;
 struct HostPipe {
@@ -896,6 +915,47 @@ int fp8_scaled_mm_bf16(const void *A, const void *B, int scale_mode, const void 
         return rc;
     return run(A_q, B_q, scale_a, scale_b, scale_mode, bias, out, M, N, K, s, o.variant, o.tile_n, o.split_k,
                o.a_type, o.b_type, o.out_type);
+}
+
+int fp8_scaled_mm_layout(const void *A, int a_major, const void *B, int b_major, const float *scale_a,
+                         const float *scale_b, int scale_mode, const void *bias, void *out, int64_t M, int64_t N,
+                         int64_t K, void *stream, const fp8mm_options *options)
+{
+    fp8mm_options o = {FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16, FP8MM_VARIANT_AUTO, 0, 0};
+    if (options)
+        o = *options;
+    if ((a_major != FP8MM_MAJOR_K && a_major != FP8MM_MAJOR_MN) || (b_major != FP8MM_MAJOR_K && b_major != FP8MM_MAJOR_MN))
+        return FP8MM_ERR_MODE;
+    int rc = check_args(A, B, scale_a, scale_b, scale_mode, bias, out, M, N, K);
+    if (rc != FP8MM_OK || M == 0 || N == 0)
+        return rc;
+    DeviceState *d = nullptr;
+    rc = device_state(&d);
+    if (rc != FP8MM_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const void *Ak = A, *Bk = B;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (a_major == FP8MM_MAJOR_MN && (rc = grow_stage(*d, 6, static_cast<size_t>(M) * K)) != FP8MM_OK)
+            return rc;
+        if (b_major == FP8MM_MAJOR_MN && (rc = grow_stage(*d, 7, static_cast<size_t>(N) * K)) != FP8MM_OK)
+            return rc;
+    }
+    if (a_major == FP8MM_MAJOR_MN) {
+        // A column-major is At [K, M] row-major; its transpose is A [M, K]
+        if ((rc = transpose_bytes(A, d->stage[6], K, M, s, d->sms)) != FP8MM_OK)
+            return rc;
+        Ak = d->stage[6];
+    }
+    if (b_major == FP8MM_MAJOR_MN) {
+        // B row-major [K, N]; its transpose is Bt [N, K], the K-major form
+        if ((rc = transpose_bytes(B, d->stage[7], K, N, s, d->sms)) != FP8MM_OK)
+            return rc;
+        Bk = d->stage[7];
+    }
+    return run(Ak, Bk, scale_a, scale_b, scale_mode, bias, out, M, N, K, s, o.variant, o.tile_n, o.split_k, o.a_type,
+               o.b_type, o.out_type);
 }
 
 int fp8_scaled_bmm(const void *A, const void *B, const float *scale_a, const float *scale_b, int scale_mode,
@@ -1064,7 +1124,7 @@ const char *fp8mm_status_string(int status)
 
 const char *fp8mm_last_error(void) { return t_last_error.c_str(); }
 
-const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mode)
+const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64_t K, int scale_mode)
 {
     (void)scale_mode;
     DeviceState *d = nullptr;
@@ -1072,11 +1132,11 @@ const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mod
         t_describe = "no device";
         return t_describe.c_str();
     }
-    if (M <= 0 || N <= 0 || K < 16) {
+    if (M <= 0 || N <= 0 || K < 16 || batch <= 0) {
         t_describe = "no-op or invalid shape";
         return t_describe.c_str();
     }
-    const Choice c = choose(M, N, K, d->sms, FP8MM_VARIANT_AUTO, 0, 0);
+    const Choice c = choose(M, N, K, d->sms, FP8MM_VARIANT_AUTO, 0, 0, batch);
     char buf[160];
     snprintf(buf, sizeof buf, "%s tile_n=%d split=%d tiles=%dx%d units=%d grid=%d",
              c.variant == FP8MM_VARIANT_TILE    ? "tile"
@@ -1088,6 +1148,11 @@ const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mod
              c.units, c.grid);
     t_describe = buf;
     return t_describe.c_str();
+}
+
+const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mode)
+{
+    return fp8mm_describe_bmm_choice(1, M, N, K, scale_mode);
 }
 
 }  // extern "C"

@@ -173,6 +173,38 @@ int fp8_scaled_mm_host(const void *A, const void *B,
                        int64_t M, int64_t N, int64_t K,
                        void *stream);
 
+/* Which dimension of an operand is contiguous in memory. */
+typedef enum {
+    FP8MM_MAJOR_K = 0,   /* K contiguous: A row-major [M, K]; B column-major [K, N] */
+    FP8MM_MAJOR_MN = 1   /* M (for A) or N (for B) contiguous: A column-major; B row-major */
+} fp8mm_major;
+
+/*
+ * fp8_scaled_mm_ex with either operand in either layout (the four layout
+ * combinations of a matrix product). The pages pass transposed layouts of
+ * A and B to their Triton matmul template as compile-time flags (PyTorch PR
+ * #142101, "Additional notes"); their FP8 scaled_mm is TN only (PR #125204,
+ * Summary). Here an MN-major operand is first transposed on the GPU into a
+ * library-owned staging buffer (an HBM-bound byte transpose, one read and
+ * one write of the operand), then the K-major kernels run. Scales keep their
+ * meaning: row-wise scale_a has one value per row of A and scale_b one per
+ * column of B, whatever the layout.
+ *
+ *   A        a_major K: [M, K] row-major; MN: [M, K] column-major (= At [K, M] row-major)
+ *   B        b_major K: [K, N] column-major (= Bt [N, K]); MN: [K, N] row-major
+ *   other arguments as fp8_scaled_mm_ex (options may be NULL).
+ *
+ * The staging buffers (M*K and N*K bytes) are grown on demand and kept per
+ * device; growing them synchronises the device, so make a first call of the
+ * largest shape before any stream capture. Calls on different streams of
+ * one device that both transpose race on the staging buffers.
+ */
+int fp8_scaled_mm_layout(const void *A, int a_major, const void *B, int b_major,
+                         const float *scale_a, const float *scale_b, int scale_mode,
+                         const void *bias, void *out,
+                         int64_t M, int64_t N, int64_t K,
+                         void *stream, const fp8mm_options *options);
+
 /*
  * Batched form: `batch` independent products of one shape,
  *
@@ -325,6 +357,10 @@ const char *fp8mm_last_error(void);
 /* The kernel fp8_scaled_mm would launch for this problem, as text
  * ("tile tile_n=256 split=1 ..."); for logs and tests. */
 const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mode);
+
+/* The same for a batch of `batch` products (fp8_scaled_bmm); tiles are per
+ * item, units count the whole batch. */
+const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64_t K, int scale_mode);
 
 #ifdef __cplusplus
 }

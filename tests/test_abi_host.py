@@ -199,3 +199,23 @@ def test_bmm_argument_errors(lib):
     assert bmm(A=0) == -1
     assert bmm(opt=fm.Options(0, 5, 0, 0, 0, 0)) == -4
     assert bmm(opt=fm.Options(0, 0, 0, 9, 0, 0)) == -4
+
+
+def test_layout_argument_errors(lib):
+    def lay(am, bm, K=64):
+        return lib.fp8_scaled_mm_layout(P(ALIGNED), am, P(ALIGNED), bm, P(ALIGNED), P(ALIGNED), 0, None,
+                                        P(ALIGNED), 64, 64, K, None, None)
+    assert lay(2, 0) == -4
+    assert lay(0, -1) == -4
+    assert lay(1, 1, K=24) == -2
+
+
+def test_python_layout_detection():
+    A = torch.zeros(6, 32, dtype=torch.float8_e4m3fn)
+    assert fm._major(A, 1) == fm.MAJOR_K
+    assert fm._major(A.t().contiguous().t(), 1) == fm.MAJOR_MN
+    B = torch.zeros(32, 8, dtype=torch.float8_e4m3fn)       # row-major [K, N]
+    assert fm._major(B, 0) == fm.MAJOR_MN
+    assert fm._major(B.t().contiguous().t(), 0) == fm.MAJOR_K
+    with pytest.raises(ValueError):
+        fm._major(torch.zeros(6, 64, dtype=torch.float8_e4m3fn)[:, ::2], 1)
