@@ -236,6 +236,57 @@ bool tile_n_supported(int variant, int tile_n)
 // costs about as much as 5 K blocks for a 128 x 16..32 partial and grows
 // with the partial's size. Fitted to GB300 timings of the skinny shapes;
 // ties keep the smaller split.
+// Time models (microseconds, GB300, fitted to timings of deep-K shapes with
+// few output tiles) for the two kernels that serve M > 128. A K block of a
+// 256 x 256 pair tile takes about 0.32 us on its two SMs, one of a 128 x 128
+// tile about 0.30 us on one SM. Split-K adds a reduction: the last slice of
+// a tile reads every slice's fp32 partial back through L2 (pair: 6.4 + 1.9 s
+// us, plus 2.5 us per wave for writing the partials; 1-SM tile: 3.5 + 1.1 s).
+double pair_time(int64_t tiles, int kblocks, int s, int pairs)
+{
+    const double waves = static_cast<double>(cdiv(tiles * s, pairs));
+    const double per_unit = static_cast<double>(cdiv(kblocks, s)) * 0.32 + (s > 1 ? 2.5 : 0.0);
+    return waves * per_unit + (s > 1 ? 6.4 + 1.9 * s : 0.0);
+}
+
+double tile128_time(int64_t tiles, int kblocks, int s, int sms)
+{
+    const double waves = static_cast<double>(cdiv(tiles * s, sms));
+    return waves * static_cast<double>(cdiv(kblocks, s)) * 0.30 + (s > 1 ? 3.5 + 1.1 * s : 0.0);
+}
+
+// Split-K factor of the pair kernel: the s in 1..8 of least modelled time,
+// each slice keeping at least 4 K blocks.
+int pick_pair_split(int64_t tiles, int kblocks, int pairs)
+{
+    int best = 1;
+    double best_t = pair_time(tiles, kblocks, 1, pairs);
+    for (int s = 2; s <= 8 && kblocks / s >= 4; ++s) {
+        const double t = pair_time(tiles, kblocks, s, pairs);
+        if (t < best_t - 1e-9) {
+            best_t = t;
+            best = s;
+        }
+    }
+    return best;
+}
+
+// Split-K factor of the 1-SM 128 x 128 kernel by the same kind of model
+// (s in 1..16, at least 2 K blocks per slice).
+int pick_tile128_split(int64_t tiles, int kblocks, int sms)
+{
+    int best = 1;
+    double best_t = tile128_time(tiles, kblocks, 1, sms);
+    for (int s = 2; s <= 16 && kblocks / s >= 2; ++s) {
+        const double t = tile128_time(tiles, kblocks, s, sms);
+        if (t < best_t - 1e-9) {
+            best_t = t;
+            best = s;
+        }
+    }
+    return best;
+}
+
 int pick_split(int64_t tiles, int kblocks, int sms, int tile_n)
 {
     const double red = tile_n <= 32 ? 5.0 : tile_n <= 64 ? 10.0 : tile_n <= 128 ? 24.0 : 48.0;
@@ -399,15 +450,23 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
             // stage buffers per epilogue warp measured 7-15 % faster
             variant = FP8MM_VARIANT_TILE;
             tile_n = 256;
-        } else if (cdiv(M, 256) * cdiv(N, 256) * batch >= sms / 4) {
-            // enough 256 x 256 pair tiles to keep most SM pairs busy
-            variant = FP8MM_VARIANT_PAIR;
-            tile_n = 256;
         } else {
-            variant = FP8MM_VARIANT_TILE;
-            tile_n = 256;
-            if (cdiv(M, 128) * cdiv(N, 256) * batch < sms)
+            // the pair kernel or the 1-SM 128 x 128 kernel, each with its best
+            // split, whichever the time model says finishes first
+            const int kb = static_cast<int>(cdiv(K, fp8mm::kBlockK));
+            const int64_t pt = cdiv(M, 256) * cdiv(N, 256) * batch;
+            const int64_t tt = cdiv(M, 128) * cdiv(N, 128) * batch;
+            const int ps = pick_pair_split(pt, kb, sms / 2);
+            const int ts = pick_tile128_split(tt, kb, sms);
+            if (pair_time(pt, kb, ps, sms / 2) <= tile128_time(tt, kb, ts, sms)) {
+                variant = FP8MM_VARIANT_PAIR;
+                tile_n = 256;
+                split = ps;
+            } else {
+                variant = FP8MM_VARIANT_TILE;
                 tile_n = 128;
+                split = ts;
+            }
         }
     }
     if (tile_n == 0)
@@ -437,8 +496,11 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
     if (variant == FP8MM_VARIANT_PAIR) {
         c.tiles_p = static_cast<int>(cdiv(M, 256));
         c.tiles_q = static_cast<int>(cdiv(N, tile_n));
-        c.split = 1;
-        c.units = static_cast<int>(static_cast<int64_t>(c.tiles_p) * c.tiles_q * batch);
+        const int64_t ptiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q * batch;
+        if (split <= 0)
+            split = pick_pair_split(ptiles, c.kblocks, sms / 2);
+        c.split = std::max(1, std::min(split, c.kblocks));
+        c.units = static_cast<int>(ptiles * c.split);
         c.grid = 2 * static_cast<int>(std::min<int64_t>(c.units, sms / 2));
         return c;
     }
@@ -613,8 +675,6 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
         return FP8MM_ERR_MODE;
     if (variant == FP8MM_VARIANT_SWAPK && split != 0 && split != 2 && split != 4 && split != 8)
         return FP8MM_ERR_MODE;
-    if (variant == FP8MM_VARIANT_PAIR && split > 1)
-        return FP8MM_ERR_MODE;
     if (variant != FP8MM_VARIANT_AUTO && tile_n != 0 && !tile_n_supported(variant, tile_n))
         return FP8MM_ERR_MODE;
     if (split < 0 || split > 16)
@@ -666,7 +726,8 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     kp.inject_stop_after = static_cast<int>(g_inject_stop_after.load());
     if (c.split > 1 && c.variant != FP8MM_VARIANT_SWAPK) {
         const int64_t tiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q * batch;
-        const size_t ws = static_cast<size_t>(tiles) * c.split * fp8mm::kTileP * c.tile_n * sizeof(float);
+        const size_t tile_rows = c.variant == FP8MM_VARIANT_PAIR ? 256 : fp8mm::kTileP;
+        const size_t ws = static_cast<size_t>(tiles) * c.split * tile_rows * c.tile_n * sizeof(float);
         rc = grow_workspace(*d, ws, static_cast<size_t>(tiles) * fp8mm::kCountersPerTile);
         if (rc != FP8MM_OK)
             return rc;
@@ -1265,7 +1326,9 @@ extern "C" int fp8_scaled_mm_noalloc(const void *A, const void *B, const float *
     const size_t tiles = static_cast<size_t>(c.tiles_p) * c.tiles_q;
     const bool global_split = c.split > 1 && c.variant != FP8MM_VARIANT_SWAPK;
     const size_t partial_bytes =
-        global_split ? tiles * c.split * fp8mm::kTileP * c.tile_n * sizeof(float) : 0;
+        global_split ? tiles * c.split * (c.variant == FP8MM_VARIANT_PAIR ? 256 : fp8mm::kTileP) * c.tile_n *
+                           sizeof(float)
+                     : 0;
     const size_t counter_bytes = global_split ? tiles * fp8mm::kCountersPerTile * sizeof(unsigned int) : 0;
     if (partial_bytes > kNoAllocPartialBytes || counter_bytes > kNoAllocCounterBytes) {
         char buf[256];

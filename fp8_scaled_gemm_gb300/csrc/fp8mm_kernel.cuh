@@ -66,8 +66,9 @@ struct EpiShape {
     static constexpr int kThreads = 64 + 32 * kWarps;
 };
 
-// Split-K arrival counters per output tile (one per epilogue warp, at most 8).
-constexpr int kCountersPerTile = 8;
+// Split-K arrival counters per output tile: one per epilogue warp of each
+// CTA (8 for the 1-SM kernels, 2 x 8 for a CTA pair).
+constexpr int kCountersPerTile = 16;
 
 // Device status codes (written once per launch, first writer wins).
 constexpr int kStatusTimeoutBase = 0x100;
@@ -605,15 +606,20 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(tempty_bar(acc));
             } else {
+                // Split-K: this slice's fp32 partial laid out as [BN/4 column
+                // groups][128 rows][4 columns]: 16 bytes per lane, 512
+                // contiguous bytes per warp access.
                 const size_t tile_elems = static_cast<size_t>(kTileP) * BN;
-                float *mine = p.ws + (static_cast<size_t>(w.tile) * p.splits + w.split) * tile_elems;
+                float4 *mine = reinterpret_cast<float4 *>(p.ws + (static_cast<size_t>(w.tile) * p.splits + w.split) *
+                                                                     tile_elems);
 #pragma unroll 1
                 for (int c = col0 / CH; c < (col0 + kWarpCols) / CH; ++c) {
                     float v[CH];
                     tmem_load_chunk<CH>(trow + c * CH, v);
 #pragma unroll
-                    for (int j = 0; j < CH; ++j)
-                        __stcg(mine + static_cast<size_t>(c * CH + j) * kTileP + row, v[j]);
+                    for (int g = 0; g < CH / 4; ++g)
+                        __stcg(mine + static_cast<size_t>(c * (CH / 4) + g) * kTileP + row,
+                               make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
                 }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(tempty_bar(acc));
@@ -625,21 +631,50 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
                     old = atomicAdd(cnt, 1u);
                 old = __shfl_sync(0xffffffffu, old, 0);
                 if (old == static_cast<unsigned int>(p.splits - 1)) {
+                    // Last slice: sum the slices in slice order, the loads of
+                    // up to three slices of a chunk issued together.
                     if (lane == 0)
                         *cnt = 0u;   // ready for the next launch
                     __threadfence();
-                    const float *base = p.ws + static_cast<size_t>(w.tile) * p.splits * tile_elems;
+                    const float4 *base =
+                        reinterpret_cast<const float4 *>(p.ws + static_cast<size_t>(w.tile) * p.splits * tile_elems);
+                    const size_t split_stride = tile_elems / 4;
 #pragma unroll 1
                     for (int c = col0 / CH; c < (col0 + kWarpCols) / CH; ++c) {
+                        const float4 *chunk = base + static_cast<size_t>(c * (CH / 4)) * kTileP + row;
+                        float4 acc4[CH / 4];
+#pragma unroll
+                        for (int g = 0; g < CH / 4; ++g)
+                            acc4[g] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 1
+                        for (int s0 = 0; s0 < p.splits; s0 += 3) {
+                            float4 r[3][CH / 4];
+#pragma unroll
+                            for (int i = 0; i < 3; ++i)
+#pragma unroll
+                                for (int g = 0; g < CH / 4; ++g)
+                                    r[i][g] = (s0 + i < p.splits)
+                                                  ? __ldcg(chunk + (s0 + i) * split_stride + static_cast<size_t>(g) * kTileP)
+                                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+                            for (int i = 0; i < 3; ++i)
+#pragma unroll
+                                for (int g = 0; g < CH / 4; ++g) {
+                                    if (s0 + i < p.splits) {
+                                        acc4[g].x += r[i][g].x;
+                                        acc4[g].y += r[i][g].y;
+                                        acc4[g].z += r[i][g].z;
+                                        acc4[g].w += r[i][g].w;
+                                    }
+                                }
+                        }
                         float v[CH];
 #pragma unroll
-                        for (int j = 0; j < CH; ++j)
-                            v[j] = 0.0f;
-                        for (int s = 0; s < p.splits; ++s) {
-                            const float *part = base + static_cast<size_t>(s) * tile_elems;
-#pragma unroll
-                            for (int j = 0; j < CH; ++j)
-                                v[j] += __ldcg(part + static_cast<size_t>(c * CH + j) * kTileP + row);
+                        for (int g = 0; g < CH / 4; ++g) {
+                            v[4 * g] = acc4[g].x;
+                            v[4 * g + 1] = acc4[g].y;
+                            v[4 * g + 2] = acc4[g].z;
+                            v[4 * g + 3] = acc4[g].w;
                         }
                         store_chunk<CH, SWAP>(pb, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
                     }

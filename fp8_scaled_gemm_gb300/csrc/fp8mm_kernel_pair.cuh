@@ -48,8 +48,10 @@ struct PairCfg {
     static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
 };
 
-// Units: (256-row tile of P, BN-row tile of Q); p.tiles_p counts 256-row
-// tiles, p.splits must be 1.
+// Units: (256-row tile of P, BN-row tile of Q, K slice); p.tiles_p counts
+// 256-row tiles. With p.splits > 1 (row-major form only) each slice writes its
+// fp32 partial to the workspace and the last slice to arrive, per epilogue
+// warp of each CTA, sums the slices in slice order and stores the result.
 template <int BN, bool SWAP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
     fp8mm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -229,24 +231,105 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
             ptx::tc_fence_after();
             const uint32_t trow =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            if constexpr (!SWAP) {
-                epilogue_rows_staged<kWarpCols, 1>(pb, &tmap_out, trow + col0,
-                                                w.tp * 256 + static_cast<int>(rank) * 128 + q * 32,
-                                                w.tq * BN + col0, lane, stage, stage_smem, chunks, s_tensor,
-                                                w.b);
-            } else {
-                const int pidx = w.tp * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
+            if (p.splits == 1) {
+                if constexpr (!SWAP) {
+                    epilogue_rows_staged<kWarpCols, 1>(pb, &tmap_out, trow + col0,
+                                                    w.tp * 256 + static_cast<int>(rank) * 128 + q * 32,
+                                                    w.tq * BN + col0, lane, stage, stage_smem, chunks, s_tensor,
+                                                    w.b);
+                } else {
+                    const int pidx = w.tp * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
 #pragma unroll 1
-                for (int c = 0; c < BN / CH; ++c) {
+                    for (int c = 0; c < BN / CH; ++c) {
+                        float v[CH];
+                        tmem_load_chunk<CH>(trow + c * CH, v);
+                        store_chunk<CH, true>(pb, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
+            } else if constexpr (!SWAP) {
+                // Split-K: this slice's fp32 partial of the tile, laid out as
+                // [BN/4 column groups][256 rows][4 columns] so that every lane
+                // moves 16 bytes and a warp 512 contiguous bytes per access.
+                const int prow = static_cast<int>(rank) * 128 + q * 32 + lane;   // row within the pair tile
+                const size_t tile_elems = static_cast<size_t>(256) * BN;
+                float4 *mine = reinterpret_cast<float4 *>(p.ws + (static_cast<size_t>(w.tile) * p.splits + w.split) *
+                                                                     tile_elems);
+#pragma unroll 1
+                for (int c = col0 / CH; c < (col0 + kWarpCols) / CH; ++c) {
                     float v[CH];
                     tmem_load_chunk<CH>(trow + c * CH, v);
-                    store_chunk<CH, true>(pb, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
+#pragma unroll
+                    for (int g = 0; g < CH / 4; ++g)
+                        __stcg(mine + static_cast<size_t>(c * (CH / 4) + g) * 256 + prow,
+                               make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));   // accumulator free
+                __threadfence();
+                __syncwarp();
+                unsigned int old = 0;
+                unsigned int *cnt = p.counters + static_cast<size_t>(w.tile) * kCountersPerTile +
+                                    static_cast<int>(rank) * 8 + ew;
+                if (lane == 0)
+                    old = atomicAdd(cnt, 1u);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                if (old == static_cast<unsigned int>(p.splits - 1)) {
+                    // Last slice: sum the slices in slice order. The loads of up
+                    // to four slices of a 32-column chunk are issued together.
+                    if (lane == 0)
+                        *cnt = 0u;   // ready for the next launch
+                    __threadfence();
+                    const float4 *base = reinterpret_cast<const float4 *>(
+                        p.ws + static_cast<size_t>(w.tile) * p.splits * tile_elems);
+                    const size_t split_stride = tile_elems / 4;   // float4 per slice
+                    const int m = w.tp * 256 + prow;
+#pragma unroll 1
+                    for (int c = col0 / CH; c < (col0 + kWarpCols) / CH; ++c) {
+                        const float4 *chunk = base + static_cast<size_t>(c * (CH / 4)) * 256 + prow;
+                        float4 acc4[CH / 4];
+#pragma unroll
+                        for (int g = 0; g < CH / 4; ++g)
+                            acc4[g] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 1
+                        for (int s0 = 0; s0 < p.splits; s0 += 3) {
+                            float4 r[3][CH / 4];
+#pragma unroll
+                            for (int i = 0; i < 3; ++i)
+#pragma unroll
+                                for (int g = 0; g < CH / 4; ++g)
+                                    r[i][g] = (s0 + i < p.splits)
+                                                  ? __ldcg(chunk + (s0 + i) * split_stride + static_cast<size_t>(g) * 256)
+                                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+                            for (int i = 0; i < 3; ++i)
+#pragma unroll
+                                for (int g = 0; g < CH / 4; ++g) {
+                                    if (s0 + i < p.splits) {
+                                        acc4[g].x += r[i][g].x;
+                                        acc4[g].y += r[i][g].y;
+                                        acc4[g].z += r[i][g].z;
+                                        acc4[g].w += r[i][g].w;
+                                    }
+                                }
+                        }
+                        float v[CH];
+#pragma unroll
+                        for (int g = 0; g < CH / 4; ++g) {
+                            v[4 * g] = acc4[g].x;
+                            v[4 * g + 1] = acc4[g].y;
+                            v[4 * g + 2] = acc4[g].z;
+                            v[4 * g + 3] = acc4[g].w;
+                        }
+                        store_chunk<CH, false>(pb, v, m, w.tq * BN + c * CH, s_tensor, lane);
+                    }
                 }
             }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;

@@ -87,7 +87,7 @@ def test_config_rejects_unsupported_choices(lib):
     assert cfg(5, 64, 2) == -4        # SWAPPAIR has no split-K
     assert cfg(4, 16, 3) == -4        # SWAPK cluster size is 2, 4 or 8
     assert cfg(3, 64, 0) == -4        # PAIR takes 128 or 256
-    assert cfg(3, 256, 2) == -4       # PAIR has no split-K
+    assert cfg(3, 256, 17) == -4      # split-K of at most 16 slices
     assert cfg(1, 64, 0) == -4        # TILE takes 128 or 256
     assert cfg(2, 256, 0) == -4       # SWAP takes 16..128
     assert cfg(1, 128, 17) == -4

@@ -54,7 +54,7 @@ def check_items(out, items):
 
 
 KERNELS = [(TILE, 128, 1), (TILE, 256, 1), (TILE, 128, 3), (SWAP, 16, 1), (SWAP, 64, 2), (SWAP, 128, 1),
-           (PAIR, 128, 0), (PAIR, 256, 0), (SWAPK, 16, 4), (SWAPK, 128, 2), (SWAPPAIR, 32, 0)]
+           (PAIR, 128, 1), (PAIR, 256, 1), (PAIR, 256, 3), (SWAPK, 16, 4), (SWAPK, 128, 2), (SWAPPAIR, 32, 0)]
 
 
 @pytest.mark.parametrize("variant,tile_n,split", KERNELS)
@@ -84,7 +84,7 @@ def test_batched_equals_single_calls_with_the_same_kernel():
     _need_gpu()
     import fp8_scaled_gemm_gb300 as fm
     items = make_batch(4, 300, 520, 400, 1, seed=70, bias=True)
-    for variant, tile_n, split in ((TILE, 256, 1), (PAIR, 256, 0), (SWAP, 64, 3)):
+    for variant, tile_n, split in ((TILE, 256, 1), (PAIR, 256, 1), (PAIR, 256, 4), (SWAP, 64, 3)):
         M = 300 if variant != SWAP else 60
         its = make_batch(4, M, 520, 400, 1, seed=70, bias=True)
         out = run_batch(its, 1, variant, tile_n, split)

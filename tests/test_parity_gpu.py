@@ -44,7 +44,7 @@ def test_every_kernel_on_a_ragged_shape(variant, tile_n, mode, split):
     M, N, K = 300, 520, 400
     stats, _, _ = run_and_compare(M, N, K, mode, seed=11, with_bias=(split == 3),
                                   variant=variant, tile_n=tile_n,
-                                  split_k=(1 if variant in (PAIR, SWAPPAIR) else split))
+                                  split_k=(1 if variant == SWAPPAIR else split))
     _assert_ok(stats, f"v{variant} n{tile_n} mode{mode} split{split}")
 
 
@@ -68,8 +68,32 @@ def test_pair_kernel_shapes(shape):
     M, N, K = shape
     for tile_n in (128, 256):
         stats, _, _ = run_and_compare(M, N, K, 1, seed=4, with_bias=True, variant=PAIR,
-                                      tile_n=tile_n, split_k=0)
+                                      tile_n=tile_n, split_k=1)
         _assert_ok(stats, f"pair{tile_n} {shape}")
+
+
+@pytest.mark.parametrize("split", [2, 3, 5, 8])
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_pair_kernel_split_k(split, tile_n):
+    _need_gpu()
+    # ragged M, N and K (K blocks not divisible by the split), bias, both modes
+    for mode in (0, 1):
+        stats, _, _ = run_and_compare(300, 520, 1296, mode, seed=24 + split, with_bias=(mode == 1),
+                                      variant=PAIR, tile_n=tile_n, split_k=split)
+        _assert_ok(stats, f"pair{tile_n} split{split} mode{mode}")
+
+
+def test_pair_split_k_is_deterministic_and_reuses_counters():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+    inp = make_inputs(512, 1024, 4096, 1, seed=31, with_bias=True)
+    A, Bt, sa, sb, bias = to_device(inp)
+    outs = [bf16_bits(fm.fp8_scaled_mm_config(A, Bt.t(), sa, sb, 1, bias=bias, variant=PAIR, tile_n=256,
+                                              split_k=4)) for _ in range(3)]
+    assert fm.fp8mm_device_status() == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    _assert_ok(compare(outs[0], inp), "pair split4")
 
 
 @pytest.mark.parametrize("tile_n", [16, 32, 64, 128])

@@ -29,8 +29,8 @@ def _need_gpu():
 
 
 @pytest.mark.parametrize("M,N,K,mode,with_bias", [
-    (200, 2048, 16384, 1, True),   # few 128 x 128 tiles: split-K over 4 slices
-    (300, 1000, 8192, 0, False),   # split-K, ragged M and N
+    (200, 300, 16384, 1, True),    # very few tiles and deep K: split-K
+    (300, 520, 8192, 0, False),    # split-K, ragged M and N
 ])
 def test_noalloc_matches_fp8_scaled_mm_on_two_calls(M, N, K, mode, with_bias):
     _need_gpu()
@@ -66,25 +66,28 @@ def test_noalloc_matches_fp8_scaled_mm_on_two_calls(M, N, K, mode, with_bias):
 
 
 def _scratch_bytes(choice: str) -> int:
-    """Split-K partial bytes of a kernel choice string ("swap tile_n=.. split=.. tiles=PxQ ...")."""
-    if not choice.startswith(("tile", "swap ")):
-        return 0   # the pair and cluster kernels use no scratch
+    """Split-K partial bytes of a kernel choice string ("pair tile_n=.. split=.. tiles=PxQ ...")."""
+    if not choice.startswith(("tile", "swap ", "pair")):
+        return 0   # the cluster kernels reduce in distributed shared memory
     f = dict(kv.split("=") for kv in choice.split()[1:])
     p, q = (int(x) for x in f["tiles"].split("x"))
     split = int(f["split"])
-    return 0 if split == 1 else p * q * split * 128 * int(f["tile_n"]) * 4
+    rows = 256 if choice.startswith("pair") else 128
+    return 0 if split == 1 else p * q * split * rows * int(f["tile_n"]) * 4
 
 
 def test_noalloc_rejects_problems_beyond_the_static_scratch():
     _need_gpu()
     import fp8_scaled_gemm_gb300 as fm
 
-    # 100 tiles of 128 x 128 (TILE variant) and very deep K: split 3 ways on
-    # 152 SMs, 300 fp32 partial tiles of 64 KiB = 18.75 MiB > the 16 MiB array.
-    M, N, K = 640, 2560, 65536
-    need = _scratch_bytes(fm.fp8mm_describe_choice(M, N, K, 1))
-    if need <= 16 * 2 ** 20:
-        pytest.skip("this device's SM count gives a smaller split for the probe shape")
+    # deep K and few output tiles: the kernel choice splits K, and its fp32
+    # partial tiles need more than the 16 MiB array (the first such shape)
+    for M, N, K in ((512, 4352, 65536), (640, 2560, 65536), (256, 8192, 65536), (512, 8192, 65536)):
+        need = _scratch_bytes(fm.fp8mm_describe_choice(M, N, K, 1))
+        if need > 16 * 2 ** 20:
+            break
+    else:
+        pytest.skip("this device's SM count gives smaller splits for the probe shapes")
     A = torch.zeros(M, K, dtype=torch.float8_e4m3fn, device="cuda")
     Bt = torch.zeros(N, K, dtype=torch.float8_e4m3fn, device="cuda")
     sa = torch.ones(M, device="cuda")
