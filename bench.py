@@ -53,11 +53,14 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--sweep", action="store_true",
                     help="time every benchmark shape instead (one JSON line per shape)")
+    ap.add_argument("--tune", action="store_true",
+                    help="with --sweep: autotune each shape (fp8mm_autotune) before timing it")
     ap.add_argument("--quant", action="store_true",
                     help="time the bf16 -> fp8 quantisation step instead (one JSON line per shape; "
                          "--shapes takes RxC[:mode[:e4m3|e5m2]])")
     ap.add_argument("--shapes", default="",
-                    help="with --sweep: comma list of [B@]MxNxK[:mode[:bias[:a_dtype:b_dtype:out_dtype]]] "
+                    help="with --sweep: 'gist' (the gist's M x K x N list, both scalings) or a comma list of "
+                         "[B@]MxNxK[:mode[:bias[:a_dtype:b_dtype:out_dtype]]] "
                          "(default: all benchmark shapes; B@ = a batch of B products, fp8_scaled_bmm; "
                          "dtypes e4m3|e5m2 and bf16|fp16)")
     return ap.parse_args(argv)
@@ -321,6 +324,11 @@ SWEEP_SHAPES = (
 )
 
 
+# The gist's benchmark list, written there as (M, K, N); here as (M, N, K).
+GIST_SHAPES = [(512, 12288, 3072), (512, 3072, 12288), (1152, 12288, 3072), (1152, 3072, 12288),
+               (2304, 12288, 3072), (2304, 3072, 12288), (4608, 12288, 3072), (4608, 3072, 12288)]
+
+
 def algorithmic_bytes(M, N, K, mode, bias, batch=1):
     # fp8 operands (1 byte), 16-bit output and bias, fp32 scales
     return batch * (M * K + N * K + 2 * M * N + (4 * (M + N) if mode == 1 else 8)) + (2 * N if bias else 0)
@@ -401,7 +409,10 @@ def run_sweep(args):
     pk = peaks()
     fp8_peak = pk["bf16_tflops"] * NOMINAL_FP8_PER_BF16
     shapes = [s + (("e4m3", "e4m3", "bf16"), 1) for s in SWEEP_SHAPES]
-    if args.shapes:
+    if args.shapes == "gist":
+        shapes = [(M, N, K, mode, False, ("e4m3", "e4m3", "bf16"), 1)
+                  for (M, N, K) in GIST_SHAPES for mode in (0, 1)]
+    elif args.shapes:
         shapes = []
         for spec in args.shapes.split(","):
             parts = spec.split(":")
@@ -415,7 +426,12 @@ def run_sweep(args):
             bias = bool(int(parts[2])) if len(parts) > 2 else False
             types = tuple(parts[3:6]) if len(parts) >= 6 else ("e4m3", "e4m3", "bf16")
             shapes.append((M, N, K, mode, bias, types, batch))
+    dts = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2, "bf16": torch.bfloat16, "fp16": torch.float16}
     for (M, N, K, mode, bias, types, batch) in shapes:
+        builtin = fm.fp8mm_describe_bmm_choice(batch, M, N, K, mode)
+        if args.tune:
+            fm.fp8mm_autotune(M, N, K, mode, batch=batch, a_dtype=dts[types[0]], b_dtype=dts[types[1]],
+                              out_dtype=dts[types[2]])
         mean, best, n_sets, choice = time_shape(M, N, K, mode, bias, args.steps, args.warmup, device,
                                                 types, batch)
         flops = 2.0 * M * N * K * batch
@@ -430,7 +446,8 @@ def run_sweep(args):
             "tflops": round(tflops, 1), "frac_fp8_peak": round(tflops / fp8_peak, 3),
             "gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3),
             "bound": "hbm" if flops / nbytes < fp8_peak * 1e12 / (pk["hbm_gbs"] * 1e9) else "tensor",
-            "rotated_sets": n_sets, "kernel": choice}), flush=True)
+            "rotated_sets": n_sets, "kernel": choice,
+            **({"tuned": True, "builtin_kernel": builtin} if args.tune else {})}), flush=True)
 
 
 QUANT_SHAPES = [(8192, 8192, 0), (8192, 8192, 1), (16384, 8192, 1), (4096, 14336, 1), (14336, 4096, 1),

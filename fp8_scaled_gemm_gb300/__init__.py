@@ -57,6 +57,8 @@ EXPORTS = (
     "fp8_scaled_mm_layout",
     "fp8mm_reserve_workspace", "fp8mm_device_status", "fp8mm_status_string",
     "fp8mm_last_error", "fp8mm_describe_choice", "fp8mm_describe_bmm_choice", "fp8mm_debug_inject",
+    "fp8mm_autotune", "fp8mm_autotune_clear", "fp8mm_autotune_count", "fp8mm_autotune_save",
+    "fp8mm_autotune_load",
 )
 
 _lib = None
@@ -123,6 +125,16 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fp8mm_debug_inject.restype = i32
         lib.fp8mm_describe_choice.argtypes = [i64, i64, i64, i32]
         lib.fp8mm_describe_choice.restype = ctypes.c_char_p
+        lib.fp8mm_autotune.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(Options), vp]
+        lib.fp8mm_autotune.restype = i32
+        lib.fp8mm_autotune_clear.argtypes = []
+        lib.fp8mm_autotune_clear.restype = i32
+        lib.fp8mm_autotune_count.argtypes = []
+        lib.fp8mm_autotune_count.restype = i32
+        lib.fp8mm_autotune_save.argtypes = [ctypes.c_char_p]
+        lib.fp8mm_autotune_save.restype = i32
+        lib.fp8mm_autotune_load.argtypes = [ctypes.c_char_p]
+        lib.fp8mm_autotune_load.restype = i32
         lib.fp8mm_describe_bmm_choice.argtypes = [i64, i64, i64, i64, i32]
         lib.fp8mm_describe_bmm_choice.restype = ctypes.c_char_p
         _lib = lib
@@ -430,3 +442,36 @@ def fp8mm_describe_choice(M: int, N: int, K: int, scale_mode: int = SCALE_TENSOR
 
 def fp8mm_describe_bmm_choice(batch: int, M: int, N: int, K: int, scale_mode: int = SCALE_TENSOR) -> str:
     return load().fp8mm_describe_bmm_choice(int(batch), int(M), int(N), int(K), int(scale_mode)).decode()
+
+
+def fp8mm_autotune(M: int, N: int, K: int, scale_mode: int = SCALE_TENSOR, batch: int = 1,
+                   a_dtype=torch.float8_e4m3fn, b_dtype=torch.float8_e4m3fn, out_dtype=torch.bfloat16,
+                   stream=None) -> str:
+    """Time the compiled kernel configurations for this problem and remember
+    the fastest for automatic choice; returns the chosen configuration."""
+    opt = Options(_FP8[a_dtype], _FP8[b_dtype], _OUT[out_dtype], VARIANT_AUTO, 0, 0)
+    _check(load().fp8mm_autotune(int(batch), int(M), int(N), int(K), int(scale_mode), ctypes.byref(opt),
+                                 _stream_handle(stream)))
+    return fp8mm_describe_bmm_choice(batch, M, N, K, scale_mode)
+
+
+def fp8mm_autotune_clear() -> None:
+    _check(load().fp8mm_autotune_clear())
+
+
+def fp8mm_autotune_count() -> int:
+    return int(load().fp8mm_autotune_count())
+
+
+def fp8mm_autotune_save(path: str) -> int:
+    rc = load().fp8mm_autotune_save(os.fsencode(path))
+    if rc < 0:
+        _check(rc)
+    return rc
+
+
+def fp8mm_autotune_load(path: str) -> int:
+    rc = load().fp8mm_autotune_load(os.fsencode(path))
+    if rc < 0:
+        _check(rc)
+    return rc

@@ -11,8 +11,11 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
+#include <tuple>
+#include <vector>
 
 #include "fp8mm.h"
 #include "fp8mm_kernel.cuh"
@@ -55,6 +58,35 @@ struct DeviceState {
     size_t stage_bytes[8] = {};
 };
 DeviceState g_dev[kMaxDevices];
+
+// Tuned kernel choices (fp8mm_autotune), keyed by device kind and problem.
+struct TuneKey {
+    int cc_major, cc_minor, sms;
+    int64_t batch, M, N, K;
+    int mode, a_type, b_type, out_type;
+    bool operator<(const TuneKey &o) const
+    {
+        return std::tie(cc_major, cc_minor, sms, batch, M, N, K, mode, a_type, b_type, out_type) <
+               std::tie(o.cc_major, o.cc_minor, o.sms, o.batch, o.M, o.N, o.K, o.mode, o.a_type, o.b_type,
+                        o.out_type);
+    }
+};
+struct TuneVal {
+    int variant, tile_n, split;
+    double us;
+};
+std::mutex g_tune_mu;
+std::map<TuneKey, TuneVal> g_tuned;
+
+bool tuned_lookup(const TuneKey &k, TuneVal *v)
+{
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    auto it = g_tuned.find(k);
+    if (it == g_tuned.end())
+        return false;
+    *v = it->second;
+    return true;
+}
 
 int cuda_fail(cudaError_t e, const char *what)
 {
@@ -695,6 +727,15 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     if (rc != FP8MM_OK)
         return rc;
 
+    if (variant == FP8MM_VARIANT_AUTO) {
+        TuneVal tv;
+        const TuneKey key{d->cc_major, d->cc_minor, d->sms, batch, M, N, K, scale_mode, a_type, b_type, out_type};
+        if (tuned_lookup(key, &tv)) {
+            variant = tv.variant;
+            tile_n = tv.tile_n;
+            split = tv.split;
+        }
+    }
     const Choice c = choose(M, N, K, d->sms, variant, tile_n, split, batch);
     fp8mm::KernelParams kp{};
     kp.scale_a = sa;
@@ -850,6 +891,67 @@ int transpose_bytes(const void *in, void *out, int64_t R, int64_t C, cudaStream_
     tp.vec_out = (R % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) ? 1 : 0;
     const int grid = static_cast<int>(std::min<int64_t>(tp.tiles_r * tp.tiles_c, static_cast<int64_t>(sms) * 8));
     return launch_pdl(fp8t::transpose_u8_kernel, grid, fp8t::kThreads, 0, stream, "transpose launch", tp);
+}
+
+// ----------------------------------------------------------- autotuning ---
+
+// Pseudo-random finite fp8 codes (a hash of the index; `mask` clears the
+// exponent bit that would make an e4m3 NaN or an e5m2 inf/NaN).
+__global__ void fill_codes_kernel(uint8_t *p, size_t n, uint32_t seed, uint8_t mask)
+{
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        uint32_t h = static_cast<uint32_t>(i) * 0x9E3779B1u ^ seed ^ static_cast<uint32_t>(i >> 32) * 0x85EBCA77u;
+        h ^= h >> 15;
+        h *= 0x2C1B3C6Du;
+        h ^= h >> 12;
+        p[i] = static_cast<uint8_t>(h) & mask;
+    }
+}
+
+__global__ void fill_f32_kernel(float *p, size_t n, float v)
+{
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        p[i] = v;
+}
+
+struct Candidate {
+    int variant, tile_n, split;
+};
+
+// The compiled configurations worth timing for a problem.
+std::vector<Candidate> tune_candidates(int64_t M, int64_t K)
+{
+    std::vector<Candidate> c;
+    const int kb = static_cast<int>(cdiv(K, fp8mm::kBlockK));
+    if (M <= 128) {
+        for (int t : {16, 32, 64, 128}) {
+            if (t < swap_tile_for(M))
+                continue;
+            for (int s : {1, 2, 3, 4, 6, 8})
+                if (s == 1 || kb / s >= 2)
+                    c.push_back({FP8MM_VARIANT_SWAP, t, s});
+            for (int cs : {2, 4, 8})
+                if (kb / cs >= 2)
+                    c.push_back({FP8MM_VARIANT_SWAPK, t, cs});
+            c.push_back({FP8MM_VARIANT_SWAPPAIR, t, 1});
+            if (t >= 2 * swap_tile_for(M))
+                break;   // one tile size above the smallest that fits is enough
+        }
+        return c;
+    }
+    for (int s : {1, 2, 3, 4, 6, 8})
+        if (s == 1 || kb / s >= 4)
+            c.push_back({FP8MM_VARIANT_PAIR, 256, s});
+    c.push_back({FP8MM_VARIANT_PAIR, 128, 1});
+    for (int s : {1, 2, 3, 4, 6, 8, 12, 16})
+        if (s == 1 || kb / s >= 2)
+            c.push_back({FP8MM_VARIANT_TILE, 128, s});
+    for (int s : {1, 2, 4})
+        if (s == 1 || kb / s >= 2)
+            c.push_back({FP8MM_VARIANT_TILE, 256, s});
+    return c;
 }
 
 // Streams and events of the host-memory entry point (one set per device).
@@ -1187,7 +1289,6 @@ const char *fp8mm_last_error(void) { return t_last_error.c_str(); }
 
 const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64_t K, int scale_mode)
 {
-    (void)scale_mode;
     DeviceState *d = nullptr;
     if (device_state(&d) != FP8MM_OK) {
         t_describe = "no device";
@@ -1197,7 +1298,16 @@ const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64
         t_describe = "no-op or invalid shape";
         return t_describe.c_str();
     }
-    const Choice c = choose(M, N, K, d->sms, FP8MM_VARIANT_AUTO, 0, 0, batch);
+    int variant = FP8MM_VARIANT_AUTO, tile_n = 0, split = 0;
+    TuneVal tv;
+    const TuneKey key{d->cc_major, d->cc_minor, d->sms, batch, M, N, K, scale_mode, FP8MM_TYPE_E4M3,
+                      FP8MM_TYPE_E4M3, FP8MM_OUT_BF16};
+    if (tuned_lookup(key, &tv)) {
+        variant = tv.variant;
+        tile_n = tv.tile_n;
+        split = tv.split;
+    }
+    const Choice c = choose(M, N, K, d->sms, variant, tile_n, split, batch);
     char buf[160];
     snprintf(buf, sizeof buf, "%s tile_n=%d split=%d tiles=%dx%d units=%d grid=%d",
              c.variant == FP8MM_VARIANT_TILE    ? "tile"
@@ -1214,6 +1324,202 @@ const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64
 const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mode)
 {
     return fp8mm_describe_bmm_choice(1, M, N, K, scale_mode);
+}
+
+int fp8mm_autotune(int64_t batch, int64_t M, int64_t N, int64_t K, int scale_mode, const fp8mm_options *options,
+                   void *stream)
+{
+    fp8mm_options o = {FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16, FP8MM_VARIANT_AUTO, 0, 0};
+    if (options)
+        o = *options;
+    if (scale_mode != FP8MM_SCALE_TENSOR && scale_mode != FP8MM_SCALE_ROWWISE)
+        return FP8MM_ERR_MODE;
+    if ((o.a_type != FP8MM_TYPE_E4M3 && o.a_type != FP8MM_TYPE_E5M2) ||
+        (o.b_type != FP8MM_TYPE_E4M3 && o.b_type != FP8MM_TYPE_E5M2) ||
+        (o.out_type != FP8MM_OUT_BF16 && o.out_type != FP8MM_OUT_F16))
+        return FP8MM_ERR_MODE;
+    if (batch < 1 || M < 1 || N < 1 || M > INT32_MAX || N > INT32_MAX || K < 16 || K % 16 != 0 ||
+        K > (int64_t(1) << 24) || batch * cdiv(M, 16) * cdiv(N, 128) * 16 > INT32_MAX)
+        return FP8MM_ERR_SHAPE;
+    DeviceState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc != FP8MM_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // scratch: rotated copies of the operands so that one set is not served
+    // from L2 when the next launch reads it
+    const size_t a_bytes = static_cast<size_t>(batch * M * K), b_bytes = static_cast<size_t>(batch * N * K);
+    const size_t o_bytes = static_cast<size_t>(batch * M * N) * 2;
+    const size_t per_set = a_bytes + b_bytes + o_bytes;
+    const int n_sets = static_cast<int>(std::max<size_t>(1, std::min<size_t>(8, (3 * (size_t(129) << 20)) / per_set)));
+    const bool rowwise = scale_mode == FP8MM_SCALE_ROWWISE;
+    const size_t na = rowwise ? static_cast<size_t>(batch * M) : static_cast<size_t>(batch);
+    const size_t nb = rowwise ? static_cast<size_t>(batch * N) : static_cast<size_t>(batch);
+    std::vector<void *> bufs;
+    auto alloc = [&](size_t bytes, void **p) {
+        cudaError_t e = cudaMalloc(p, std::max<size_t>(bytes, 16));
+        if (e == cudaSuccess)
+            bufs.push_back(*p);
+        return e;
+    };
+    auto release = [&]() {
+        cudaDeviceSynchronize();
+        for (void *p : bufs)
+            cudaFree(p);
+        bufs.clear();
+    };
+    std::vector<void *> A(n_sets), B(n_sets), O(n_sets);
+    float *sa = nullptr, *sb = nullptr;
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < n_sets && e == cudaSuccess; ++i) {
+        if ((e = alloc(a_bytes, &A[i])) != cudaSuccess || (e = alloc(b_bytes, &B[i])) != cudaSuccess ||
+            (e = alloc(o_bytes, &O[i])) != cudaSuccess)
+            break;
+        fill_codes_kernel<<<d->sms * 4, 256, 0, st>>>(static_cast<uint8_t *>(A[i]), a_bytes, 0x1234u + i,
+                                                       o.a_type == FP8MM_TYPE_E4M3 ? 0xF7 : 0xFB);
+        fill_codes_kernel<<<d->sms * 4, 256, 0, st>>>(static_cast<uint8_t *>(B[i]), b_bytes, 0x9876u + i,
+                                                       o.b_type == FP8MM_TYPE_E4M3 ? 0xF7 : 0xFB);
+    }
+    if (e == cudaSuccess && (e = alloc(na * 4, reinterpret_cast<void **>(&sa))) == cudaSuccess &&
+        (e = alloc(nb * 4, reinterpret_cast<void **>(&sb))) == cudaSuccess) {
+        fill_f32_kernel<<<d->sms, 256, 0, st>>>(sa, na, 1.0f / 1024.0f);
+        fill_f32_kernel<<<d->sms, 256, 0, st>>>(sb, nb, 1.0f / 1024.0f);
+        e = cudaGetLastError();
+    }
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (e == cudaSuccess && (e = cudaEventCreate(&e0)) == cudaSuccess)
+        e = cudaEventCreate(&e1);
+    if (e != cudaSuccess) {
+        release();
+        if (e0)
+            cudaEventDestroy(e0);
+        return cuda_fail(e, "autotune set-up");
+    }
+
+    TuneVal best{FP8MM_VARIANT_AUTO, 0, 0, 1e300};
+    int launches = 0;
+    for (const Candidate &cand : tune_candidates(M, K)) {
+        auto one = [&](int i) {
+            const int k = i % n_sets;
+            return run(A[k], B[k], sa, sb, scale_mode, nullptr, O[k], M, N, K, st, cand.variant, cand.tile_n,
+                       cand.split, o.a_type, o.b_type, o.out_type, batch);
+        };
+        rc = FP8MM_OK;
+        for (int i = 0; i < 2 && rc == FP8MM_OK; ++i)
+            rc = one(launches++);
+        if (rc != FP8MM_OK)
+            continue;   // a configuration this problem cannot take
+        float times[5];
+        for (int r = 0; r < 5 && rc == FP8MM_OK; ++r) {
+            cudaEventRecord(e0, st);
+            rc = one(launches++);
+            cudaEventRecord(e1, st);
+            if (cudaEventSynchronize(e1) != cudaSuccess || cudaEventElapsedTime(&times[r], e0, e1) != cudaSuccess)
+                rc = FP8MM_ERR_CUDA;
+        }
+        if (rc != FP8MM_OK)
+            continue;
+        std::sort(times, times + 5);
+        const double us = times[2] * 1000.0;
+        if (us < best.us)
+            best = TuneVal{cand.variant, cand.tile_n, cand.split, us};
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    release();
+    rc = fp8mm_device_status(stream);
+    if (rc != FP8MM_OK)
+        return rc;
+    if (best.variant == FP8MM_VARIANT_AUTO) {
+        t_last_error = "fp8mm_autotune: no configuration ran";
+        return FP8MM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    g_tuned[TuneKey{d->cc_major, d->cc_minor, d->sms, batch, M, N, K, scale_mode, o.a_type, o.b_type, o.out_type}] =
+        best;
+    return FP8MM_OK;
+}
+
+int fp8mm_autotune_clear(void)
+{
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    g_tuned.clear();
+    return FP8MM_OK;
+}
+
+int fp8mm_autotune_count(void)
+{
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    return static_cast<int>(g_tuned.size());
+}
+
+int fp8mm_autotune_save(const char *path)
+{
+    if (!path)
+        return FP8MM_ERR_NULL;
+    FILE *f = fopen(path, "w");
+    if (!f) {
+        t_last_error = std::string("cannot write ") + path;
+        return FP8MM_ERR_NULL;
+    }
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    fprintf(f, "# cc_major cc_minor sms batch M N K scale_mode a_type b_type out_type variant tile_n split us\n");
+    for (const auto &kv : g_tuned) {
+        const TuneKey &k = kv.first;
+        const TuneVal &v = kv.second;
+        fprintf(f, "%d %d %d %lld %lld %lld %lld %d %d %d %d %d %d %d %.3f\n", k.cc_major, k.cc_minor, k.sms,
+                static_cast<long long>(k.batch), static_cast<long long>(k.M), static_cast<long long>(k.N),
+                static_cast<long long>(k.K), k.mode, k.a_type, k.b_type, k.out_type, v.variant, v.tile_n, v.split,
+                v.us);
+    }
+    const bool ok = fclose(f) == 0;
+    return ok ? static_cast<int>(g_tuned.size()) : FP8MM_ERR_NULL;
+}
+
+int fp8mm_autotune_load(const char *path)
+{
+    if (!path)
+        return FP8MM_ERR_NULL;
+    FILE *f = fopen(path, "r");
+    if (!f) {
+        t_last_error = std::string("cannot read ") + path;
+        return FP8MM_ERR_NULL;
+    }
+    char line[512];
+    int n = 0;
+    int rc = FP8MM_OK;
+    while (fgets(line, sizeof line, f)) {
+        if (line[0] == '#' || line[0] == '\n')
+            continue;
+        TuneKey k{};
+        TuneVal v{};
+        long long b, m, nn, kk;
+        const int got = sscanf(line, "%d %d %d %lld %lld %lld %lld %d %d %d %d %d %d %d %lf", &k.cc_major,
+                               &k.cc_minor, &k.sms, &b, &m, &nn, &kk, &k.mode, &k.a_type, &k.b_type, &k.out_type,
+                               &v.variant, &v.tile_n, &v.split, &v.us);
+        k.batch = b;
+        k.M = m;
+        k.N = nn;
+        k.K = kk;
+        const bool valid = got == 15 && b >= 1 && m >= 1 && nn >= 1 && kk >= 16 && kk % 16 == 0 &&
+                           (k.mode == 0 || k.mode == 1) && (k.a_type == 0 || k.a_type == 1) &&
+                           (k.b_type == 0 || k.b_type == 1) && (k.out_type == 0 || k.out_type == 1) &&
+                           v.variant >= FP8MM_VARIANT_TILE && v.variant <= FP8MM_VARIANT_SWAPPAIR &&
+                           tile_n_supported(v.variant, v.tile_n) && v.split >= 1 && v.split <= 16 &&
+                           !(v.variant == FP8MM_VARIANT_SWAPK && v.split != 2 && v.split != 4 && v.split != 8) &&
+                           !(v.variant == FP8MM_VARIANT_SWAPPAIR && v.split != 1);
+        if (!valid) {
+            t_last_error = std::string("fp8mm_autotune_load: malformed line: ") + line;
+            rc = FP8MM_ERR_SHAPE;
+            break;
+        }
+        std::lock_guard<std::mutex> lock(g_tune_mu);
+        g_tuned[k] = v;
+        ++n;
+    }
+    fclose(f);
+    return rc == FP8MM_OK ? n : rc;
 }
 
 }  // extern "C"

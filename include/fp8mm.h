@@ -322,6 +322,49 @@ int fp8_scaled_mm_noalloc(const void *A, const void *B,
                           void *stream);
 
 /*
+ * Shape-keyed autotuning. The pages tune their kernels per problem shape
+ * (gist "matmul_fp8.py", the `triton.autotune` configs keyed on M, N, K and
+ * the scaling; PyTorch PR #130422, max-autotune of scaled_mm). Here the
+ * candidates are the kernel configurations compiled into the library (pair
+ * and 1-SM kernels with their split-K factors for M > 128; SWAP, cluster-K
+ * and pair-SWAP kernels for M <= 128).
+ *
+ * fp8mm_autotune times every candidate for a (batch, M, N, K, scale_mode,
+ * element types) problem on the current device and remembers the fastest;
+ * from then on fp8_scaled_mm, _ex, _bmm, _layout, _bf16 and _host calls of
+ * that shape with automatic kernel choice (variant FP8MM_VARIANT_AUTO) use
+ * it. The operands are scratch buffers the call allocates, fills with
+ * pseudo-random finite fp8 codes and frees (copies rotated so that they
+ * exceed L2); each candidate runs 2 warm-up launches and is timed over 5
+ * launches with CUDA events on `stream`; the call synchronises the device
+ * and must not run during stream capture. options: element types only (NULL
+ * for e4m3 operands and bf16 output); batch >= 1. Returns FP8MM_OK, an
+ * argument error, FP8MM_ERR_CUDA, or FP8MM_ERR_TIMEOUT if a candidate's
+ * bounded wait ran out. fp8_scaled_mm_noalloc ignores tuned choices (its
+ * scratch bound is that of the built-in choice).
+ */
+int fp8mm_autotune(int64_t batch, int64_t M, int64_t N, int64_t K, int scale_mode,
+                   const fp8mm_options *options, void *stream);
+
+/* Forget every tuned choice of this process. */
+int fp8mm_autotune_clear(void);
+
+/* Number of tuned choices held. */
+int fp8mm_autotune_count(void);
+
+/*
+ * Write the tuned choices to a text file (one line per shape: device
+ * compute capability and SM count, batch, M, N, K, scale mode, element
+ * types, then the kernel, tile_n, split and the measured microseconds), or
+ * read such a file and add its entries (entries for other devices are kept
+ * and only used on a matching device). Load returns the number of entries
+ * read, or FP8MM_ERR_NULL / FP8MM_ERR_SHAPE (unreadable file or a malformed
+ * line; entries before it are kept).
+ */
+int fp8mm_autotune_save(const char *path);
+int fp8mm_autotune_load(const char *path);
+
+/*
  * Grow the current device's split-K workspace to at least `bytes` now, so
  * that later calls do not allocate.
  */
@@ -359,7 +402,8 @@ const char *fp8mm_last_error(void);
 const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mode);
 
 /* The same for a batch of `batch` products (fp8_scaled_bmm); tiles are per
- * item, units count the whole batch. */
+ * item, units count the whole batch. Both report a tuned choice
+ * (fp8mm_autotune) for e4m3 operands and bf16 output when one is held. */
 const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64_t K, int scale_mode);
 
 #ifdef __cplusplus

@@ -219,3 +219,43 @@ def test_python_layout_detection():
     assert fm._major(B.t().contiguous().t(), 0) == fm.MAJOR_K
     with pytest.raises(ValueError):
         fm._major(torch.zeros(6, 64, dtype=torch.float8_e4m3fn)[:, ::2], 1)
+
+
+def test_autotune_table_save_and_load_without_a_gpu(lib, tmp_path):
+    assert lib.fp8mm_autotune_clear() == 0
+    assert lib.fp8mm_autotune_count() == 0
+    good = tmp_path / "tuned.txt"
+    good.write_text("# comment\n10 3 152 1 512 3072 12288 1 0 0 0 3 256 3 27.5\n"
+                    "10 3 152 4 16 4096 4096 0 1 0 1 4 16 4 7.1\n")
+    assert lib.fp8mm_autotune_load(str(good).encode()) == 2
+    assert lib.fp8mm_autotune_count() == 2
+    out = tmp_path / "saved.txt"
+    assert lib.fp8mm_autotune_save(str(out).encode()) == 2
+    lines = [l for l in out.read_text().splitlines() if not l.startswith("#")]
+    assert sorted(l.split()[:14] for l in lines) == sorted(
+        l.split()[:14] for l in good.read_text().splitlines() if not l.startswith("#"))
+    assert lib.fp8mm_autotune_clear() == 0 and lib.fp8mm_autotune_count() == 0
+    assert lib.fp8mm_autotune_load(str(out).encode()) == 2
+    lib.fp8mm_autotune_clear()
+
+
+@pytest.mark.parametrize("line", [
+    "10 3 152 1 512 3072 12288 1 0 0 0 3 256 3",          # missing the time
+    "10 3 152 1 512 3072 12300 1 0 0 0 3 256 1 1.0",      # K not a multiple of 16
+    "10 3 152 1 512 3072 12288 1 0 0 0 4 16 3 1.0",       # cluster size 3
+    "10 3 152 1 512 3072 12288 1 0 0 0 1 64 1 1.0",       # TILE takes 128 or 256
+    "10 3 152 1 512 3072 12288 2 0 0 0 3 256 1 1.0",      # scale mode 2
+])
+def test_autotune_load_rejects_malformed_lines(lib, tmp_path, line):
+    f = tmp_path / "bad.txt"
+    f.write_text(line + "\n")
+    assert lib.fp8mm_autotune_load(str(f).encode()) == -2
+    assert lib.fp8mm_autotune_load(str(tmp_path / "absent.txt").encode()) == -1
+    lib.fp8mm_autotune_clear()
+
+
+def test_autotune_argument_errors(lib):
+    assert lib.fp8mm_autotune(1, 64, 64, 24, 0, None, None) == -2
+    assert lib.fp8mm_autotune(0, 64, 64, 64, 0, None, None) == -2
+    assert lib.fp8mm_autotune(1, 64, 64, 64, 3, None, None) == -4
+    assert lib.fp8mm_autotune(1, 64, 64, 64, 0, ctypes.byref(fm.Options(0, 0, 7, 0, 0, 0)), None) == -4
