@@ -502,7 +502,9 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
         }
     }
     if (tile_n == 0)
-        tile_n = variant == FP8MM_VARIANT_SWAP ? swap_tile_for(M) : 256;
+        tile_n = (variant == FP8MM_VARIANT_SWAP || variant == FP8MM_VARIANT_SWAPK || variant == FP8MM_VARIANT_SWAPPAIR)
+                     ? swap_tile_for(M)
+                     : 256;
     c.variant = variant;
     c.tile_n = tile_n;
     if (variant == FP8MM_VARIANT_SWAPK) {

@@ -7,13 +7,16 @@
 // N), so the accumulator is a 128 x BN slice of out^T. A cluster of CS CTAs
 // computes one tile: CTA r multiplies K blocks [r KB / CS, (r+1) KB / CS) into
 // its tensor memory, then copies the fp32 partial into its own shared memory
-// (the drained operand ring). After one cluster barrier, CTA r owns rows
-// [r 128 / CS, +128 / CS) of the tile: it sums the CS partials of those rows
-// in slice order 0..CS-1 (reading its peers' shared memory with
-// ld.shared::cluster), applies scale and bias, rounds to bf16 and stores.
-// A second cluster barrier keeps every CTA alive until its peers have read
-// its partial. With a batch, cluster c / (tiles_p tiles_q) picks the item. There is no global workspace, no atomic and no memory fence,
-// and the result does not depend on timing.
+// (the drained operand ring), row-major with a pitch of BN + 1 floats. CTA r
+// owns rows [r 128 / CS, +128 / CS) of the tile. After one cluster barrier
+// every CTA pushes each peer's rows of its partial into that peer's shared
+// memory with one bulk copy (cp.async.bulk shared::cta -> shared::cluster,
+// completing on the peer's mbarrier), so each owner sums the CS partials of
+// its rows from local shared memory, in slice order 0..CS-1, applies scale
+// and bias, rounds and stores. A second cluster barrier keeps every CTA alive
+// until the copies into it have landed. With a batch, cluster c / (tiles_p
+// tiles_q) picks the item. There is no global workspace, no atomic and no
+// memory fence, and the result does not depend on timing.
 //
 // One tile per cluster (no persistence): every thread executes exactly two
 // cluster barriers on every path, including after a bounded wait ran out, so
@@ -28,14 +31,28 @@ template <int BN, int CS>
 struct ClusterKCfg {
     static_assert(CS == 2 || CS == 4 || CS == 8, "cluster of 2, 4 or 8 CTAs");
     using Base = TileCfg<BN, true>;
-    static constexpr int kStages = Base::kStages;
     static constexpr int kStageBytes = Base::kStageBytes;
     static constexpr int kPBytes = Base::kPBytes;
     static constexpr int kTmemCols = BN < 32 ? 32 : BN;      // one fp32 accumulator
-    static constexpr int kPartialBytes = BN * kTileP * 4;    // [BN columns][128 rows] fp32
+    static constexpr int kPitch = BN + 1;                    // floats per partial row (bank spread)
+    static constexpr int kRows = kTileP / CS;                // rows each CTA owns
+    static constexpr int kSliceBytes = kRows * kPitch * 4;   // one owner's rows of one partial
+    static constexpr int kPartialBytes = kTileP * kPitch * 4;  // this CTA's partial [128][BN + 1]
+    static constexpr int kRecvBytes = (CS - 1) * kSliceBytes;  // peers' partials of the owned rows
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
-    static_assert(kPartialBytes <= kStages * kStageBytes, "partial must fit in the drained ring");
+    static constexpr int kScaleBytes = BN * 4;               // the tile's row-wise scales of A
+    // ring | receive buffer (its own, so peers may send at any time) | barriers | scales.
+    // Tiles up to 64 wide keep two CTAs per SM (at most ~113 KB each) so that
+    // clusters of a grid larger than the SMs fit at once; wider tiles use the SM.
+    static constexpr int kFixedBytes = 1024 + kRecvBytes + kBarBytes + kScaleBytes;
+    static constexpr int kBudget = BN <= 64 ? 115712 : 232448;
+    static constexpr int kStages = Base::kStages * kStageBytes + kFixedBytes <= kBudget
+                                       ? Base::kStages
+                                       : (kBudget - kFixedBytes) / kStageBytes;
+    static constexpr int kSmemBytes = kFixedBytes + kStages * kStageBytes;
+    static_assert(kStages >= 2, "operand ring too shallow");
+    static_assert(kPartialBytes <= kStages * kStageBytes, "the partial must fit in the drained ring");
+    static_assert(kSliceBytes % 16 == 0 && kPartialBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
     static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory");
 };
 
@@ -54,15 +71,21 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + pad;
     const uint32_t sbase = raw + pad;
 
-    const uint32_t bar0 = sbase + S * C::kStageBytes;
-    // full[S] | empty[S] | tfull | done
+    const uint32_t recv0 = sbase + S * C::kStageBytes;
+    const uint32_t bar0 = recv0 + C::kRecvBytes;
+    // full[S] | empty[S] | tfull | done | recv
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     const uint32_t tfull_bar = bar0 + 8u * (2 * S);
     const uint32_t done_bar = bar0 + 8u * (2 * S + 1);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + (bar0 - sbase) + 8 * (2 * S + 2));
+    const uint32_t recv_bar = bar0 + 8u * (2 * S + 2);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + (bar0 - sbase) + 8 * (2 * S + 3));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *partial = reinterpret_cast<float *>(smem);        // reuses the drained ring
+    // the drained operand ring holds this CTA's partial; the peers' slices
+    // land in a buffer of their own
+    float *partial = reinterpret_cast<float *>(smem);                                    // [128][kPitch]
+    const float *received = reinterpret_cast<const float *>(smem + (recv0 - sbase));    // [CS-1][kRows][kPitch]
+    float *scale_a_tile = reinterpret_cast<float *>(smem + (bar0 - sbase) + C::kBarBytes);   // [BN]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -82,8 +105,11 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(tfull_bar, 1);
         ptx::mbar_init(done_bar, 1);
+        ptx::mbar_init(recv_bar, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
+        // the peers' slices complete this barrier's phase 0 as transaction bytes
+        ptx::mbar_arrive_expect_tx(recv_bar, C::kRecvBytes);
         ptx::prefetch_tmap(&tmap_p);
         ptx::prefetch_tmap(&tmap_q);
     }
@@ -92,7 +118,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cluster_sync();    // every CTA's receive barrier is armed before any peer can send
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -102,6 +128,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::grid_dependency_wait();
 
     const Waiter W{abort_flag, p.status, p.timeout_cycles};
+    float red_sb = 0.0f, red_bias = 0.0f, red_stensor = 0.0f;   // loaded early by the epilogue threads
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer ---
@@ -169,12 +196,28 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------- accumulator -> fp32 partial in smem ---
+        constexpr int P = C::kPitch;
         const int q = warp & 3;
         const int row = q * 32 + lane;
+        // the tile's row-wise scales of A, staged while the main loop runs
+        if (p.rowwise && row < BN) {
+            const int m = tq * BN + row;
+            scale_a_tile[row] = m < p.M ? __ldg(for_item(p, item).scale_a + m) : 0.0f;
+        }
+        // this thread's output column n in the reduction below, its scale and bias
+        {
+            const KernelParams pb = for_item(p, item);
+            const int t = threadIdx.x - 64;   // the reduction's thread index
+            const int n = tp * kTileP + rank * C::kRows + (t % C::kRows);
+            const bool n_in = n < p.N;
+            red_sb = (pb.rowwise && n_in) ? __ldg(pb.scale_b + n) : 0.0f;
+            red_bias = (pb.bias != nullptr && n_in) ? bias_value(pb, n) : 0.0f;
+            red_stensor = tensor_scale(pb);
+        }
         if (kb1 == kb0) {
             // fewer K blocks than CTAs: this slice is empty and contributes zeros
             for (int col = 0; col < BN; ++col)
-                partial[col * kTileP + row] = 0.0f;
+                partial[row * P + col] = 0.0f;
         } else if (W.wait(tfull_bar, 0, 5)) {
             ptx::tc_fence_after();
             const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -184,63 +227,67 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
                 tmem_load_chunk<CH>(trow + c * CH, v);
 #pragma unroll
                 for (int j = 0; j < CH; ++j)
-                    partial[(c * CH + j) * kTileP + row] = v[j];
+                    partial[row * P + c * CH + j] = v[j];
+            }
+        }
+        ptx::fence_proxy_async_smem();   // the bulk copies read the partial through the async proxy
+        __syncwarp();
+        asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps: partial and scales written
+
+        if (threadIdx.x == 64) {
+            // --------- push each peer's rows of this partial to that peer ---
+            // The receiver keeps source slices in rank order, skipping itself.
+            // Sent even after an abort here (the launch is already marked
+            // failed in the status word), so that no peer waits out its budget.
+            for (int d = 0; d < CS; ++d) {
+                if (d == rank)
+                    continue;
+                const int slot = rank < d ? rank : rank - 1;
+                const uint32_t src = sbase + static_cast<uint32_t>(d * C::kSliceBytes);
+                const uint32_t dst = ptx::mapa_shared(recv0 + static_cast<uint32_t>(slot * C::kSliceBytes),
+                                                      static_cast<uint32_t>(d));
+                ptx::bulk_copy_to_peer(dst, src, C::kSliceBytes, ptx::mapa_shared(recv_bar, static_cast<uint32_t>(d)));
+            }
+        }
+
+        // Every epilogue thread waits (bounded) for the peers' copies into this
+        // CTA, even after an abort here: the peers send regardless, and the CTA
+        // must not leave while those copies land in its shared memory.
+        const bool received_all = W.drain(recv_bar, 0, 7);
+        if (received_all && !*abort_flag) {
+            // --------------------- reduce rows [rank * 128/CS, +128/CS) ---
+            constexpr int kRows = C::kRows;
+            constexpr int kColStep = 128 / kRows;               // = CS
+            const KernelParams pb = for_item(p, item);
+            const int t = threadIdx.x - 64;                     // 0..127
+            const int rl = t % kRows;                           // owned row, local index
+            const int r = rank * kRows + rl;                    // row of the tile (a column n of out)
+            const int n = tp * kTileP + r;
+            const bool n_in = n < p.N;
+            const int col0 = t / kRows;
+            constexpr int kItems = BN / kColStep;
+#pragma unroll 4
+            for (int i = 0; i < kItems; ++i) {
+                const int col = col0 + i * kColStep;
+                float acc = 0.0f;
+#pragma unroll
+                for (int sl = 0; sl < CS; ++sl) {
+                    const float v = sl == rank ? partial[r * P + col]
+                                               : received[((sl < rank ? sl : sl - 1) * kRows + rl) * P + col];
+                    acc = sl == 0 ? v : acc + v;
+                }
+                const int m = tq * BN + col;
+                if (n_in && m < p.M) {
+                    const float sc = pb.rowwise ? scale_a_tile[col] * red_sb : red_stensor;
+                    pb.out[static_cast<size_t>(m) * pb.N + n] = to_out(fmaf(acc, sc, red_bias), pb.out_f16);
+                }
             }
         }
         __syncwarp();
     }
 
     ptx::tc_fence_before();
-    ptx::cluster_sync();    // every slice's partial is in its CTA's shared memory
-
-    if (warp >= 2 && !*abort_flag) {
-        // ------------------------- reduce rows [rank * 128/CS, +128/CS) ---
-        const KernelParams pb = for_item(p, item);
-        constexpr int kRows = kTileP / CS;
-        constexpr int kColStep = 128 / kRows;               // = CS
-        const int t = threadIdx.x - 64;                     // 0..127
-        const int r = rank * kRows + t % kRows;             // row of the tile (a column n of out)
-        const int n = tp * kTileP + r;
-        const bool n_in = n < p.N;
-        const float sb = (pb.rowwise && n_in) ? __ldg(pb.scale_b + n) : 0.0f;
-        const float b = (pb.bias != nullptr && n_in) ? bias_value(pb, n) : 0.0f;
-        const float s_tensor = tensor_scale(pb);
-        const uint32_t local0 = ptx::smem_addr(partial);
-        // columns t / kRows, + CS, + 2 CS, ...: kItems per thread, processed
-        // kBatch at a time so that kBatch x CS remote loads are in flight
-        constexpr int kItems = BN / kColStep;
-        constexpr int kBatch = kItems < 8 ? kItems : 8;
-        static_assert(kItems % kBatch == 0, "column batches");
-        const int col0 = t / kRows;
-#pragma unroll 1
-        for (int i0 = 0; i0 < kItems; i0 += kBatch) {
-            float part[kBatch][CS];
-#pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-                const int col = col0 + (i0 + i) * kColStep;
-                const uint32_t off = static_cast<uint32_t>((col * kTileP + r) * 4);
-#pragma unroll
-                for (int s = 0; s < CS; ++s)
-                    part[i][s] =
-                        ptx::ld_shared_cluster_f32(ptx::mapa_shared(local0 + off, static_cast<uint32_t>(s)));
-            }
-#pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-                float acc = part[i][0];
-#pragma unroll
-                for (int s = 1; s < CS; ++s)
-                    acc += part[i][s];
-                const int m = tq * BN + col0 + (i0 + i) * kColStep;
-                if (n_in && m < p.M) {
-                    const float sc = pb.rowwise ? __ldg(pb.scale_a + m) * sb : s_tensor;
-                    pb.out[static_cast<size_t>(m) * pb.N + n] = to_out(fmaf(acc, sc, b), pb.out_f16);
-                }
-            }
-        }
-    }
-
-    __syncwarp();
-    ptx::cluster_sync();    // no CTA leaves while a peer may still read its partial
+    ptx::cluster_sync();    // no CTA leaves while a peer's copies or reads may involve it
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, C::kTmemCols);

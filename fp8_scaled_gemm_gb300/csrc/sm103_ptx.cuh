@@ -347,6 +347,19 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
     return v;
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory into a peer CTA's shared memory (cluster
+// address); completion is signalled as transaction bytes on the peer's
+// mbarrier (cluster address).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                  uint32_t bar_cluster)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster),
+                 "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+                 : "memory");
+}
+
 
 // ------------------------------------------ programmatic dependent launch ---
 
