@@ -220,10 +220,10 @@ int encode_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t
 
 // 16-bit output [batch, M, N] (N contiguous) written in boxes of 32 rows x
 // 64 columns of one item from a 128-byte-swizzled shared-memory stage.
-int encode_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N, bool f16, int64_t batch = 1)
+int encode_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N, bool f16, int64_t batch, int64_t ldo)
 {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(batch)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(N) * 2 * static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldo) * 2, static_cast<cuuint64_t>(ldo) * 2 * static_cast<cuuint64_t>(M)};
     cuuint32_t box[3] = {64, 32, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out,
@@ -651,9 +651,9 @@ int encode_and_dispatch(const Choice &c, const void *A, const void *B, void *out
                       c.variant == FP8MM_VARIANT_SWAPPAIR;
     // Row-major epilogues store through TMA when the output rows are 16-byte
     // aligned (TILE without split-K, PAIR); otherwise through plain stores.
-    if (!swap && c.split == 1 && (N % 8) == 0 &&
+    if (!swap && c.split == 1 && (N % 8) == 0 && (kp.ldo % 8) == 0 &&
         (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
-        int rc = encode_out_map(&mo, out, M, N, kp.out_f16 != 0, batch);
+        int rc = encode_out_map(&mo, out, M, N, kp.out_f16 != 0, batch, kp.ldo);
         if (rc != FP8MM_OK)
             return rc;
         kp.out_tma = 1;
@@ -697,7 +697,7 @@ uint32_t fmt_code(int t) { return t == FP8MM_TYPE_E5M2 ? 1u : 0u; }
 int run(const void *A, const void *B, const float *sa, const float *sb, int scale_mode, const void *bias,
         void *out, int64_t M, int64_t N, int64_t K, cudaStream_t stream, int variant, int tile_n, int split,
         int a_type = FP8MM_TYPE_E4M3, int b_type = FP8MM_TYPE_E4M3, int out_type = FP8MM_OUT_BF16,
-        int64_t batch = 1)
+        int64_t batch = 1, int64_t ldo = 0)
 {
     int rc = check_args(A, B, sa, sb, scale_mode, bias, out, M, N, K);
     if (rc != FP8MM_OK)
@@ -744,6 +744,7 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     kp.scale_b = sb;
     kp.bias = static_cast<const unsigned short *>(bias);
     kp.out = static_cast<unsigned short *>(out);
+    kp.ldo = ldo > 0 ? ldo : N;
     kp.status = d->status;
     {
         // The MMA's A side is the P operand: A for TILE / PAIR, Bt for the SWAP kinds.
@@ -764,7 +765,7 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     kp.num_units = c.units;
     kp.rowwise = scale_mode == FP8MM_SCALE_ROWWISE ? 1 : 0;
     kp.group = 8;
-    kp.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % 8) == 0) ? 1 : 0;
+    kp.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % 8) == 0 && (kp.ldo % 8) == 0) ? 1 : 0;
     kp.timeout_cycles = wait_limit();
     kp.inject_stop_after = static_cast<int>(g_inject_stop_after.load());
     if (c.split > 1 && c.variant != FP8MM_VARIANT_SWAPK) {
@@ -957,12 +958,13 @@ std::vector<Candidate> tune_candidates(int64_t M, int64_t K)
 }
 
 // Streams and events of the host-memory entry point (one set per device).
-constexpr int kHostChunks = 8;
+constexpr int kHostChunks = 4;   // chunks of A's rows and of Bt's rows: up to 4 x 4 output blocks
 struct HostPipe {
     bool ready = false;
     cudaStream_t in = nullptr, mm = nullptr, out = nullptr;
     cudaEvent_t start = nullptr, done = nullptr;
-    cudaEvent_t a_ready[kHostChunks] = {}, mm_done[kHostChunks] = {};
+    cudaEvent_t a_ready[kHostChunks] = {}, b_ready[kHostChunks] = {};
+    cudaEvent_t mm_done[kHostChunks * kHostChunks] = {};
 };
 HostPipe g_pipe[kMaxDevices];
 
@@ -983,7 +985,11 @@ int host_pipe(HostPipe **out)
             return cuda_fail(e, "host pipeline set-up");
         for (int i = 0; i < kHostChunks; ++i) {
             if ((e = cudaEventCreateWithFlags(&hp.a_ready[i], cudaEventDisableTiming)) != cudaSuccess ||
-                (e = cudaEventCreateWithFlags(&hp.mm_done[i], cudaEventDisableTiming)) != cudaSuccess)
+                (e = cudaEventCreateWithFlags(&hp.b_ready[i], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e, "host pipeline set-up");
+        }
+        for (int i = 0; i < kHostChunks * kHostChunks; ++i) {
+            if ((e = cudaEventCreateWithFlags(&hp.mm_done[i], cudaEventDisableTiming)) != cudaSuccess)
                 return cuda_fail(e, "host pipeline set-up");
         }
         hp.ready = true;
@@ -1177,11 +1183,16 @@ int fp8_scaled_mm_host(const void *A, const void *B, const float *scale_a, const
     void *dbias = bias ? d->stage[4] : nullptr;
     uint8_t *dout = static_cast<uint8_t *>(d->stage[5]);
 
-    // Rows of A and out are cut into chunks: chunk i's GEMM starts as soon
-    // as its rows of A have arrived (after the scales, bias and all of B),
-    // and its rows of out leave while later chunks copy in and compute.
-    const int64_t rows = std::max<int64_t>(1024, ((cdiv(M, kHostChunks) + 255) / 256) * 256);
-    const int chunks = static_cast<int>(cdiv(M, rows));
+    // A's rows and Bt's rows (B's columns) are cut into up to 4 chunks each,
+    // and out into the blocks they make. Inputs arrive in a growing square:
+    // after A chunk k and Bt chunk k, every block (k, j <= k) and (i < k, k)
+    // has its operands, so it is computed and copied back while later
+    // chunks arrive; both directions of the host link stay busy.
+    const int64_t pa = std::min<int64_t>(kHostChunks, cdiv(M, 1024));
+    const int64_t pb = std::min<int64_t>(kHostChunks, cdiv(N, 1024));
+    const int64_t rows_a = ((cdiv(M, pa) + 255) / 256) * 256, rows_b = ((cdiv(N, pb) + 255) / 256) * 256;
+    const int ca = static_cast<int>(cdiv(M, rows_a)), cb = static_cast<int>(cdiv(N, rows_b));
+    const bool rowwise = scale_mode == FP8MM_SCALE_ROWWISE;
     cudaError_t e;
 #define FP8MM_TRY(call, what)      \
     if ((e = (call)) != cudaSuccess) \
@@ -1192,23 +1203,50 @@ int fp8_scaled_mm_host(const void *A, const void *B, const float *scale_a, const
     FP8MM_TRY(cudaMemcpyAsync(dsb, scale_b, bytes[3], cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync(H2D)");
     if (bias)
         FP8MM_TRY(cudaMemcpyAsync(dbias, bias, bytes[4], cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync(H2D)");
-    FP8MM_TRY(cudaMemcpyAsync(dB, B, bytes[1], cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync(H2D)");
-    for (int i = 0; i < chunks; ++i) {
-        const int64_t r0 = i * rows, mi = std::min<int64_t>(rows, M - r0);
-        FP8MM_TRY(cudaMemcpyAsync(dA + r0 * K, static_cast<const uint8_t *>(A) + r0 * K,
-                                  static_cast<size_t>(mi * K), cudaMemcpyHostToDevice, hp->in),
-                  "cudaMemcpyAsync(H2D)");
-        FP8MM_TRY(cudaEventRecord(hp->a_ready[i], hp->in), "cudaEventRecord");
+    auto block = [&](int i, int j) -> int {
+        const int64_t r0 = i * rows_a, mi = std::min<int64_t>(rows_a, M - r0);
+        const int64_t c0 = j * rows_b, nj = std::min<int64_t>(rows_b, N - c0);
         FP8MM_TRY(cudaStreamWaitEvent(hp->mm, hp->a_ready[i], 0), "cudaStreamWaitEvent");
-        rc = run(dA + r0 * K, dB, scale_mode == FP8MM_SCALE_ROWWISE ? dsa + r0 : dsa, dsb, scale_mode, dbias,
-                 dout + r0 * N * 2, mi, N, K, hp->mm, FP8MM_VARIANT_AUTO, 0, 0);
-        if (rc != FP8MM_OK)
-            return rc;
-        FP8MM_TRY(cudaEventRecord(hp->mm_done[i], hp->mm), "cudaEventRecord");
-        FP8MM_TRY(cudaStreamWaitEvent(hp->out, hp->mm_done[i], 0), "cudaStreamWaitEvent");
-        FP8MM_TRY(cudaMemcpyAsync(static_cast<uint8_t *>(out) + r0 * N * 2, dout + r0 * N * 2,
-                                  static_cast<size_t>(mi * N * 2), cudaMemcpyDeviceToHost, hp->out),
-                  "cudaMemcpyAsync(D2H)");
+        FP8MM_TRY(cudaStreamWaitEvent(hp->mm, hp->b_ready[j], 0), "cudaStreamWaitEvent");
+        const int brc = run(dA + r0 * K, dB + c0 * K, rowwise ? dsa + r0 : dsa, rowwise ? dsb + c0 : dsb, scale_mode,
+                            bias ? static_cast<uint8_t *>(dbias) + c0 * 2 : nullptr, dout + (r0 * N + c0) * 2, mi, nj,
+                            K, hp->mm, FP8MM_VARIANT_AUTO, 0, 0, FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16,
+                            1, N);
+        if (brc != FP8MM_OK)
+            return brc;
+        cudaEvent_t done_ij = hp->mm_done[i * kHostChunks + j];
+        FP8MM_TRY(cudaEventRecord(done_ij, hp->mm), "cudaEventRecord");
+        FP8MM_TRY(cudaStreamWaitEvent(hp->out, done_ij, 0), "cudaStreamWaitEvent");
+        FP8MM_TRY(cudaMemcpy2DAsync(static_cast<uint8_t *>(out) + (r0 * N + c0) * 2, static_cast<size_t>(N) * 2,
+                                    dout + (r0 * N + c0) * 2, static_cast<size_t>(N) * 2, static_cast<size_t>(nj) * 2,
+                                    static_cast<size_t>(mi), cudaMemcpyDeviceToHost, hp->out),
+                  "cudaMemcpy2DAsync(D2H)");
+        return FP8MM_OK;
+    };
+    for (int k = 0; k < std::max(ca, cb); ++k) {
+        if (k < ca) {
+            const int64_t r0 = k * rows_a, mi = std::min<int64_t>(rows_a, M - r0);
+            FP8MM_TRY(cudaMemcpyAsync(dA + r0 * K, static_cast<const uint8_t *>(A) + r0 * K, static_cast<size_t>(mi * K),
+                                      cudaMemcpyHostToDevice, hp->in),
+                      "cudaMemcpyAsync(H2D)");
+            FP8MM_TRY(cudaEventRecord(hp->a_ready[k], hp->in), "cudaEventRecord");
+        }
+        if (k < cb) {
+            const int64_t c0 = k * rows_b, nj = std::min<int64_t>(rows_b, N - c0);
+            FP8MM_TRY(cudaMemcpyAsync(dB + c0 * K, static_cast<const uint8_t *>(B) + c0 * K, static_cast<size_t>(nj * K),
+                                      cudaMemcpyHostToDevice, hp->in),
+                      "cudaMemcpyAsync(H2D)");
+            FP8MM_TRY(cudaEventRecord(hp->b_ready[k], hp->in), "cudaEventRecord");
+        }
+        // the blocks that chunk k completes: row k against columns 0..k, then column k against rows 0..k-1
+        if (k < ca)
+            for (int j = 0; j <= std::min(k, cb - 1); ++j)
+                if ((rc = block(k, j)) != FP8MM_OK)
+                    return rc;
+        if (k < cb)
+            for (int i = 0; i < std::min(k, ca); ++i)
+                if ((rc = block(i, k)) != FP8MM_OK)
+                    return rc;
     }
     FP8MM_TRY(cudaEventRecord(hp->done, hp->out), "cudaEventRecord");
     FP8MM_TRY(cudaStreamWaitEvent(s, hp->done, 0), "cudaStreamWaitEvent");
@@ -1656,6 +1694,7 @@ extern "C" int fp8_scaled_mm_noalloc(const void *A, const void *B, const float *
     kp.scale_b = scale_b;
     kp.bias = static_cast<const unsigned short *>(bias);
     kp.out = static_cast<unsigned short *>(out);
+    kp.ldo = N;
     kp.status = reinterpret_cast<int *>(d->scratch);
     kp.counters = reinterpret_cast<unsigned int *>(d->scratch + kNoAllocStatusBytes);
     kp.ws = reinterpret_cast<float *>(d->scratch + kNoAllocStatusBytes + kNoAllocCounterBytes);

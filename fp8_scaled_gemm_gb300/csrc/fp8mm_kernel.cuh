@@ -82,6 +82,7 @@ struct KernelParams {
     const float *scale_b;           // batch x (1 or N) values
     const unsigned short *bias;     // N values (output type) or nullptr
     unsigned short *out;            // [batch, M, N] row-major, bf16 or fp16 bit patterns
+    long long ldo;                  // elements between output rows (N, or more for a block of a larger matrix)
     float *ws;                      // split-K partial tiles (splits > 1)
     unsigned int *counters;         // split-K arrivals, kCountersPerTile per output tile
     int *status;                    // device status word
@@ -217,7 +218,7 @@ __device__ __forceinline__ KernelParams for_item(const KernelParams &p, int b)
     KernelParams q = p;
     q.scale_a += p.rowwise ? static_cast<size_t>(b) * p.M : static_cast<size_t>(b);
     q.scale_b += p.rowwise ? static_cast<size_t>(b) * p.N : static_cast<size_t>(b);
-    q.out += static_cast<size_t>(b) * p.M * p.N;
+    q.out += static_cast<size_t>(b) * p.M * p.ldo;
     return q;
 }
 
@@ -273,7 +274,7 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
         }
         if (m >= p.M)
             return;
-        unsigned short *orow = p.out + static_cast<size_t>(m) * p.N;
+        unsigned short *orow = p.out + static_cast<size_t>(m) * p.ldo;
         if (p.vec_store && qbase + CH <= p.N) {
 #pragma unroll
             for (int j = 0; j < CH; j += 8) {
@@ -307,7 +308,7 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
         for (int j = 0; j < CH; ++j) {
             const int m = qbase + j;
             if (m < p.M)
-                p.out[static_cast<size_t>(m) * p.N + n] = to_out(y[j], p.out_f16);
+                p.out[static_cast<size_t>(m) * p.ldo + n] = to_out(y[j], p.out_f16);
         }
     }
 }
@@ -391,7 +392,7 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                 const uint8_t *src =
                     stage + buf * 4096u + r * 128 + ((((lane >> 2) ^ (r & 7)) & 7) * 16) + (lane & 3) * 4;
                 const uint32_t pr = *reinterpret_cast<const uint32_t *>(src);
-                unsigned short *dst = p.out + static_cast<size_t>(mm) * p.N + col;
+                unsigned short *dst = p.out + static_cast<size_t>(mm) * p.ldo + col;
                 if (col < p.N)
                     dst[0] = static_cast<unsigned short>(pr & 0xFFFFu);
                 if (col + 1 < p.N)

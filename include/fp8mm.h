@@ -160,12 +160,15 @@ int fp8_scaled_mm_ex(const void *A, const void *B,
  * pointers (pinned memory gives full copy bandwidth; pageable works). The
  * call copies the inputs to device staging buffers owned by the library
  * (grown on demand, kept per device), computes, copies the result back into
- * `out` and synchronises `stream` before returning. Internally the rows of A
- * and out are cut into up to 8 chunks on three library streams, so that
- * chunk i computes while later rows of A arrive and earlier rows of out
- * leave; the work is ordered after everything already queued on `stream`.
- * Same layouts, constraints and result as fp8_scaled_mm (the chunks run the
- * same kernels as fp8_scaled_mm would for their row counts).
+ * `out` and synchronises `stream` before returning. Internally A's rows and
+ * B's columns are cut into up to 4 chunks each and out into the blocks they
+ * form; the chunks arrive in a growing square (A chunk k, then B chunk k,
+ * after which every block of row k and column k has its operands), so that
+ * blocks are computed and copied back while later chunks arrive, on three
+ * library streams; the work is ordered after everything already queued on
+ * `stream`. Same layouts, constraints and result as fp8_scaled_mm within the
+ * parity tolerance (each block runs the kernel fp8_scaled_mm would choose
+ * for the block's shape; blocks start at multiples of 256 rows and columns).
  */
 int fp8_scaled_mm_host(const void *A, const void *B,
                        const float *scale_a, const float *scale_b, int scale_mode,

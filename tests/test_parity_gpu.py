@@ -253,3 +253,17 @@ def test_rowwise_sweep_sampled(M, N, K):
     _need_gpu()
     stats, _, _ = run_and_compare(M, N, K, 1, 42, False, sample=True, n_random=32)
     _assert_ok(stats, f"sweep {(M, N, K)}")
+
+
+def test_host_entry_in_blocks():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+    # 3000 x 2500: 3 x 3 blocks of the growing-square schedule, ragged in
+    # both directions; row-wise scales and bias are sliced per block
+    for mode, bias in ((1, True), (0, False)):
+        inp = make_inputs(3000, 2500, 528, mode, seed=13, with_bias=bias)
+        host = fm.fp8_scaled_mm_host(inp.a_q.pin_memory(), inp.bt_q.pin_memory().t(),
+                                     inp.scale_a.pin_memory(), inp.scale_b.pin_memory(), mode,
+                                     bias=None if inp.bias is None else inp.bias.pin_memory())
+        _assert_ok(compare(bf16_bits(host), inp), f"host blocks mode{mode}")
