@@ -50,6 +50,9 @@ struct DeviceState {
     int cc_major = 0, cc_minor = 0;
     int *status = nullptr;               // in-kernel status word
     unsigned int *qscratch = nullptr;    // per-tensor quantisation: per-CTA maxima + counter
+    float *sk_ws = nullptr;              // stream-K: one fp32 partial tile per CTA pair
+    size_t sk_ws_bytes = 0;
+    unsigned int *sk_flags = nullptr;    // stream-K: 16 flags per CTA pair (zero between launches)
     float *ws = nullptr;                 // split-K partial tiles
     size_t ws_bytes = 0;
     unsigned int *counters = nullptr;    // split-K arrivals
@@ -245,6 +248,7 @@ struct Choice {
     int tile_n;
     int split;
     int tiles_p, tiles_q, kblocks, units, grid;
+    int sk_tiles;  // PAIR: tiles whose K blocks are spread over all pairs (stream-K), 0: none
 };
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -285,6 +289,39 @@ double tile128_time(int64_t tiles, int kblocks, int s, int sms)
 {
     const double waves = static_cast<double>(cdiv(tiles * s, sms));
     return waves * static_cast<double>(cdiv(kblocks, s)) * 0.30 + (s > 1 ? 3.5 + 1.1 * s : 0.0);
+}
+
+// Stream-K for the pair kernel: the tiles of the last partial wave plus one
+// full wave (or all tiles when there is less than one wave) have their K
+// blocks spread evenly over all pairs, so that every pair does the same work.
+// Returns the number of such tiles, 0 when the tiles already fill whole waves
+// or the pieces would be too short (under 4 K blocks per pair) or split a
+// tile over more than 8 pairs.
+int64_t stream_k_tiles(int64_t tiles, int kblocks, int pairs)
+{
+    const int64_t full = tiles / pairs, rem = tiles % pairs;
+    if (rem == 0)
+        return 0;
+    const int64_t sk = rem + (full >= 1 ? pairs : 0);
+    const double share = static_cast<double>(sk) * kblocks / pairs;   // K blocks per pair
+    if (share < 4.0 || kblocks > 7.0 * share)
+        return 0;
+    return sk;
+}
+
+// Modelled time (us) of the pair kernel with stream-K, for at least one full
+// wave of tiles: the last partial wave's idle time, (1 - rem / pairs) x a
+// tile's K blocks, is saved, and each owner's fix-up (reading a piece's fp32
+// partial back through L2 at the end) costs about 8 us. Fitted to GB300
+// timings: stream-K won at 8192^3 (rem 36 of 76, 64 K blocks) and
+// 2304 x 3072 x 12288 (rem 32, 96 K blocks) and lost where the saving is
+// smaller (4096^3, the K = 3072 shapes, a nearly full last wave).
+double pair_sk_time(int64_t tiles, int kblocks, int pairs)
+{
+    if (tiles < pairs || stream_k_tiles(tiles, kblocks, pairs) == 0)
+        return 1e300;
+    const double rem = static_cast<double>(tiles % pairs);
+    return pair_time(tiles, kblocks, 1, pairs) - (1.0 - rem / pairs) * kblocks * 0.32 + 8.0;
 }
 
 // Split-K factor of the pair kernel: the s in 1..8 of least modelled time,
@@ -490,10 +527,11 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
             const int64_t tt = cdiv(M, 128) * cdiv(N, 128) * batch;
             const int ps = pick_pair_split(pt, kb, sms / 2);
             const int ts = pick_tile128_split(tt, kb, sms);
-            if (pair_time(pt, kb, ps, sms / 2) <= tile128_time(tt, kb, ts, sms)) {
+            const double t_pair = std::min(pair_time(pt, kb, ps, sms / 2), pair_sk_time(pt, kb, sms / 2));
+            if (t_pair <= tile128_time(tt, kb, ts, sms)) {
                 variant = FP8MM_VARIANT_PAIR;
                 tile_n = 256;
-                split = ps;
+                split = pair_sk_time(pt, kb, sms / 2) < pair_time(pt, kb, ps, sms / 2) ? -1 : ps;   // -1: stream-K
             } else {
                 variant = FP8MM_VARIANT_TILE;
                 tile_n = 128;
@@ -531,7 +569,15 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
         c.tiles_p = static_cast<int>(cdiv(M, 256));
         c.tiles_q = static_cast<int>(cdiv(N, tile_n));
         const int64_t ptiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q * batch;
-        if (split <= 0)
+        if (split < 0) {
+            // stream-K (chosen above, or asked for with split_k = -1)
+            c.sk_tiles = static_cast<int>(stream_k_tiles(ptiles, c.kblocks, sms / 2));
+            c.split = 1;
+            c.units = static_cast<int>(ptiles - c.sk_tiles);
+            c.grid = c.sk_tiles > 0 ? 2 * (sms / 2) : 2 * static_cast<int>(std::min<int64_t>(c.units, sms / 2));
+            return c;
+        }
+        if (split == 0)
             split = pick_pair_split(ptiles, c.kblocks, sms / 2);
         c.split = std::max(1, std::min(split, c.kblocks));
         c.units = static_cast<int>(ptiles * c.split);
@@ -711,7 +757,7 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
         return FP8MM_ERR_MODE;
     if (variant != FP8MM_VARIANT_AUTO && tile_n != 0 && !tile_n_supported(variant, tile_n))
         return FP8MM_ERR_MODE;
-    if (split < 0 || split > 16)
+    if (split < -1 || split > 16 || (split == -1 && variant != FP8MM_VARIANT_PAIR))
         return FP8MM_ERR_MODE;
     if ((a_type != FP8MM_TYPE_E4M3 && a_type != FP8MM_TYPE_E5M2) ||
         (b_type != FP8MM_TYPE_E4M3 && b_type != FP8MM_TYPE_E5M2) ||
@@ -768,6 +814,36 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     kp.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % 8) == 0 && (kp.ldo % 8) == 0) ? 1 : 0;
     kp.timeout_cycles = wait_limit();
     kp.inject_stop_after = static_cast<int>(g_inject_stop_after.load());
+    if (c.sk_tiles > 0) {
+        const int pairs = d->sms / 2;
+        const size_t ws_bytes = static_cast<size_t>(pairs) * 256 * c.tile_n * sizeof(float);
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!d->sk_flags) {
+            cudaError_t e = cudaMalloc(&d->sk_flags, static_cast<size_t>(pairs) * 16 * sizeof(unsigned int));
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaMalloc(stream-K flags)");
+            e = cudaMemset(d->sk_flags, 0, static_cast<size_t>(pairs) * 16 * sizeof(unsigned int));
+            if (e == cudaSuccess)
+                e = cudaDeviceSynchronize();
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaMemset(stream-K flags)");
+        }
+        if (ws_bytes > d->sk_ws_bytes) {
+            cudaError_t e = cudaDeviceSynchronize();
+            if (e == cudaSuccess && d->sk_ws)
+                e = cudaFree(d->sk_ws);
+            d->sk_ws = nullptr;
+            d->sk_ws_bytes = 0;
+            if (e == cudaSuccess)
+                e = cudaMalloc(&d->sk_ws, ws_bytes);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaMalloc(stream-K workspace)");
+            d->sk_ws_bytes = ws_bytes;
+        }
+        kp.sk_tiles = c.sk_tiles;
+        kp.sk_ws = d->sk_ws;
+        kp.sk_flags = d->sk_flags;
+    }
     if (c.split > 1 && c.variant != FP8MM_VARIANT_SWAPK) {
         const int64_t tiles = static_cast<int64_t>(c.tiles_p) * c.tiles_q * batch;
         const size_t tile_rows = c.variant == FP8MM_VARIANT_PAIR ? 256 : fp8mm::kTileP;
@@ -947,6 +1023,7 @@ std::vector<Candidate> tune_candidates(int64_t M, int64_t K)
     for (int s : {1, 2, 3, 4, 6, 8})
         if (s == 1 || kb / s >= 4)
             c.push_back({FP8MM_VARIANT_PAIR, 256, s});
+    c.push_back({FP8MM_VARIANT_PAIR, 256, -1});   // stream-K
     c.push_back({FP8MM_VARIANT_PAIR, 128, 1});
     for (int s : {1, 2, 3, 4, 6, 8, 12, 16})
         if (s == 1 || kb / s >= 2)
@@ -1349,14 +1426,14 @@ const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64
     }
     const Choice c = choose(M, N, K, d->sms, variant, tile_n, split, batch);
     char buf[160];
-    snprintf(buf, sizeof buf, "%s tile_n=%d split=%d tiles=%dx%d units=%d grid=%d",
+    snprintf(buf, sizeof buf, "%s tile_n=%d split=%d tiles=%dx%d units=%d grid=%d%s",
              c.variant == FP8MM_VARIANT_TILE    ? "tile"
              : c.variant == FP8MM_VARIANT_PAIR  ? "pair"
              : c.variant == FP8MM_VARIANT_SWAPK ? "swapk"
              : c.variant == FP8MM_VARIANT_SWAPPAIR ? "swappair"
                                                 : "swap",
              c.tile_n, c.split, c.tiles_p, c.tiles_q,
-             c.units, c.grid);
+             c.units, c.grid, c.sk_tiles > 0 ? (" stream_k_tiles=" + std::to_string(c.sk_tiles)).c_str() : "");
     t_describe = buf;
     return t_describe.c_str();
 }
@@ -1546,7 +1623,8 @@ int fp8mm_autotune_load(const char *path)
                            (k.mode == 0 || k.mode == 1) && (k.a_type == 0 || k.a_type == 1) &&
                            (k.b_type == 0 || k.b_type == 1) && (k.out_type == 0 || k.out_type == 1) &&
                            v.variant >= FP8MM_VARIANT_TILE && v.variant <= FP8MM_VARIANT_SWAPPAIR &&
-                           tile_n_supported(v.variant, v.tile_n) && v.split >= 1 && v.split <= 16 &&
+                           tile_n_supported(v.variant, v.tile_n) &&
+                           (v.split >= 1 || (v.split == -1 && v.variant == FP8MM_VARIANT_PAIR)) && v.split <= 16 &&
                            !(v.variant == FP8MM_VARIANT_SWAPK && v.split != 2 && v.split != 4 && v.split != 8) &&
                            !(v.variant == FP8MM_VARIANT_SWAPPAIR && v.split != 1);
         if (!valid) {

@@ -98,6 +98,12 @@ struct KernelParams {
     int inject_stop_after;          // test hook: CTA 0's producer stops after this many K blocks (-1: off)
     uint32_t idesc_fmt;             // operand format bits of the MMA instruction descriptor
     int out_f16;                    // 1: fp16 output and bias, 0: bf16
+    // Stream-K (pair kernel, splits == 1): the last sk_tiles tiles of the tile
+    // order are not given out whole; their K blocks are divided evenly over
+    // all CTA pairs (num_units then counts the whole tiles before them).
+    int sk_tiles;
+    float *sk_ws;                   // per pair: one fp32 partial tile, [BN/4][256][4]
+    unsigned int *sk_flags;         // per pair: 16 "partial written" flags (one per epilogue warp)
     unsigned long long timeout_cycles;
 };
 
@@ -161,6 +167,26 @@ struct Waiter {
         const unsigned long long t0 = static_cast<unsigned long long>(clock64());
         while (true) {
             if (ptx::mbar_try_wait_cluster(bar, parity))
+                return true;
+            if (*abort_flag)
+                return false;
+            if (static_cast<unsigned long long>(clock64()) - t0 > limit) {
+                *abort_flag = 1;
+                atomicCAS(status, 0, kStatusTimeoutBase | where);
+                return false;
+            }
+        }
+    }
+
+    // Bounded wait until the global flag *f is non-zero (set by another CTA
+    // with a release store); false when this CTA is aborting.
+    __device__ __forceinline__ bool wait_flag(const unsigned int *f, int where) const
+    {
+        if (ptx::ld_acquire_gpu_u32(f) != 0u)
+            return true;
+        const unsigned long long t0 = static_cast<unsigned long long>(clock64());
+        while (true) {
+            if (ptx::ld_acquire_gpu_u32(f) != 0u)
                 return true;
             if (*abort_flag)
                 return false;
@@ -324,11 +350,19 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
 // segments. `chunks` counts the blocks this warp has staged so far; before
 // the stage is rewritten, the TMA store of the previous block must have read
 // it (that wait comes after the next block's TMEM loads and arithmetic).
+//
+// With add_count > 0 (stream-K owner), the fp32 partials of add_count later
+// pieces of the tile are added to the accumulator first, in piece order:
+// piece k's partial starts at add_base + k add_stride (float4 units), laid out
+// [column / 4][256 rows][4]; this thread's row in it is prow, and the warp's
+// first column within the tile is colt0.
 template <int BN, int NBUF>
 __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, const CUtensorMap *tmap_out,
                                                      uint32_t trow, int m_row0, int n0, int lane,
                                                      uint8_t *stage, uint32_t stage_smem, uint32_t &chunks,
-                                                     float s_tensor, int item)
+                                                     float s_tensor, int item, const float4 *add_base = nullptr,
+                                                     int add_count = 0, size_t add_stride = 0, int prow = 0,
+                                                     int colt0 = 0)
 {
     constexpr unsigned kAll = 0xffffffffu;
     const int m = m_row0 + lane;
@@ -341,6 +375,21 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
         for (int h = 0; h < 2; ++h) {
             float v[32];
             ptx::tmem_ld_32cols(trow + static_cast<uint32_t>(c * 64 + h * 32), v);
+            for (int k = 0; k < add_count; ++k) {
+                const float4 *src = add_base + static_cast<size_t>(k) * add_stride +
+                                    static_cast<size_t>((colt0 + c * 64 + h * 32) / 4) * 256 + prow;
+                float4 x[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    x[g] = __ldcg(src + g * 256);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    v[4 * g] += x[g].x;
+                    v[4 * g + 1] += x[g].y;
+                    v[4 * g + 2] += x[g].z;
+                    v[4 * g + 3] += x[g].w;
+                }
+            }
             const int nl = nb + h * 32 + lane;
             const bool in = nl < p.N;
             const float sbl = (p.rowwise && in) ? __ldg(p.scale_b + nl) : 0.0f;

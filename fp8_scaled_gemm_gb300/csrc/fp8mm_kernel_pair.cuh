@@ -48,6 +48,61 @@ struct PairCfg {
     static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
 };
 
+// The work of one CTA pair, in order: whole units (tile, K slice) as in the
+// 1-SM kernels, cluster, cluster + pairs, ..., then, with stream-K, the pair's
+// share of the K blocks of the last p.sk_tiles tiles: iterations
+// [c I / P, (c+1) I / P) of I = sk_tiles x kblocks, tile-major with K inner,
+// cut at tile boundaries into pieces. The piece of a tile that starts at K
+// block 0 (kind 1) is the last of the tile's pieces in time (it ends its
+// pair's range); it adds the partials of the tile's later pieces (kind 2),
+// which start the ranges of the following pairs and were written first.
+struct PairWork {
+    Unit u;
+    int kind;   // 0: a unit as in the 1-SM kernels; 1: stream-K owner; 2: stream-K contributor
+};
+
+struct PairSchedule {
+    int next_u, step, units;
+    long long it, end;
+    int kblocks, first_sk_tile;
+
+    __device__ __forceinline__ PairSchedule(const KernelParams &p, int pair, int pairs)
+        : next_u(pair), step(pairs), units(p.num_units), kblocks(p.kblocks),
+          first_sk_tile(p.num_units)
+    {
+        const long long iters = static_cast<long long>(p.sk_tiles) * p.kblocks;
+        it = iters * pair / pairs;
+        end = iters * (pair + 1) / pairs;
+    }
+
+    __device__ __forceinline__ bool next(const KernelParams &p, PairWork &w)
+    {
+        if (next_u < units) {
+            w.u = decode_unit(next_u, p);
+            w.kind = 0;
+            next_u += step;
+            return true;
+        }
+        if (it >= end)
+            return false;
+        const long long t = it / kblocks;
+        const int k0 = static_cast<int>(it - t * kblocks);
+        const long long stop = min(end, (t + 1) * kblocks);
+        w.u = decode_unit(first_sk_tile + static_cast<int>(t), p);   // splits == 1 with stream-K
+        w.u.kb0 = k0;
+        w.u.kb1 = k0 + static_cast<int>(stop - it);
+        w.kind = (k0 == 0 && w.u.kb1 == kblocks) ? 0 : (k0 == 0 ? 1 : 2);
+        it = stop;
+        return true;
+    }
+};
+
+// Iteration where pair c's stream-K range starts.
+__device__ __forceinline__ long long sk_range_start(const KernelParams &p, int c, int pairs)
+{
+    return static_cast<long long>(p.sk_tiles) * p.kblocks * c / pairs;
+}
+
 // Units: (256-row tile of P, BN-row tile of Q, K slice); p.tiles_p counts
 // 256-row tiles. With p.splits > 1 (row-major form only) each slice writes its
 // fp32 partial to the workspace and the last slice to arrive, per epilogue
@@ -125,8 +180,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
-                const Unit w = decode_unit(u, p);
+            PairSchedule sched(p, cluster_id, num_clusters);
+            PairWork pw;
+            while (ok && sched.next(p, pw)) {
+                const Unit &w = pw.u;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!W.wait(empty_bar(stage), phase ^ 1u, 0)) {
                         ok = false;
@@ -174,8 +231,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
-                const Unit w = decode_unit(u, p);
+            PairSchedule sched(p, cluster_id, num_clusters);
+            PairWork pw;
+            while (ok && sched.next(p, pw)) {
+                const Unit &w = pw.u;
                 if (!W.wait_cluster(tempty_bar(acc), acc_phase ^ 1u, 1))
                     break;
                 ptx::tc_fence_after();
@@ -222,8 +281,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
         uint32_t chunks = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int u = cluster_id; u < p.num_units; u += num_clusters) {
-            const Unit w = decode_unit(u, p);
+        PairSchedule sched(p, cluster_id, num_clusters);
+        PairWork pw;
+        while (sched.next(p, pw)) {
+            const Unit &w = pw.u;
             const KernelParams pb = for_item(p, w.b);
             const float s_tensor = tensor_scale(pb);
             if (!W.wait(tfull_bar(acc), acc_phase, 5))
@@ -231,12 +292,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
             ptx::tc_fence_after();
             const uint32_t trow =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            if (p.splits == 1) {
+            constexpr size_t kSlot = static_cast<size_t>(256) * BN / 4;   // float4 per stream-K partial
+            const int prow_sk = static_cast<int>(rank) * 128 + q * 32 + lane;  // row within the pair tile
+            unsigned int *flag_base = p.sk_flags + static_cast<int>(rank) * 8 + ew;   // + 16 per pair
+            if (pw.kind == 2) {
                 if constexpr (!SWAP) {
+                    // stream-K contributor: this piece's partial into the pair's
+                    // slot, then the warp's flag (release) for the tile's owner
+                    float4 *mine = reinterpret_cast<float4 *>(p.sk_ws) + static_cast<size_t>(cluster_id) * kSlot;
+#pragma unroll 1
+                    for (int c = col0 / CH; c < (col0 + kWarpCols) / CH; ++c) {
+                        float v[CH];
+                        tmem_load_chunk<CH>(trow + c * CH, v);
+#pragma unroll
+                        for (int g = 0; g < CH / 4; ++g)
+                            __stcg(mine + static_cast<size_t>(c * (CH / 4) + g) * 256 + prow_sk,
+                                   make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
+                    }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(acc), 0));   // accumulator free
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::st_release_gpu_u32(flag_base + cluster_id * 16, 1u);
+                }
+            } else if (p.splits == 1) {
+                if constexpr (!SWAP) {
+                    int add_count = 0;
+                    int last_pair = cluster_id;
+                    if (pw.kind == 1) {
+                        // stream-K owner: the tile's later pieces start the ranges
+                        // of the following pairs; wait for each of their partials
+                        const long long tile_end = static_cast<long long>(w.tile - p.num_units + 1) * p.kblocks;
+                        bool ok_all = true;
+                        while (last_pair + 1 < num_clusters &&
+                               sk_range_start(p, last_pair + 1, num_clusters) < tile_end) {
+                            ++last_pair;
+                            ok_all = ok_all && W.wait_flag(flag_base + last_pair * 16, 6);
+                        }
+                        add_count = ok_all ? last_pair - cluster_id : 0;
+                    }
                     epilogue_rows_staged<kWarpCols, 1>(pb, &tmap_out, trow + col0,
                                                     w.tp * 256 + static_cast<int>(rank) * 128 + q * 32,
                                                     w.tq * BN + col0, lane, stage, stage_smem, chunks, s_tensor,
-                                                    w.b);
+                                                    w.b,
+                                                    reinterpret_cast<const float4 *>(p.sk_ws) +
+                                                        static_cast<size_t>(cluster_id + 1) * kSlot,
+                                                    add_count, kSlot, prow_sk, col0);
+                    if (pw.kind == 1) {
+                        __syncwarp();
+                        if (lane == 0)
+                            for (int cc = cluster_id + 1; cc <= last_pair; ++cc)
+                                flag_base[cc * 16] = 0u;   // ready for the next launch
+                    }
                 } else {
                     const int pidx = w.tp * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
 #pragma unroll 1

@@ -347,6 +347,20 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
     return v;
 }
 
+// GPU-scope acquire load of a 32-bit flag in global memory.
+__device__ __forceinline__ unsigned int ld_acquire_gpu_u32(const unsigned int *p)
+{
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// GPU-scope release store of a 32-bit flag in global memory.
+__device__ __forceinline__ void st_release_gpu_u32(unsigned int *p, unsigned int v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
 // from this CTA's shared memory into a peer CTA's shared memory (cluster
 // address); completion is signalled as transaction bytes on the peer's

@@ -82,7 +82,8 @@ typedef enum fp8mm_variant {
     FP8MM_VARIANT_AUTO = 0,   /* heuristic choice (what fp8_scaled_mm uses)     */
     FP8MM_VARIANT_TILE = 1,   /* 128 x tile_n output tiles; tile rows over M    */
     FP8MM_VARIANT_SWAP = 2,   /* operands swapped: 128-row tiles over N, tile_n columns over M */
-    FP8MM_VARIANT_PAIR = 3,   /* 2-SM MMA: a CTA pair computes 256 x tile_n tiles (no split-K) */
+    FP8MM_VARIANT_PAIR = 3,   /* 2-SM MMA: a CTA pair computes 256 x tile_n tiles, with split-K
+                                 or stream-K (split_k = -1) */
     FP8MM_VARIANT_SWAPK = 4,  /* SWAP tiles with K spread over a cluster of split_k CTAs,
                                  reduced through distributed shared memory (no workspace) */
     FP8MM_VARIANT_SWAPPAIR = 5 /* SWAP with 2-SM MMA: a CTA pair covers 256 rows of N and
@@ -108,9 +109,13 @@ int fp8_scaled_mm(const void *A, const void *B,
  *             ceil(M / tile_n) column tiles). PAIR: 128 or 256. SWAPK: as
  *             SWAP. SWAPPAIR: 16, 32, 64 or 128. 0 = heuristic.
  *   split_k   1 .. 16 K-slices per output tile (reduced deterministically in
- *             slice order by the last slice to arrive); PAIR and SWAPPAIR
- *             take 0 or 1;
- *             SWAPK takes the cluster size 2, 4 or 8 (0 = 4). 0 = heuristic.
+ *             slice order by the last slice to arrive); SWAPPAIR takes 0 or 1;
+ *             SWAPK takes the cluster size 2, 4 or 8 (0 = 4); PAIR also takes
+ *             -1: stream-K, where the tiles of the last partial wave (plus one
+ *             full wave) have their K blocks divided evenly over all CTA
+ *             pairs and each such tile is finished by the pair holding its
+ *             first K block, which adds the other pieces' fp32 partials in K
+ *             order (deterministic). 0 = heuristic.
  * Returns FP8MM_ERR_MODE for an unsupported combination.
  */
 int fp8_scaled_mm_config(const void *A, const void *B,

@@ -54,7 +54,8 @@ def check_items(out, items):
 
 
 KERNELS = [(TILE, 128, 1), (TILE, 256, 1), (TILE, 128, 3), (SWAP, 16, 1), (SWAP, 64, 2), (SWAP, 128, 1),
-           (PAIR, 128, 1), (PAIR, 256, 1), (PAIR, 256, 3), (SWAPK, 16, 4), (SWAPK, 128, 2), (SWAPPAIR, 32, 0)]
+           (PAIR, 128, 1), (PAIR, 256, 1), (PAIR, 256, 3), (PAIR, 256, -1), (SWAPK, 16, 4), (SWAPK, 128, 2),
+           (SWAPPAIR, 32, 0)]
 
 
 @pytest.mark.parametrize("variant,tile_n,split", KERNELS)

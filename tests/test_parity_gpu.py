@@ -267,3 +267,44 @@ def test_host_entry_in_blocks():
                                      inp.scale_a.pin_memory(), inp.scale_b.pin_memory(), mode,
                                      bias=None if inp.bias is None else inp.bias.pin_memory())
         _assert_ok(compare(bf16_bits(host), inp), f"host blocks mode{mode}")
+
+
+# ------------------------------------------------------------- stream-K -----
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_pair_stream_k_ragged(mode):
+    _need_gpu()
+    # 2 x 11 pair tiles (fewer than the pairs) with 33 K blocks (a K tail of
+    # 16): every tile's K blocks are spread over several pairs, and each tile
+    # is finished by the pair holding its first K block
+    stats, _, _ = run_and_compare(300, 2600, 4112, mode, seed=61, with_bias=(mode == 1), variant=PAIR,
+                                  tile_n=256, split_k=-1)
+    _assert_ok(stats, f"stream-K ragged mode{mode}")
+
+
+def test_pair_stream_k_between_one_and_two_waves():
+    _need_gpu()
+    # 9 x 10 = 90 pair tiles: all of them in the stream-K region
+    stats, _, _ = run_and_compare(2304, 2560, 1296, 1, seed=62, with_bias=True, variant=PAIR, tile_n=256,
+                                  split_k=-1, sample=True, n_random=48)
+    _assert_ok(stats, "stream-K 90 tiles")
+
+
+def test_pair_stream_k_is_deterministic():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+    inp = make_inputs(512, 3072, 4096, 1, seed=63, with_bias=True)
+    A, Bt, sa, sb, bias = to_device(inp)
+    outs = [bf16_bits(fm.fp8_scaled_mm_config(A, Bt.t(), sa, sb, 1, bias=bias, variant=PAIR, tile_n=256,
+                                              split_k=-1)) for _ in range(3)]
+    assert fm.fp8mm_device_status() == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    _assert_ok(compare(outs[0], inp), "stream-K det")
+
+
+def test_pair_stream_k_other_types():
+    _need_gpu()
+    stats, _, _ = run_and_compare(300, 2600, 4112, 1, seed=64, with_bias=True, variant=PAIR, tile_n=256,
+                                  split_k=-1, a_dtype="e5m2", out_dtype="fp16")
+    _assert_ok(stats, "stream-K e5m2/fp16")
