@@ -311,11 +311,15 @@ int64_t stream_k_tiles(int64_t tiles, int kblocks, int pairs)
 
 // Modelled time (us) of the pair kernel with stream-K, for at least one full
 // wave of tiles: the last partial wave's idle time, (1 - rem / pairs) x a
-// tile's K blocks, is saved, and each owner's fix-up (reading a piece's fp32
-// partial back through L2 at the end) costs about 8 us. Fitted to GB300
-// timings: stream-K won at 8192^3 (rem 36 of 76, 64 K blocks) and
-// 2304 x 3072 x 12288 (rem 32, 96 K blocks) and lost where the saving is
-// smaller (4096^3, the K = 3072 shapes, a nearly full last wave).
+// tile's K blocks, is saved, against a cost of about 8 us. Per-launch traces
+// on GB300 put that cost in two places: each pair runs one or two more
+// epilogues (the contributor's fp32 partial, the owner's fix-up), which
+// serialise behind the accumulator hand-off; and with no idle tail the chip
+// draws more power, so under the power cap the SM clock runs 5-10 % lower
+// for the whole launch. Fitted to GB300 timings: stream-K won at 8192^3
+// (rem 36 of 76, 64 K blocks) and 2304 x 3072 x 12288 (rem 32, 96 K blocks)
+// and lost where the saving is smaller (4096^3, the K = 3072 shapes, a
+// nearly full last wave).
 double pair_sk_time(int64_t tiles, int kblocks, int pairs)
 {
     if (tiles < pairs || stream_k_tiles(tiles, kblocks, pairs) == 0)

@@ -339,6 +339,36 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
     }
 }
 
+// Where a stream-K owner finds the fp32 partials of its tile's later pieces.
+// Each partial covers this CTA's 128 rows of the pair tile, laid out
+// [column / 4][128 rows][4 columns], so that a warp's 32 rows of one column
+// group are 512 contiguous bytes. The partials are either in global memory
+// (piece k at glob + k gstep, in float4) or, when there is one, copied into
+// this CTA's operand ring: 16 KB blocks of 32 columns, block j in stage
+// first_stage + j / blocks_per_stage (mod stages) at offset
+// (j % blocks_per_stage) x 16 KB.
+struct PartialSrc {
+    const float4 *glob;
+    size_t gstep;
+    const uint8_t *ring;   // non-null: the single partial is in shared memory
+    int count;
+    int first_stage, stages, stage_bytes, blocks_per_stage;
+    int prow;    // this thread's row within the 128
+    int colt0;   // the warp's first column within the tile
+
+    __device__ __forceinline__ const float4 *chunk(int k, int col) const
+    {
+        if (ring != nullptr) {
+            const int j = col >> 5;
+            int s = first_stage + j / blocks_per_stage;
+            if (s >= stages)
+                s -= stages;
+            return reinterpret_cast<const float4 *>(ring + s * stage_bytes + (j % blocks_per_stage) * 16384) + prow;
+        }
+        return glob + static_cast<size_t>(k) * gstep + static_cast<size_t>(col >> 2) * 128 + prow;
+    }
+};
+
 // Row-major epilogue of one warp's 32 accumulator rows (TMEM lanes) x BN
 // columns, 64 columns at a time, through a 4 KB shared-memory stage per
 // warp. Each thread converts its row's 64 values to bf16 and writes them as
@@ -351,18 +381,13 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
 // the stage is rewritten, the TMA store of the previous block must have read
 // it (that wait comes after the next block's TMEM loads and arithmetic).
 //
-// With add_count > 0 (stream-K owner), the fp32 partials of add_count later
-// pieces of the tile are added to the accumulator first, in piece order:
-// piece k's partial starts at add_base + k add_stride (float4 units), laid out
-// [column / 4][256 rows][4]; this thread's row in it is prow, and the warp's
-// first column within the tile is colt0.
+// With add.count > 0 (stream-K owner), the fp32 partials that add describes
+// are added to the accumulator first, in piece order.
 template <int BN, int NBUF>
 __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, const CUtensorMap *tmap_out,
                                                      uint32_t trow, int m_row0, int n0, int lane,
                                                      uint8_t *stage, uint32_t stage_smem, uint32_t &chunks,
-                                                     float s_tensor, int item, const float4 *add_base = nullptr,
-                                                     int add_count = 0, size_t add_stride = 0, int prow = 0,
-                                                     int colt0 = 0)
+                                                     float s_tensor, int item, const PartialSrc add = PartialSrc{})
 {
     constexpr unsigned kAll = 0xffffffffu;
     const int m = m_row0 + lane;
@@ -375,13 +400,18 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
         for (int h = 0; h < 2; ++h) {
             float v[32];
             ptx::tmem_ld_32cols(trow + static_cast<uint32_t>(c * 64 + h * 32), v);
-            for (int k = 0; k < add_count; ++k) {
-                const float4 *src = add_base + static_cast<size_t>(k) * add_stride +
-                                    static_cast<size_t>((colt0 + c * 64 + h * 32) / 4) * 256 + prow;
+            for (int k = 0; k < add.count; ++k) {
+                const float4 *src = add.chunk(k, add.colt0 + c * 64 + h * 32);
                 float4 x[8];
+                if (add.ring == nullptr) {
 #pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    x[g] = __ldcg(src + g * 256);
+                    for (int g = 0; g < 8; ++g)
+                        x[g] = __ldcg(src + g * 128);
+                } else {
+#pragma unroll
+                    for (int g = 0; g < 8; ++g)
+                        x[g] = src[g * 128];
+                }
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
                     v[4 * g] += x[g].x;

@@ -46,6 +46,12 @@ struct PairCfg {
     static_assert(kBBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
     static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory");
     static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
+    // stream-K: one partial of this CTA's 128 rows, in 16 KB blocks of 32
+    // columns, fits in the ring once the ring has drained
+    static constexpr int kSkBlocks = BN / 32;
+    static constexpr int kSkBlocksPerStage = kStageBytes / 16384;
+    static constexpr int kSkStages = SWAP ? 0 : (kSkBlocks + kSkBlocksPerStage - 1) / kSkBlocksPerStage;
+    static_assert(SWAP || (kSkBlocksPerStage >= 1 && kSkStages <= kStages), "stream-K partial must fit the ring");
 };
 
 // The work of one CTA pair, in order: whole units (tile, K slice) as in the
@@ -103,6 +109,17 @@ __device__ __forceinline__ long long sk_range_start(const KernelParams &p, int c
     return static_cast<long long>(p.sk_tiles) * p.kblocks * c / pairs;
 }
 
+// Number of later pieces of the stream-K tile `tile` whose owner is pair c:
+// one per following pair whose range starts inside the tile.
+__device__ __forceinline__ int sk_partials(const KernelParams &p, int c, int pairs, int tile)
+{
+    const long long tile_end = static_cast<long long>(tile - p.num_units + 1) * p.kblocks;
+    int n = 0;
+    while (c + n + 1 < pairs && sk_range_start(p, c + n + 1, pairs) < tile_end)
+        ++n;
+    return n;
+}
+
 // Units: (256-row tile of P, BN-row tile of Q, K slice); p.tiles_p counts
 // 256-row tiles. With p.splits > 1 (row-major form only) each slice writes its
 // fp32 partial to the workspace and the last slice to arrive, per epilogue
@@ -133,6 +150,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
     const uint32_t done_bar = bar0 + 8u * (2 * S + 4);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + (bar0 - sbase) + 8 * (2 * S + 5));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const uint32_t sk_bar = bar0 + 8u * (2 * S + 6);   // stream-K partial copied into the ring
+    static_assert(8 * (2 * S + 7) <= C::kBarBytes, "barrier area");
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -150,6 +169,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
             ptx::mbar_init(tempty_bar(a), 2 * C::kEpiWarps);   // every epilogue warp of both CTAs
         }
         ptx::mbar_init(done_bar, 1);
+        ptx::mbar_init(sk_bar, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmap_a);
@@ -182,8 +202,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
             bool ok = true;
             PairSchedule sched(p, cluster_id, num_clusters);
             PairWork pw;
+            int last_kind = 0, last_tile = 0;
             while (ok && sched.next(p, pw)) {
                 const Unit &w = pw.u;
+                last_kind = pw.kind;
+                last_tile = w.tile;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!W.wait(empty_bar(stage), phase ^ 1u, 0)) {
                         ok = false;
@@ -204,9 +227,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
                     }
                 }
             }
+            // Stream-K owner with a single later piece: that piece's partial
+            // (this CTA's rows) is copied into the ring while the MMA works
+            // through the last stages, each stage as soon as the MMA has
+            // released it for the last time, oldest first.
+            bool sk_copy = false;
+            if constexpr (!SWAP) {
+                if (ok && last_kind == 1 && p.splits == 1 &&
+                    sk_partials(p, cluster_id, num_clusters, last_tile) == 1) {
+                    sk_copy = true;
+                    const unsigned int *f = p.sk_flags + (cluster_id + 1) * 16 + static_cast<int>(rank) * 8;
+                    bool ready = true;
+                    for (int e = 0; e < 8 && ready; ++e)
+                        ready = W.wait_flag(f + e, 6);
+                    if (ready) {
+                        ptx::fence_proxy_async_global();
+                        const uint8_t *src = reinterpret_cast<const uint8_t *>(p.sk_ws) +
+                                             (static_cast<size_t>(cluster_id + 1) * 256 + rank * 128) * BN * 4;
+                        for (int jj = 0; jj < C::kSkStages; ++jj) {
+                            const int s = (stage + jj) % S;
+                            const int last_load = issued - S + jj;   // the stage's last fill, if any
+                            if (last_load >= 0 && !W.wait(empty_bar(s), static_cast<uint32_t>(last_load / S) & 1u, 7))
+                                break;
+                            for (int b = 0; b < C::kSkBlocksPerStage; ++b) {
+                                const int j = jj * C::kSkBlocksPerStage + b;
+                                if (j >= C::kSkBlocks)
+                                    break;
+                                ptx::mbar_expect_tx(sk_bar, 16384u);
+                                ptx::bulk_copy_g2s(sbase + s * C::kStageBytes + b * 16384, src + j * 16384, 16384u,
+                                                   sk_bar);
+                            }
+                        }
+                    }
+                    ptx::mbar_arrive(sk_bar);   // completes once the copies issued have landed
+                }
+            }
             // Own copies must land before the CTA may exit: the even CTA sees
             // both CTAs' bytes on its full barriers; the odd CTA waits until
             // its stages were consumed (released by the pair MMA).
+            if (sk_copy)
+                W.drain(sk_bar, 0, 8);
             const int n = issued < S ? issued : S;
             int s = stage;
             uint32_t ph = phase;
@@ -283,8 +343,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
         uint32_t acc_phase = 0;
         PairSchedule sched(p, cluster_id, num_clusters);
         PairWork pw;
+        int kb_total = 0;   // K blocks loaded into the ring so far, this piece's included
         while (sched.next(p, pw)) {
             const Unit &w = pw.u;
+            kb_total += w.kb1 - w.kb0;
             const KernelParams pb = for_item(p, w.b);
             const float s_tensor = tensor_scale(pb);
             if (!W.wait(tfull_bar(acc), acc_phase, 5))
@@ -292,21 +354,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
             ptx::tc_fence_after();
             const uint32_t trow =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            // A stream-K partial: 256 x BN fp32 per pair, this CTA's 128 rows at
+            // rank x 128 x BN, laid out [column / 4][128 rows][4 columns].
             constexpr size_t kSlot = static_cast<size_t>(256) * BN / 4;   // float4 per stream-K partial
-            const int prow_sk = static_cast<int>(rank) * 128 + q * 32 + lane;  // row within the pair tile
+            constexpr size_t kHalf = static_cast<size_t>(128) * BN / 4;
+            const int prow_sk = q * 32 + lane;   // row within this CTA's 128
             unsigned int *flag_base = p.sk_flags + static_cast<int>(rank) * 8 + ew;   // + 16 per pair
             if (pw.kind == 2) {
                 if constexpr (!SWAP) {
                     // stream-K contributor: this piece's partial into the pair's
                     // slot, then the warp's flag (release) for the tile's owner
-                    float4 *mine = reinterpret_cast<float4 *>(p.sk_ws) + static_cast<size_t>(cluster_id) * kSlot;
+                    float4 *mine = reinterpret_cast<float4 *>(p.sk_ws) + static_cast<size_t>(cluster_id) * kSlot + rank * kHalf;
 #pragma unroll 1
                     for (int c = col0 / CH; c < (col0 + kWarpCols) / CH; ++c) {
                         float v[CH];
                         tmem_load_chunk<CH>(trow + c * CH, v);
 #pragma unroll
                         for (int g = 0; g < CH / 4; ++g)
-                            __stcg(mine + static_cast<size_t>(c * (CH / 4) + g) * 256 + prow_sk,
+                            __stcg(mine + static_cast<size_t>(c * (CH / 4) + g) * 128 + prow_sk,
                                    make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
                     }
                     ptx::tc_fence_before();
@@ -320,27 +385,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(EpiShape<SWAP>::kThr
                 }
             } else if (p.splits == 1) {
                 if constexpr (!SWAP) {
-                    int add_count = 0;
                     int last_pair = cluster_id;
+                    PartialSrc add{reinterpret_cast<const float4 *>(p.sk_ws) +
+                                       static_cast<size_t>(cluster_id + 1) * kSlot + rank * kHalf,
+                                   kSlot, nullptr, 0, 0, S, C::kStageBytes, C::kSkBlocksPerStage, prow_sk, col0};
                     if (pw.kind == 1) {
                         // stream-K owner: the tile's later pieces start the ranges
-                        // of the following pairs; wait for each of their partials
-                        const long long tile_end = static_cast<long long>(w.tile - p.num_units + 1) * p.kblocks;
+                        // of the following pairs. A single partial was copied into
+                        // the ring by the producer (it has waited for the flags);
+                        // several are read through L2 once their flags are set.
+                        const int n_add = sk_partials(p, cluster_id, num_clusters, w.tile);
+                        last_pair = cluster_id + n_add;
                         bool ok_all = true;
-                        while (last_pair + 1 < num_clusters &&
-                               sk_range_start(p, last_pair + 1, num_clusters) < tile_end) {
-                            ++last_pair;
-                            ok_all = ok_all && W.wait_flag(flag_base + last_pair * 16, 6);
+                        if (n_add == 1) {
+                            ok_all = W.wait(sk_bar, 0, 7);
+                            add.ring = smem;
+                            add.first_stage = kb_total % S;
+                        } else {
+                            for (int cc = cluster_id + 1; cc <= last_pair; ++cc)
+                                ok_all = ok_all && W.wait_flag(flag_base + cc * 16, 6);
                         }
-                        add_count = ok_all ? last_pair - cluster_id : 0;
+                        add.count = ok_all ? n_add : 0;
                     }
                     epilogue_rows_staged<kWarpCols, 1>(pb, &tmap_out, trow + col0,
                                                     w.tp * 256 + static_cast<int>(rank) * 128 + q * 32,
                                                     w.tq * BN + col0, lane, stage, stage_smem, chunks, s_tensor,
-                                                    w.b,
-                                                    reinterpret_cast<const float4 *>(p.sk_ws) +
-                                                        static_cast<size_t>(cluster_id + 1) * kSlot,
-                                                    add_count, kSlot, prow_sk, col0);
+                                                    w.b, add);
                     if (pw.kind == 1) {
                         __syncwarp();
                         if (lane == 0)

@@ -347,6 +347,30 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
     return v;
 }
 
+// Raise the transaction count of the current phase of `bar` by `bytes`
+// without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global memory into this CTA's shared memory; completion is signalled
+// as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to global memory before
+// its later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // GPU-scope acquire load of a 32-bit flag in global memory.
 __device__ __forceinline__ unsigned int ld_acquire_gpu_u32(const unsigned int *p)
 {

@@ -290,6 +290,18 @@ def test_pair_stream_k_between_one_and_two_waves():
     _assert_ok(stats, "stream-K 90 tiles")
 
 
+@pytest.mark.parametrize("tile_n", [256, 128])
+def test_pair_stream_k_partial_through_ring(tile_n):
+    _need_gpu()
+    # 7 x 11 (tile_n 256) or 7 x 22 (128) pair tiles, 5 K blocks with a tail
+    # of 16: more tiles than pairs, so every pair's stream-K range covers at
+    # least a whole tile and an owner adds exactly one partial, which its
+    # producer copies into the drained operand ring; full-output compare
+    stats, _, _ = run_and_compare(1700, 2700, 528, 1, seed=65, with_bias=True, variant=PAIR, tile_n=tile_n,
+                                  split_k=-1)
+    _assert_ok(stats, f"stream-K ring tile_n={tile_n}")
+
+
 def test_pair_stream_k_is_deterministic():
     _need_gpu()
     import fp8_scaled_gemm_gb300 as fm
