@@ -1373,6 +1373,11 @@ int fp8mm_device_status(void *stream)
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaMemset(counters)");
     }
+    if (d->sk_flags) {   // a stream-K owner that gave up leaves its flags set
+        e = cudaMemset(d->sk_flags, 0, static_cast<size_t>(d->sms / 2) * 16 * sizeof(unsigned int));
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(stream-K flags)");
+    }
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaDeviceSynchronize");

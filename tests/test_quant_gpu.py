@@ -196,3 +196,58 @@ def test_bf16_path_other_types():
 def test_bf16_path_full_size_sampled(mode):
     _need_gpu()
     _bf16_path(8192, 8192, 8192, mode, seed=42, bias=False, sample=True)
+
+
+# ------------------------------------------- per-tensor amax placement ---
+# The per-tensor amax is a reduction over every CTA's share of the tensor and
+# the scale reaches every element: the extreme value placed at the start, in
+# the middle and in the last group must decide the scale, and every code must
+# still match the oracle.
+
+@pytest.mark.parametrize("where", ["first", "middle", "last"])
+def test_per_tensor_amax_from_anywhere(where):
+    _need_gpu()
+    R, C = 8192, 4104
+    x = bf16_matrix(R, C, seed=71)
+    n = R * C
+    pos = {"first": 3, "middle": n // 2 + 11, "last": n - 1}[where]
+    x.view(-1)[pos] = -1000.0
+    _, s = quantize_and_compare(x, 0, 0)
+    assert float(s[0]) == float(np.float32(1000.0) / np.float32(448.0))
+
+
+@pytest.mark.parametrize("where", ["first", "middle", "last"])
+def test_per_tensor_nan_anywhere(where):
+    _need_gpu()
+    R, C = 8192, 4104
+    x = bf16_matrix(R, C, seed=72)
+    n = R * C
+    pos = {"first": 0, "middle": n // 3, "last": n - 2}[where]
+    x.view(-1)[pos] = float("nan")
+    _, s = quantize_and_compare(x, 0, 1)
+    assert np.isnan(s.cpu().numpy()[0])
+
+
+def test_per_tensor_zero_and_odd_shapes():
+    _need_gpu()
+    # all +-0: zero scale, codes of +-0
+    x = torch.zeros(2048, 1024, dtype=torch.bfloat16)
+    x.view(-1)[1::3] = -0.0
+    _, s = quantize_and_compare(x, 0, 0)
+    assert float(s[0]) == 0.0
+    quantize_and_compare(bf16_matrix(1, 1 << 20, seed=73, kind="wide"), 0, 0)
+    quantize_and_compare(bf16_matrix(4001, 264, seed=74, kind="wide"), 0, 1)
+
+
+def test_per_tensor_back_to_back_large_calls():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    xs = [bf16_matrix(2048 + 8 * s, 1032, seed=80 + s, kind="wide") for s in range(5)]
+    dev = [x.cuda() for x in xs]
+    outs = [fm.fp8_quantize(d, 0, DT[s % 2]) for s, d in enumerate(dev)]   # queued on one stream
+    torch.cuda.synchronize()
+    assert fm.fp8mm_device_status() == 0
+    for s, (x, (q, sc)) in enumerate(zip(xs, outs)):
+        q_ref, s_ref = oracle.quantize(_bits(x), 0, s % 2)
+        assert np.array_equal(q.view(torch.uint8).cpu().numpy(), q_ref)
+        assert _same_scales(sc.cpu().numpy(), s_ref)
