@@ -55,6 +55,9 @@ def parse_args(argv=None):
                     help="time every benchmark shape instead (one JSON line per shape)")
     ap.add_argument("--tune", action="store_true",
                     help="with --sweep: autotune each shape (fp8mm_autotune) before timing it")
+    ap.add_argument("--plain-launches", action="store_true",
+                    help="with --sweep: no timing and no CUDA graph; per shape, --warmup launches and one more "
+                         "on one input set, for a profiler's launch list")
     ap.add_argument("--quant", action="store_true",
                     help="time the bf16 -> fp8 quantisation step instead (one JSON line per shape; "
                          "--shapes takes RxC[:mode[:e4m3|e5m2]])")
@@ -334,6 +337,37 @@ def algorithmic_bytes(M, N, K, mode, bias, batch=1):
     return batch * (M * K + N * K + 2 * M * N + (4 * (M + N) if mode == 1 else 8)) + (2 * N if bias else 0)
 
 
+def plain_launches(M, N, K, mode, bias, n, device, types=("e4m3", "e4m3", "bf16"), batch=1):
+    """n launches of one shape on one input set, no graph, then a synchronize."""
+    import torch
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+
+    inp = make_inputs(M, N, K, mode, SEED, with_bias=bias, a_dtype=types[0], b_dtype=types[1],
+                      out_dtype=types[2])
+    odt = torch.bfloat16 if types[2] == "bf16" else torch.float16
+    b = None if inp.bias is None else inp.bias.to(device)
+    if batch == 1:
+        A, B = inp.a_q.to(device), inp.bt_q.to(device).t()
+        sa, sb = inp.scale_a.to(device), inp.scale_b.to(device)
+        out = torch.empty((M, N), dtype=odt, device=device)
+    else:
+        A = inp.a_q.to(device).unsqueeze(0).expand(batch, M, K).contiguous()
+        B = inp.bt_q.to(device).unsqueeze(0).expand(batch, N, K).contiguous().transpose(1, 2)
+        sa, sb = inp.scale_a.to(device).repeat(batch), inp.scale_b.to(device).repeat(batch)
+        out = torch.empty((batch, M, N), dtype=odt, device=device)
+    for _ in range(n):
+        if batch > 1:
+            fm.fp8_scaled_bmm(A, B, sa, sb, mode, bias=b, out=out)
+        elif tuple(types) != ("e4m3", "e4m3", "bf16"):
+            fm.fp8_scaled_mm_ex(A, B, sa, sb, mode, bias=b, out=out)
+        else:
+            fm.fp8_scaled_mm(A, B, sa, sb, mode, bias=b, out=out)
+    torch.cuda.synchronize(device)
+    assert fm.fp8mm_device_status() == 0
+    return n
+
+
 def time_shape(M, N, K, mode, bias, steps, warmup, device, types=("e4m3", "e4m3", "bf16"), batch=1):
     import torch
     import fp8_scaled_gemm_gb300 as fm
@@ -429,6 +463,13 @@ def run_sweep(args):
     dts = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2, "bf16": torch.bfloat16, "fp16": torch.float16}
     for (M, N, K, mode, bias, types, batch) in shapes:
         builtin = fm.fp8mm_describe_bmm_choice(batch, M, N, K, mode)
+        if args.plain_launches:
+            n = plain_launches(M, N, K, mode, bias, args.warmup + 1, device, types, batch)
+            print(json.dumps({"shape": [M, N, K], "batch": batch, "scale_mode": "row-wise" if mode else "per-tensor",
+                              "bias": bias, "types": list(types), "launches": n, "kernel": builtin,
+                              "algorithmic_bytes": algorithmic_bytes(M, N, K, mode, bias, batch),
+                              "flops": 2 * M * N * K * batch}), flush=True)
+            continue
         if args.tune:
             fm.fp8mm_autotune(M, N, K, mode, batch=batch, a_dtype=dts[types[0]], b_dtype=dts[types[1]],
                               out_dtype=dts[types[2]])
