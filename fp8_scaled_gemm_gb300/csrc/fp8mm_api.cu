@@ -254,15 +254,21 @@ struct Choice {
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Tile rows per group of the tile order (columns run inside a group): a
-// group's A strips stay in L2 while Bt is swept once per group. Pair
-// launches with K <= 8192 and at least 16 tile rows take groups of 16
-// (Bt read half as often; on GB300 1.5 % faster at 8192^3 and 1.7 % at
-// 16384 x 14336 x 4096); deeper K keeps 8, where the pairs drift apart in K
-// and a larger group's strips no longer stay in L2 (16 was 0.4-1.3 % slower
-// at K = 14336).
+// group's A strips stay in L2 while Bt is swept once per group, so Bt's
+// DRAM reads fall as the group grows until the strips no longer fit. Pair
+// launches size the group so that its strips (group x 256 rows x K bytes)
+// fill about 32 MiB of L2, a multiple of 4 in [4, 32]: 16 at K = 8192,
+// 8 at K = 14336, 32 at K = 4096. Measured on GB300 against fixed groups:
+// 8192^3 is fastest at 16 (12 is 0.3 % slower, 8 and 24 1.5 %); K = 14336
+// at 8 (4 and 6 are 1-3 % slower); 16384 x 14336 x 4096 at 24-32 (16 is
+// 1-4 % slower). The other kernels keep groups of 8.
 int tile_group(const Choice &c)
 {
-    return (c.variant == FP8MM_VARIANT_PAIR && c.kblocks <= 64 && c.tiles_p >= 16) ? 16 : 8;
+    if (c.variant != FP8MM_VARIANT_PAIR)
+        return 8;
+    const int64_t strip = int64_t(256) * 128 * c.kblocks;   // bytes of one tile row's A strip
+    const int64_t g = ((int64_t(32) << 20) / strip) / 4 * 4;
+    return static_cast<int>(std::max<int64_t>(4, std::min<int64_t>(32, g)));
 }
 
 bool tile_n_supported(int variant, int tile_n)
