@@ -329,21 +329,23 @@ int64_t stream_k_tiles(int64_t tiles, int kblocks, int pairs)
 
 // Modelled time (us) of the pair kernel with stream-K, for at least one full
 // wave of tiles: the last partial wave's idle time, (1 - rem / pairs) x a
-// tile's K blocks, is saved, against a cost of about 8 us. Per-launch traces
-// on GB300 put that cost in two places: each pair runs one or two more
-// epilogues (the contributor's fp32 partial, the owner's fix-up), which
-// serialise behind the accumulator hand-off; and with no idle tail the chip
-// draws more power, so under the power cap the SM clock runs 5-10 % lower
-// for the whole launch. Fitted to GB300 timings: stream-K won at 8192^3
-// (rem 36 of 76, 64 K blocks) and 2304 x 3072 x 12288 (rem 32, 96 K blocks)
-// and lost where the saving is smaller (4096^3, the K = 3072 shapes, a
-// nearly full last wave).
+// tile's K blocks, is saved, against two costs that per-launch traces on
+// GB300 show. Each pair runs one or two more epilogues (the contributor's
+// fp32 partial, the owner's fix-up), which serialise behind the accumulator
+// hand-off: about 8 us. And with no idle tail the chip draws more power, so
+// under the power cap the SM clock runs lower for the whole launch: charged
+// as 0.5 % of the launch. Fitted to GB300 timings: stream-K won at 8192^3
+// (rem 36 of 76, 64 K blocks; by 0.2-1 %), 2304 x 3072 x 12288 (7 %) and
+// 3000 x 5000 x 4112 (5 %), and lost where the saving is smaller against the
+// launch (4096^3, the K = 3072 shapes, a nearly full last wave, and
+// 16384 x 14336 x 4096: 8.6 us of 600, 1.2 % slower).
 double pair_sk_time(int64_t tiles, int kblocks, int pairs)
 {
     if (tiles < pairs || stream_k_tiles(tiles, kblocks, pairs) == 0)
         return 1e300;
     const double rem = static_cast<double>(tiles % pairs);
-    return pair_time(tiles, kblocks, 1, pairs) - (1.0 - rem / pairs) * kblocks * 0.32 + 8.0;
+    const double t1 = pair_time(tiles, kblocks, 1, pairs);
+    return t1 - (1.0 - rem / pairs) * kblocks * 0.32 + 8.0 + 0.005 * t1;
 }
 
 // Split-K factor of the pair kernel: the s in 1..8 of least modelled time,
