@@ -418,6 +418,7 @@ def time_shape(M, N, K, mode, bias, steps, warmup, device, types=("e4m3", "e4m3"
     graph.replay()
     torch.cuda.synchronize(device)
     per = []
+    t_rep = time.time()
     for _ in range(5):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -426,6 +427,7 @@ def time_shape(M, N, K, mode, bias, steps, warmup, device, types=("e4m3", "e4m3"
         e1.record(stream)
         torch.cuda.synchronize(device)
         per.append(e0.elapsed_time(e1) / steps)
+    time_shape.window = (t_rep, time.time())   # the timed replays, for the clock samples
     if fm.fp8mm_device_status(stream) != 0:
         raise RuntimeError("in-kernel wait ran out: " + fm.fp8mm_last_error())
     del graph, sets
@@ -461,6 +463,10 @@ def run_sweep(args):
             types = tuple(parts[3:6]) if len(parts) >= 6 else ("e4m3", "e4m3", "bf16")
             shapes.append((M, N, K, mode, bias, types, batch))
     dts = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2, "bf16": torch.bfloat16, "fp16": torch.float16}
+    sampler = None
+    if not args.plain_launches:
+        sampler = ClockSampler(device.index if device.index is not None else 0)
+        sampler.start()
     for (M, N, K, mode, bias, types, batch) in shapes:
         builtin = fm.fp8mm_describe_bmm_choice(batch, M, N, K, mode)
         if args.plain_launches:
@@ -475,6 +481,7 @@ def run_sweep(args):
                               out_dtype=dts[types[2]])
         mean, best, n_sets, choice = time_shape(M, N, K, mode, bias, args.steps, args.warmup, device,
                                                 types, batch)
+        clocks = sampler.summary(*time_shape.window)
         flops = 2.0 * M * N * K * batch
         nbytes = algorithmic_bytes(M, N, K, mode, bias, batch)
         tflops = flops / (mean * 1e-3) / 1e12
@@ -487,8 +494,10 @@ def run_sweep(args):
             "tflops": round(tflops, 1), "frac_fp8_peak": round(tflops / fp8_peak, 3),
             "gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3),
             "bound": "hbm" if flops / nbytes < fp8_peak * 1e12 / (pk["hbm_gbs"] * 1e9) else "tensor",
-            "rotated_sets": n_sets, "kernel": choice,
+            "rotated_sets": n_sets, "kernel": choice, "clocks": clocks,
             **({"tuned": True, "builtin_kernel": builtin} if args.tune else {})}), flush=True)
+    if sampler is not None:
+        sampler.stop()
 
 
 QUANT_SHAPES = [(8192, 8192, 0), (8192, 8192, 1), (16384, 8192, 1), (4096, 14336, 1), (14336, 4096, 1),
