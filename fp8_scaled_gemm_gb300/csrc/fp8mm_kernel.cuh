@@ -395,6 +395,18 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
 #pragma unroll 1
     for (int c = 0; c < BN / 64; ++c) {
         const int nb = n0 + c * 64;
+        // the block's column scales and biases first, so that their loads
+        // are in flight during the TMEM loads (per-tensor without bias has none)
+        float sbl2[2] = {0.0f, 0.0f}, bl2[2] = {0.0f, 0.0f};
+        if (p.rowwise || p.bias != nullptr) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int nl = nb + h * 32 + lane;
+                const bool in = nl < p.N;
+                sbl2[h] = (p.rowwise && in) ? __ldg(p.scale_b + nl) : 0.0f;
+                bl2[h] = (p.bias != nullptr && in) ? bias_value(p, nl) : 0.0f;
+            }
+        }
         uint32_t w[32];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -420,10 +432,8 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                     v[4 * g + 3] += x[g].w;
                 }
             }
-            const int nl = nb + h * 32 + lane;
-            const bool in = nl < p.N;
-            const float sbl = (p.rowwise && in) ? __ldg(p.scale_b + nl) : 0.0f;
-            const float bl = (p.bias != nullptr && in) ? bias_value(p, nl) : 0.0f;
+            const float sbl = sbl2[h];
+            const float bl = bl2[h];
             const bool has_bias = p.bias != nullptr;
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
