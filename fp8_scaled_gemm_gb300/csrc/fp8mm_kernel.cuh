@@ -275,6 +275,31 @@ __device__ __forceinline__ float bias_value(const KernelParams &p, int n)
     return p.out_f16 ? __half2float(__ushort_as_half(b)) : __bfloat162float(__ushort_as_bfloat16(b));
 }
 
+// SWAP epilogue for CH accumulator columns held by one thread, with its
+// operands already loaded: the thread owns output column n, rows
+// m = qbase + j; lane l holds the row scale of row qbase + (l % CH) in sal
+// (broadcast with shuffles), and sb, b are column n's scale and bias.
+template <int CH>
+__device__ __forceinline__ void store_swap_chunk(const KernelParams &p, const float (&v)[CH], int n, int qbase,
+                                                 float s_tensor, float sal, float sb, float b)
+{
+    constexpr unsigned kAll = 0xffffffffu;
+    float y[CH];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+        const float s = p.rowwise ? __shfl_sync(kAll, sal, j) * sb : s_tensor;
+        y[j] = fmaf(v[j], s, b);
+    }
+    if (n >= p.N)
+        return;
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+        const int m = qbase + j;
+        if (m < p.M)
+            p.out[static_cast<size_t>(m) * p.ldo + n] = to_out(y[j], p.out_f16);
+    }
+}
+
 // Epilogue for CH accumulator columns held by one thread; the whole warp
 // calls it together (the per-column scale and bias are loaded once per lane
 // and broadcast with shuffles).
@@ -323,19 +348,7 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
         const float sal = (p.rowwise && ql < p.M) ? __ldg(p.scale_a + ql) : 0.0f;
         const float sb = (p.rowwise && n_in) ? __ldg(p.scale_b + n) : 0.0f;
         const float b = (p.bias != nullptr && n_in) ? bias_value(p, n) : 0.0f;
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-            const float s = p.rowwise ? __shfl_sync(kAll, sal, j) * sb : s_tensor;
-            y[j] = fmaf(v[j], s, b);
-        }
-        if (!n_in)
-            return;
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-            const int m = qbase + j;
-            if (m < p.M)
-                p.out[static_cast<size_t>(m) * p.ldo + n] = to_out(y[j], p.out_f16);
-        }
+        store_swap_chunk<CH>(p, v, n, qbase, s_tensor, sal, sb, b);
     }
 }
 
@@ -674,12 +687,25 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
             const Unit w = decode_unit(u, p);
             const KernelParams pb = for_item(p, w.b);
             const float s_tensor = tensor_scale(pb);
+            const int pidx = w.tp * kTileP + row;
+            // SWAP: this thread's column scale and bias and each chunk's row
+            // scales, loaded while the accumulator is still being computed
+            float sw_sal[BN / CH] = {}, sw_sb = 0.0f, sw_b = 0.0f;
+            if (SWAP && p.splits == 1 && (p.rowwise || p.bias != nullptr)) {
+                const bool n_in = pidx < pb.N;
+                sw_sb = (pb.rowwise && n_in) ? __ldg(pb.scale_b + pidx) : 0.0f;
+                sw_b = (pb.bias != nullptr && n_in) ? bias_value(pb, pidx) : 0.0f;
+#pragma unroll
+                for (int c = 0; c < BN / CH; ++c) {
+                    const int ql = w.tq * BN + c * CH + (lane % CH);
+                    sw_sal[c] = (pb.rowwise && ql < pb.M) ? __ldg(pb.scale_a + ql) : 0.0f;
+                }
+            }
             if (!W.wait(tfull_bar(acc), acc_phase, 5))
                 break;
             ptx::tc_fence_after();
             const uint32_t trow =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            const int pidx = w.tp * kTileP + row;
             if (p.splits == 1) {
                 if constexpr (!SWAP) {
                     epilogue_rows_staged<kWarpCols, C::kStageBufs>(pb, &tmap_out, trow + col0, w.tp * kTileP + q * 32,
@@ -688,9 +714,13 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
                 } else {
 #pragma unroll 1
                     for (int c = 0; c < BN / CH; ++c) {
+                        float sal = sw_sal[0];   // chunk c's, selected without indexing registers
+#pragma unroll
+                        for (int i = 1; i < BN / CH; ++i)
+                            sal = (c == i) ? sw_sal[i] : sal;
                         float v[CH];
                         tmem_load_chunk<CH>(trow + c * CH, v);
-                        store_chunk<CH, SWAP>(pb, v, pidx, w.tq * BN + c * CH, s_tensor, lane);
+                        store_swap_chunk<CH>(pb, v, pidx, w.tq * BN + c * CH, s_tensor, sal, sw_sb, sw_b);
                     }
                 }
                 ptx::tc_fence_before();
