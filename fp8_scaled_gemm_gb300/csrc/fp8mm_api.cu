@@ -1059,7 +1059,36 @@ std::vector<Candidate> tune_candidates(int64_t M, int64_t K)
 }
 
 // Streams and events of the host-memory entry point (one set per device).
-constexpr int kHostChunks = 4;   // chunks of A's rows and of Bt's rows: up to 4 x 4 output blocks
+constexpr int kHostChunks = 8;   // most chunks of A's rows and of Bt's rows: up to 8 x 8 output blocks
+
+// Relative sizes of the chunks A's rows and Bt's rows are cut into for the
+// host pipeline (fp8_scaled_mm_host), first chunk first.
+constexpr int kHostPlan[] = {1, 1, 1, 1};
+constexpr int kHostPlanLen = sizeof(kHostPlan) / sizeof(kHostPlan[0]);
+static_assert(kHostPlanLen <= kHostChunks, "host plan");
+
+// Chunk boundaries of R rows by the plan, at multiples of 256 rows and at
+// least 1024 rows each (fewer chunks for short R): start[0] = 0 < start[1]
+// < ... < start[n] = R. Returns n.
+int host_chunks(int64_t R, int64_t *start)
+{
+    const int n = static_cast<int>(std::min<int64_t>(kHostPlanLen, std::max<int64_t>(1, R / 1024)));
+    const int *w = kHostPlan + (kHostPlanLen - n);   // the plan's last n sizes
+    int total = 0;
+    for (int i = 0; i < n; ++i)
+        total += w[i];
+    start[0] = 0;
+    int acc = 0;
+    for (int i = 0; i < n; ++i) {
+        acc += w[i];
+        start[i + 1] = i + 1 == n ? R : std::min<int64_t>(R, (R * acc / total + 255) / 256 * 256);
+    }
+    int m = 0;   // drop empty chunks left by the rounding
+    for (int i = 1; i <= n; ++i)
+        if (start[i] > start[m])
+            start[++m] = start[i];
+    return m;
+}
 struct HostPipe {
     bool ready = false;
     cudaStream_t in = nullptr, mm = nullptr, out = nullptr;
@@ -1289,10 +1318,8 @@ int fp8_scaled_mm_host(const void *A, const void *B, const float *scale_a, const
     // after A chunk k and Bt chunk k, every block (k, j <= k) and (i < k, k)
     // has its operands, so it is computed and copied back while later
     // chunks arrive; both directions of the host link stay busy.
-    const int64_t pa = std::min<int64_t>(kHostChunks, cdiv(M, 1024));
-    const int64_t pb = std::min<int64_t>(kHostChunks, cdiv(N, 1024));
-    const int64_t rows_a = ((cdiv(M, pa) + 255) / 256) * 256, rows_b = ((cdiv(N, pb) + 255) / 256) * 256;
-    const int ca = static_cast<int>(cdiv(M, rows_a)), cb = static_cast<int>(cdiv(N, rows_b));
+    int64_t sa_[kHostChunks + 1], sb_[kHostChunks + 1];
+    const int ca = host_chunks(M, sa_), cb = host_chunks(N, sb_);
     const bool rowwise = scale_mode == FP8MM_SCALE_ROWWISE;
     cudaError_t e;
 #define FP8MM_TRY(call, what)      \
@@ -1305,8 +1332,8 @@ int fp8_scaled_mm_host(const void *A, const void *B, const float *scale_a, const
     if (bias)
         FP8MM_TRY(cudaMemcpyAsync(dbias, bias, bytes[4], cudaMemcpyHostToDevice, hp->in), "cudaMemcpyAsync(H2D)");
     auto block = [&](int i, int j) -> int {
-        const int64_t r0 = i * rows_a, mi = std::min<int64_t>(rows_a, M - r0);
-        const int64_t c0 = j * rows_b, nj = std::min<int64_t>(rows_b, N - c0);
+        const int64_t r0 = sa_[i], mi = sa_[i + 1] - r0;
+        const int64_t c0 = sb_[j], nj = sb_[j + 1] - c0;
         FP8MM_TRY(cudaStreamWaitEvent(hp->mm, hp->a_ready[i], 0), "cudaStreamWaitEvent");
         FP8MM_TRY(cudaStreamWaitEvent(hp->mm, hp->b_ready[j], 0), "cudaStreamWaitEvent");
         const int brc = run(dA + r0 * K, dB + c0 * K, rowwise ? dsa + r0 : dsa, rowwise ? dsb + c0 : dsb, scale_mode,
@@ -1326,14 +1353,14 @@ int fp8_scaled_mm_host(const void *A, const void *B, const float *scale_a, const
     };
     for (int k = 0; k < std::max(ca, cb); ++k) {
         if (k < ca) {
-            const int64_t r0 = k * rows_a, mi = std::min<int64_t>(rows_a, M - r0);
+            const int64_t r0 = sa_[k], mi = sa_[k + 1] - r0;
             FP8MM_TRY(cudaMemcpyAsync(dA + r0 * K, static_cast<const uint8_t *>(A) + r0 * K, static_cast<size_t>(mi * K),
                                       cudaMemcpyHostToDevice, hp->in),
                       "cudaMemcpyAsync(H2D)");
             FP8MM_TRY(cudaEventRecord(hp->a_ready[k], hp->in), "cudaEventRecord");
         }
         if (k < cb) {
-            const int64_t c0 = k * rows_b, nj = std::min<int64_t>(rows_b, N - c0);
+            const int64_t c0 = sb_[k], nj = sb_[k + 1] - c0;
             FP8MM_TRY(cudaMemcpyAsync(dB + c0 * K, static_cast<const uint8_t *>(B) + c0 * K, static_cast<size_t>(nj * K),
                                       cudaMemcpyHostToDevice, hp->in),
                       "cudaMemcpyAsync(H2D)");
