@@ -21,9 +21,22 @@
 //   empty[s]  in both CTAs: released by a multicast tcgen05.commit.
 //   tfull[a]  in both CTAs: multicast commit after the last K block of a tile.
 //   tempty[a] in the even CTA: one arrival per epilogue warp of both CTAs (16).
+//   sk_bar    in both CTAs: a stream-K owner's producer counts the bytes of
+//             the partial it copies into its own ring (below).
 // Every wait is bounded as in fp8mm_kernel.cuh. The pair meets at a cluster
 // barrier after initialisation and before tensor memory is released, so no
 // CTA leaves while its peer may still signal it.
+//
+// Stream-K (p.sk_tiles > 0): the K blocks of the last sk_tiles tiles are
+// dealt evenly over the pairs (PairSchedule). A tile split between pairs is
+// finished by the pair holding its first K block (the owner), whose piece is
+// the last of its range; the later pieces open the following pairs' ranges
+// and write fp32 partials, each CTA's 128 rows contiguous, then set release
+// flags. With one partial (always the case with at least a full wave of
+// split tiles) the owner's producer acquires the flags after its last TMA
+// load and copies the partial into the ring stages as the last MMAs free
+// them; the epilogue adds it from shared memory. Several partials are read
+// through L2.
 #pragma once
 
 #include "fp8mm_kernel.cuh"
