@@ -405,8 +405,15 @@ const char *fp8mm_status_string(int status);
 /* Detail of the last FP8MM_ERR_CUDA on this host thread ("" if none). */
 const char *fp8mm_last_error(void);
 
-/* The kernel fp8_scaled_mm would launch for this problem, as text
- * ("tile tile_n=256 split=1 ..."); for logs and tests. */
+/* The kernel fp8_scaled_mm would launch for this problem, as text; for logs
+ * and tests. Format: the variant ("tile", "swap", "pair", "swapk",
+ * "swappair") followed by key=value fields: tile_n, split (K slices; the
+ * cluster size for swapk), tiles (row tiles x column tiles per item), units
+ * (work units dealt round-robin), grid (CTAs), and when they apply
+ * stream_k_tiles (tiles whose K blocks are spread over all CTA pairs) and
+ * group (tile rows per group of the tile order, when not 8). Example:
+ * "pair tile_n=256 split=1 tiles=32x32 units=912 grid=152
+ * stream_k_tiles=112 group=16". */
 const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mode);
 
 /* The same for a batch of `batch` products (fp8_scaled_bmm); tiles are per
