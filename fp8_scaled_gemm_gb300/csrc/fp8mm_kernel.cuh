@@ -95,14 +95,15 @@ struct KernelParams {
     int group;                      // P tiles per rasterisation group
     int vec_store;                  // 16-byte output stores allowed (TILE)
     int out_tma;                    // tmap_out is valid: rows leave through TMA stores
-    int inject_stop_after;          // test hook: CTA 0's producer stops after this many K blocks (-1: off)
+    int inject_stop_after;          // test hook (-1: off): CTA 0's producer stops after this many K blocks;
+                                    // in the pair kernel, pair 1's stream-K partials are never flagged
     uint32_t idesc_fmt;             // operand format bits of the MMA instruction descriptor
     int out_f16;                    // 1: fp16 output and bias, 0: bf16
     // Stream-K (pair kernel, splits == 1): the last sk_tiles tiles of the tile
     // order are not given out whole; their K blocks are divided evenly over
     // all CTA pairs (num_units then counts the whole tiles before them).
     int sk_tiles;
-    float *sk_ws;                   // per pair: one fp32 partial tile, [BN/4][256][4]
+    float *sk_ws;                   // per pair: one fp32 partial tile, [CTA half][BN/4][128][4]
     unsigned int *sk_flags;         // per pair: 16 "partial written" flags (one per epilogue warp)
     unsigned long long timeout_cycles;
 };

@@ -390,7 +390,9 @@ int fp8mm_device_status(void *stream);
  * Test hook for the bounded in-kernel waits (failure detection without a GPU
  * fault). From the next launch on, in the 128-row kernels (TILE, SWAP), the
  * TMA producer of CTA 0 stops after `stop_after_kblocks` K blocks, so the
- * MMA thread's wait for the next block runs out: the kernel records
+ * MMA thread's wait for the next block runs out; in the pair kernel's
+ * stream-K schedule, the partials of CTA pair 1 are never flagged, so the
+ * owner's wait for them runs out. Either way the kernel records
  * FP8MM_ERR_TIMEOUT in the device status word, releases its tensor memory
  * and returns; that launch's output is undefined. `wait_limit_cycles` > 0
  * replaces the wait budget of every kernel (default 4e9 clock64 cycles).

@@ -18,7 +18,7 @@ from tests._parity import compare, bf16_bits, run_and_compare, to_device
 
 pytestmark = pytest.mark.gpu
 
-TILE, SWAP = 1, 2
+TILE, SWAP, PAIR = 1, 2, 3
 SHORT = 1 << 22
 
 
@@ -59,3 +59,29 @@ def test_auto_path_unaffected_after_a_timeout():
     import fp8_scaled_gemm_gb300 as fm
     stats, _, _ = run_and_compare(1024, 1024, 512, 0, 5, False)
     assert stats["violations"] == 0, stats
+
+
+def test_stream_k_flag_wait_runs_out_and_the_context_survives():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+
+    # 9 x 10 pair tiles, 11 K blocks: every tile is split between two pairs;
+    # pair 1's range starts inside tile 1, which pair 0 finishes
+    M, N, K = 2304, 2560, 1296
+    inp = make_inputs(M, N, K, 1, seed=33, with_bias=True)
+    A, Bt, sa, sb, bias = to_device(inp)
+    assert fm.fp8mm_device_status() == 0
+    # test hook: pair 1's partials are never flagged; pair 0's wait gives up
+    fm.fp8mm_debug_inject(stop_after_kblocks=0, wait_limit_cycles=SHORT)
+    try:
+        fm.fp8_scaled_mm_config(A, Bt.t(), sa, sb, 1, bias=bias, variant=PAIR, tile_n=256, split_k=-1)
+        status = fm.fp8mm_device_status()
+    finally:
+        fm.fp8mm_debug_inject(-1, 0)
+    assert status == -7, f"expected FP8MM_ERR_TIMEOUT, got {status}"
+    # the status read cleared the flags: the same launch is exact again, twice
+    for _ in range(2):
+        stats, _, _ = run_and_compare(M, N, K, 1, 33, True, variant=PAIR, tile_n=256, split_k=-1, inp=inp,
+                                      sample=True, n_random=32)
+        assert stats["violations"] == 0, stats
+    assert fm.fp8mm_device_status() == 0
