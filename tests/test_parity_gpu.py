@@ -259,10 +259,11 @@ def test_host_entry_in_blocks():
     _need_gpu()
     import fp8_scaled_gemm_gb300 as fm
     from fp8_scaled_gemm_gb300.inputs import make_inputs
-    # 3000 x 2500: 3 x 3 blocks of the growing-square schedule, ragged in
-    # both directions; row-wise scales and bias are sliced per block
+    # 3300 x 3100: 3 x 3 blocks of the growing-square schedule (chunks of
+    # 1280, 1024 and 996 / 796 rows), ragged in both directions; row-wise
+    # scales and bias are sliced per block
     for mode, bias in ((1, True), (0, False)):
-        inp = make_inputs(3000, 2500, 528, mode, seed=13, with_bias=bias)
+        inp = make_inputs(3300, 3100, 528, mode, seed=13, with_bias=bias)
         host = fm.fp8_scaled_mm_host(inp.a_q.pin_memory(), inp.bt_q.pin_memory().t(),
                                      inp.scale_a.pin_memory(), inp.scale_b.pin_memory(), mode,
                                      bias=None if inp.bias is None else inp.bias.pin_memory())
