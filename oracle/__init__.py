@@ -17,9 +17,14 @@ gist "matmul_fp8.py" (FP8 Matmul), ``matmul_fp8_kernel`` scale epilogue;
 PyTorch PR #125204 "fp8 row-scaling kernel for scaled_mm", Summary (row-wise
 scale lengths M and N, TN layout); PyTorch PR #142045, Summary (bias).
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` against values
-fixed by the pages or by mathematics (closed forms, exact rational brute
-force, torch's independent float8/bf16 conversions). No function is unpinned.
+Every function here is pinned against values fixed by the pages or by
+mathematics: the matmul, the decoders and the output rounding by
+``tests/test_oracle_pins.py`` (closed forms, exact rational brute force,
+torch's independent float8/bf16 conversions), the quantiser by
+``tests/test_oracle_quant_pins.py``, and ``tolerance`` with its ``absum``
+input by ``tests/test_oracle_tolerance_pins.py`` (hand-worked literals, the
+one-step property of the output formats, planted slips). No function is
+unpinned.
 """
 from __future__ import annotations
 
