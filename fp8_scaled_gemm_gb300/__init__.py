@@ -56,7 +56,7 @@ EXPORTS = (
     "fp8_scaled_mm_noalloc", "fp8_quantize", "fp8_scaled_mm_bf16", "fp8_scaled_bmm",
     "fp8_scaled_mm_layout",
     "fp8mm_reserve_workspace", "fp8mm_device_status", "fp8mm_status_string",
-    "fp8mm_last_error", "fp8mm_describe_choice", "fp8mm_describe_bmm_choice", "fp8mm_debug_inject",
+    "fp8mm_last_cuda_error", "fp8mm_last_error", "fp8mm_describe_choice", "fp8mm_describe_bmm_choice", "fp8mm_debug_inject",
     "fp8mm_autotune", "fp8mm_autotune_clear", "fp8mm_autotune_count", "fp8mm_autotune_save",
     "fp8mm_autotune_load",
 )
@@ -119,6 +119,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fp8mm_device_status.restype = i32
         lib.fp8mm_status_string.argtypes = [i32]
         lib.fp8mm_status_string.restype = ctypes.c_char_p
+        lib.fp8mm_last_cuda_error.argtypes = []
+        lib.fp8mm_last_cuda_error.restype = ctypes.c_char_p
         lib.fp8mm_last_error.argtypes = []
         lib.fp8mm_last_error.restype = ctypes.c_char_p
         lib.fp8mm_debug_inject.argtypes = [i64, i64]
@@ -143,7 +145,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
 
 def _check(rc: int):
     if rc != 0:
-        detail = load().fp8mm_last_error().decode(errors="replace")
+        detail = load().fp8mm_last_cuda_error().decode(errors="replace")
         raise Fp8mmError(rc, detail)
 
 
@@ -426,7 +428,13 @@ def fp8mm_status_string(status: int) -> str:
     return load().fp8mm_status_string(int(status)).decode()
 
 
+def fp8mm_last_cuda_error() -> str:
+    """Detail of the last failure on this host thread ("" if none)."""
+    return load().fp8mm_last_cuda_error().decode(errors="replace")
+
+
 def fp8mm_last_error() -> str:
+    """Alias of fp8mm_last_cuda_error."""
     return load().fp8mm_last_error().decode(errors="replace")
 
 

@@ -1458,6 +1458,8 @@ const char *fp8mm_status_string(int status)
     }
 }
 
+const char *fp8mm_last_cuda_error(void) { return t_last_error.c_str(); }
+
 const char *fp8mm_last_error(void) { return t_last_error.c_str(); }
 
 const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64_t K, int scale_mode)
@@ -1713,7 +1715,8 @@ int fp8mm_autotune_load(const char *path)
 // Layout of the scratch array (every call on a device shares it; it keeps
 // the last call's contents):
 //   [0, 256)                      status word of the in-kernel bounded waits
-//   [256, 256 + 64 KiB)           split-K arrival counters (4 per output tile)
+//   [256, 256 + 64 KiB)           split-K arrival counters (16 per output tile:
+//                                 1024 split tiles)
 //   [.., + 16 MiB)                fp32 split-K partial tiles
 // The status word and the counters a call uses are cleared on the caller's
 // stream before the kernel runs; the partial tiles are fully written before
@@ -1799,13 +1802,22 @@ extern "C" int fp8_scaled_mm_noalloc(const void *A, const void *B, const float *
         return rc;
     if (M == 0 || N == 0)
         return FP8MM_OK;
+    // work units (tiles x K slices) are counted in int, as in run()
+    if (cdiv(M, 16) * cdiv(N, 128) * 16 > INT32_MAX)
+        return FP8MM_ERR_SHAPE;
     NoAllocDevice *d = nullptr;
     rc = noalloc_setup(&d);
     if (rc != FP8MM_OK)
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    const Choice c = choose(M, N, K, d->sms, FP8MM_VARIANT_AUTO, 0, 0);
+    Choice c = choose(M, N, K, d->sms, FP8MM_VARIANT_AUTO, 0, 0);
+    // Stream-K needs its own partials (one 256 x 256 fp32 tile per CTA pair,
+    // 19 MiB on 152 SMs) and flags that stay zero between launches; this
+    // entry point takes the pair kernel's whole-tile schedule instead, with
+    // the split-K factor the time model gives it.
+    if (c.sk_tiles > 0)
+        c = choose(M, N, K, d->sms, FP8MM_VARIANT_PAIR, 256, 0);
     const size_t tiles = static_cast<size_t>(c.tiles_p) * c.tiles_q;
     const bool global_split = c.split > 1 && c.variant != FP8MM_VARIANT_SWAPK;
     const size_t partial_bytes =

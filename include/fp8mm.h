@@ -47,10 +47,10 @@
  *
  * Errors: argument errors are found on the host before anything is enqueued
  * and come back as a negative fp8mm_status; nothing is launched then. A
- * failing CUDA call returns FP8MM_ERR_CUDA and fp8mm_last_error() describes
- * it. Kernels never trap: every wait inside them is bounded, and a wait that
- * runs out records FP8MM_ERR_TIMEOUT in a per-device status word that
- * fp8mm_device_status() reads.
+ * failing CUDA call returns FP8MM_ERR_CUDA and fp8mm_last_cuda_error()
+ * describes it. Kernels never trap: every wait inside them is bounded, and a
+ * wait that runs out records FP8MM_ERR_TIMEOUT in a per-device status word
+ * that fp8mm_device_status() reads.
  */
 #ifndef FP8MM_H_
 #define FP8MM_H_
@@ -72,7 +72,7 @@ typedef enum fp8mm_status {
     FP8MM_ERR_SHAPE = -2,     /* M, N or K out of range, or K % 16 != 0        */
     FP8MM_ERR_ALIGN = -3,     /* a pointer is not aligned as required          */
     FP8MM_ERR_MODE = -4,      /* unknown scale_mode or kernel variant          */
-    FP8MM_ERR_CUDA = -5,      /* a CUDA call failed; see fp8mm_last_error()    */
+    FP8MM_ERR_CUDA = -5,      /* a CUDA call failed; see fp8mm_last_cuda_error() */
     FP8MM_ERR_NODEV = -6,     /* no CUDA device, or not an sm_103 device       */
     FP8MM_ERR_TIMEOUT = -7    /* a bounded in-kernel wait ran out              */
 } fp8mm_status;
@@ -374,7 +374,16 @@ int fp8mm_autotune_load(const char *path);
 
 /*
  * Grow the current device's split-K workspace to at least `bytes` now, so
- * that later calls do not allocate.
+ * that later calls do not allocate (for example before a CUDA graph
+ * capture). The pages' persistent TMA scaled_mm template is launched with a
+ * device workspace argument beside its operands (PyTorch PR #142045, review
+ * of torch/_inductor/kernel/mm_scaled.py, `get_tma_workspace_arg`); here the
+ * library owns that memory and holds the fp32 partial tiles of the split-K
+ * reduction (gist "matmul_fp8.py", `matmul_fp8_kernel`, SPLIT_K).
+ *   bytes  >= 0; FP8MM_ERR_SHAPE if negative. Growing synchronises the
+ *          device (the old buffer may be in use) and frees the old buffer.
+ * Returns FP8MM_OK, FP8MM_ERR_NODEV or FP8MM_ERR_CUDA (cudaMalloc failed;
+ * fp8mm_last_cuda_error() says why).
  */
 int fp8mm_reserve_workspace(int64_t bytes);
 
@@ -401,10 +410,32 @@ int fp8mm_device_status(void *stream);
  */
 int fp8mm_debug_inject(int64_t stop_after_kblocks, int64_t wait_limit_cycles);
 
-/* Static description of a status code. */
+/*
+ * Static description of a status code (never NULL; "unknown status" for a
+ * code not in fp8mm_status). The codes report the operand conditions the
+ * pages state for the TMA scaled_mm path, 16-byte aligned contiguous
+ * operands and K * itemsize a multiple of 16 (PyTorch PR #142101,
+ * description, and the review reply on K not divisible by the K block), and
+ * the pages' rejection of an unknown scaling granularity (gist
+ * "matmul_fp8.py", `get_scale`, which raises for anything but per-tensor and
+ * per-row). The returned string is static; the caller must not free it.
+ */
 const char *fp8mm_status_string(int status);
 
-/* Detail of the last FP8MM_ERR_CUDA on this host thread ("" if none). */
+/*
+ * Detail of the last failure on this host thread, "" if none: set whenever
+ * a call returns FP8MM_ERR_CUDA (the failing CUDA call with its error name
+ * and message) or FP8MM_ERR_TIMEOUT from fp8mm_device_status (the wait that
+ * ran out), and for the few argument errors that need more than a status
+ * code (a tensor-map encoding the driver refused, a problem beyond
+ * fp8_scaled_mm_noalloc's scratch). Thread-local; the pointer stays valid
+ * until the next call on this thread. The pages raise Python exceptions
+ * with a message at the same points (gist "matmul_fp8.py", `get_scale`).
+ */
+const char *fp8mm_last_cuda_error(void);
+
+/* The same string as fp8mm_last_cuda_error (an alias kept for callers of
+ * earlier builds). */
 const char *fp8mm_last_error(void);
 
 /* The kernel fp8_scaled_mm would launch for this problem, as text; for logs

@@ -40,6 +40,32 @@ def test_library_exports_every_header_function(lib):
         assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
 
 
+# The boundary the scope table fixes: these names, these codes.
+BOUNDARY_CALLS = ("fp8_scaled_mm", "fp8mm_status_string", "fp8mm_last_cuda_error",
+                  "fp8mm_reserve_workspace")
+BOUNDARY_ENUMS = {
+    "FP8MM_SCALE_TENSOR": 0, "FP8MM_SCALE_ROWWISE": 1,
+    "FP8MM_OK": 0, "FP8MM_ERR_NULL": -1, "FP8MM_ERR_SHAPE": -2, "FP8MM_ERR_ALIGN": -3,
+    "FP8MM_ERR_MODE": -4, "FP8MM_ERR_CUDA": -5, "FP8MM_ERR_NODEV": -6, "FP8MM_ERR_TIMEOUT": -7,
+}
+
+
+def test_boundary_names_are_exported_and_callable(lib):
+    for name in BOUNDARY_CALLS:
+        assert name in header_functions(), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr), name
+    text = open(HEADER).read()
+    for name, value in BOUNDARY_ENUMS.items():
+        m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
+        assert m and int(m.group(1)) == value, name
+    # each call answers without a GPU on these arguments
+    assert fm.fp8mm_status_string(-5) == "CUDA call failed"
+    assert isinstance(fm.fp8mm_last_cuda_error(), str)
+    assert fm.fp8mm_last_cuda_error() == fm.fp8mm_last_error()
+    assert lib.fp8mm_reserve_workspace(-1) == -2
+    assert call(lib, mode=7) == -4
+
+
 def test_status_strings(lib):
     for code, name in fm.STATUS.items():
         s = fm.fp8mm_status_string(code)

@@ -8,7 +8,11 @@ library instead. These tests call it through the C ABI twice in a row on
 problems whose kernel choice uses split-K (so the scratch array is really
 used, and reused with the previous call's contents still in it) and compare
 its output with fp8_scaled_mm's within the parity tolerance of the other GPU
-tests. This file is collected last on purpose.
+tests. Problems for which fp8_scaled_mm picks stream-K (the 8192^3 benchmark
+shape among them) take a whole-tile schedule here; those cases are checked
+against the oracle element by element (on sampled rows and columns at
+8192^3) and for unwritten elements over the whole output. This file is
+collected last on purpose.
 """
 from __future__ import annotations
 
@@ -18,7 +22,7 @@ import torch
 
 import oracle
 from fp8_scaled_gemm_gb300.inputs import make_inputs
-from tests._parity import bf16_bits, to_device
+from tests._parity import bf16_bits, compare, sample_indices, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -63,6 +67,51 @@ def test_noalloc_matches_fp8_scaled_mm_on_two_calls(M, N, K, mode, with_bias):
         bad = int((~(np.abs(got - ref) <= tol)).sum())
         assert bad == 0, f"call {call}: {bad} elements outside the tolerance"
     assert free_after == free_before
+
+
+@pytest.mark.parametrize("M,N,K,mode,with_bias,sample", [
+    (8192, 8192, 8192, 0, False, True),    # the benchmark shape, per-tensor
+    (3000, 5000, 4112, 1, True, True),     # ragged tiles and K tail, row-wise + bias
+])
+def test_noalloc_on_stream_k_shapes_matches_the_oracle(M, N, K, mode, with_bias, sample):
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+
+    choice = fm.fp8mm_describe_choice(M, N, K, mode)
+    assert "stream_k_tiles" in choice, f"expected fp8_scaled_mm to pick stream-K, got {choice}"
+    inp = make_inputs(M, N, K, mode, seed=42, with_bias=with_bias)
+    A, Bt, sa, sb, bias = to_device(inp)
+    ref_out = fm.fp8_scaled_mm(A, Bt.t(), sa, sb, mode, bias=bias)
+    assert fm.fp8mm_device_status() == 0
+    rows = sample_indices(M, 128, 96, 11) if sample else None
+    cols = sample_indices(N, 128, 96, 12) if sample else None
+
+    outs = [torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    for out in outs:
+        fm.fp8_scaled_mm_noalloc(A, Bt.t(), sa, sb, mode, bias=bias, out=out)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+    ref_bits = bf16_bits(ref_out)
+    for call, out in enumerate(outs):
+        # every element written (the inputs give finite results), on the whole output
+        unwritten = int(torch.isnan(out).sum().item())
+        assert unwritten == 0, f"call {call}: {unwritten} elements never written"
+        bits = bf16_bits(out)
+        if sample:
+            bits = bits[np.ix_(rows, cols)]
+        st = compare(bits, inp, rows, cols)
+        assert st["violations"] == 0, f"call {call} vs oracle: {st}"
+    # and against fp8_scaled_mm's stream-K result on the same grid
+    got = bf16_bits(outs[1])
+    if sample:
+        got, ref_bits = got[np.ix_(rows, cols)], ref_bits[np.ix_(rows, cols)]
+    _, _, absum = oracle.scaled_mm(inp.a_u8(), inp.bt_u8(), inp.sa_np(), inp.sb_np(), mode,
+                                   bias=inp.bias_u16(), rows=rows, cols=cols)
+    tol = oracle.tolerance(ref_bits, absum)
+    diff = np.abs(oracle.bf16_to_f64(got) - oracle.bf16_to_f64(ref_bits))
+    assert int((~(diff <= tol)).sum()) == 0
 
 
 def _scratch_bytes(choice: str) -> int:
