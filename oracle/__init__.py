@@ -10,7 +10,8 @@ What it computes, with its sources on the pages:
 
     out[i, j] = round( sum_k dec(A[i, k]) * dec(Bt[j, k]) * S_ij + bias[j] )
 
-(dec: e4m3fn or e5m2 codes; round: fp64 -> bf16 or fp16, one RNE step)
+(dec: e4m3fn or e5m2 codes; round: fp64 -> bf16, fp16 or fp32, one RNE
+step, or fp64 -> e4m3fn, one RNE step saturating at +-448)
 
 with ``S_ij = s_a * s_b`` (per-tensor) or ``s_a[i] * s_b[j]`` (row-wise):
 gist "matmul_fp8.py" (FP8 Matmul), ``matmul_fp8_kernel`` scale epilogue;
@@ -82,6 +83,10 @@ def _load():
         lib.oracle_f64_to_f16_array.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
         lib.oracle_f16_to_f64.restype = ctypes.c_double
         lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_f64_to_f32_rne.restype = ctypes.c_uint32
+        lib.oracle_f64_to_f32_rne.argtypes = [ctypes.c_double]
+        lib.oracle_f64_to_e4m3_sat.restype = ctypes.c_uint8
+        lib.oracle_f64_to_e4m3_sat.argtypes = [ctypes.c_double]
         lib.oracle_scaled_mm_typed.restype = ctypes.c_int
         lib.oracle_scaled_mm_typed.argtypes = [
             ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
@@ -134,7 +139,10 @@ def bf16_rne(x) -> np.ndarray:
 
 
 E4M3, E5M2 = 0, 1
-BF16, F16 = 0, 1
+BF16, F16, F32, E4M3_OUT = 0, 1, 2, 3
+# numpy container of each output type's bit patterns, and of its bias
+OUT_BITS = {BF16: np.uint16, F16: np.uint16, F32: np.uint32, E4M3_OUT: np.uint8}
+BIAS_BITS = {BF16: np.uint16, F16: np.uint16, F32: np.uint32, E4M3_OUT: np.uint16}
 
 
 def e5m2_table() -> np.ndarray:
@@ -158,8 +166,39 @@ def f16_to_f64(bits) -> np.ndarray:
     return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
 
 
+def f32_rne(x) -> np.ndarray:
+    """fp64 values -> IEEE binary32 bit patterns (uint32), one round-to-nearest-even."""
+    lib = _load()
+    v = np.asarray(x, dtype=np.float64)
+    flat = v.reshape(-1)
+    return np.fromiter((lib.oracle_f64_to_f32_rne(float(a)) for a in flat), dtype=np.uint32,
+                       count=flat.size).reshape(v.shape)
+
+
+def e4m3_sat(x) -> np.ndarray:
+    """fp64 values -> e4m3fn codes of an e4m3 output: one round-to-nearest-even,
+    saturating at +-448 (also for +-inf); NaN -> 0x7F."""
+    lib = _load()
+    v = np.asarray(x, dtype=np.float64)
+    flat = v.reshape(-1)
+    return np.fromiter((lib.oracle_f64_to_e4m3_sat(float(a)) for a in flat), dtype=np.uint8,
+                       count=flat.size).reshape(v.shape)
+
+
+def f32_to_f64(bits) -> np.ndarray:
+    """binary32 bit patterns (uint32) -> fp64 values."""
+    return np.asarray(bits, dtype=np.uint32).view(np.float32).astype(np.float64)
+
+
 def out_to_f64(bits, out_type: int) -> np.ndarray:
-    return bf16_to_f64(bits) if out_type == BF16 else f16_to_f64(bits)
+    """Output bit patterns of ``out_type`` -> fp64 values."""
+    if out_type == BF16:
+        return bf16_to_f64(bits)
+    if out_type == F16:
+        return f16_to_f64(bits)
+    if out_type == F32:
+        return f32_to_f64(bits)
+    return e4m3_table()[np.asarray(bits, dtype=np.uint8)]
 
 
 def bf16_to_f64(bits) -> np.ndarray:
@@ -180,11 +219,13 @@ def scaled_mm(A, Bt, scale_a, scale_b, scale_mode: int, bias=None,
     A: uint8 [M, K] fp8 codes (a_type 0 e4m3fn, 1 e5m2); Bt: uint8 [N, K]
     codes (B column-major, b_type likewise); scale_a / scale_b: float32
     arrays of 1 value (scale_mode 0) or M / N values (scale_mode 1); bias:
-    uint16 bit patterns [N] of the output type or None; out_type 0 bf16,
-    1 fp16.
+    [N] bit patterns (``BIAS_BITS[out_type]``: bf16 for bf16 and e4m3
+    outputs, fp16 for fp16, fp32 for fp32) or None; out_type 0 bf16, 1 fp16,
+    2 fp32, 3 e4m3fn.
 
-    Returns ``(out_bits uint16, ref64 float64, absum float64)``, each of
-    shape [len(rows), len(cols)]; ``absum`` is S_ij * sum_k |a_ik b_kj|.
+    Returns ``(out_bits, ref64 float64, absum float64)``, each of shape
+    [len(rows), len(cols)]; ``out_bits`` has the dtype ``OUT_BITS[out_type]``;
+    ``absum`` is S_ij * sum_k |a_ik b_kj|.
     """
     A = np.ascontiguousarray(A, dtype=np.uint8)
     Bt = np.ascontiguousarray(Bt, dtype=np.uint8)
@@ -204,14 +245,14 @@ def scaled_mm(A, Bt, scale_a, scale_b, scale_mode: int, bias=None,
         raise ValueError("scale_mode must be 0 or 1")
     bias_arr = None
     if bias is not None:
-        bias_arr = np.ascontiguousarray(bias, dtype=np.uint16).reshape(-1)
+        bias_arr = np.ascontiguousarray(bias, dtype=BIAS_BITS[int(out_type)]).reshape(-1)
         if bias_arr.size != N:
             raise ValueError("bias must hold N values")
     r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)
     nr = M if r is None else r.size
     nc = N if c is None else c.size
-    out = np.zeros((nr, nc), dtype=np.uint16)
+    out = np.zeros((nr, nc), dtype=OUT_BITS[int(out_type)])
     ref = np.zeros((nr, nc), dtype=np.float64)
     mag = np.zeros((nr, nc), dtype=np.float64)
     c_i64p = ctypes.POINTER(ctypes.c_int64)
@@ -261,10 +302,17 @@ def tolerance(ref_bits, absum, out_type: int = BF16) -> np.ndarray:
     ``ref`` is the rounded oracle value; the first term admits one unit in
     the last place of the output type (2^-7 relative for bf16, 2^-10 for
     fp16; a rounding boundary crossed by fp32 accumulation), the second the
-    fp32 accumulation error near cancellation. For fp16 outputs one quantum
-    of the subnormal range (2^-24) is also admitted.
+    fp32 accumulation error near cancellation. For the other output types
+    the same form with their unit in the last place and, because a relative
+    term cannot cover the subnormal range, one subnormal quantum: fp16
+    2^-10 |ref| + 2^-24, fp32 2^-23 |ref| + 2^-149, e4m3 2^-3 |ref| + 2^-9.
     """
     ref = out_to_f64(ref_bits, out_type)
+    acc = np.asarray(absum) * 2.0 ** -20
     if out_type == BF16:
-        return np.abs(ref) * 2.0 ** -7 + np.asarray(absum) * 2.0 ** -20
-    return np.abs(ref) * 2.0 ** -10 + np.asarray(absum) * 2.0 ** -20 + 2.0 ** -24
+        return np.abs(ref) * 2.0 ** -7 + acc
+    if out_type == F16:
+        return np.abs(ref) * 2.0 ** -10 + acc + 2.0 ** -24
+    if out_type == F32:
+        return np.abs(ref) * 2.0 ** -23 + acc + 2.0 ** -149
+    return np.abs(ref) * 2.0 ** -3 + acc + 2.0 ** -9

@@ -12,6 +12,8 @@
  *   S_ij   = s_a * s_b           (per-tensor)   or s_a[i] * s_b[j]  (row-wise)
  *   ref_ij = dot_ij * S_ij + bias[j]            (bias optional)     in fp64
  *   out_ij = bf16_rne(ref_ij)                   one rounding, fp64 -> bf16
+ *            (or fp16 / fp32 RNE, or e4m3 RNE with saturation, for the other
+ *            output types)
  *
  * Sources:
  *  - the product with scales applied after an fp32-or-better accumulation and
@@ -216,17 +218,105 @@ void oracle_f64_to_bf16_array(const double *x, uint16_t *out, int64_t n)
 }
 
 /*
+ * fp64 -> IEEE binary32 bit pattern, round to nearest, ties to even, in one
+ * step, by the same quantum method: quantum 2^(e-23) for 2^e <= |x| <
+ * 2^(e+1), e clamped at -126 below (subnormal quantum 2^-149); results of
+ * 2^128 or more (from 2^128 - 2^103, the tie above the largest finite
+ * value) overflow to infinity. NaN maps to a quiet NaN with the input's
+ * sign. The fp32 output of the scaled matmul (gist "matmul_fp8.py",
+ * `benchmark()`, which takes the output dtype as an argument).
+ */
+uint32_t oracle_f64_to_f32_rne(double x)
+{
+    const uint32_t sign = signbit(x) ? 0x80000000u : 0u;
+    double a, quantum, q, v;
+    int e;
+    float f;
+    uint32_t w;
+    if (isnan(x))
+        return sign | 0x7FC00000u;
+    a = fabs(x);
+    if (isinf(a))
+        return sign | 0x7F800000u;
+    if (a == 0.0)
+        return sign;
+    (void)frexp(a, &e);
+    e -= 1;
+    if (e < -126)
+        e = -126;
+    quantum = ldexp(1.0, e - 23);
+    q = nearbyint(a / quantum);
+    v = q * quantum;
+    if (v >= ldexp(1.0, 128))
+        return sign | 0x7F800000u;
+    f = (float)v;             /* exact: v is an fp32 value */
+    memcpy(&w, &f, sizeof w);
+    return sign | w;
+}
+
+/* binary32 bit pattern -> value (exact). */
+double oracle_f32_to_f64(uint32_t bits)
+{
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/*
+ * fp64 -> e4m3fn code for an e4m3 OUTPUT, one round-to-nearest-even step
+ * with saturation: the cast of the fp32 accumulator to an fp8 output dtype
+ * (gist "matmul_fp8.py", `matmul_fp8_kernel`, "Cast the accumulator to
+ * output dtype (fp8)"). The pages do not say what happens beyond the
+ * format's range; this reading saturates, as the hardware conversion such a
+ * cast lowers to does: every |x| that rounds above 448 (and +-inf) gives
+ * +-448 (0x7E / 0xFE). NaN gives 0x7F. Quantum 2^(e-3) for 2^e <= |x| <
+ * 2^(e+1), e clamped at -6 below (subnormal quantum 2^-9).
+ */
+uint8_t oracle_f64_to_e4m3_sat(double x)
+{
+    const uint8_t sign = signbit(x) ? 0x80u : 0u;
+    double a, q;
+    int e;
+    if (isnan(x))
+        return 0x7Fu;
+    a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a) || a >= 448.0)
+        return (uint8_t)(sign | 0x7Eu);
+    (void)frexp(a, &e);
+    e -= 1;
+    if (e < -6)
+        e = -6;
+    q = nearbyint(a / ldexp(1.0, e - 3));   /* significand in eighths */
+    if (q == 0.0)
+        return sign;                          /* below half the smallest subnormal */
+    if (q < 8.0)
+        return (uint8_t)(sign | (uint8_t)q);  /* subnormal (e == -6): m * 2^-9 */
+    if (q >= 16.0) {                          /* rounding carried into the next binade */
+        q /= 2.0;
+        e += 1;
+    }
+    if (e > 8 || (e == 8 && q > 14.0))        /* rounded above 448: saturate */
+        return (uint8_t)(sign | 0x7Eu);
+    return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)((int)q - 8));
+}
+
+/*
  * The scaled matrix multiply on a grid of selected outputs.
  *
  *   A        fp8 codes, [M, K] row-major; a_type 0 = e4m3fn, 1 = e5m2
  *   Bt       fp8 codes, [N, K] row-major (B[K, N] column-major); b_type likewise
  *   scale_a  1 value (scale_mode 0) or M values (scale_mode 1)
  *   scale_b  1 value (scale_mode 0) or N values (scale_mode 1)
- *   bias     [N] bit patterns of the output type, or NULL
- *   out_type 0 = bf16, 1 = fp16 (IEEE binary16)
+ *   bias     [N] values, or NULL: bf16 bit patterns (out_type 0 and 3),
+ *            binary16 (1) or binary32 (2)
+ *   out_type 0 = bf16, 1 = fp16 (IEEE binary16), 2 = fp32 (IEEE binary32),
+ *            3 = e4m3fn (saturating, see oracle_f64_to_e4m3_sat)
  *   rows     n_rows row indices into [0, M), or NULL for all rows (n_rows = M)
  *   cols     n_cols column indices into [0, N), or NULL for all (n_cols = N)
- *   out      [n_rows, n_cols] bit patterns of the output type
+ *   out      [n_rows, n_cols] bit patterns of the output type (2, 2, 4 or
+ *            1 bytes each)
  *   ref64    [n_rows, n_cols] unrounded fp64 result, or NULL
  *   absum    [n_rows, n_cols] S_ij * sum_k |a_ik * b_kj| (fp64), or NULL
  *
@@ -237,13 +327,35 @@ void oracle_f64_to_bf16_array(const double *x, uint16_t *out, int64_t n)
  *
  * Returns 0, or -1 on a bad argument, -2 when out of memory.
  */
+/* One output element's bias value and rounding, by output type. */
+static double bias_value(const void *bias, int64_t j, int out_type)
+{
+    if (out_type == 1)
+        return oracle_f16_to_f64(((const uint16_t *)bias)[j]);
+    if (out_type == 2)
+        return oracle_f32_to_f64(((const uint32_t *)bias)[j]);
+    return oracle_bf16_to_f64(((const uint16_t *)bias)[j]);   /* bf16 and e4m3 outputs */
+}
+
+static void store_rounded(void *out, int64_t idx, double ref, int out_type)
+{
+    if (out_type == 0)
+        ((uint16_t *)out)[idx] = oracle_f64_to_bf16_rne(ref);
+    else if (out_type == 1)
+        ((uint16_t *)out)[idx] = oracle_f64_to_f16_rne(ref);
+    else if (out_type == 2)
+        ((uint32_t *)out)[idx] = oracle_f64_to_f32_rne(ref);
+    else
+        ((uint8_t *)out)[idx] = oracle_f64_to_e4m3_sat(ref);
+}
+
 int oracle_scaled_mm_typed(const uint8_t *A, int a_type, const uint8_t *Bt, int b_type,
                            int64_t M, int64_t N, int64_t K,
                            const float *scale_a, const float *scale_b, int scale_mode,
-                           const uint16_t *bias, int out_type,
+                           const void *bias, int out_type,
                            const int64_t *rows, int64_t n_rows,
                            const int64_t *cols, int64_t n_cols,
-                           uint16_t *out, double *ref64, double *absum,
+                           void *out, double *ref64, double *absum,
                            int n_threads)
 {
     double table_a[256], table_b[256];
@@ -255,7 +367,7 @@ int oracle_scaled_mm_typed(const uint8_t *A, int a_type, const uint8_t *Bt, int 
         return -1;
     if (scale_mode != 0 && scale_mode != 1)
         return -1;
-    if ((a_type != 0 && a_type != 1) || (b_type != 0 && b_type != 1) || (out_type != 0 && out_type != 1))
+    if ((a_type != 0 && a_type != 1) || (b_type != 0 && b_type != 1) || out_type < 0 || out_type > 3)
         return -1;
     if (!rows)
         n_rows = M;
@@ -322,8 +434,8 @@ int oracle_scaled_mm_typed(const uint8_t *A, int a_type, const uint8_t *Bt, int 
                 S = (double)scale_a[i] * (double)scale_b[j];
             ref = dot * S;
             if (bias)
-                ref += out_type == 0 ? oracle_bf16_to_f64(bias[j]) : oracle_f16_to_f64(bias[j]);
-            out[r * n_cols + cc] = out_type == 0 ? oracle_f64_to_bf16_rne(ref) : oracle_f64_to_f16_rne(ref);
+                ref += bias_value(bias, j, out_type);
+            store_rounded(out, r * n_cols + cc, ref, out_type);
             if (ref64)
                 ref64[r * n_cols + cc] = ref;
             if (absum)
