@@ -71,16 +71,21 @@ def test_fp16_bound_literals(ref, absum, want):
 
 # ------------------------------------------ format property (exhaustive) ---
 
+_FMT = {"bf16": oracle.BF16, "fp16": oracle.F16, "fp32": oracle.F32, "e4m3": oracle.E4M3_OUT}
+
+
 def _neighbours(bits: np.ndarray, fmt: str, step: int) -> np.ndarray:
-    """Value ``step`` representable values away from each positive pattern
-    (same sign; patterns are positive here so +step is away from zero)."""
-    return (bits.astype(np.int64) + step).astype(np.uint16)
+    """Value ``step`` representable values away from each pattern (the sign
+    bit is the top bit, so +step moves away from zero on either sign)."""
+    return (bits.astype(np.int64) + step).astype(bits.dtype)
 
 
 def _check_ulp_property(fmt: str, bits: np.ndarray, tol_fn=oracle.tolerance):
     """absum = 0: +1 and -1 steps admitted, +2 and -3 steps refused."""
-    out_type = oracle.BF16 if fmt == "bf16" else oracle.F16
-    dec = oracle.bf16_to_f64 if fmt == "bf16" else oracle.f16_to_f64
+    out_type = _FMT[fmt]
+
+    def dec(b):
+        return oracle.out_to_f64(b, out_type)
     ref = dec(bits)
     tol = tol_fn(bits, np.zeros(bits.shape), out_type)
     for step, admitted in ((1, True), (-1, True), (2, False), (-3, False)):
@@ -109,6 +114,31 @@ def test_bound_admits_one_step_and_refuses_two_on_every_value(fmt):
     bits = _positive_normals(fmt)
     _check_ulp_property(fmt, bits)
     _check_ulp_property(fmt, bits | np.uint16(0x8000))  # negative values mirror it
+
+
+def test_bound_one_step_property_fp32_and_e4m3_outputs():
+    # e4m3: every code from 2^-2 (0x28) up; below it the 2^-9 term is no
+    # longer small against two steps. fp32: a million normal values from
+    # 2^-100 up (the 2^-149 term is negligible there).
+    e4 = np.arange(0x28, 0x7F, dtype=np.uint8)
+    _check_ulp_property("e4m3", e4)
+    _check_ulp_property("e4m3", e4 | np.uint8(0x80))
+    rng = np.random.default_rng(5)
+    f32 = rng.integers(0x0D800000, 0x7F7FFFFD, size=1_000_000, dtype=np.int64).astype(np.uint32)
+    _check_ulp_property("fp32", f32)
+    _check_ulp_property("fp32", f32 | np.uint32(0x80000000))
+
+
+@pytest.mark.parametrize("out_type,ref_bits,absum,want", [
+    (oracle.F32, np.uint32(0x3F800000), 0.0, 2.0 ** -23 + 2.0 ** -149),      # ref 1.0
+    (oracle.F32, np.uint32(0x00000000), 1048576.0, 1.0 + 2.0 ** -149),      # ref 0
+    (oracle.E4M3_OUT, np.uint8(0x38), 0.0, 0.126953125),                   # ref 1.0: 1/8 + 1/512
+    (oracle.E4M3_OUT, np.uint8(0xFE), 0.0, 56.001953125),                  # ref -448: 56 + 1/512
+    (oracle.E4M3_OUT, np.uint8(0x00), 0.0, 0.001953125),                   # ref 0: 2^-9
+])
+def test_fp32_and_e4m3_bound_literals(out_type, ref_bits, absum, want):
+    got = oracle.tolerance(np.array([ref_bits]), np.array([absum]), out_type)
+    assert got[0] == want
 
 
 # ----------------------------------------------------- absum, hand-worked ---
