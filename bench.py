@@ -65,7 +65,7 @@ def parse_args(argv=None):
                     help="with --sweep: 'gist' (the gist's M x K x N list, both scalings) or a comma list of "
                          "[B@]MxNxK[:mode[:bias[:a_dtype:b_dtype:out_dtype]]] "
                          "(default: all benchmark shapes; B@ = a batch of B products, fp8_scaled_bmm; "
-                         "dtypes e4m3|e5m2 and bf16|fp16)")
+                         "dtypes e4m3|e5m2 and bf16|fp16|fp32|e4m3)")
     return ap.parse_args(argv)
 
 
@@ -332,9 +332,21 @@ GIST_SHAPES = [(512, 12288, 3072), (512, 3072, 12288), (1152, 12288, 3072), (115
                (2304, 12288, 3072), (2304, 3072, 12288), (4608, 12288, 3072), (4608, 3072, 12288)]
 
 
-def algorithmic_bytes(M, N, K, mode, bias, batch=1):
-    # fp8 operands (1 byte), 16-bit output and bias, fp32 scales
-    return batch * (M * K + N * K + 2 * M * N + (4 * (M + N) if mode == 1 else 8)) + (2 * N if bias else 0)
+# bytes per output element and per bias element, by output dtype name
+OUT_BYTES = {"bf16": 2, "fp16": 2, "fp32": 4, "e4m3": 1}
+BIAS_BYTES = {"bf16": 2, "fp16": 2, "fp32": 4, "e4m3": 2}
+
+
+def algorithmic_bytes(M, N, K, mode, bias, batch=1, out="bf16"):
+    # fp8 operands (1 byte), the output and bias of the output dtype, fp32 scales
+    return (batch * (M * K + N * K + OUT_BYTES[out] * M * N + (4 * (M + N) if mode == 1 else 8)) +
+            (BIAS_BYTES[out] * N if bias else 0))
+
+
+def out_dtype_of(name):
+    import torch
+    return {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32,
+            "e4m3": torch.float8_e4m3fn}[name]
 
 
 def plain_launches(M, N, K, mode, bias, n, device, types=("e4m3", "e4m3", "bf16"), batch=1):
@@ -345,7 +357,7 @@ def plain_launches(M, N, K, mode, bias, n, device, types=("e4m3", "e4m3", "bf16"
 
     inp = make_inputs(M, N, K, mode, SEED, with_bias=bias, a_dtype=types[0], b_dtype=types[1],
                       out_dtype=types[2])
-    odt = torch.bfloat16 if types[2] == "bf16" else torch.float16
+    odt = out_dtype_of(types[2])
     b = None if inp.bias is None else inp.bias.to(device)
     if batch == 1:
         A, B = inp.a_q.to(device), inp.bt_q.to(device).t()
@@ -375,9 +387,9 @@ def time_shape(M, N, K, mode, bias, steps, warmup, device, types=("e4m3", "e4m3"
 
     inp = make_inputs(M, N, K, mode, SEED, with_bias=bias, a_dtype=types[0], b_dtype=types[1],
                       out_dtype=types[2])
-    odt = torch.bfloat16 if types[2] == "bf16" else torch.float16
+    odt = out_dtype_of(types[2])
     typed = tuple(types) != ("e4m3", "e4m3", "bf16")
-    per_set = algorithmic_bytes(M, N, K, mode, bias, batch)
+    per_set = algorithmic_bytes(M, N, K, mode, bias, batch, types[2])
     n_sets = max(1, min(64, -(-3 * L2_BYTES // per_set)))
     sets = []
     for _ in range(n_sets):
@@ -462,7 +474,8 @@ def run_sweep(args):
             bias = bool(int(parts[2])) if len(parts) > 2 else False
             types = tuple(parts[3:6]) if len(parts) >= 6 else ("e4m3", "e4m3", "bf16")
             shapes.append((M, N, K, mode, bias, types, batch))
-    dts = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2, "bf16": torch.bfloat16, "fp16": torch.float16}
+    dts = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2, "bf16": torch.bfloat16, "fp16": torch.float16,
+           "fp32": torch.float32}
     sampler = None
     if not args.plain_launches:
         sampler = ClockSampler(device.index if device.index is not None else 0)
@@ -473,7 +486,7 @@ def run_sweep(args):
             n = plain_launches(M, N, K, mode, bias, args.warmup + 1, device, types, batch)
             print(json.dumps({"shape": [M, N, K], "batch": batch, "scale_mode": "row-wise" if mode else "per-tensor",
                               "bias": bias, "types": list(types), "launches": n, "kernel": builtin,
-                              "algorithmic_bytes": algorithmic_bytes(M, N, K, mode, bias, batch),
+                              "algorithmic_bytes": algorithmic_bytes(M, N, K, mode, bias, batch, types[2]),
                               "flops": 2 * M * N * K * batch}), flush=True)
             continue
         if args.tune:
@@ -483,7 +496,7 @@ def run_sweep(args):
                                                 types, batch)
         clocks = sampler.summary(*time_shape.window)
         flops = 2.0 * M * N * K * batch
-        nbytes = algorithmic_bytes(M, N, K, mode, bias, batch)
+        nbytes = algorithmic_bytes(M, N, K, mode, bias, batch, types[2])
         tflops = flops / (mean * 1e-3) / 1e12
         gbs = nbytes / (mean * 1e-3) / 1e9
         print(json.dumps({

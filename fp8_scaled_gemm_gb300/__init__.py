@@ -34,9 +34,13 @@ VARIANT_SWAPPAIR = 5
 
 TYPE_E4M3, TYPE_E5M2 = 0, 1
 MAJOR_K, MAJOR_MN = 0, 1
-OUT_BF16, OUT_F16 = 0, 1
+OUT_BF16, OUT_F16, OUT_F32, OUT_E4M3 = 0, 1, 2, 3
 _FP8 = {torch.float8_e4m3fn: TYPE_E4M3, torch.float8_e5m2: TYPE_E5M2}
-_OUT = {torch.bfloat16: OUT_BF16, torch.float16: OUT_F16}
+_OUT = {torch.bfloat16: OUT_BF16, torch.float16: OUT_F16, torch.float32: OUT_F32,
+        torch.float8_e4m3fn: OUT_E4M3}
+# the bias dtype each output dtype takes (an e4m3 output takes a bf16 bias)
+_BIAS = {torch.bfloat16: torch.bfloat16, torch.float16: torch.float16, torch.float32: torch.float32,
+         torch.float8_e4m3fn: torch.bfloat16}
 
 
 class Options(ctypes.Structure):
@@ -183,9 +187,11 @@ def _validate(A, B, scale_a, scale_b, scale_mode, bias, out, device_side: bool, 
     outs = tuple(_OUT) if typed else (torch.bfloat16,)
     if out.dtype not in outs or tuple(out.shape) != (M, N) or not out.is_contiguous():
         raise ValueError("out must be a contiguous [M, N] tensor of " +
-                         ("bfloat16 or float16" if typed else "bfloat16"))
-    if bias is not None and (bias.dtype != out.dtype or bias.numel() != N or not bias.is_contiguous()):
-        raise ValueError("bias must be a contiguous tensor of N values with out's dtype")
+                         ("bfloat16, float16, float32 or float8_e4m3fn" if typed else "bfloat16"))
+    if bias is not None and (bias.dtype != _BIAS[out.dtype] or bias.numel() != N or
+                             not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous tensor of N values of out's dtype "
+                         "(bfloat16 for a float8_e4m3fn output)")
     tensors = [A, B, scale_a, scale_b, out] + ([bias] if bias is not None else [])
     for t in tensors:
         if device_side and not t.is_cuda:
@@ -221,8 +227,9 @@ def fp8_scaled_mm_config(A, B, scale_a, scale_b, scale_mode: int, bias=None, out
 def fp8_scaled_mm_ex(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=None, stream=None,
                      out_dtype=torch.bfloat16, variant: int = VARIANT_AUTO, tile_n: int = 0,
                      split_k: int = 0):
-    """The operation with e4m3fn / e5m2 operands and a bf16 / fp16 output
-    (types taken from the tensors; bias has out's dtype)."""
+    """The operation with e4m3fn / e5m2 operands and a bf16 / fp16 / fp32 /
+    e4m3fn output (types taken from the tensors; bias has out's dtype, bf16
+    for an e4m3fn output, which saturates at +-448)."""
     if out is None:
         out = torch.empty((A.shape[0], B.shape[1]), dtype=out_dtype, device=A.device)
     M, N, K = _validate(A, B, scale_a, scale_b, scale_mode, bias, out, True, typed=True)
@@ -267,8 +274,8 @@ def fp8_scaled_mm_layout(A, B, scale_a, scale_b, scale_mode: int, bias=None, out
         if s.dtype != torch.float32 or s.numel() != n or not s.is_contiguous():
             raise ValueError(f"{name} must be a contiguous float32 tensor of {n} values")
     if out.dtype not in _OUT or tuple(out.shape) != (M, N) or not out.is_contiguous():
-        raise ValueError("out must be a contiguous [M, N] bfloat16 or float16 tensor")
-    if bias is not None and (bias.dtype != out.dtype or bias.numel() != N or not bias.is_contiguous()):
+        raise ValueError("out must be a contiguous [M, N] bfloat16, float16, float32 or float8_e4m3fn tensor")
+    if bias is not None and (bias.dtype != _BIAS.get(out.dtype) or bias.numel() != N or not bias.is_contiguous()):
         raise ValueError("bias must be a contiguous tensor of N values with out's dtype")
     for t in [A, B, scale_a, scale_b, out] + ([bias] if bias is not None else []):
         if not t.is_cuda:
@@ -308,8 +315,8 @@ def fp8_scaled_bmm(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=None,
         if s.dtype != torch.float32 or s.numel() != n or not s.is_contiguous():
             raise ValueError(f"{name} must be a contiguous float32 tensor of {n} values")
     if out.dtype not in _OUT or tuple(out.shape) != (nb, M, N) or not out.is_contiguous():
-        raise ValueError("out must be a contiguous [batch, M, N] bfloat16 or float16 tensor")
-    if bias is not None and (bias.dtype != out.dtype or bias.numel() != N or not bias.is_contiguous()):
+        raise ValueError("out must be a contiguous [batch, M, N] bfloat16, float16, float32 or float8_e4m3fn tensor")
+    if bias is not None and (bias.dtype != _BIAS.get(out.dtype) or bias.numel() != N or not bias.is_contiguous()):
         raise ValueError("bias must be a contiguous tensor of N values with out's dtype")
     for t in [A, B, scale_a, scale_b, out] + ([bias] if bias is not None else []):
         if not t.is_cuda:

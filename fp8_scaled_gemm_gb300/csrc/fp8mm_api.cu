@@ -719,11 +719,13 @@ int encode_and_dispatch(const Choice &c, const void *A, const void *B, void *out
     kp.out_tma = 0;
     const bool swap = c.variant == FP8MM_VARIANT_SWAP || c.variant == FP8MM_VARIANT_SWAPK ||
                       c.variant == FP8MM_VARIANT_SWAPPAIR;
-    // Row-major epilogues store through TMA when the output rows are 16-byte
-    // aligned (TILE without split-K, PAIR); otherwise through plain stores.
-    if (!swap && c.split == 1 && (N % 8) == 0 && (kp.ldo % 8) == 0 &&
+    // Row-major epilogues store 16-bit outputs through TMA when the output
+    // rows are 16-byte aligned (TILE without split-K, PAIR); otherwise, and
+    // for fp32 / e4m3 outputs, through plain stores.
+    const bool out16 = kp.out_type == FP8MM_OUT_BF16 || kp.out_type == FP8MM_OUT_F16;
+    if (!swap && out16 && c.split == 1 && (N % 8) == 0 && (kp.ldo % 8) == 0 &&
         (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
-        int rc = encode_out_map(&mo, out, M, N, kp.out_f16 != 0, batch, kp.ldo);
+        int rc = encode_out_map(&mo, out, M, N, kp.out_type == FP8MM_OUT_F16, batch, kp.ldo);
         if (rc != FP8MM_OK)
             return rc;
         kp.out_tma = 1;
@@ -785,8 +787,10 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
         return FP8MM_ERR_MODE;
     if ((a_type != FP8MM_TYPE_E4M3 && a_type != FP8MM_TYPE_E5M2) ||
         (b_type != FP8MM_TYPE_E4M3 && b_type != FP8MM_TYPE_E5M2) ||
-        (out_type != FP8MM_OUT_BF16 && out_type != FP8MM_OUT_F16))
+        (out_type < FP8MM_OUT_BF16 || out_type > FP8MM_OUT_E4M3))
         return FP8MM_ERR_MODE;
+    if (out_type == FP8MM_OUT_F32 && (reinterpret_cast<uintptr_t>(bias) & 3))
+        return FP8MM_ERR_ALIGN;   // an fp32 bias
     if (batch < 0)
         return FP8MM_ERR_SHAPE;
     if (M == 0 || N == 0 || batch == 0)
@@ -812,8 +816,8 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     fp8mm::KernelParams kp{};
     kp.scale_a = sa;
     kp.scale_b = sb;
-    kp.bias = static_cast<const unsigned short *>(bias);
-    kp.out = static_cast<unsigned short *>(out);
+    kp.bias = bias;
+    kp.out = out;
     kp.ldo = ldo > 0 ? ldo : N;
     kp.status = d->status;
     {
@@ -822,7 +826,7 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
                           c.variant == FP8MM_VARIANT_SWAPPAIR;
         const uint32_t fp = fmt_code(swap ? b_type : a_type), fq = fmt_code(swap ? a_type : b_type);
         kp.idesc_fmt = (fp << 7) | (fq << 10);
-        kp.out_f16 = out_type == FP8MM_OUT_F16 ? 1 : 0;
+        kp.out_type = out_type;
     }
     kp.M = static_cast<int>(M);
     kp.N = static_cast<int>(N);
@@ -835,7 +839,12 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     kp.num_units = c.units;
     kp.rowwise = scale_mode == FP8MM_SCALE_ROWWISE ? 1 : 0;
     kp.group = tile_group(c);
-    kp.vec_store = ((reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % 8) == 0 && (kp.ldo % 8) == 0) ? 1 : 0;
+    {
+        // 16-byte stores need 16-byte aligned rows: N and ldo in multiples of 16 bytes
+        const int64_t per16 = out_type == FP8MM_OUT_F32 ? 4 : out_type == FP8MM_OUT_E4M3 ? 16 : 8;
+        kp.vec_store =
+            ((reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % per16) == 0 && (kp.ldo % per16) == 0) ? 1 : 0;
+    }
     kp.timeout_cycles = wait_limit();
     kp.inject_stop_after = static_cast<int>(g_inject_stop_after.load());
     if (c.sk_tiles > 0) {
@@ -1514,7 +1523,7 @@ int fp8mm_autotune(int64_t batch, int64_t M, int64_t N, int64_t K, int scale_mod
         return FP8MM_ERR_MODE;
     if ((o.a_type != FP8MM_TYPE_E4M3 && o.a_type != FP8MM_TYPE_E5M2) ||
         (o.b_type != FP8MM_TYPE_E4M3 && o.b_type != FP8MM_TYPE_E5M2) ||
-        (o.out_type != FP8MM_OUT_BF16 && o.out_type != FP8MM_OUT_F16))
+        (o.out_type < FP8MM_OUT_BF16 || o.out_type > FP8MM_OUT_E4M3))
         return FP8MM_ERR_MODE;
     if (batch < 1 || M < 1 || N < 1 || M > INT32_MAX || N > INT32_MAX || K < 16 || K % 16 != 0 ||
         K > (int64_t(1) << 24) || batch * cdiv(M, 16) * cdiv(N, 128) * 16 > INT32_MAX)
@@ -1528,7 +1537,8 @@ int fp8mm_autotune(int64_t batch, int64_t M, int64_t N, int64_t K, int scale_mod
     // scratch: rotated copies of the operands so that one set is not served
     // from L2 when the next launch reads it
     const size_t a_bytes = static_cast<size_t>(batch * M * K), b_bytes = static_cast<size_t>(batch * N * K);
-    const size_t o_bytes = static_cast<size_t>(batch * M * N) * 2;
+    const size_t o_bytes =
+        static_cast<size_t>(batch * M * N) * (o.out_type == FP8MM_OUT_F32 ? 4 : o.out_type == FP8MM_OUT_E4M3 ? 1 : 2);
     const size_t per_set = a_bytes + b_bytes + o_bytes;
     const int n_sets = static_cast<int>(std::max<size_t>(1, std::min<size_t>(8, (3 * (size_t(129) << 20)) / per_set)));
     const bool rowwise = scale_mode == FP8MM_SCALE_ROWWISE;
@@ -1682,7 +1692,7 @@ int fp8mm_autotune_load(const char *path)
         k.K = kk;
         const bool valid = got == 15 && b >= 1 && m >= 1 && nn >= 1 && kk >= 16 && kk % 16 == 0 &&
                            (k.mode == 0 || k.mode == 1) && (k.a_type == 0 || k.a_type == 1) &&
-                           (k.b_type == 0 || k.b_type == 1) && (k.out_type == 0 || k.out_type == 1) &&
+                           (k.b_type == 0 || k.b_type == 1) && (k.out_type >= 0 && k.out_type <= 3) &&
                            v.variant >= FP8MM_VARIANT_TILE && v.variant <= FP8MM_VARIANT_SWAPPAIR &&
                            tile_n_supported(v.variant, v.tile_n) &&
                            (v.split >= 1 || (v.split == -1 && v.variant == FP8MM_VARIANT_PAIR)) && v.split <= 16 &&
@@ -1841,8 +1851,8 @@ extern "C" int fp8_scaled_mm_noalloc(const void *A, const void *B, const float *
     fp8mm::KernelParams kp{};
     kp.scale_a = scale_a;
     kp.scale_b = scale_b;
-    kp.bias = static_cast<const unsigned short *>(bias);
-    kp.out = static_cast<unsigned short *>(out);
+    kp.bias = bias;
+    kp.out = out;
     kp.ldo = N;
     kp.status = reinterpret_cast<int *>(d->scratch);
     kp.counters = reinterpret_cast<unsigned int *>(d->scratch + kNoAllocStatusBytes);

@@ -73,6 +73,12 @@ constexpr int kCountersPerTile = 16;
 // Device status codes (written once per launch, first writer wins).
 constexpr int kStatusTimeoutBase = 0x100;
 
+// Output element types (KernelParams::out_type): bf16 and fp16 leave the
+// row-major kernels through a shared-memory stage and TMA stores; fp32 and
+// e4m3fn (round to nearest even, saturating at +-448) are stored from
+// registers.
+constexpr int kOutBF16 = 0, kOutF16 = 1, kOutF32 = 2, kOutE4M3 = 3;
+
 // A batch of `batch` independent problems of one shape: operand tensor maps
 // are 3-D ({K, rows, batch}); item b has its own scales (scale_a + b, or
 // + b M row-wise; likewise scale_b) and output (out + b M N); the bias is
@@ -80,8 +86,8 @@ constexpr int kStatusTimeoutBase = 0x100;
 struct KernelParams {
     const float *scale_a;           // batch x (1 or M) values
     const float *scale_b;           // batch x (1 or N) values
-    const unsigned short *bias;     // N values (output type) or nullptr
-    unsigned short *out;            // [batch, M, N] row-major, bf16 or fp16 bit patterns
+    const void *bias;               // N values or nullptr: bf16 (bf16 and e4m3 outputs), fp16 or fp32
+    void *out;                      // [batch, M, N] row-major, elements of out_type
     long long ldo;                  // elements between output rows (N, or more for a block of a larger matrix)
     float *ws;                      // split-K partial tiles (splits > 1)
     unsigned int *counters;         // split-K arrivals, kCountersPerTile per output tile
@@ -98,7 +104,7 @@ struct KernelParams {
     int inject_stop_after;          // test hook (-1: off): CTA 0's producer stops after this many K blocks;
                                     // in the pair kernel, pair 1's stream-K partials are never flagged
     uint32_t idesc_fmt;             // operand format bits of the MMA instruction descriptor
-    int out_f16;                    // 1: fp16 output and bias, 0: bf16
+    int out_type;                   // kOutBF16, kOutF16, kOutF32 or kOutE4M3
     // Stream-K (pair kernel, splits == 1): the last sk_tiles tiles of the tile
     // order are not given out whole; their K blocks are divided evenly over
     // all CTA pairs (num_units then counts the whole tiles before them).
@@ -239,13 +245,25 @@ __device__ __forceinline__ Unit decode_unit(int u, const KernelParams &p)
     return w;
 }
 
+// Bytes per output element.
+__device__ __forceinline__ int out_esize(int out_type)
+{
+    return out_type == kOutF32 ? 4 : out_type == kOutE4M3 ? 1 : 2;
+}
+
+// First byte of output row m.
+__device__ __forceinline__ uint8_t *out_row(const KernelParams &p, int m)
+{
+    return static_cast<uint8_t *>(p.out) + static_cast<size_t>(m) * p.ldo * out_esize(p.out_type);
+}
+
 // The parameters of batch item b: its scales and its output matrix.
 __device__ __forceinline__ KernelParams for_item(const KernelParams &p, int b)
 {
     KernelParams q = p;
     q.scale_a += p.rowwise ? static_cast<size_t>(b) * p.M : static_cast<size_t>(b);
     q.scale_b += p.rowwise ? static_cast<size_t>(b) * p.N : static_cast<size_t>(b);
-    q.out += static_cast<size_t>(b) * p.M * p.ldo;
+    q.out = static_cast<uint8_t *>(p.out) + static_cast<size_t>(b) * p.M * p.ldo * out_esize(p.out_type);
     return q;
 }
 
@@ -254,10 +272,11 @@ __device__ __forceinline__ float tensor_scale(const KernelParams &q)
     return q.rowwise ? 0.0f : __ldg(q.scale_a) * __ldg(q.scale_b);
 }
 
-// Output conversions (round to nearest even) for bf16 or fp16.
-__device__ __forceinline__ uint32_t pack_out2(float lo, float hi, int f16)
+// Output conversions (round to nearest even) of two values for the 16-bit
+// output types, bf16 or fp16.
+__device__ __forceinline__ uint32_t pack_out2(float lo, float hi, int out_type)
 {
-    if (f16) {
+    if (out_type == kOutF16) {
         __half2 h = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t *>(&h);
     }
@@ -265,15 +284,70 @@ __device__ __forceinline__ uint32_t pack_out2(float lo, float hi, int f16)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ unsigned short to_out(float y, int f16)
+// Four values to e4m3fn codes (round to nearest even, saturating at the
+// largest finite value, NaN -> NaN), first value in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d)
 {
-    return f16 ? __half_as_ushort(__float2half_rn(y)) : __bfloat16_as_ushort(__float2bfloat16_rn(y));
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// One output element, idx elements from p.out.
+__device__ __forceinline__ void store_out1(const KernelParams &p, size_t idx, float y)
+{
+    if (p.out_type == kOutF32) {
+        static_cast<float *>(p.out)[idx] = y;
+    } else if (p.out_type == kOutE4M3) {
+        static_cast<uint8_t *>(p.out)[idx] = static_cast<uint8_t>(pack_e4m3x4(y, 0.0f, 0.0f, 0.0f) & 0xFFu);
+    } else {
+        static_cast<unsigned short *>(p.out)[idx] =
+            p.out_type == kOutF16 ? __half_as_ushort(__float2half_rn(y)) : __bfloat16_as_ushort(__float2bfloat16_rn(y));
+    }
 }
 
 __device__ __forceinline__ float bias_value(const KernelParams &p, int n)
 {
-    const unsigned short b = p.bias[n];
-    return p.out_f16 ? __half2float(__ushort_as_half(b)) : __bfloat162float(__ushort_as_bfloat16(b));
+    if (p.out_type == kOutF32)
+        return __ldg(static_cast<const float *>(p.bias) + n);
+    const unsigned short b = static_cast<const unsigned short *>(p.bias)[n];
+    return p.out_type == kOutF16 ? __half2float(__ushort_as_half(b)) : __bfloat162float(__ushort_as_bfloat16(b));
+}
+
+// CH consecutive values of output row m from column n0, for the fp32 and
+// e4m3 outputs: 16-byte stores when the row segment is aligned and whole
+// (p.vec_store), element stores otherwise. Rows m >= M are skipped.
+template <int CH>
+__device__ __forceinline__ void store_row_wide(const KernelParams &p, const float (&y)[CH], int m, int n0)
+{
+    if (m >= p.M)
+        return;
+    uint8_t *row = out_row(p, m);
+    if (p.vec_store && n0 + CH <= p.N) {
+        if (p.out_type == kOutF32) {
+#pragma unroll
+            for (int j = 0; j < CH; j += 4)
+                *reinterpret_cast<float4 *>(row + static_cast<size_t>(n0 + j) * 4) =
+                    make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < CH; j += 16) {
+                uint4 w;
+                w.x = pack_e4m3x4(y[j + 0], y[j + 1], y[j + 2], y[j + 3]);
+                w.y = pack_e4m3x4(y[j + 4], y[j + 5], y[j + 6], y[j + 7]);
+                w.z = pack_e4m3x4(y[j + 8], y[j + 9], y[j + 10], y[j + 11]);
+                w.w = pack_e4m3x4(y[j + 12], y[j + 13], y[j + 14], y[j + 15]);
+                *reinterpret_cast<uint4 *>(row + n0 + j) = w;
+            }
+        }
+    } else {
+        const size_t base = static_cast<size_t>(m) * p.ldo;
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+            if (n0 + j < p.N)
+                store_out1(p, base + n0 + j, y[j]);
+    }
 }
 
 // SWAP epilogue for CH accumulator columns held by one thread, with its
@@ -297,7 +371,7 @@ __device__ __forceinline__ void store_swap_chunk(const KernelParams &p, const fl
     for (int j = 0; j < CH; ++j) {
         const int m = qbase + j;
         if (m < p.M)
-            p.out[static_cast<size_t>(m) * p.ldo + n] = to_out(y[j], p.out_f16);
+            store_out1(p, static_cast<size_t>(m) * p.ldo + n, y[j]);
     }
 }
 
@@ -326,22 +400,26 @@ __device__ __forceinline__ void store_chunk(const KernelParams &p, const float (
         }
         if (m >= p.M)
             return;
-        unsigned short *orow = p.out + static_cast<size_t>(m) * p.ldo;
+        if (p.out_type == kOutF32 || p.out_type == kOutE4M3) {
+            store_row_wide<CH>(p, y, m, qbase);
+            return;
+        }
+        unsigned short *orow = reinterpret_cast<unsigned short *>(out_row(p, m));
         if (p.vec_store && qbase + CH <= p.N) {
 #pragma unroll
             for (int j = 0; j < CH; j += 8) {
                 uint4 w;
-                w.x = pack_out2(y[j + 0], y[j + 1], p.out_f16);
-                w.y = pack_out2(y[j + 2], y[j + 3], p.out_f16);
-                w.z = pack_out2(y[j + 4], y[j + 5], p.out_f16);
-                w.w = pack_out2(y[j + 6], y[j + 7], p.out_f16);
+                w.x = pack_out2(y[j + 0], y[j + 1], p.out_type);
+                w.y = pack_out2(y[j + 2], y[j + 3], p.out_type);
+                w.z = pack_out2(y[j + 4], y[j + 5], p.out_type);
+                w.w = pack_out2(y[j + 6], y[j + 7], p.out_type);
                 *reinterpret_cast<uint4 *>(orow + qbase + j) = w;
             }
         } else {
 #pragma unroll
             for (int j = 0; j < CH; ++j)
                 if (qbase + j < p.N)
-                    orow[qbase + j] = to_out(y[j], p.out_f16);
+                    store_out1(p, static_cast<size_t>(m) * p.ldo + qbase + j, y[j]);
         }
     } else {
         const int n = pidx;
@@ -383,9 +461,50 @@ struct PartialSrc {
     }
 };
 
+// Row-major epilogue for the fp32 and e4m3 outputs: one warp's 32
+// accumulator rows (TMEM lanes) x BN columns, 32 columns at a time; each
+// thread stores its row's 32 values from registers (16-byte stores when the
+// rows are aligned). Stream-K partials in `add` are added first, as in the
+// staged epilogue below.
+template <int BN>
+__device__ __forceinline__ void epilogue_rows_wide(const KernelParams &p, uint32_t trow, int m_row0, int n0, int lane,
+                                                float s_tensor, const PartialSrc add)
+{
+    constexpr unsigned kAll = 0xffffffffu;
+    const int m = m_row0 + lane;
+    const float sa = (p.rowwise && m < p.M) ? __ldg(p.scale_a + m) : 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        const int nl = n0 + c * 32 + lane;
+        const bool in = nl < p.N;
+        const float sbl = (p.rowwise && in) ? __ldg(p.scale_b + nl) : 0.0f;
+        const float bl = (p.bias != nullptr && in) ? bias_value(p, nl) : 0.0f;
+        float v[32];
+        ptx::tmem_ld_32cols(trow + static_cast<uint32_t>(c * 32), v);
+        for (int k = 0; k < add.count; ++k) {
+            const float4 *src = add.chunk(k, add.colt0 + c * 32);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const float4 x = add.ring == nullptr ? __ldcg(src + g * 128) : src[g * 128];
+                v[4 * g] += x.x;
+                v[4 * g + 1] += x.y;
+                v[4 * g + 2] += x.z;
+                v[4 * g + 3] += x.w;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float s = p.rowwise ? sa * __shfl_sync(kAll, sbl, j) : s_tensor;
+            v[j] = fmaf(v[j], s, __shfl_sync(kAll, bl, j));
+        }
+        store_row_wide<32>(p, v, m, n0 + c * 32);
+    }
+}
+
 // Row-major epilogue of one warp's 32 accumulator rows (TMEM lanes) x BN
 // columns, 64 columns at a time, through a 4 KB shared-memory stage per
-// warp. Each thread converts its row's 64 values to bf16 and writes them as
+// warp (bf16 and fp16 outputs; fp32 and e4m3 go to epilogue_rows_wide).
+// Each thread converts its row's 64 values to bf16 and writes them as
 // one 128-byte line of the stage, 16-byte chunks rotated by (row % 8) (the
 // 128-byte swizzle, so the eight threads of a quarter-warp hit distinct
 // banks). The block then leaves as one TMA tensor store of 32 rows x 64
@@ -403,6 +522,10 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                                                      uint8_t *stage, uint32_t stage_smem, uint32_t &chunks,
                                                      float s_tensor, int item, const PartialSrc add = PartialSrc{})
 {
+    if (p.out_type == kOutF32 || p.out_type == kOutE4M3) {
+        epilogue_rows_wide<BN>(p, trow, m_row0, n0, lane, s_tensor, add);
+        return;
+    }
     constexpr unsigned kAll = 0xffffffffu;
     const int m = m_row0 + lane;
     const float sa = (p.rowwise && m < p.M) ? __ldg(p.scale_a + m) : 0.0f;
@@ -457,7 +580,7 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                 const float b1 = has_bias ? __shfl_sync(kAll, bl, j + 1) : 0.0f;
                 const float y0 = fmaf(v[j], s0, b0);
                 const float y1 = fmaf(v[j + 1], s1, b1);
-                w[h * 16 + j / 2] = pack_out2(y0, y1, p.out_f16);
+                w[h * 16 + j / 2] = pack_out2(y0, y1, p.out_type);
             }
         }
         const uint32_t buf = NBUF == 1 ? 0u : (chunks & 1u);
@@ -495,7 +618,7 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                 const uint8_t *src =
                     stage + buf * 4096u + r * 128 + ((((lane >> 2) ^ (r & 7)) & 7) * 16) + (lane & 3) * 4;
                 const uint32_t pr = *reinterpret_cast<const uint32_t *>(src);
-                unsigned short *dst = p.out + static_cast<size_t>(mm) * p.ldo + col;
+                unsigned short *dst = reinterpret_cast<unsigned short *>(out_row(p, mm)) + col;
                 if (col < p.N)
                     dst[0] = static_cast<unsigned short>(pr & 0xFFFFu);
                 if (col + 1 < p.N)

@@ -279,7 +279,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kThreads, 1)
                 const int m = tq * BN + col;
                 if (n_in && m < p.M) {
                     const float sc = pb.rowwise ? scale_a_tile[col] * red_sb : red_stensor;
-                    pb.out[static_cast<size_t>(m) * pb.ldo + n] = to_out(fmaf(acc, sc, red_bias), pb.out_f16);
+                    store_out1(pb, static_cast<size_t>(m) * pb.ldo + n, fmaf(acc, sc, red_bias));
                 }
             }
         }

@@ -14,7 +14,9 @@ input recipe the pages use to make FP8 operands from bf16 data:
   * B made column-major, i.e. stored as Bt[N, K] row-major (same page,
     ``b.to(dtype).t().contiguous().t()``);
   * the optional bias is ``randn(N) * 0.1`` in bf16, drawn from the same
-    generator right after ``b`` (the pages fix no distribution for it).
+    generator right after ``b`` (the pages fix no distribution for it), then
+    held in the bias dtype of the output type: fp16 for an fp16 output, fp32
+    for an fp32 output, bf16 for bf16 and e4m3fn outputs.
 
 Generation runs on the CPU so the bytes depend only on (shape, seed, mode).
 """
@@ -27,6 +29,9 @@ import torch
 
 E4M3_MAX = 448.0  # torch.finfo(torch.float8_e4m3fn).max
 FP8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+OUT_TYPES = {"bf16": 0, "fp16": 1, "fp32": 2, "e4m3": 3}
+OUT_DTYPES = {0: torch.bfloat16, 1: torch.float16, 2: torch.float32, 3: torch.float8_e4m3fn}
+BIAS_DTYPES = {0: torch.bfloat16, 1: torch.float16, 2: torch.float32, 3: torch.bfloat16}
 
 
 @dataclass
@@ -39,10 +44,10 @@ class ScaledMMInputs:
     bt_q: torch.Tensor              # float8_e4m3fn [N, K] row-major (B column-major)
     scale_a: torch.Tensor           # float32 [1] or [M]
     scale_b: torch.Tensor           # float32 [1] or [N]
-    bias: Optional[torch.Tensor]    # bfloat16 / float16 [N] or None
+    bias: Optional[torch.Tensor]    # bfloat16 / float16 / float32 [N] or None
     a_type: int = 0                 # 0 e4m3fn, 1 e5m2
     b_type: int = 0
-    out_type: int = 0               # 0 bf16, 1 fp16
+    out_type: int = 0               # 0 bf16, 1 fp16, 2 fp32, 3 e4m3fn
 
     # numpy views for the oracle (uint8 codes, float32 scales, uint16 bias bits)
     def a_u8(self):
@@ -58,9 +63,16 @@ class ScaledMMInputs:
         return self.scale_b.numpy()
 
     def bias_u16(self):
+        """The bias bit patterns (uint16 for 16-bit bias dtypes, uint32 for fp32)."""
         if self.bias is None:
             return None
+        if self.bias.dtype == torch.float32:
+            return self.bias.view(torch.int32).numpy().view("uint32")
         return self.bias.view(torch.int16).numpy().view("uint16")
+
+    @property
+    def out_dtype(self) -> torch.dtype:
+        return OUT_DTYPES[self.out_type]
 
     def oracle_types(self):
         """Keyword arguments of oracle.scaled_mm for this input set's types."""
@@ -76,7 +88,8 @@ def make_inputs(M: int, N: int, K: int, scale_mode: int, seed: int,
                 with_bias: bool = False, a_dtype: str = "e4m3", b_dtype: str = "e4m3",
                 out_dtype: str = "bf16") -> ScaledMMInputs:
     """The recipe above; ``a_dtype`` / ``b_dtype`` pick e4m3fn or e5m2 (scale
-    = amax / finfo(dtype).max), ``out_dtype`` the bias dtype (bf16 or fp16)."""
+    = amax / finfo(dtype).max), ``out_dtype`` ("bf16", "fp16", "fp32",
+    "e4m3") the output type, and with it the bias dtype."""
     if scale_mode not in (0, 1):
         raise ValueError("scale_mode must be 0 (per-tensor) or 1 (row-wise)")
     g = torch.Generator(device="cpu")
@@ -86,8 +99,7 @@ def make_inputs(M: int, N: int, K: int, scale_mode: int, seed: int,
     bias = None
     if with_bias:
         bias = (torch.randn(N, dtype=torch.bfloat16, generator=g) * 0.1).contiguous()
-        if out_dtype == "fp16":
-            bias = bias.to(torch.float16)
+        bias = bias.to(BIAS_DTYPES[OUT_TYPES[out_dtype]])
     ta, tb = FP8[a_dtype], FP8[b_dtype]
     qa, qb = torch.finfo(ta).max, torch.finfo(tb).max
     if scale_mode == 0:
@@ -107,7 +119,7 @@ def make_inputs(M: int, N: int, K: int, scale_mode: int, seed: int,
         a_q=a_q.contiguous(), bt_q=bt_q,
         scale_a=sa.reshape(-1).contiguous(), scale_b=sb.reshape(-1).contiguous(),
         bias=bias, a_type=0 if a_dtype == "e4m3" else 1, b_type=0 if b_dtype == "e4m3" else 1,
-        out_type=0 if out_dtype == "bf16" else 1)
+        out_type=OUT_TYPES[out_dtype])
 
 
 def from_codes(A_u8, Bt_u8, scale_a, scale_b, scale_mode: int,

@@ -132,7 +132,9 @@ typedef enum fp8mm_type {
 
 typedef enum fp8mm_out_type {
     FP8MM_OUT_BF16 = 0,       /* bf16 output and bias                           */
-    FP8MM_OUT_F16 = 1         /* IEEE fp16 output and bias                      */
+    FP8MM_OUT_F16 = 1,        /* IEEE fp16 output and bias                      */
+    FP8MM_OUT_F32 = 2,        /* IEEE fp32 output and bias (bias 4-byte aligned) */
+    FP8MM_OUT_E4M3 = 3        /* float8_e4m3fn output, saturating at +-448; bf16 bias */
 } fp8mm_out_type;
 
 typedef struct fp8mm_options {
@@ -147,12 +149,18 @@ typedef struct fp8mm_options {
 /*
  * The operation with other element types: A and B each e4m3fn or e5m2
  * (mixed allowed; the tensor cores multiply them exactly and sum in fp32),
- * out and bias bf16 or fp16 (one round-to-nearest-even of the fp32 result).
- * Sources: the gist "matmul_fp8.py", `benchmark()`, quantises to
- * float8_e4m3fn or float8_e5m2 and casts the accumulator to the output's
- * dtype (`matmul_fp8_kernel`, fp16 output when SPLIT_K is used). Layouts,
- * alignment and the other arguments as fp8_scaled_mm / _config; unknown
- * type codes return FP8MM_ERR_MODE; options == NULL returns FP8MM_ERR_NULL.
+ * and the output bf16, fp16, fp32 or e4m3fn: one conversion of the fp32
+ * result acc * scale + bias, round to nearest even. bf16 / fp16 / fp32
+ * outputs take a bias of their own type; an e4m3fn output takes a bf16
+ * bias, and values that round above 448 in magnitude (and infinities)
+ * saturate to +-448 while NaN stays NaN (0x7F), as the hardware conversion
+ * does. Sources: the gist "matmul_fp8.py", `benchmark()`, quantises to
+ * float8_e4m3fn or float8_e5m2 and takes the output dtype as an argument,
+ * and `matmul_fp8_kernel` casts the accumulator to the output's dtype
+ * ("Cast the accumulator to output dtype (fp8)"). out is [M, N] row-major
+ * with elements of 2, 2, 4 or 1 bytes. Layouts, alignment and the other
+ * arguments as fp8_scaled_mm / _config; unknown type codes return
+ * FP8MM_ERR_MODE; options == NULL returns FP8MM_ERR_NULL.
  */
 int fp8_scaled_mm_ex(const void *A, const void *B,
                      const float *scale_a, const float *scale_b, int scale_mode,

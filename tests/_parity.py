@@ -18,6 +18,25 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def out_bits(t: torch.Tensor) -> np.ndarray:
+    """Bit patterns of an output tensor of any output dtype (uint16 for
+    bf16 / fp16, uint32 for fp32, uint8 for e4m3fn)."""
+    t = t.contiguous()
+    if t.dtype == torch.float32:
+        return t.view(torch.int32).cpu().numpy().view(np.uint32)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).cpu().numpy()
+    return bf16_bits(t)
+
+
+def unwritten_out(shape, dtype, device="cuda") -> torch.Tensor:
+    """An output buffer pre-filled with NaN (0x7F for e4m3fn), so that an
+    element the kernel never writes fails the comparison."""
+    if dtype == torch.float8_e4m3fn:
+        return torch.full(shape, 0x7F, dtype=torch.uint8, device=device).view(dtype)
+    return torch.full(shape, float("nan"), dtype=dtype, device=device)
+
+
 def sample_indices(n: int, tile: int, n_random: int, seed: int) -> np.ndarray:
     """Tile-edge indices (first/last of every tile, the last index) plus random ones."""
     idx = {0, n - 1}
@@ -69,8 +88,7 @@ def run_and_compare(M, N, K, mode, seed, with_bias, variant=0, tile_n=0, split_k
         inp = make_inputs(M, N, K, mode, seed, with_bias=with_bias, a_dtype=a_dtype,
                           b_dtype=b_dtype, out_dtype=out_dtype)
     A, Bt, sa, sb, bias = to_device(inp)
-    odt = torch.bfloat16 if inp.out_type == 0 else torch.float16
-    out = torch.full((M, N), float("nan"), dtype=odt, device="cuda")
+    out = unwritten_out((M, N), inp.out_dtype)
     if (inp.a_type, inp.b_type, inp.out_type) == (0, 0, 0):
         fm.fp8_scaled_mm_config(A, Bt.t(), sa, sb, mode, bias=bias, out=out,
                                 variant=variant, tile_n=tile_n, split_k=split_k)
@@ -79,7 +97,7 @@ def run_and_compare(M, N, K, mode, seed, with_bias, variant=0, tile_n=0, split_k
                             variant=variant, tile_n=tile_n, split_k=split_k)
     status = fm.fp8mm_device_status()
     assert status == 0, f"device status {status}: {fm.fp8mm_last_error()}"
-    bits = bf16_bits(out)
+    bits = out_bits(out)
     rows = cols = None
     if sample:
         rows = sample_indices(M, 128, n_random, seed + 1)

@@ -127,7 +127,14 @@ def test_ex_rejects_unknown_types(lib):
                                     64, 64, 64, None, ctypes.byref(opt))
     assert ex(2, 0, 0) == -4
     assert ex(0, -1, 0) == -4
-    assert ex(0, 0, 2) == -4
+    assert ex(0, 0, 4) == -4          # output types are 0..3 (bf16, fp16, fp32, e4m3fn)
+    assert ex(0, 0, -1) == -4
+
+    def ex_bias(ot, bias_addr):
+        opt = fm.Options(0, 0, ot, 0, 0, 0)
+        return lib.fp8_scaled_mm_ex(P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), 0, P(bias_addr),
+                                    P(ALIGNED), 64, 64, 64, None, ctypes.byref(opt))
+    assert ex_bias(2, ALIGNED + 2) == -3   # an fp32 bias must be 4-byte aligned
     assert lib.fp8_scaled_mm_ex(P(ALIGNED), P(ALIGNED), P(ALIGNED), P(ALIGNED), 0, None, P(ALIGNED),
                                 64, 64, 64, None, None) == -1
 

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from fp8_scaled_gemm_gb300.inputs import make_inputs
-from tests._parity import bf16_bits, compare
+from tests._parity import bf16_bits, compare, out_bits, unwritten_out
 
 pytestmark = pytest.mark.gpu
 
@@ -38,9 +38,8 @@ def run_batch(items, mode, variant=0, tile_n=0, split_k=0):
     sa = torch.cat([it.scale_a for it in items]).cuda()
     sb = torch.cat([it.scale_b for it in items]).cuda()
     bias = None if items[0].bias is None else items[0].bias.cuda()
-    odt = torch.bfloat16 if items[0].out_type == 0 else torch.float16
     nb, M, N = len(items), items[0].M, items[0].N
-    out = torch.full((nb, M, N), float("nan"), dtype=odt, device="cuda")
+    out = unwritten_out((nb, M, N), items[0].out_dtype)
     fm.fp8_scaled_bmm(A, Bt.transpose(1, 2), sa, sb, mode, bias=bias, out=out, variant=variant,
                       tile_n=tile_n, split_k=split_k)
     assert fm.fp8mm_device_status() == 0, fm.fp8mm_last_error()
@@ -49,7 +48,7 @@ def run_batch(items, mode, variant=0, tile_n=0, split_k=0):
 
 def check_items(out, items):
     for i, it in enumerate(items):
-        stats = compare(bf16_bits(out[i]), it)
+        stats = compare(out_bits(out[i]), it)
         assert stats["violations"] == 0, f"item {i}: {stats}"
 
 
@@ -114,3 +113,14 @@ def test_batched_full_size_sampled():
     for i, it in enumerate(items):
         stats = compare(bf16_bits(out[i])[np.ix_(rows, cols)], it, rows, cols)
         assert stats["violations"] == 0, f"item {i}: {stats}"
+
+
+@pytest.mark.parametrize("variant,tile_n,split", [(TILE, 256, 1), (PAIR, 256, 1), (PAIR, 256, -1),
+                                                  (TILE, 128, 3), (SWAP, 32, 1), (SWAPK, 64, 2)])
+@pytest.mark.parametrize("out_dtype", ["fp32", "e4m3"])
+def test_bmm_fp32_and_e4m3_outputs(variant, tile_n, split, out_dtype):
+    """Items sit back to back in an output of 4- or 1-byte elements."""
+    _need_gpu()
+    M = 200 if variant in (TILE, PAIR) else 40
+    items = make_batch(3, M, 264, 1040, 1, 70, True, out_dtype=out_dtype)
+    check_items(run_batch(items, 1, variant=variant, tile_n=tile_n, split_k=split), items)

@@ -198,7 +198,8 @@ def test_host_entry_in_several_chunks():
 
 # ------------------------------------------------- other element types ------
 
-TYPES = [("e5m2", "e5m2", "bf16"), ("e4m3", "e5m2", "fp16"), ("e5m2", "e4m3", "fp16")]
+TYPES = [("e5m2", "e5m2", "bf16"), ("e4m3", "e5m2", "fp16"), ("e5m2", "e4m3", "fp16"),
+         ("e4m3", "e4m3", "fp32"), ("e4m3", "e4m3", "e4m3"), ("e5m2", "e4m3", "e4m3")]
 
 
 @pytest.mark.parametrize("variant,tile_n,split", [
@@ -316,8 +317,37 @@ def test_pair_stream_k_is_deterministic():
     _assert_ok(compare(outs[0], inp), "stream-K det")
 
 
-def test_pair_stream_k_other_types():
+@pytest.mark.parametrize("at,ot", [("e5m2", "fp16"), ("e4m3", "fp32"), ("e4m3", "e4m3")])
+def test_pair_stream_k_other_types(at, ot):
     _need_gpu()
-    stats, _, _ = run_and_compare(300, 2600, 4112, 1, seed=64, with_bias=True, variant=PAIR, tile_n=256,
-                                  split_k=-1, a_dtype="e5m2", out_dtype="fp16")
-    _assert_ok(stats, "stream-K e5m2/fp16")
+    # 300 x 2600 has fewer tiles than pairs (partials read through L2);
+    # 2304 x 3072 has more (one partial, copied into the ring)
+    for M, N, K in ((300, 2600, 4112), (2304, 3072, 2048)):
+        stats, _, _ = run_and_compare(M, N, K, 1, seed=64, with_bias=True, variant=PAIR, tile_n=256,
+                                      split_k=-1, a_dtype=at, out_dtype=ot, sample=M > 1000)
+        _assert_ok(stats, f"stream-K {(M, N, K)} {at}/{ot}")
+
+
+@pytest.mark.parametrize("ot", ["fp32", "e4m3"])
+@pytest.mark.parametrize("N", [4099, 4104, 4112])
+def test_fp32_and_e4m3_outputs_unaligned_rows(ot, N):
+    """Rows that are not 16-byte aligned take element stores; aligned ones 16-byte stores."""
+    _need_gpu()
+    for variant, tile_n, split in ((TILE, 256, 1), (PAIR, 256, 1), (TILE, 128, 2), (SWAP, 32, 1)):
+        M = 37 if variant == SWAP else 300
+        stats, _, _ = run_and_compare(M, N, 160, 1, seed=65, with_bias=True, variant=variant,
+                                      tile_n=tile_n, split_k=split, out_dtype=ot)
+        _assert_ok(stats, f"{ot} N={N} v{variant}")
+
+
+def test_e4m3_output_saturates_like_the_oracle():
+    """Large scales push most outputs past 448: both sides saturate."""
+    _need_gpu()
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+    inp = make_inputs(256, 384, 512, 0, seed=66, out_dtype="e4m3")
+    inp.scale_a = inp.scale_a * 64
+    stats, out, _ = run_and_compare(256, 384, 512, 0, 66, False, inp=inp)
+    _assert_ok(stats, "e4m3 saturation")
+    codes = out.view(torch.uint8).cpu().numpy()
+    assert ((codes & 0x7F) == 0x7E).mean() > 0.2     # many saturated
+    assert not ((codes & 0x7F) == 0x7F).any()        # no NaN
