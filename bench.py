@@ -49,6 +49,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-variant", action="store_true", help="skip the second scaling mode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-skinny", action="store_true", help="skip the M <= 128 HBM-roofline record")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--sweep", action="store_true",
@@ -192,6 +193,88 @@ class ClockSampler:
                 "samples": len(inside), "window": window}
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (libnvidia-ml, read-only
+    queries via ctypes) every ~1 ms in a background thread, so that a timed
+    region of a few milliseconds holds several samples. ``ok`` is False when
+    NVML cannot be loaded or queried; the caller then falls back to
+    ClockSampler (nvidia-smi)."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, index: int, pci_bus_id: str = "", period_s: float = 0.001):
+        import ctypes
+        self.samples = []
+        self.period_s = period_s
+        self.thread = None
+        self.running = False
+        self.ok = False
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            handle = ctypes.c_void_p()
+            rc = -1
+            if pci_bus_id:
+                rc = lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(handle))
+            if rc != 0:
+                rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(handle))
+            if rc != 0:
+                return
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            if reasons is None:
+                reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.lib, self.handle, self.reasons_fn, self.ct = lib, handle, reasons, ctypes
+            self.ok = self._read_one() is not None
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _read_one(self):
+        ct = self.ct
+        sm, mx, mask = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if (self.lib.nvmlDeviceGetClockInfo(self.handle, self.NVML_CLOCK_SM, ct.byref(sm)) != 0 or
+                self.lib.nvmlDeviceGetMaxClockInfo(self.handle, self.NVML_CLOCK_SM, ct.byref(mx)) != 0 or
+                self.reasons_fn(self.handle, ct.byref(mask)) != 0):
+            return None
+        return (time.time(), float(sm.value), float(mx.value), int(mask.value))
+
+    def _loop(self):
+        while self.running:
+            s = self._read_one()
+            if s is not None:
+                self.samples.append(s)
+            time.sleep(self.period_s)
+
+    def start(self):
+        self.running = True
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.running = False
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    summary = ClockSampler.summary
+
+
+def clock_sampler(device):
+    """NVML sampling at ~1 ms where NVML answers, else nvidia-smi at 100 ms."""
+    import torch
+    props = torch.cuda.get_device_properties(device)
+    index = device.index if device.index is not None else 0
+    bus = ""
+    if all(hasattr(props, a) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+        bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    s = NvmlSampler(index, bus)
+    if s.ok:
+        s.source = "nvml, 1 ms"
+        return s
+    c = ClockSampler(index)
+    c.source = "nvidia-smi, 100 ms"
+    return c
+
+
 # ------------------------------------------------------------ GPU arm --------
 
 def make_device_sets(mode: int, device, n_sets: int):
@@ -253,6 +336,108 @@ def time_device(mode: int, steps: int, warmup: int, device, sampler=None):
         "wall": (t0, t1), "n_sets": n_sets, "inp": inp,
         "choice": fm.fp8mm_describe_choice(M, N, K, mode),
     }
+
+
+# M <= 128 shapes of the benchmark set, bound by streaming B from HBM:
+# (M, N, K, scale_mode, bias)
+SKINNY_SHAPES = [(16, 4096, 4096, 1, False), (128, 4096, 4096, 1, False), (1, 8192, 8192, 1, True)]
+
+
+def time_skinny(device, sampler, hbm_gbs: float, launches: int = 1000, region_s: float = 0.2):
+    """The skinny-M record: per shape, a CUDA graph of `launches` launches
+    (inputs rotated over more than 3x L2) replayed until the timed region is
+    about `region_s` long (at least 5 replays); the time per launch, the
+    algorithmic GB/s and the fraction of the measured HBM copy bandwidth, with
+    the clock samples of that region."""
+    import torch
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+
+    stream = torch.cuda.current_stream(device)
+    out = []
+    for (m, n, k, mode, bias) in SKINNY_SHAPES:
+        inp = make_inputs(m, n, k, mode, SEED, with_bias=bias)
+        nbytes = algorithmic_bytes(m, n, k, mode, bias)
+        n_sets = max(1, min(64, -(-3 * L2_BYTES // nbytes)))
+        sets = [(inp.a_q.to(device), inp.bt_q.to(device).t(), inp.scale_a.to(device),
+                 inp.scale_b.to(device), None if inp.bias is None else inp.bias.to(device),
+                 torch.empty((m, n), dtype=torch.bfloat16, device=device)) for _ in range(n_sets)]
+
+        def step(i):
+            A, B, sa, sb, b, o = sets[i % n_sets]
+            fm.fp8_scaled_mm(A, B, sa, sb, mode, bias=b, out=o, stream=cap)
+
+        cap = torch.cuda.Stream(device)
+        for i in range(3):
+            step(i)
+        torch.cuda.synchronize(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                for i in range(launches):
+                    step(i)
+        for _ in range(3):   # warm-up replays
+            graph.replay()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        reps = max(5, int(region_s * 1e3 / max(e0.elapsed_time(e1), 1e-3)))
+        t0 = time.time()
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        t1 = time.time()
+        ms = e0.elapsed_time(e1)
+        if fm.fp8mm_device_status(stream) != 0:
+            raise RuntimeError("in-kernel wait ran out: " + fm.fp8mm_last_error())
+        us = ms * 1e3 / (reps * launches)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        clocks = sampler.summary(t0, t1)
+        host_us, eager_us = eager_launches(sets, mode, m, n, k, stream, device)
+        out.append({"shape": [m, n, k], "scale_mode": "row-wise" if mode else "per-tensor", "bias": bias,
+                    "us": round(us, 3), "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4),
+                    "algorithmic_bytes": nbytes, "launches": reps * launches, "timed_ms": round(ms, 2),
+                    "eager_us": round(eager_us, 3), "host_us_per_call": round(host_us, 3),
+                    "kernel": fm.fp8mm_describe_choice(m, n, k, mode), "clocks": clocks})
+        del graph, sets
+        torch.cuda.empty_cache()
+    return {"peak_gbs": hbm_gbs, "peak_source": "measured HBM copy bandwidth",
+            "timing": "CUDA-graph replays of 1000 launches, inputs rotated over > 3x L2", "shapes": out}
+
+
+def eager_launches(sets, mode, m, n, k, stream, device, calls: int = 200):
+    """Calls of the C entry point without a CUDA graph, through ctypes with the
+    pointers prepared beforehand: the host time per call (the enqueue, no
+    synchronisation) and the device time per launch (events around the
+    calls)."""
+    import ctypes
+    import torch
+    import fp8_scaled_gemm_gb300 as fm
+
+    lib = fm.load()
+    vp = ctypes.c_void_p
+    args = [(vp(A.data_ptr()), vp(B.data_ptr()), vp(sa.data_ptr()), vp(sb.data_ptr()), mode,
+             None if b is None else vp(b.data_ptr()), vp(o.data_ptr()), m, n, k, vp(int(stream.cuda_stream)))
+            for (A, B, sa, sb, b, o) in sets]
+    for i in range(10):
+        lib.fp8_scaled_mm(*args[i % len(args)])
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    t0 = time.perf_counter()
+    for i in range(calls):
+        rc = lib.fp8_scaled_mm(*args[i % len(args)])
+    host = (time.perf_counter() - t0) / calls
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    if rc != 0:
+        raise RuntimeError(f"fp8_scaled_mm returned {rc}")
+    return host * 1e6, e0.elapsed_time(e1) * 1e3 / calls
 
 
 def time_e2e(mode: int, steps: int, inp):
@@ -631,13 +816,12 @@ def run_ours(args):
     flops = 2.0 * M * N * K
     head_mode = 0 if args.workload == "tensor" else 1
 
-    sampler = ClockSampler(torch.cuda.get_device_properties(device).index
-                           if hasattr(torch.cuda.get_device_properties(device), "index") else local)
+    sampler = clock_sampler(device)
     sampler.start()
     time.sleep(0.3)
     res = time_device(head_mode, args.steps, args.warmup, device)
-    sampler.stop()
     clocks = sampler.summary(*res["wall"])
+    clocks["sampler"] = sampler.source
 
     total_ms = max_over_ranks(res["total_ms"], device)
     ms_per_step = total_ms / args.steps
@@ -679,6 +863,9 @@ def run_ours(args):
             "kernel_ms_mean": round(r2["kernel_ms_mean"], 5), "achieved": round(a2, 2),
             "frac": round(a2 / fp8_peak, 4), "kernel": r2["choice"]}
         line["gpu_launches"] += args.steps
+    if not args.no_skinny and world == 1:
+        line["skinny"] = time_skinny(device, sampler, pk["hbm_gbs"])
+    sampler.stop()
     if not args.no_e2e:
         line["e2e"] = time_e2e(head_mode, min(args.steps, 100), res["inp"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

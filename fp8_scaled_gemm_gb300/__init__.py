@@ -46,7 +46,8 @@ _BIAS = {torch.bfloat16: torch.bfloat16, torch.float16: torch.float16, torch.flo
 class Options(ctypes.Structure):
     """fp8mm_options of include/fp8mm.h."""
     _fields_ = [("a_type", ctypes.c_int), ("b_type", ctypes.c_int), ("out_type", ctypes.c_int),
-                ("variant", ctypes.c_int), ("tile_n", ctypes.c_int), ("split_k", ctypes.c_int)]
+                ("variant", ctypes.c_int), ("tile_n", ctypes.c_int), ("split_k", ctypes.c_int),
+                ("ldo", ctypes.c_int64)]
 
 
 STATUS = {
@@ -185,9 +186,12 @@ def _validate(A, B, scale_a, scale_b, scale_mode, bias, out, device_side: bool, 
         if s.dtype != torch.float32 or s.numel() != n or not s.is_contiguous():
             raise ValueError(f"{name} must be a contiguous float32 tensor of {n} values")
     outs = tuple(_OUT) if typed else (torch.bfloat16,)
-    if out.dtype not in outs or tuple(out.shape) != (M, N) or not out.is_contiguous():
-        raise ValueError("out must be a contiguous [M, N] tensor of " +
-                         ("bfloat16, float16, float32 or float8_e4m3fn" if typed else "bfloat16"))
+    # typed calls also take a row-strided out (row stride >= N, columns contiguous)
+    strided_ok = typed and out.dim() == 2 and (out.stride(1) == 1 or N == 1) and out.stride(0) >= N
+    if out.dtype not in outs or tuple(out.shape) != (M, N) or not (out.is_contiguous() or strided_ok):
+        raise ValueError("out must be a [M, N] tensor of " +
+                         ("bfloat16, float16, float32 or float8_e4m3fn with contiguous rows" if typed
+                          else "bfloat16, contiguous"))
     if bias is not None and (bias.dtype != _BIAS[out.dtype] or bias.numel() != N or
                              not bias.is_contiguous()):
         raise ValueError("bias must be a contiguous tensor of N values of out's dtype "
@@ -229,11 +233,13 @@ def fp8_scaled_mm_ex(A, B, scale_a, scale_b, scale_mode: int, bias=None, out=Non
                      split_k: int = 0):
     """The operation with e4m3fn / e5m2 operands and a bf16 / fp16 / fp32 /
     e4m3fn output (types taken from the tensors; bias has out's dtype, bf16
-    for an e4m3fn output, which saturates at +-448)."""
+    for an e4m3fn output, which saturates at +-448). ``out`` may be a view
+    with a row stride of at least N (e.g. columns of a wider matrix)."""
     if out is None:
         out = torch.empty((A.shape[0], B.shape[1]), dtype=out_dtype, device=A.device)
     M, N, K = _validate(A, B, scale_a, scale_b, scale_mode, bias, out, True, typed=True)
-    opt = Options(_FP8[A.dtype], _FP8[B.dtype], _OUT[out.dtype], int(variant), int(tile_n), int(split_k))
+    ldo = 0 if out.is_contiguous() else int(out.stride(0))
+    opt = Options(_FP8[A.dtype], _FP8[B.dtype], _OUT[out.dtype], int(variant), int(tile_n), int(split_k), ldo)
     _check(load().fp8_scaled_mm_ex(_ptr(A), _ptr(B), _ptr(scale_a), _ptr(scale_b), scale_mode,
                                    _ptr(bias), _ptr(out), M, N, K, _stream_handle(stream),
                                    ctypes.byref(opt)))
@@ -413,7 +419,8 @@ def fp8_scaled_mm_bf16(A, B, scale_mode: int, bias=None, out=None, stream=None,
     scale_a = torch.empty(ns_a, dtype=torch.float32, device=dev)
     scale_b = torch.empty(ns_b, dtype=torch.float32, device=dev)
     _validate(a_q, bt_q.t(), scale_a, scale_b, scale_mode, bias, out, True, typed=True)
-    opt = Options(_FP8[a_dtype], _FP8[b_dtype], _OUT[out.dtype], int(variant), int(tile_n), int(split_k))
+    ldo = 0 if out.is_contiguous() else int(out.stride(0))
+    opt = Options(_FP8[a_dtype], _FP8[b_dtype], _OUT[out.dtype], int(variant), int(tile_n), int(split_k), ldo)
     _check(load().fp8_scaled_mm_bf16(_ptr(A), _ptr(Bt), int(scale_mode), _ptr(bias), _ptr(out), M, N, K,
                                      _ptr(a_q), _ptr(bt_q), _ptr(scale_a), _ptr(scale_b),
                                      _stream_handle(stream), ctypes.byref(opt)))

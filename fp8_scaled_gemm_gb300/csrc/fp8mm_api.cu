@@ -13,6 +13,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <set>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -241,6 +242,86 @@ int encode_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N, bool f16, 
         return FP8MM_ERR_CUDA;
     }
     return FP8MM_OK;
+}
+
+// Tensor maps of recent calls, per host thread: a map depends only on what
+// its key holds (device, address, sizes, box, element type, leading
+// dimension), so a hit is the map encoding would produce again. Encoding
+// three maps is most of the host time of a call; repeated calls on the same
+// buffers (a training or serving loop) skip it. Entries are replaced round
+// robin.
+struct MapKey {
+    int dev, kind;            // kind 0: fp8 operand; 1: bf16 output; 2: fp16 output
+    const void *base;
+    int64_t rows, cols, batch, ld;
+    int box_rows;
+    bool operator==(const MapKey &o) const
+    {
+        return dev == o.dev && kind == o.kind && base == o.base && rows == o.rows && cols == o.cols &&
+               batch == o.batch && ld == o.ld && box_rows == o.box_rows;
+    }
+};
+constexpr int kMapCacheSize = 32;
+struct MapCache {
+    MapKey key[kMapCacheSize];
+    CUtensorMap map[kMapCacheSize];
+    bool used[kMapCacheSize] = {};
+    int next = 0;
+    long long hits = 0, misses = 0;
+};
+thread_local MapCache t_maps;
+
+const CUtensorMap *map_lookup(const MapKey &k)
+{
+    for (int i = 0; i < kMapCacheSize; ++i)
+        if (t_maps.used[i] && t_maps.key[i] == k) {
+            ++t_maps.hits;
+            return &t_maps.map[i];
+        }
+    ++t_maps.misses;
+    return nullptr;
+}
+
+void map_insert(const MapKey &k, const CUtensorMap &m)
+{
+    const int i = t_maps.next;
+    t_maps.next = (i + 1) % kMapCacheSize;
+    t_maps.key[i] = k;
+    t_maps.map[i] = m;
+    t_maps.used[i] = true;
+}
+
+int current_device()
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return dev;
+}
+
+int cached_operand_map(CUtensorMap *map, const void *base, int64_t rows, int64_t K, int box_rows, int64_t batch)
+{
+    const MapKey k{current_device(), 0, base, rows, K, batch, K, box_rows};
+    if (const CUtensorMap *m = map_lookup(k)) {
+        *map = *m;
+        return FP8MM_OK;
+    }
+    const int rc = encode_operand_map(map, base, rows, K, box_rows, batch);
+    if (rc == FP8MM_OK)
+        map_insert(k, *map);
+    return rc;
+}
+
+int cached_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N, bool f16, int64_t batch, int64_t ldo)
+{
+    const MapKey k{current_device(), f16 ? 2 : 1, out, M, N, batch, ldo, 32};
+    if (const CUtensorMap *m = map_lookup(k)) {
+        *map = *m;
+        return FP8MM_OK;
+    }
+    const int rc = encode_out_map(map, out, M, N, f16, batch, ldo);
+    if (rc == FP8MM_OK)
+        map_insert(k, *map);
+    return rc;
 }
 
 struct Choice {
@@ -622,6 +703,55 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
     return c;
 }
 
+// The text form of a kernel choice (fp8mm_describe_choice's format).
+std::string describe(const Choice &c)
+{
+    char buf[160];
+    snprintf(buf, sizeof buf, "%s tile_n=%d split=%d tiles=%dx%d units=%d grid=%d%s",
+             c.variant == FP8MM_VARIANT_TILE       ? "tile"
+             : c.variant == FP8MM_VARIANT_PAIR     ? "pair"
+             : c.variant == FP8MM_VARIANT_SWAPK    ? "swapk"
+             : c.variant == FP8MM_VARIANT_SWAPPAIR ? "swappair"
+                                                   : "swap",
+             c.tile_n, c.split, c.tiles_p, c.tiles_q, c.units, c.grid,
+             c.sk_tiles > 0 ? (" stream_k_tiles=" + std::to_string(c.sk_tiles)).c_str() : "");
+    std::string d = buf;
+    if (tile_group(c) != 8)
+        d += " group=" + std::to_string(tile_group(c));
+    return d;
+}
+
+// FP8MM_LOG=1 in the environment: one line on stderr for each new problem
+// (device, batch, shape, scaling, element types, requested kernel) with the
+// kernel chosen for it and where the choice came from.
+bool log_enabled()
+{
+    static const bool on = [] {
+        const char *v = getenv("FP8MM_LOG");
+        return v != nullptr && v[0] != '\0' && v[0] != '0';
+    }();
+    return on;
+}
+
+void log_choice(int dev, int64_t batch, int64_t M, int64_t N, int64_t K, int mode, int a_type, int b_type,
+                int out_type, int req_variant, int req_tile_n, int req_split, const Choice &c, bool tuned)
+{
+    static std::mutex mu;
+    static std::set<std::vector<int64_t>> seen;
+    const std::vector<int64_t> key{dev, batch, M, N, K, mode, a_type, b_type, out_type, req_variant, req_tile_n,
+                                   req_split};
+    std::lock_guard<std::mutex> lock(mu);
+    if (!seen.insert(key).second)
+        return;
+    static const char *types[] = {"e4m3", "e5m2"};
+    static const char *outs[] = {"bf16", "fp16", "fp32", "e4m3"};
+    fprintf(stderr, "fp8mm: device %d batch %lld %lldx%lldx%lld %s %s x %s -> %s: %s (%s)\n", dev,
+            static_cast<long long>(batch), static_cast<long long>(M), static_cast<long long>(N),
+            static_cast<long long>(K), mode == FP8MM_SCALE_ROWWISE ? "row-wise" : "per-tensor", types[a_type & 1],
+            types[b_type & 1], outs[out_type & 3], describe(c).c_str(),
+            req_variant != FP8MM_VARIANT_AUTO ? "requested" : tuned ? "tuned" : "model");
+}
+
 template <int BN, bool SWAP>
 int launch_kernel(const CUtensorMap &mp, const CUtensorMap &mq, const CUtensorMap &mo,
                   const fp8mm::KernelParams &kp, int grid, cudaStream_t stream)
@@ -725,7 +855,7 @@ int encode_and_dispatch(const Choice &c, const void *A, const void *B, void *out
     const bool out16 = kp.out_type == FP8MM_OUT_BF16 || kp.out_type == FP8MM_OUT_F16;
     if (!swap && out16 && c.split == 1 && (N % 8) == 0 && (kp.ldo % 8) == 0 &&
         (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
-        int rc = encode_out_map(&mo, out, M, N, kp.out_type == FP8MM_OUT_F16, batch, kp.ldo);
+        int rc = cached_out_map(&mo, out, M, N, kp.out_type == FP8MM_OUT_F16, batch, kp.ldo);
         if (rc != FP8MM_OK)
             return rc;
         kp.out_tma = 1;
@@ -733,10 +863,10 @@ int encode_and_dispatch(const Choice &c, const void *A, const void *B, void *out
     const bool pair = c.variant == FP8MM_VARIANT_PAIR || c.variant == FP8MM_VARIANT_SWAPPAIR;
     const int q_box = pair ? c.tile_n / 2 : c.tile_n;
     // B column-major [K, N] is Bt[N, K] row-major.
-    int rc = encode_operand_map(&mp, swap ? B : A, swap ? N : M, K, fp8mm::kTileP, batch);
+    int rc = cached_operand_map(&mp, swap ? B : A, swap ? N : M, K, fp8mm::kTileP, batch);
     if (rc != FP8MM_OK)
         return rc;
-    rc = encode_operand_map(&mq, swap ? A : B, swap ? M : N, K, q_box, batch);
+    rc = cached_operand_map(&mq, swap ? A : B, swap ? M : N, K, q_box, batch);
     if (rc != FP8MM_OK)
         return rc;
     return dispatch(c, mp, mq, mo, kp, stream);
@@ -791,6 +921,8 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
         return FP8MM_ERR_MODE;
     if (out_type == FP8MM_OUT_F32 && (reinterpret_cast<uintptr_t>(bias) & 3))
         return FP8MM_ERR_ALIGN;   // an fp32 bias
+    if (ldo < 0 || (ldo > 0 && ldo < N) || ldo >= (int64_t(1) << 36))
+        return FP8MM_ERR_SHAPE;   // the output's leading dimension: 0 (= N) or at least N
     if (batch < 0)
         return FP8MM_ERR_SHAPE;
     if (M == 0 || N == 0 || batch == 0)
@@ -803,6 +935,8 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
     if (rc != FP8MM_OK)
         return rc;
 
+    const int req_variant = variant, req_tile_n = tile_n, req_split = split;
+    bool tuned = false;
     if (variant == FP8MM_VARIANT_AUTO) {
         TuneVal tv;
         const TuneKey key{d->cc_major, d->cc_minor, d->sms, batch, M, N, K, scale_mode, a_type, b_type, out_type};
@@ -810,9 +944,13 @@ int run(const void *A, const void *B, const float *sa, const float *sb, int scal
             variant = tv.variant;
             tile_n = tv.tile_n;
             split = tv.split;
+            tuned = true;
         }
     }
     const Choice c = choose(M, N, K, d->sms, variant, tile_n, split, batch);
+    if (log_enabled())
+        log_choice(current_device(), batch, M, N, K, scale_mode, a_type, b_type, out_type, req_variant, req_tile_n,
+                   req_split, c, tuned);
     fp8mm::KernelParams kp{};
     kp.scale_a = sa;
     kp.scale_b = sb;
@@ -1183,7 +1321,7 @@ int fp8_scaled_mm_ex(const void *A, const void *B, const float *scale_a, const f
         return FP8MM_ERR_NULL;
     return run(A, B, scale_a, scale_b, scale_mode, bias, out, M, N, K, static_cast<cudaStream_t>(stream),
                options->variant, options->tile_n, options->split_k, options->a_type, options->b_type,
-               options->out_type);
+               options->out_type, 1, options->ldo);
 }
 
 int fp8_quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, void *q, float *scale,
@@ -1203,7 +1341,7 @@ int fp8_scaled_mm_bf16(const void *A, const void *B, int scale_mode, const void 
                        int64_t N, int64_t K, void *A_q, void *B_q, float *scale_a, float *scale_b, void *stream,
                        const fp8mm_options *options)
 {
-    fp8mm_options o = {FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16, FP8MM_VARIANT_AUTO, 0, 0};
+    fp8mm_options o = {FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16, FP8MM_VARIANT_AUTO, 0, 0, 0};
     if (options)
         o = *options;
     // the GEMM's own checks first (its operands are the quantised copies)
@@ -1224,14 +1362,14 @@ int fp8_scaled_mm_bf16(const void *A, const void *B, int scale_mode, const void 
         (rc = quantize(B, N, K, scale_mode, o.b_type, B_q, scale_b, s, *d)) != FP8MM_OK)
         return rc;
     return run(A_q, B_q, scale_a, scale_b, scale_mode, bias, out, M, N, K, s, o.variant, o.tile_n, o.split_k,
-               o.a_type, o.b_type, o.out_type);
+               o.a_type, o.b_type, o.out_type, 1, o.ldo);
 }
 
 int fp8_scaled_mm_layout(const void *A, int a_major, const void *B, int b_major, const float *scale_a,
                          const float *scale_b, int scale_mode, const void *bias, void *out, int64_t M, int64_t N,
                          int64_t K, void *stream, const fp8mm_options *options)
 {
-    fp8mm_options o = {FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16, FP8MM_VARIANT_AUTO, 0, 0};
+    fp8mm_options o = {FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16, FP8MM_VARIANT_AUTO, 0, 0, 0};
     if (options)
         o = *options;
     if ((a_major != FP8MM_MAJOR_K && a_major != FP8MM_MAJOR_MN) || (b_major != FP8MM_MAJOR_K && b_major != FP8MM_MAJOR_MN))
@@ -1265,14 +1403,14 @@ int fp8_scaled_mm_layout(const void *A, int a_major, const void *B, int b_major,
         Bk = d->stage[7];
     }
     return run(Ak, Bk, scale_a, scale_b, scale_mode, bias, out, M, N, K, s, o.variant, o.tile_n, o.split_k, o.a_type,
-               o.b_type, o.out_type);
+               o.b_type, o.out_type, 1, o.ldo);
 }
 
 int fp8_scaled_bmm(const void *A, const void *B, const float *scale_a, const float *scale_b, int scale_mode,
                    const void *bias, void *out, int64_t batch, int64_t M, int64_t N, int64_t K, void *stream,
                    const fp8mm_options *options)
 {
-    fp8mm_options o = {FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16, FP8MM_VARIANT_AUTO, 0, 0};
+    fp8mm_options o = {FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16, FP8MM_VARIANT_AUTO, 0, 0, 0};
     if (options)
         o = *options;
     if (batch < 0)
@@ -1280,7 +1418,7 @@ int fp8_scaled_bmm(const void *A, const void *B, const float *scale_a, const flo
     // an empty batch is an empty problem: nothing is read or written, pointers may be NULL
     return run(A, B, scale_a, scale_b, scale_mode, bias, out, batch == 0 ? 0 : M, N, K,
                static_cast<cudaStream_t>(stream), o.variant, o.tile_n, o.split_k, o.a_type, o.b_type, o.out_type,
-               batch);
+               batch, o.ldo);
 }
 
 int fp8_scaled_mm_host(const void *A, const void *B, const float *scale_a, const float *scale_b,
@@ -1492,19 +1630,7 @@ const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64
         split = tv.split;
     }
     const Choice c = choose(M, N, K, d->sms, variant, tile_n, split, batch);
-    char buf[160];
-    snprintf(buf, sizeof buf, "%s tile_n=%d split=%d tiles=%dx%d units=%d grid=%d%s",
-             c.variant == FP8MM_VARIANT_TILE    ? "tile"
-             : c.variant == FP8MM_VARIANT_PAIR  ? "pair"
-             : c.variant == FP8MM_VARIANT_SWAPK ? "swapk"
-             : c.variant == FP8MM_VARIANT_SWAPPAIR ? "swappair"
-                                                : "swap",
-             c.tile_n, c.split, c.tiles_p, c.tiles_q,
-             c.units, c.grid, c.sk_tiles > 0 ? (" stream_k_tiles=" + std::to_string(c.sk_tiles)).c_str() : "");
-    if (tile_group(c) != 8)
-        t_describe = std::string(buf) + " group=" + std::to_string(tile_group(c));
-    else
-        t_describe = buf;
+    t_describe = describe(c);
     return t_describe.c_str();
 }
 
@@ -1516,7 +1642,7 @@ const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mod
 int fp8mm_autotune(int64_t batch, int64_t M, int64_t N, int64_t K, int scale_mode, const fp8mm_options *options,
                    void *stream)
 {
-    fp8mm_options o = {FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16, FP8MM_VARIANT_AUTO, 0, 0};
+    fp8mm_options o = {FP8MM_TYPE_E4M3, FP8MM_TYPE_E4M3, FP8MM_OUT_BF16, FP8MM_VARIANT_AUTO, 0, 0, 0};
     if (options)
         o = *options;
     if (scale_mode != FP8MM_SCALE_TENSOR && scale_mode != FP8MM_SCALE_ROWWISE)

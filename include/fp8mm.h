@@ -40,6 +40,16 @@
  * or frees them. The library owns a per-device split-K workspace (fp32
  * partial tiles plus per-tile arrival counters) and the staging buffers of
  * fp8_scaled_mm_host, both grown on demand and kept until the process exits.
+ * Each host thread keeps the TMA tensor maps of its last 32 operand and
+ * output buffers (keyed on device, address, sizes, box, element type and
+ * leading dimension: everything a map encodes), so repeated calls on the
+ * same buffers skip encoding them; a buffer freed and reallocated at the
+ * same address with the same shape gets the same, still correct, map.
+ *
+ * Logging: with FP8MM_LOG=1 in the environment, the first call of each
+ * problem (device, batch, shape, scaling, element types, requested kernel)
+ * prints one line on stderr naming the kernel chosen and whether the time
+ * model, a tuned entry (fp8mm_autotune) or the caller chose it.
  *
  * Threading: calls may come from any host thread. Calls that use the split-K
  * workspace and run concurrently on different streams of one device race on
@@ -144,6 +154,12 @@ typedef struct fp8mm_options {
     int variant;              /* fp8mm_variant (0 = heuristic)                  */
     int tile_n;               /* as in fp8_scaled_mm_config (0 = heuristic)     */
     int split_k;              /* as in fp8_scaled_mm_config (0 = heuristic)     */
+    int64_t ldo;              /* elements between consecutive rows of out: 0 = N
+                                 (contiguous), otherwise >= N, e.g. to write the
+                                 product into columns of a wider matrix; batched
+                                 items then sit M * ldo elements apart. Rows whose
+                                 byte pitch is not a multiple of 16 are written
+                                 with plain stores instead of TMA. */
 } fp8mm_options;
 
 /*

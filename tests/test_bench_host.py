@@ -77,3 +77,38 @@ def test_default_arguments_keep_the_contract():
     assert a.gpus == 1 and a.impl == "ours" and a.workload == "tensor"
     assert a.warmup >= 3 and a.steps >= 1
     assert not a.sweep and not a.quant and not a.plain_launches
+
+
+def test_algorithmic_bytes_of_the_other_output_types():
+    # fp32 output: 4 bytes per element and an fp32 bias; e4m3: 1 byte and a bf16 bias
+    M, N, K = 512, 1024, 2048
+    base = M * K + N * K + 4 * (M + N)
+    assert bench.algorithmic_bytes(M, N, K, 1, True, out="fp32") == base + 4 * M * N + 4 * N
+    assert bench.algorithmic_bytes(M, N, K, 1, True, out="e4m3") == base + M * N + 2 * N
+    assert bench.algorithmic_bytes(M, N, K, 1, True, out="fp16") == bench.algorithmic_bytes(M, N, K, 1, True)
+
+
+def test_nvml_sampler_without_nvml_reports_unavailable(monkeypatch):
+    import ctypes
+
+    def no_lib(*a, **k):
+        raise OSError("no libnvidia-ml here")
+    monkeypatch.setattr(ctypes, "CDLL", no_lib)
+    s = bench.NvmlSampler(0)
+    assert s.ok is False
+    # its summary is the same as the nvidia-smi sampler's
+    s.samples = [(1.000, 1800.0, 2070.0, 0x4), (1.001, 1810.0, 2070.0, 0x4), (1.002, 1790.0, 2070.0, 0x0)]
+    c = s.summary(0.9995, 1.0025)
+    assert c["window"] == "timed" and c["samples"] == 3 and c["sm_mhz"] == 1800.0
+    assert c["reasons"] == ["sw_power_cap"]
+
+
+def test_skinny_shapes_are_the_memory_bound_benchmark_shapes():
+    pk_hbm = 6747.0
+    for (m, n, k, mode, bias) in bench.SKINNY_SHAPES:
+        assert m <= 128
+        flops = 2 * m * n * k
+        nbytes = bench.algorithmic_bytes(m, n, k, mode, bias)
+        # below the ridge point of the measured peaks (fp8 ~ 3846 TFLOP/s / 6747 GB/s)
+        assert flops / nbytes < 3846e12 / (pk_hbm * 1e9)
+    assert bench.parse_args([]).no_skinny is False
