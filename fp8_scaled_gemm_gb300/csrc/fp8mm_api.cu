@@ -324,6 +324,48 @@ int cached_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N, bool f16, 
     return rc;
 }
 
+// Output [batch, M, N] of any output type written in boxes of 128 columns
+// (n) x box_m rows (m), no swizzle: the SWAP and cluster-K kernels stage a
+// tile's outputs as [box_m][128] elements and store them with one TMA copy.
+// The row pitch ldo * element size must be a multiple of 16 bytes.
+int encode_col_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N, int out_type, int64_t batch, int64_t ldo,
+                       int box_m)
+{
+    const cuuint64_t es = out_type == FP8MM_OUT_F32 ? 4 : out_type == FP8MM_OUT_E4M3 ? 1 : 2;
+    const CUtensorMapDataType dt = out_type == FP8MM_OUT_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : out_type == FP8MM_OUT_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : out_type == FP8MM_OUT_F16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldo) * es, static_cast<cuuint64_t>(ldo) * es * static_cast<cuuint64_t>(M)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(fp8mm::kTileP), static_cast<cuuint32_t>(box_m), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, dt, 3, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[128];
+        snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled(out columns) failed (%d) M=%lld N=%lld", static_cast<int>(r),
+                 static_cast<long long>(M), static_cast<long long>(N));
+        t_last_error = buf;
+        return FP8MM_ERR_CUDA;
+    }
+    return FP8MM_OK;
+}
+
+int cached_col_out_map(CUtensorMap *map, void *out, int64_t M, int64_t N, int out_type, int64_t batch, int64_t ldo,
+                       int box_m)
+{
+    const MapKey k{current_device(), 10 + out_type, out, M, N, batch, ldo, box_m};
+    if (const CUtensorMap *m = map_lookup(k)) {
+        *map = *m;
+        return FP8MM_OK;
+    }
+    const int rc = encode_col_out_map(map, out, M, N, out_type, batch, ldo, box_m);
+    if (rc == FP8MM_OK)
+        map_insert(k, *map);
+    return rc;
+}
+
 struct Choice {
     int variant;   // FP8MM_VARIANT_TILE, _SWAP, _PAIR, _SWAPK or _SWAPPAIR
     int tile_n;
@@ -859,6 +901,22 @@ int encode_and_dispatch(const Choice &c, const void *A, const void *B, void *out
         if (rc != FP8MM_OK)
             return rc;
         kp.out_tma = 1;
+    }
+    // The SWAP kernel without split-K writes the staged last tile of a CTA,
+    // [rows of M][128 columns of N], with one TMA store when the
+    // output's rows start and end on 16-byte boundaries: a TMA store clips
+    // the box at the tensor's last column in whole 16-byte units, so a row
+    // whose length is not a multiple of 16 bytes would get the bytes after
+    // it written (seen with an fp32 output, N = 523 and a leading dimension
+    // of 528).
+    const int64_t es = kp.out_type == FP8MM_OUT_F32 ? 4 : kp.out_type == FP8MM_OUT_E4M3 ? 1 : 2;
+    if (c.variant == FP8MM_VARIANT_SWAP && c.split == 1) {
+        if ((kp.ldo * es) % 16 == 0 && (N * es) % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+            int rc = cached_col_out_map(&mo, out, M, N, kp.out_type, batch, kp.ldo, c.tile_n);
+            if (rc != FP8MM_OK)
+                return rc;
+            kp.out_tma = 1;
+        }
     }
     const bool pair = c.variant == FP8MM_VARIANT_PAIR || c.variant == FP8MM_VARIANT_SWAPPAIR;
     const int q_box = pair ? c.tile_n / 2 : c.tile_n;

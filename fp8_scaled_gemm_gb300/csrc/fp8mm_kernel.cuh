@@ -138,6 +138,7 @@ struct TileCfg {
     static constexpr int kChunk = BN < 32 ? BN : 32;   // TMEM columns per tcgen05.ld
     static_assert(kQBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
     static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory");
+    static_assert(!SWAP || BN * kTileP * 4 <= kStages * kStageBytes, "the last tile's outputs must fit the ring");
 };
 
 // Bounded mbarrier waits.
@@ -307,6 +308,53 @@ __device__ __forceinline__ void store_out1(const KernelParams &p, size_t idx, fl
     }
 }
 
+// One output element's bit pattern into shared memory (element idx of an
+// array of the output type).
+__device__ __forceinline__ void stage_out1(uint8_t *base, int idx, float y, int out_type)
+{
+    if (out_type == kOutF32)
+        reinterpret_cast<float *>(base)[idx] = y;
+    else if (out_type == kOutE4M3)
+        base[idx] = static_cast<uint8_t>(pack_e4m3x4(y, 0.0f, 0.0f, 0.0f) & 0xFFu);
+    else
+        reinterpret_cast<unsigned short *>(base)[idx] =
+            out_type == kOutF16 ? __half_as_ushort(__float2half_rn(y)) : __bfloat16_as_ushort(__float2bfloat16_rn(y));
+}
+
+// Four consecutive output elements (m, n .. n + 3) whose bit patterns are at
+// src (shared memory, 4-, 8- or 16-byte aligned): one st.global of 4, 8 or 16
+// bytes when the four are inside the row and aligned (n % 4 == 0, a 16-byte
+// aligned base and ldo % 4 == 0), element stores otherwise.
+__device__ __forceinline__ void store_bits4(const KernelParams &p, int m, int n, const uint8_t *src)
+{
+    const int es = out_esize(p.out_type);
+    uint8_t *dst = out_row(p, m) + static_cast<size_t>(n) * es;
+    if (n + 3 < p.N && (n & 3) == 0 && (p.ldo & 3) == 0 && (reinterpret_cast<uintptr_t>(p.out) & 15) == 0) {
+        const size_t g = __cvta_generic_to_global(dst);
+        if (es == 4) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(src);
+            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(g), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+        } else if (es == 2) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(src);
+            asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(g), "r"(v.x), "r"(v.y) : "memory");
+        } else {
+            asm volatile("st.global.b32 [%0], %1;" ::"l"(g), "r"(*reinterpret_cast<const uint32_t *>(src)) : "memory");
+        }
+        return;
+    }
+    for (int i = 0; i < 4; ++i) {
+        if (n + i >= p.N)
+            break;
+        if (es == 4)
+            reinterpret_cast<uint32_t *>(dst)[i] = reinterpret_cast<const uint32_t *>(src)[i];
+        else if (es == 2)
+            reinterpret_cast<unsigned short *>(dst)[i] = reinterpret_cast<const unsigned short *>(src)[i];
+        else
+            dst[i] = src[i];
+    }
+}
+
 __device__ __forceinline__ float bias_value(const KernelParams &p, int n)
 {
     if (p.out_type == kOutF32)
@@ -367,11 +415,51 @@ __device__ __forceinline__ void store_swap_chunk(const KernelParams &p, const fl
     }
     if (n >= p.N)
         return;
+    if (p.out_type == kOutBF16 || p.out_type == kOutF16) {
+        unsigned short *o = static_cast<unsigned short *>(p.out) + n;
+        const bool f16 = p.out_type == kOutF16;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const int m = qbase + j;
+            if (m < p.M)
+                o[static_cast<size_t>(m) * p.ldo] =
+                    f16 ? __half_as_ushort(__float2half_rn(y[j])) : __bfloat16_as_ushort(__float2bfloat16_rn(y[j]));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const int m = qbase + j;
+            if (m < p.M)
+                store_out1(p, static_cast<size_t>(m) * p.ldo + n, y[j]);
+        }
+    }
+}
+
+// SWAP epilogue of a chunk of the CTA's last tile: the CH values of tile row
+// `row` (output column n) go to the staging array [BN][128] of output
+// elements in the drained operand ring, at [qloc + j][row].
+template <int CH>
+__device__ __forceinline__ void stage_swap_chunk(const KernelParams &p, const float (&v)[CH], uint8_t *stage, int row,
+                                                 int qloc, float s_tensor, float sal, float sb, float b)
+{
+    constexpr unsigned kAll = 0xffffffffu;
+    float y[CH];
 #pragma unroll
     for (int j = 0; j < CH; ++j) {
-        const int m = qbase + j;
-        if (m < p.M)
-            store_out1(p, static_cast<size_t>(m) * p.ldo + n, y[j]);
+        const float s = p.rowwise ? __shfl_sync(kAll, sal, j) * sb : s_tensor;
+        y[j] = fmaf(v[j], s, b);
+    }
+    // one type test per chunk, not per element (a per-element test in this
+    // unrolled loop measured 28 % slower at 128 x 14336 x 4096)
+    if (p.out_type == kOutBF16) {
+        unsigned short *st = reinterpret_cast<unsigned short *>(stage) + qloc * kTileP + row;
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+            st[j * kTileP] = __bfloat16_as_ushort(__float2bfloat16_rn(y[j]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < CH; ++j)
+            stage_out1(stage, (qloc + j) * kTileP + row, y[j], p.out_type);
     }
 }
 
@@ -460,6 +548,34 @@ struct PartialSrc {
         return glob + static_cast<size_t>(k) * gstep + static_cast<size_t>(col >> 2) * 128 + prow;
     }
 };
+
+// Four consecutive output elements (m, n .. n + 3), any output type: one
+// 4-, 8- or 16-byte st.global when the four are inside the row and aligned
+// (n % 4 == 0, a 16-byte aligned base and ldo % 4 == 0), element stores
+// otherwise. Rows m >= M are the caller's to skip.
+__device__ __forceinline__ void store_out4(const KernelParams &p, int m, int n, const float (&y)[4])
+{
+    const bool vec = n + 3 < p.N && (n & 3) == 0 && (p.ldo & 3) == 0 &&
+                     (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
+    if (vec) {
+        const size_t g = __cvta_generic_to_global(out_row(p, m) + static_cast<size_t>(n) * out_esize(p.out_type));
+        if (p.out_type == kOutF32) {
+            asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(g), "f"(y[0]), "f"(y[1]), "f"(y[2]),
+                         "f"(y[3]) : "memory");
+        } else if (p.out_type == kOutE4M3) {
+            asm volatile("st.global.b32 [%0], %1;" ::"l"(g), "r"(pack_e4m3x4(y[0], y[1], y[2], y[3])) : "memory");
+        } else {
+            asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(g), "r"(pack_out2(y[0], y[1], p.out_type)),
+                         "r"(pack_out2(y[2], y[3], p.out_type)) : "memory");
+        }
+        return;
+    }
+    const size_t base = static_cast<size_t>(m) * p.ldo + n;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (n + i < p.N)
+            store_out1(p, base + i, y[i]);
+}
 
 // Row-major epilogue for the fp32 and e4m3 outputs: one warp's 32
 // accumulator rows (TMEM lanes) x BN columns, 32 columns at a time; each
@@ -686,7 +802,7 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmap_p);
         ptx::prefetch_tmap(&tmap_q);
-        if (!SWAP && p.out_tma)
+        if (p.out_tma)
             ptx::prefetch_tmap(&tmap_out);
     }
     if (warp == 1) {
@@ -807,6 +923,10 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
         uint32_t chunks = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
+        // SWAP: the CTA's last tile is staged in the drained operand ring and
+        // written row by row after the loop (see below)
+        bool staged = false;
+        int staged_tp = 0, staged_tq = 0, staged_b = 0;
         for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
             const Unit w = decode_unit(u, p);
             const KernelParams pb = for_item(p, w.b);
@@ -836,6 +956,10 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
                                                     w.tq * BN + col0, lane, stage, stage_smem, chunks,
                                                     s_tensor, w.b);
                 } else {
+                    // The last tile of the CTA: every MMA has read its stages
+                    // (the accumulator is full) and no TMA load follows, so the
+                    // ring holds the tile's outputs, [BN][128] elements.
+                    const bool last = u + static_cast<int>(gridDim.x) >= p.num_units;
 #pragma unroll 1
                     for (int c = 0; c < BN / CH; ++c) {
                         float sal = sw_sal[0];   // chunk c's, selected without indexing registers
@@ -844,7 +968,16 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
                             sal = (c == i) ? sw_sal[i] : sal;
                         float v[CH];
                         tmem_load_chunk<CH>(trow + c * CH, v);
-                        store_swap_chunk<CH>(pb, v, pidx, w.tq * BN + c * CH, s_tensor, sal, sw_sb, sw_b);
+                        if (last)
+                            stage_swap_chunk<CH>(pb, v, smem, row, c * CH, s_tensor, sal, sw_sb, sw_b);
+                        else
+                            store_swap_chunk<CH>(pb, v, pidx, w.tq * BN + c * CH, s_tensor, sal, sw_sb, sw_b);
+                    }
+                    if (last) {
+                        staged = true;
+                        staged_tp = w.tp;
+                        staged_tq = w.tq;
+                        staged_b = w.b;
                     }
                 }
                 ptx::tc_fence_before();
@@ -927,6 +1060,41 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
+            }
+        }
+        if constexpr (SWAP) {
+            if (p.splits == 1) {
+                // The staged tile leaves with one TMA store of [BN rows of
+                // M][128 columns of N] (rows and columns outside out are
+                // clipped) when out's rows are 16-byte aligned; otherwise row
+                // by row: warp ew takes tile columns (output rows m) ew, ew +
+                // 4, ...; lane l output columns n .. n + 3. (Such a loop at
+                // the end of the kernel measured ~90 ns per iteration, a
+                // third of a 128-wide launch's epilogue; the TMA store takes
+                // one instruction.) Every epilogue warp meets this barrier
+                // once, also after a wait ran out (then nothing is written).
+                if (staged)
+                    ptx::fence_proxy_async_smem();   // the staged writes, read by the TMA store
+                __syncwarp();
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (staged && !*abort_flag) {
+                    if (p.out_tma) {
+                        if (threadIdx.x == 64) {
+                            ptx::tma_store_3d(&tmap_out, sbase, staged_tp * kTileP, staged_tq * BN, staged_b);
+                            ptx::bulk_commit_group();
+                            ptx::bulk_wait_group_read<0>();   // the CTA's shared memory stays until read
+                        }
+                    } else {
+                        const KernelParams pb = for_item(p, staged_b);
+                        const int es = out_esize(pb.out_type);
+                        for (int r = ew; r < BN; r += 4) {
+                            const int m = staged_tq * BN + r;
+                            if (m >= pb.M)
+                                break;
+                            store_bits4(pb, m, staged_tp * kTileP + 4 * lane, smem + (r * kTileP + 4 * lane) * es);
+                        }
+                    }
+                }
             }
         }
         // TMA stores must have finished reading the stage before the CTA exits

@@ -109,14 +109,16 @@ def test_no_stray_writes_single_row(variant, tile_n, split):
     _run(1, 777, 512, 1, True, variant, tile_n, split)
 
 
-@pytest.mark.parametrize("ld_extra", [40, 3])       # 16-byte pitch (TMA) and an odd pitch
-@pytest.mark.parametrize("variant,tile_n,split", [(TILE, 256, 1), (TILE, 128, 2), (PAIR, 256, 1),
-                                                  (SWAP, 32, 1), (SWAPK, 64, 2)])
-def test_no_stray_writes_between_rows(ld_extra, variant, tile_n, split):
-    """Leading dimension > N: the gap after every row stays untouched."""
+@pytest.mark.parametrize("N,ld", [(520, 560), (520, 523), (523, 528)])   # 16-byte pitch and rows;
+@pytest.mark.parametrize("variant,tile_n,split", [(TILE, 256, 1), (TILE, 128, 2), (PAIR, 256, 1),  # odd pitch;
+                                                  (SWAP, 32, 1), (SWAPK, 64, 2)])                   # 16-byte pitch, odd rows
+def test_no_stray_writes_between_rows(N, ld, variant, tile_n, split):
+    """Leading dimension > N: the gap after every row stays untouched (a TMA
+    store that ended a row of 523 elements in the middle of a 16-byte unit
+    wrote the rest of that unit)."""
     _need_gpu()
     M = 300 if variant in (TILE, PAIR) else 50
-    _run(M, 520, 272, 1, True, variant, tile_n, split, out_dtype="fp16", ld=520 + ld_extra)
+    _run(M, N, 272, 1, True, variant, tile_n, split, out_dtype="fp16", ld=ld)
 
 
 @pytest.mark.parametrize("variant,tile_n,split", [(TILE, 256, 1), (PAIR, 256, 1), (TILE, 128, 3)])
@@ -144,10 +146,11 @@ def test_no_stray_writes_stream_k():
     _run(2304, 3075, 2048, 0, False, PAIR, 256, -1)
 
 
-def test_no_stray_writes_batched():
+@pytest.mark.parametrize("N", [263, 264])   # plain stores; 16-byte rows (TMA stores of batch items)
+def test_no_stray_writes_batched(N):
     _need_gpu()
     import fp8_scaled_gemm_gb300 as fm
-    nb, M, N, K = 3, 200, 263, 272
+    nb, M, K = 3, 200, 272
     items = [make_inputs(M, N, K, 1, 90 + i, with_bias=True) for i in range(nb)]
     for it in items:
         it.bias = items[0].bias
@@ -155,7 +158,7 @@ def test_no_stray_writes_batched():
     Bt = torch.stack([it.bt_q for it in items]).cuda()
     sa = torch.cat([it.scale_a for it in items]).cuda()
     sb = torch.cat([it.scale_b for it in items]).cuda()
-    for variant, tile_n, split in ((TILE, 256, 1), (PAIR, 256, 1), (SWAP, 32, 1), (TILE, 128, 3)):
+    for variant, tile_n, split in ((TILE, 256, 1), (PAIR, 256, 1), (SWAP, 32, 1), (TILE, 128, 3), (SWAPK, 64, 2)):
         g = Guarded(M, N, torch.bfloat16, batch=nb)
         fm.fp8_scaled_bmm(A, Bt.transpose(1, 2), sa, sb, 1, bias=items[0].bias.cuda(), out=g.out,
                           variant=variant, tile_n=tile_n, split_k=split)
