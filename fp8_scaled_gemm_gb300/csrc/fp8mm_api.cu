@@ -562,65 +562,13 @@ int launch_swapk(const CUtensorMap &mp, const CUtensorMap &mq, const fp8mm::Kern
     return launch_pdl(kern, grid, fp8mm::kThreads, C::kSmemBytes, stream, "cluster-K kernel launch", mp, mq, kp);
 }
 
-// Clusters of CS CTAs of the cluster-K kernel that fit on the device at once.
-template <int BN, int CS>
-int max_active_clusters_for()
-{
-    using C = fp8mm::ClusterKCfg<BN, CS>;
-    auto kern = fp8mm::fp8mm_swap_ck_kernel<BN, CS>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
-        return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CS * 64, 1, 1);
-    cfg.blockDim = dim3(fp8mm::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = CS;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    return n;
-}
-
-int cs_index(int cs) { return cs == 2 ? 0 : cs == 4 ? 1 : 2; }
-int bn_index(int bn) { return bn == 16 ? 0 : bn == 32 ? 1 : bn == 64 ? 2 : 3; }
-
-// Cached per device: [tile_n][cluster size] -> resident clusters.
-int max_active_clusters(int tile_n, int cs)
-{
-    static int cache[kMaxDevices][4][3];
-    static bool have[kMaxDevices][4][3];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const int b = bn_index(tile_n), c = cs_index(cs);
-    if (!have[dev][b][c]) {
-        int n = 0;
-        switch (tile_n * 10 + cs) {
-        case 162: n = max_active_clusters_for<16, 2>(); break;
-        case 164: n = max_active_clusters_for<16, 4>(); break;
-        case 168: n = max_active_clusters_for<16, 8>(); break;
-        case 322: n = max_active_clusters_for<32, 2>(); break;
-        case 324: n = max_active_clusters_for<32, 4>(); break;
-        case 328: n = max_active_clusters_for<32, 8>(); break;
-        case 642: n = max_active_clusters_for<64, 2>(); break;
-        case 644: n = max_active_clusters_for<64, 4>(); break;
-        case 648: n = max_active_clusters_for<64, 8>(); break;
-        case 1282: n = max_active_clusters_for<128, 2>(); break;
-        case 1284: n = max_active_clusters_for<128, 4>(); break;
-        case 1288: n = max_active_clusters_for<128, 8>(); break;
-        }
-        cache[dev][b][c] = n;
-        have[dev][b][c] = true;
-    }
-    return cache[dev][b][c];
-}
+// Cluster-K CTAs resident per SM: tiles up to 64 wide keep the CTA under
+// half of the SM's shared memory (fp8mm::ClusterKCfg), so two fit.
+// (cudaOccupancyMaxActiveClusters reports one CTA per SM for these clusters,
+// but launches of more CTAs than SMs measured as single waves: 16 x 14336 x
+// 4096 with 224 CTAs in clusters of 2 ran 12.6 us against 14.0 us for 112
+// unsplit CTAs.)
+int ck_ctas_per_sm(int tile_n) { return tile_n <= 64 ? 2 : 1; }
 
 int swap_tile_for(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
 
@@ -632,24 +580,36 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
         split = 0;
         if (M <= 128) {
             // Unsplit persistent SWAP kernel, or K spread over a cluster of
-            // 2/4/8 CTAs reduced through distributed shared memory: cost in K
-            // blocks of one tile = waves x (K blocks per CTA + reduction).
+            // 2/4/8 CTAs reduced through distributed shared memory. These
+            // launches stream Bt from HBM: cost in K blocks of one CTA =
+            // waves x (all K blocks of the wave / the SMs it keeps busy, at
+            // most the ~140 that saturate HBM) + the reduction, which grows
+            // with the cluster. Two CTAs fit on an SM for tiles up to 64
+            // wide (ck_ctas_per_sm). Fitted to
+            // GB300 CUDA-graph timings of the M <= 128 benchmark shapes:
+            // 16 x 14336 x 4096 takes clusters of 2 (12.6 against 14.0 us
+            // unsplit), 1 x 8192 x 8192 clusters of 4 (13.5 against 13.9),
+            // 16 x 4096 x 4096 keeps 4 (6.1 against 6.9 with 8).
             variant = FP8MM_VARIANT_SWAP;
             tile_n = swap_tile_for(M);
             const int64_t tiles = cdiv(N, fp8mm::kTileP) * cdiv(M, tile_n) * batch;
             const int64_t kb = cdiv(K, fp8mm::kBlockK);
-            double best = static_cast<double>(cdiv(tiles, sms) * kb);
-            const double red = tile_n <= 32 ? 2.0 : tile_n <= 64 ? 3.0 : 4.0;
+            const double kSaturating = 140.0;   // SMs whose streams saturate HBM
+            auto stream_cost = [&](int64_t ctas_per_wave, int64_t waves, int64_t kb_per_cta) {
+                const double busy = std::min<double>({static_cast<double>(ctas_per_wave), static_cast<double>(sms),
+                                                      kSaturating});
+                return static_cast<double>(waves) * static_cast<double>(ctas_per_wave) * kb_per_cta / busy;
+            };
+            const int64_t swap_wave = std::min<int64_t>(tiles, sms);
+            double best = stream_cost(swap_wave, cdiv(tiles, sms), kb);
+            const double red0 = tile_n <= 32 ? 1.0 : tile_n <= 64 ? 2.0 : 3.0;
             for (int cs : {2, 4, 8}) {
                 if (kb / cs < 2)
                     break;
-                // clusters that fit at once, counted in SMs: a second resident
-                // CTA on an SM adds no streaming bandwidth
-                const int active = std::min(max_active_clusters(tile_n, cs), sms / cs);
-                if (active <= 0)
-                    continue;
-                const double cost = static_cast<double>(cdiv(tiles, active)) *
-                                    (static_cast<double>(cdiv(kb, cs)) + red);
+                const int active = sms * ck_ctas_per_sm(tile_n) / cs;   // clusters resident at once
+                const int64_t waves = cdiv(tiles, active);
+                const int64_t per_wave = std::min<int64_t>(tiles, active) * cs;
+                const double cost = stream_cost(per_wave, waves, cdiv(kb, cs)) + waves * (red0 + 0.6 * cs);
                 if (cost < best - 1e-9) {
                     best = cost;
                     variant = FP8MM_VARIANT_SWAPK;

@@ -632,11 +632,35 @@ __device__ __forceinline__ void epilogue_rows_wide(const KernelParams &p, uint32
 //
 // With add.count > 0 (stream-K owner), the fp32 partials that add describes
 // are added to the accumulator first, in piece order.
-template <int BN, int NBUF>
+// A warp's column scales and biases for one tile, loaded before the
+// accumulator wait (lane l holds columns n0 + 32 i + l).
+template <int BN>
+struct ColPre {
+    static constexpr int kN = BN >= 32 ? BN / 32 : 1;
+    float sb[kN];
+    float b[kN];
+};
+
+template <int BN>
+__device__ __forceinline__ ColPre<BN> load_col_pre(const KernelParams &p, int n0, int lane)
+{
+    ColPre<BN> c{};
+#pragma unroll
+    for (int i = 0; i < BN / 32; ++i) {
+        const int n = n0 + 32 * i + lane;
+        const bool in = n < p.N;
+        c.sb[i] = (p.rowwise && in) ? __ldg(p.scale_b + n) : 0.0f;
+        c.b[i] = (p.bias != nullptr && in) ? bias_value(p, n) : 0.0f;
+    }
+    return c;
+}
+
+template <int BN, int NBUF, bool PRE = false>
 __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, const CUtensorMap *tmap_out,
                                                      uint32_t trow, int m_row0, int n0, int lane,
                                                      uint8_t *stage, uint32_t stage_smem, uint32_t &chunks,
-                                                     float s_tensor, int item, const PartialSrc add = PartialSrc{})
+                                                     float s_tensor, int item, const PartialSrc add = PartialSrc{},
+                                                     ColPre<BN> pre = ColPre<BN>{})
 {
     if (p.out_type == kOutF32 || p.out_type == kOutE4M3) {
         epilogue_rows_wide<BN>(p, trow, m_row0, n0, lane, s_tensor, add);
@@ -651,7 +675,19 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
         // the block's column scales and biases first, so that their loads
         // are in flight during the TMEM loads (per-tensor without bias has none)
         float sbl2[2] = {0.0f, 0.0f}, bl2[2] = {0.0f, 0.0f};
-        if (p.rowwise || p.bias != nullptr) {
+        if constexpr (PRE) {
+            // loaded before the accumulator wait; the front of a register
+            // queue that moves on by two after every block
+            sbl2[0] = pre.sb[0];
+            sbl2[1] = pre.sb[ColPre<BN>::kN > 1 ? 1 : 0];
+            bl2[0] = pre.b[0];
+            bl2[1] = pre.b[ColPre<BN>::kN > 1 ? 1 : 0];
+#pragma unroll
+            for (int i = 0; i + 2 < ColPre<BN>::kN; ++i) {
+                pre.sb[i] = pre.sb[i + 2];
+                pre.b[i] = pre.b[i + 2];
+            }
+        } else if (p.rowwise || p.bias != nullptr) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int nl = nb + h * 32 + lane;
@@ -945,6 +981,11 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
                     sw_sal[c] = (pb.rowwise && ql < pb.M) ? __ldg(pb.scale_a + ql) : 0.0f;
                 }
             }
+            // TILE: this warp's column scales and biases for the tile, in flight
+            // during the wait (per-tensor without bias has none to load)
+            ColPre<kWarpCols> pre{};
+            if (!SWAP && p.splits == 1 && (p.rowwise || p.bias != nullptr))
+                pre = load_col_pre<kWarpCols>(pb, w.tq * BN + col0, lane);
             if (!W.wait(tfull_bar(acc), acc_phase, 5))
                 break;
             ptx::tc_fence_after();
@@ -952,9 +993,9 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             if (p.splits == 1) {
                 if constexpr (!SWAP) {
-                    epilogue_rows_staged<kWarpCols, C::kStageBufs>(pb, &tmap_out, trow + col0, w.tp * kTileP + q * 32,
-                                                    w.tq * BN + col0, lane, stage, stage_smem, chunks,
-                                                    s_tensor, w.b);
+                    epilogue_rows_staged<kWarpCols, C::kStageBufs, true>(pb, &tmap_out, trow + col0,
+                                                    w.tp * kTileP + q * 32, w.tq * BN + col0, lane, stage,
+                                                    stage_smem, chunks, s_tensor, w.b, PartialSrc{}, pre);
                 } else {
                     // The last tile of the CTA: every MMA has read its stages
                     // (the accumulator is full) and no TMA load follows, so the
