@@ -572,6 +572,13 @@ int ck_ctas_per_sm(int tile_n) { return tile_n <= 64 ? 2 : 1; }
 
 int swap_tile_for(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
 
+// The 256-wide 1-SM kernel runs 16 epilogue warps up to this K. Measured on
+// GB300 (CUDA-graph replays, row-wise + bias) against 8 warps: 8191 x 8193 x
+// 32 87.0 -> 71.3 us, 8192 x 8192 x 32 52.6 -> 44.8, 8192 x 8192 x 512
+// 54.8 -> 46.1; at K = 1024 16 warps lost (16384 x 8192 x 1024 127.7 ->
+// 141.1, 4096 x 4096 x 1024 21.3 -> 23.2).
+constexpr int64_t kTileWideMaxK = 512;
+
 Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n, int split, int64_t batch = 1)
 {
     Choice c{};
@@ -720,6 +727,8 @@ std::string describe(const Choice &c)
     std::string d = buf;
     if (tile_group(c) != 8)
         d += " group=" + std::to_string(tile_group(c));
+    if (c.variant == FP8MM_VARIANT_TILE && c.tile_n == 256 && c.kblocks * int64_t(fp8mm::kBlockK) <= kTileWideMaxK)
+        d += " epilogue_warps=16";
     return d;
 }
 
@@ -754,12 +763,12 @@ void log_choice(int dev, int64_t batch, int64_t M, int64_t N, int64_t K, int mod
             req_variant != FP8MM_VARIANT_AUTO ? "requested" : tuned ? "tuned" : "model");
 }
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, bool WIDE = false>
 int launch_kernel(const CUtensorMap &mp, const CUtensorMap &mq, const CUtensorMap &mo,
                   const fp8mm::KernelParams &kp, int grid, cudaStream_t stream)
 {
-    using C = fp8mm::TileCfg<BN, SWAP>;
-    auto kern = fp8mm::fp8mm_tc_kernel<BN, SWAP>;
+    using C = fp8mm::TileCfg<BN, SWAP, WIDE>;
+    auto kern = fp8mm::fp8mm_tc_kernel<BN, SWAP, WIDE>;
     static bool attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -769,7 +778,7 @@ int launch_kernel(const CUtensorMap &mp, const CUtensorMap &mq, const CUtensorMa
             return cuda_fail(e, "cudaFuncSetAttribute");
         attr_set[dev] = true;
     }
-    return launch_pdl(kern, grid, fp8mm::EpiShape<SWAP>::kThreads, C::kSmemBytes, stream, "kernel launch", mp, mq,
+    return launch_pdl(kern, grid, C::kThreads, C::kSmemBytes, stream, "kernel launch", mp, mq,
                       mo, kp);
 }
 
@@ -827,7 +836,12 @@ int dispatch(const Choice &c, const CUtensorMap &mp, const CUtensorMap &mq, cons
     } else if (c.variant == FP8MM_VARIANT_TILE) {
         switch (c.tile_n) {
         case 128: return launch_kernel<128, false>(mp, mq, mo, kp, c.grid, stream);
-        case 256: return launch_kernel<256, false>(mp, mq, mo, kp, c.grid, stream);
+        case 256:
+            // shallow K: 16 epilogue warps (the epilogue sets the time per
+            // tile); deeper K keeps 8 and two stage buffers per warp
+            if (kp.K <= kTileWideMaxK)
+                return launch_kernel<256, false, true>(mp, mq, mo, kp, c.grid, stream);
+            return launch_kernel<256, false>(mp, mq, mo, kp, c.grid, stream);
         }
     } else {
         switch (c.tile_n) {

@@ -114,8 +114,12 @@ struct KernelParams {
     unsigned long long timeout_cycles;
 };
 
-template <int BN, bool SWAP>
+// WIDE: the 256-wide row-major kernel with 16 epilogue warps (four per TMEM
+// lane quarter, one 64-column block each) for very shallow K, where the
+// epilogue, not the MMA, sets the time per tile.
+template <int BN, bool SWAP, bool WIDE = false>
 struct TileCfg {
+    static_assert(!WIDE || (!SWAP && BN == 256), "the 16-warp epilogue is for the 256-wide row-major kernel");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is 16..256 step 16");
     static_assert(SWAP || BN % 64 == 0, "row epilogue works in 64-column blocks");
     // SWAP rings up to tile_n = 64 stay under ~110 KB so a CTA of the next
@@ -126,11 +130,14 @@ struct TileCfg {
     // epilogue warp.
     static constexpr int kStages = SWAP ? (BN >= 128 ? 6 : BN >= 64 ? 4 : BN >= 32 ? 5 : 6)
                                         : (BN >= 256 ? 3 : 6);
-    static constexpr int kStageBufs = (!SWAP && BN >= 256) ? 2 : 1;   // 4 KB epilogue stages per warp
+    static constexpr int kEpiWarps = SWAP ? 4 : (WIDE ? 16 : 8);
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    // 4 KB epilogue stages per warp (16 warps: one each, to fit the ring)
+    static constexpr int kStageBufs = (!SWAP && BN >= 256 && !WIDE) ? 2 : 1;
     static constexpr int kPBytes = kTileP * kBlockK;
     static constexpr int kQBytes = BN * kBlockK;
     static constexpr int kStageBytes = kPBytes + kQBytes;
-    static constexpr int kStagingBytes = SWAP ? 0 : EpiShape<SWAP>::kWarps * 4096 * kStageBufs;
+    static constexpr int kStagingBytes = SWAP ? 0 : kEpiWarps * 4096 * kStageBufs;
     static constexpr int kTmemCols =
         (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
     static constexpr int kBarBytes = 256;
@@ -696,7 +703,11 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                 bl2[h] = (p.bias != nullptr && in) ? bias_value(p, nl) : 0.0f;
             }
         }
-        uint32_t w[32];
+        // Each 32-column half is converted and written to the stage on its
+        // own (16 packed words live, not 32), so that the 16-warp 1-SM kernel
+        // fits its registers.
+        const uint32_t buf = NBUF == 1 ? 0u : (chunks & 1u);
+        uint8_t *rowp = stage + buf * 4096u + lane * 128;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             float v[32];
@@ -724,6 +735,7 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
             const float sbl = sbl2[h];
             const float bl = bl2[h];
             const bool has_bias = p.bias != nullptr;
+            uint32_t w[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
                 const float s0 = p.rowwise ? sa * __shfl_sync(kAll, sbl, j) : s_tensor;
@@ -732,25 +744,24 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                 const float b1 = has_bias ? __shfl_sync(kAll, bl, j + 1) : 0.0f;
                 const float y0 = fmaf(v[j], s0, b0);
                 const float y1 = fmaf(v[j + 1], s1, b1);
-                w[h * 16 + j / 2] = pack_out2(y0, y1, p.out_type);
+                w[j / 2] = pack_out2(y0, y1, p.out_type);
             }
-        }
-        const uint32_t buf = NBUF == 1 ? 0u : (chunks & 1u);
-        if (p.out_tma && chunks >= NBUF) {
-            // the TMA store issued NBUF blocks ago must have read this stage
-            if (lane == 0)
-                ptx::bulk_wait_group_read<NBUF - 1>();
-            __syncwarp();
-        }
-        uint8_t *rowp = stage + buf * 4096u + lane * 128;
+            if (h == 0 && p.out_tma && chunks >= NBUF) {
+                // the TMA store issued NBUF blocks ago must have read this stage
+                if (lane == 0)
+                    ptx::bulk_wait_group_read<NBUF - 1>();
+                __syncwarp();
+            }
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-            uint4 val;
-            val.x = w[4 * cc + 0];
-            val.y = w[4 * cc + 1];
-            val.z = w[4 * cc + 2];
-            val.w = w[4 * cc + 3];
-            *reinterpret_cast<uint4 *>(rowp + ((cc ^ (lane & 7)) * 16)) = val;
+            for (int i = 0; i < 4; ++i) {
+                const int cc = h * 4 + i;
+                uint4 val;
+                val.x = w[4 * i + 0];
+                val.y = w[4 * i + 1];
+                val.z = w[4 * i + 2];
+                val.w = w[4 * i + 3];
+                *reinterpret_cast<uint4 *>(rowp + ((cc ^ (lane & 7)) * 16)) = val;
+            }
         }
         if (p.out_tma) {
             ptx::fence_proxy_async_smem();
@@ -791,16 +802,16 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float (&v)[CH])
         ptx::tmem_ld_16cols(taddr, v);
 }
 
-template <int BN, bool SWAP>
-__global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
+template <int BN, bool SWAP, bool WIDE = false>
+__global__ void __launch_bounds__(TileCfg<BN, SWAP, WIDE>::kThreads, 1)
     fp8mm_tc_kernel(const __grid_constant__ CUtensorMap tmap_p,
                     const __grid_constant__ CUtensorMap tmap_q,
                     const __grid_constant__ CUtensorMap tmap_out, const KernelParams p)
 {
-    using C = TileCfg<BN, SWAP>;
+    using C = TileCfg<BN, SWAP, WIDE>;
     constexpr int CH = C::kChunk;
     constexpr int S = C::kStages;
-    constexpr int kEpiWarps = EpiShape<SWAP>::kWarps;
+    constexpr int kEpiWarps = C::kEpiWarps;
     constexpr int kWarpCols = BN / (kEpiWarps / 4);     // columns of one epilogue warp
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1064,18 +1075,20 @@ __global__ void __launch_bounds__(EpiShape<SWAP>::kThreads, 1)
 #pragma unroll
                         for (int g = 0; g < CH / 4; ++g)
                             acc4[g] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        // slices loaded together: one with 16 epilogue warps (96 registers)
+                        constexpr int kBatch = kEpiWarps > 8 ? 1 : 3;
 #pragma unroll 1
-                        for (int s0 = 0; s0 < p.splits; s0 += 3) {
-                            float4 r[3][CH / 4];
+                        for (int s0 = 0; s0 < p.splits; s0 += kBatch) {
+                            float4 r[kBatch][CH / 4];
 #pragma unroll
-                            for (int i = 0; i < 3; ++i)
+                            for (int i = 0; i < kBatch; ++i)
 #pragma unroll
                                 for (int g = 0; g < CH / 4; ++g)
                                     r[i][g] = (s0 + i < p.splits)
                                                   ? __ldcg(chunk + (s0 + i) * split_stride + static_cast<size_t>(g) * kTileP)
                                                   : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-                            for (int i = 0; i < 3; ++i)
+                            for (int i = 0; i < kBatch; ++i)
 #pragma unroll
                                 for (int g = 0; g < CH / 4; ++g) {
                                     if (s0 + i < p.splits) {
