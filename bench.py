@@ -62,6 +62,9 @@ def parse_args(argv=None):
     ap.add_argument("--quant", action="store_true",
                     help="time the bf16 -> fp8 quantisation step instead (one JSON line per shape; "
                          "--shapes takes RxC[:mode[:e4m3|e5m2]])")
+    ap.add_argument("--layout", action="store_true",
+                    help="time fp8_scaled_mm_layout's four operand layouts against the TN call (one JSON line "
+                         "each; --shapes takes MxNxK[:mode], default 8192x8192x8192:0)")
     ap.add_argument("--shapes", default="",
                     help="with --sweep: 'gist' (the gist's M x K x N list, both scalings) or a comma list of "
                          "[B@]MxNxK[:mode[:bias[:a_dtype:b_dtype:out_dtype]]] "
@@ -780,6 +783,79 @@ def run_quant(args):
             "launches_per_call": 2 if mode == 0 else 1, "rotated_sets": n_sets}), flush=True)
 
 
+def run_layout(args):
+    """fp8_scaled_mm_layout with A and B each K-major (the TN layout) or
+    MN-major, against fp8_scaled_mm on the TN operands: CUDA-graph replays
+    with inputs rotated over more than L2; the MN-major operands are the same
+    matrices stored transposed, so every call computes the same product."""
+    import torch
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import make_inputs
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    fm.load()
+    pk = peaks()
+    fp8_peak = pk["bf16_tflops"] * NOMINAL_FP8_PER_BF16
+    specs = args.shapes.split(",") if args.shapes else ["8192x8192x8192:0"]
+    for spec in specs:
+        parts = spec.split(":")
+        M, N, K = (int(v) for v in parts[0].split("x"))
+        mode = int(parts[1]) if len(parts) > 1 else 0
+        inp = make_inputs(M, N, K, mode, SEED)
+        per_set = M * K + N * K + 2 * M * N
+        n_sets = max(2, -(-3 * L2_BYTES // per_set))
+        sets = []
+        for _ in range(n_sets):
+            a = inp.a_q.to(device)                      # [M, K] row-major
+            bt = inp.bt_q.to(device)                    # [N, K] row-major = B column-major
+            sets.append({"a_k": a, "a_mn": a.t().contiguous().t(), "b_k": bt.t(), "b_mn": bt.contiguous().t().contiguous(),
+                         "sa": inp.scale_a.to(device), "sb": inp.scale_b.to(device),
+                         "out": torch.empty((M, N), dtype=torch.bfloat16, device=device)})
+        stream = torch.cuda.current_stream(device)
+        base = None
+        for name in ("TN (fp8_scaled_mm)", "K/K", "MN/K", "K/MN", "MN/MN"):
+            def step(i, name=name):
+                s = sets[i % n_sets]
+                if name.startswith("TN"):
+                    fm.fp8_scaled_mm(s["a_k"], s["b_k"], s["sa"], s["sb"], mode, out=s["out"])
+                    return
+                a = s["a_mn"] if name.startswith("MN/") else s["a_k"]
+                b = s["b_mn"] if name.endswith("/MN") else s["b_k"]
+                fm.fp8_scaled_mm_layout(a, b, s["sa"], s["sb"], mode, out=s["out"])
+            for i in range(3):
+                step(i)
+            torch.cuda.synchronize(device)
+            steps = max(10, min(200, args.steps))
+            graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(device)
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(graph, stream=cap):
+                    for i in range(steps):
+                        step(i)
+            graph.replay()
+            torch.cuda.synchronize(device)
+            per = []
+            for _ in range(5):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize(device)
+                per.append(e0.elapsed_time(e1) / steps)
+            us = statistics.median(per) * 1e3
+            base = base or us
+            tflops = 2.0 * M * N * K / (us * 1e-6) / 1e12
+            print(json.dumps({"op": "fp8_scaled_mm_layout", "shape": [M, N, K], "layout_a/b": name,
+                              "scale_mode": "row-wise" if mode else "per-tensor", "us": round(us, 2),
+                              "tflops": round(tflops, 1), "frac_fp8_peak": round(tflops / fp8_peak, 3),
+                              "vs_tn": round(us / base, 3), "timing": f"median of 5 CUDA-graph replays of {steps}"}),
+                  flush=True)
+            del graph
+        del sets
+        torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------ ranks ----------
 
 def max_over_ranks(total_ms: float, device) -> float:
@@ -917,6 +993,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.quant:
         return run_quant(args)
+    if args.layout:
+        return run_layout(args)
     if args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
