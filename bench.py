@@ -780,7 +780,7 @@ def run_quant(args):
             "type": qt, "kernel_us": round(mean * 1e3, 2), "kernel_us_best": round(best * 1e3, 2),
             "timing": f"median of 5 CUDA-graph replays of {args.steps} calls",
             "gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3), "bound": "hbm",
-            "launches_per_call": 2 if mode == 0 else 1, "rotated_sets": n_sets}), flush=True)
+            "launches_per_call": 1, "rotated_sets": n_sets}), flush=True)
 
 
 def run_layout(args):

@@ -61,7 +61,7 @@ EXPORTS = (
     "fp8_scaled_mm_noalloc", "fp8_quantize", "fp8_scaled_mm_bf16", "fp8_scaled_bmm",
     "fp8_scaled_mm_layout",
     "fp8mm_reserve_workspace", "fp8mm_device_status", "fp8mm_status_string",
-    "fp8mm_last_cuda_error", "fp8mm_last_error", "fp8mm_describe_choice", "fp8mm_describe_bmm_choice", "fp8mm_debug_inject",
+    "fp8mm_last_cuda_error", "fp8mm_last_error", "fp8mm_describe_choice", "fp8mm_describe_bmm_choice", "fp8mm_debug_inject", "fp8mm_debug_quant",
     "fp8mm_autotune", "fp8mm_autotune_clear", "fp8mm_autotune_count", "fp8mm_autotune_save",
     "fp8mm_autotune_load",
 )
@@ -130,6 +130,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fp8mm_last_error.restype = ctypes.c_char_p
         lib.fp8mm_debug_inject.argtypes = [i64, i64]
         lib.fp8mm_debug_inject.restype = i32
+        lib.fp8mm_debug_quant.argtypes = [i32]
+        lib.fp8mm_debug_quant.restype = i32
         lib.fp8mm_describe_choice.argtypes = [i64, i64, i64, i32]
         lib.fp8mm_describe_choice.restype = ctypes.c_char_p
         lib.fp8mm_autotune.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(Options), vp]
@@ -450,6 +452,13 @@ def fp8mm_last_cuda_error() -> str:
 def fp8mm_last_error() -> str:
     """Alias of fp8mm_last_cuda_error."""
     return load().fp8mm_last_error().decode(errors="replace")
+
+
+def fp8mm_debug_quant(mode: int = 0) -> None:
+    """Test hook for per-tensor quantisation (see include/fp8mm.h): 1 forces
+    the two-launch form, 2 makes the one-launch kernel's grid-wide wait run
+    out; fp8mm_debug_quant() restores normal operation."""
+    _check(load().fp8mm_debug_quant(int(mode)))
 
 
 def fp8mm_debug_inject(stop_after_kblocks: int = -1, wait_limit_cycles: int = 0) -> None:

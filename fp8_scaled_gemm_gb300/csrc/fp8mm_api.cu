@@ -35,6 +35,7 @@ thread_local std::string t_last_error;
 // Test hooks (fp8mm_debug_inject): apply to every launch until reset.
 std::atomic<long long> g_inject_stop_after{-1};
 std::atomic<unsigned long long> g_wait_limit{0};
+std::atomic<int> g_quant_mode{0};   // fp8mm_debug_quant
 
 unsigned long long wait_limit() {
     const unsigned long long v = g_wait_limit.load();
@@ -143,7 +144,7 @@ int device_state(DeviceState **out)
         e = cudaMemset(d.status, 0, sizeof(int));
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaMemset(status)");
-        const size_t qbytes = (fp8q::kMaxPartials + 1) * sizeof(unsigned int);
+        const size_t qbytes = fp8q::kScratchWords * sizeof(unsigned int);
         e = cudaMalloc(&d.qscratch, qbytes);
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaMalloc(quantisation scratch)");
@@ -1092,6 +1093,48 @@ int launch_quant_rows(const fp8q::QuantParams &p, int sms, cudaStream_t stream)
                       "quantisation launch", p);
 }
 
+// L2 the one-launch per-tensor form asks to keep its streamed part in
+// between its passes (64 to 128 MB measured alike at 8192 x 8192).
+constexpr int64_t kFusedL2Bytes = int64_t(96) << 20;
+
+// Per-tensor quantisation in one cooperative launch (fp8q::quant_tensor_kernel).
+// Returns FP8MM_OK, FP8MM_ERR_CUDA, or 1 if the device cannot hold the grid
+// at once (cudaErrorCooperativeLaunchTooLarge: fewer SMs available to this
+// process), for the caller to take the two-launch form instead.
+int launch_quant_tensor(fp8q::QuantParams p, const DeviceState &d, cudaStream_t stream)
+{
+    // at least 64 KB of x per CTA; one CTA per SM at most
+    const int grid = static_cast<int>(
+        std::max<int64_t>(1, std::min<int64_t>({d.sms, fp8q::kMaxFusedCtas, cdiv(p.total, 4096)})));
+    const int64_t per_cta = cdiv(p.total, grid);
+    p.stash_groups = fp8q::kStashGroups;
+    p.withhold = g_quant_mode.load() == 2 ? 1 : 0;
+    const int64_t streamed = std::max<int64_t>(0, per_cta - p.stash_groups);
+    p.keep = std::min<int64_t>(streamed, kFusedL2Bytes / 16 / grid);
+    p.status = d.status;
+    p.timeout_cycles = wait_limit();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(fp8q::kFusedThreads, 1, 1);
+    cfg.dynamicSmemBytes = fp8q::kStashBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: the kernel has a grid-wide barrier
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fp8q::quant_tensor_kernel, p);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+        cudaGetLastError();   // not sticky: clear it
+        return 1;
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "per-tensor quantisation launch");
+    return FP8MM_OK;
+}
+
 // Enqueues the quantisation of x [R, C]; arguments already checked, R, C > 0.
 int quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, void *q, float *scale,
              cudaStream_t stream, const DeviceState &d)
@@ -1106,10 +1149,28 @@ int quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, vo
     p.total = R * (C / 8);
     p.q_type = q_type;
     if (scale_mode == FP8MM_SCALE_TENSOR) {
-        // one wave of each kernel: at most what the SMs hold at once
-        static int occ_amax[kMaxDevices] = {}, occ_conv[kMaxDevices] = {};
+        static int fused_ready[kMaxDevices] = {};   // 1: attribute set, -1: a CTA does not fit an SM
         int dev = 0;
         cudaGetDevice(&dev);
+        if (!fused_ready[dev]) {
+            int occ = 0;
+            cudaError_t e = cudaFuncSetAttribute(fp8q::quant_tensor_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, fp8q::kStashBytes);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fp8q::quant_tensor_kernel,
+                                                                  fp8q::kFusedThreads, fp8q::kStashBytes);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "per-tensor quantisation set-up");
+            fused_ready[dev] = occ >= 1 ? 1 : -1;
+        }
+        if (fused_ready[dev] == 1 && g_quant_mode.load() != 1) {
+            const int rc = launch_quant_tensor(p, d, stream);
+            if (rc <= 0)
+                return rc;
+        }
+        // Two launches: an amax kernel (its last CTA writes the scale), then a
+        // convert kernel; one wave of each, at most what the SMs hold at once.
+        static int occ_amax[kMaxDevices] = {}, occ_conv[kMaxDevices] = {};
         if (!occ_amax[dev]) {
             int a = 0, c = 0;
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, fp8q::quant_amax_kernel, fp8q::kThreads, 0);
@@ -1599,6 +1660,11 @@ int fp8mm_device_status(void *stream)
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaMemset(counters)");
     }
+    // a per-tensor quantisation that gave up leaves arrivals counted and an amax slot set
+    e = cudaMemset(d->qscratch + fp8q::kCounterWord, 0,
+                   (fp8q::kScratchWords - fp8q::kCounterWord) * sizeof(unsigned int));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemset(quantisation counter)");
     if (d->sk_flags) {   // a stream-K owner that gave up leaves its flags set
         e = cudaMemset(d->sk_flags, 0, static_cast<size_t>(d->sms / 2) * 16 * sizeof(unsigned int));
         if (e != cudaSuccess)
@@ -1611,6 +1677,14 @@ int fp8mm_device_status(void *stream)
     snprintf(buf, sizeof buf, "in-kernel wait ran out (site 0x%x)", h);
     t_last_error = buf;
     return FP8MM_ERR_TIMEOUT;
+}
+
+int fp8mm_debug_quant(int mode)
+{
+    if (mode < 0 || mode > 2)
+        return FP8MM_ERR_MODE;
+    g_quant_mode.store(mode);
+    return FP8MM_OK;
 }
 
 int fp8mm_debug_inject(int64_t stop_after_kblocks, int64_t wait_limit_cycles)

@@ -11,11 +11,15 @@
 // The work is HBM-bound: 2 bytes read and 1 byte written per element. Row-wise
 // scaling is one kernel: a team of threads holds a row in registers (16-byte
 // loads, 8 bf16 per load), reduces amax over the team, then converts from
-// registers. Per-tensor scaling needs the global amax before any division:
-// an amax kernel (the last CTA to finish turns the per-CTA maxima into the
-// scale) and a convert kernel that walks the tensor in reverse, so that the
-// part the amax pass read last is still in L2 (the amax pass marks the last
-// 64 MB it reads evict-last, everything else evict-first).
+// registers. Per-tensor scaling needs the global amax before any division.
+// It is one cooperative launch (quant_tensor_kernel): each CTA keeps the
+// head of its share in shared memory and the rest in L2, and a grid-wide
+// amax exchange sits between the two passes. Where the device cannot hold
+// that grid at once, two launches take its place: an amax kernel (the last
+// CTA to finish turns the per-CTA maxima into the scale) and a convert
+// kernel that walks the tensor in reverse, so that the part the amax pass
+// read last is still in L2 (the amax pass marks the last 64 MB it reads
+// evict-last, everything else evict-first).
 //
 // amax runs on the bf16 bit patterns: |x| is the pattern with the sign bit
 // cleared, and unsigned order on those patterns is the order of |x| with NaN
@@ -46,6 +50,11 @@ namespace fp8q {
 
 constexpr int kThreads = 256;
 constexpr int kMaxPartials = 1024;   // per-tensor amax: CTAs of the amax kernel
+constexpr int kMaxFusedCtas = 1024;  // per-tensor, one launch: CTAs of the kernel
+// Scratch words: the two-launch form's per-CTA maxima and arrival counter,
+// then the one-launch form's call number and its per-CTA 64-bit slots.
+constexpr int kCounterWord = kMaxPartials, kGenerationWord = kMaxPartials + 1, kSlotWords = kMaxPartials + 4,
+              kScratchWords = kSlotWords + 2 * kMaxFusedCtas;
 
 struct QuantParams {
     const uint4 *x;          // bf16 [R, C] as 16-byte groups of 8 elements
@@ -56,7 +65,12 @@ struct QuantParams {
     long long groups;        // groups of 8 per row (C / 8)
     long long total;         // R * groups
     int q_type;              // 0 e4m3fn, 1 e5m2
-    long long keep;          // per-tensor: groups at the end of x that the amax pass marks evict-last in L2
+    long long keep;          // per-tensor: groups the first pass marks evict-last in L2 (two-launch form:
+                             // at the end of x; one-launch form: at the end of each CTA's streamed part)
+    int stash_groups;        // one-launch per-tensor form: groups per CTA held in shared memory
+    int withhold;            // test hook: CTA 0 of the one-launch form never publishes its amax
+    int *status;             // one-launch per-tensor form: device status word
+    unsigned long long timeout_cycles;   // its bound on each wait
 };
 
 __device__ __forceinline__ float qmax_of(int q_type) { return q_type == 0 ? 448.0f : 57344.0f; }
@@ -125,15 +139,37 @@ __device__ __forceinline__ uint32_t cvt_pair(float lo, float hi, int q_type)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// The reciprocal path on both halves of a word of two bf16 at once, with
+// the packed two-lane fp32 operations (mul/fma .f32x2): the same three
+// roundings as div_fast, written on -x so that no operand needs negating:
+// q0 = RN(-x * -r), e = RN(q0 s + -x), q1 = RN(e * -r + q0). Each is the
+// same real value as in div_fast and x = +-0 gives +-0 (checked by hand:
+// -0 -> q0 = -0, e = +0, q1 = -0).
+__device__ __forceinline__ uint32_t div_fast_word(const Divider &d, uint32_t w, int q_type)
+{
+    const uint32_t nlo = w * 65536u + 0x80000000u;          // -x of the low bf16, as fp32 bits
+    const uint32_t nhi = (w & 0xFFFF0000u) ^ 0x80000000u;   // -x of the high bf16
+    const uint32_t nr = __float_as_uint(-d.r), sb = __float_as_uint(d.s);
+    uint32_t lo, hi;
+    asm("{\n\t.reg .b64 nx, nr2, s2, q0, e, q1;\n\t"
+        "mov.b64 nx, {%2, %3};\n\t"
+        "mov.b64 nr2, {%4, %4};\n\t"
+        "mov.b64 s2, {%5, %5};\n\t"
+        "mul.rn.f32x2 q0, nx, nr2;\n\t"
+        "fma.rn.f32x2 e, q0, s2, nx;\n\t"
+        "fma.rn.f32x2 q1, e, nr2, q0;\n\t"
+        "mov.b64 {%0, %1}, q1;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(nlo), "r"(nhi), "r"(nr), "r"(sb));
+    return cvt_pair(__uint_as_float(lo), __uint_as_float(hi), q_type);
+}
+
 template <bool FAST>
 __device__ __forceinline__ uint32_t convert_word_pair(const Divider &d, uint32_t w0, uint32_t w1, int q_type)
 {
     float v0, v1, v2, v3;
     if (FAST) {
-        v0 = div_fast(d, bf16_lo(w0));
-        v1 = div_fast(d, bf16_hi(w0));
-        v2 = div_fast(d, bf16_lo(w1));
-        v3 = div_fast(d, bf16_hi(w1));
+        return div_fast_word(d, w0, q_type) | (div_fast_word(d, w1, q_type) << 16);
     } else {
         v0 = div_slow(d, bf16_lo(w0));
         v1 = div_slow(d, bf16_hi(w0));
@@ -343,7 +379,7 @@ __global__ void __launch_bounds__(kThreads) quant_amax_kernel(const QuantParams 
             acc = max(acc, red[w]);
         p.partial[blockIdx.x] = acc;
         __threadfence();
-        const unsigned int ticket = atomicAdd(p.partial + kMaxPartials, 1u);
+        const unsigned int ticket = atomicAdd(p.partial + kCounterWord, 1u);
         last = ticket == gridDim.x - 1;
     }
     __syncthreads();
@@ -364,7 +400,7 @@ __global__ void __launch_bounds__(kThreads) quant_amax_kernel(const QuantParams 
         for (int w = 0; w < kThreads / 32; ++w)
             m = max(m, red[w]);
         p.scale[0] = __fdiv_rn(__uint_as_float(m << 16), qmax_of(p.q_type));
-        p.partial[kMaxPartials] = 0;   // ready for the next call on this stream
+        p.partial[kCounterWord] = 0;   // ready for the next call on this stream
     }
 }
 
@@ -398,6 +434,221 @@ __global__ void __launch_bounds__(kThreads) quant_convert_kernel(const QuantPara
         convert_tensor<true>(p, d);
     else
         convert_tensor<false>(p, d);
+}
+
+// ------------------------------------------------ per-tensor, one launch ---
+// One CTA per SM, each owning a contiguous run of groups, all CTAs resident
+// at once (cooperative launch). Pass 1 copies the head of the run into
+// shared memory (bulk copies) and streams the rest through registers,
+// marking it evict-last in L2, and reduces amax over both. A grid-wide
+// barrier publishes the CTA maxima, so every CTA derives the same scale.
+// Pass 2 converts the streamed part, read again from L2 with its last group
+// first, then the shared-memory part. While the streamed parts fit in L2,
+// HBM sees the tensor once and the codes once: 3 bytes per element, as
+// row-wise scaling, instead of the two-launch form's 5.
+constexpr int kFusedThreads = 1024;
+constexpr int kStashBytes = 192 * 1024;            // dynamic shared memory per CTA
+constexpr int kStashGroups = kStashBytes / 16;
+constexpr int kStashPiece = 32 * 1024;             // bytes per bulk copy
+constexpr int kFusedUnroll = 8;
+constexpr int kSiteStash = 0x20, kSiteGridBarrier = 0x21;   // wait sites in the status word
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, const QuantParams &p, int site)
+{
+    if (fp8mm::ptx::mbar_try_wait(bar, 0))
+        return true;
+    const unsigned long long t0 = static_cast<unsigned long long>(clock64());
+    while (!fp8mm::ptx::mbar_try_wait(bar, 0)) {
+        if (static_cast<unsigned long long>(clock64()) - t0 > p.timeout_cycles) {
+            atomicCAS(p.status, 0, 0x100 | site);
+            return false;
+        }
+    }
+    return true;
+}
+
+// CTA-wide max of one value per thread (every thread gets the result).
+__device__ __forceinline__ uint32_t cta_max(uint32_t v, uint32_t *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x / 32] = v;
+    __syncthreads();
+    v = 0;
+#pragma unroll
+    for (int w = 0; w < kFusedThreads / 32; ++w)
+        v = max(v, red[w]);
+    __syncthreads();
+    return v;
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t *p, uint64_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Grid-wide amax, by warp 0 of every CTA, without atomics. Every CTA writes
+// one 64-bit slot, (call tag << 32) | CTA amax, and reads all the grid's
+// slots until each carries this call's tag; the tag is the call number plus
+// one, so zeroed slots never match. CTA 0 advances the call number once it
+// has seen every slot: no CTA of this call reads it after that, each has
+// already written its tag. Returns false if the wait ran out (recorded in
+// the status word).
+__device__ __forceinline__ bool grid_amax(const QuantParams &p, uint32_t cta_amax, uint32_t *amax)
+{
+    const int lane = threadIdx.x & 31;
+    unsigned int *gen = p.partial + kGenerationWord;
+    uint64_t *slots = reinterpret_cast<uint64_t *>(p.partial + kSlotWords);
+    // read here rather than at the kernel's start: measured faster (fewer
+    // slot reads compete with the last CTAs' slot writes)
+    const unsigned int tag = fp8mm::ptx::ld_acquire_gpu_u32(gen) + 1u;
+    if (lane == 0 && !(p.withhold && blockIdx.x == 0))
+        st_relaxed_gpu_u64(slots + blockIdx.x, (static_cast<uint64_t>(tag) << 32) | cta_amax);
+    const int n = static_cast<int>(gridDim.x);
+    const unsigned long long t0 = static_cast<unsigned long long>(clock64());
+    uint32_t m;
+    while (true) {
+        bool seen = true;
+        m = 0;
+        for (int i = lane; i < n; i += 32) {
+            const uint64_t v = ld_relaxed_gpu_u64(slots + i);
+            seen = seen && static_cast<unsigned int>(v >> 32) == tag;
+            m = max(m, static_cast<uint32_t>(v));
+        }
+        if (__all_sync(0xFFFFFFFFu, seen))
+            break;
+        if (static_cast<unsigned long long>(clock64()) - t0 > p.timeout_cycles) {
+            if (lane == 0)
+                atomicCAS(p.status, 0, 0x100 | kSiteGridBarrier);
+            return false;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (blockIdx.x == 0 && lane == 0)
+        fp8mm::ptx::st_release_gpu_u32(gen, tag);
+    *amax = m;
+    return true;
+}
+
+template <bool FAST>
+__device__ __forceinline__ void convert_run(const QuantParams &p, const Divider &d, long long g0, int stashed,
+                                            long long g1, const uint4 *stash)
+{
+    constexpr int U = kUnroll;
+    const uint64_t pol = l2_evict_first();
+    const int T = kFusedThreads;
+    // streamed part, last group first (the most recently read lines first)
+    const long long rest = g1 - (g0 + stashed);
+    long long i = threadIdx.x;
+    for (; i + (U - 1) * T < rest; i += U * T) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            v[u] = load_group(p.x + (g1 - 1 - (i + u * T)), pol);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            store_group(p.q + (g1 - 1 - (i + u * T)), convert_group<FAST>(d, v[u], p.q_type), pol);
+    }
+    for (; i < rest; i += T)
+        store_group(p.q + (g1 - 1 - i), convert_group<FAST>(d, load_group(p.x + (g1 - 1 - i), pol), p.q_type), pol);
+    // shared-memory part
+    for (int j = threadIdx.x; j < stashed; j += T)
+        store_group(p.q + g0 + j, convert_group<FAST>(d, stash[j], p.q_type), pol);
+}
+
+__global__ void __launch_bounds__(kFusedThreads, 1) quant_tensor_kernel(const QuantParams p)
+{
+    extern __shared__ __align__(128) uint4 stash[];
+    __shared__ uint32_t red[kFusedThreads / 32];
+    __shared__ __align__(8) uint64_t stash_bar;
+    __shared__ int ok_all;
+    __shared__ uint32_t grid_max;
+    fp8mm::ptx::grid_launch_dependents();
+    fp8mm::ptx::grid_dependency_wait();
+
+    const long long g0 = p.total * blockIdx.x / gridDim.x;
+    const long long g1 = p.total * (blockIdx.x + 1) / gridDim.x;
+    const int stashed = static_cast<int>(min(g1 - g0, static_cast<long long>(p.stash_groups)));
+    const uint32_t bar = fp8mm::ptx::smem_addr(&stash_bar);
+    if (threadIdx.x == 0) {
+        ok_all = 1;
+        fp8mm::ptx::mbar_init(bar, 1);
+        fp8mm::ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && stashed > 0) {
+        const uint64_t first = l2_evict_first();     // these lines are not read from L2 again
+        const uint32_t bytes = static_cast<uint32_t>(stashed) * 16u;
+        fp8mm::ptx::mbar_arrive_expect_tx(bar, bytes);
+        const uint32_t dst = fp8mm::ptx::smem_addr(stash);
+        for (uint32_t o = 0; o < bytes; o += kStashPiece)
+            fp8mm::ptx::bulk_copy_g2s_hint(dst + o, reinterpret_cast<const char *>(p.x + g0) + o,
+                                           min(static_cast<uint32_t>(kStashPiece), bytes - o), bar, first);
+    }
+
+    // pass 1: amax over the streamed part, then over the shared-memory part
+    const uint64_t keep_pol = l2_evict_last(), pass_pol = l2_evict_first();
+    const long long s0 = g0 + stashed;
+    const long long keep_from = max(s0, g1 - p.keep);
+    uint32_t acc = 0;
+    long long g = s0 + threadIdx.x;
+    for (; g + (kFusedUnroll - 1) * kFusedThreads < g1; g += kFusedUnroll * kFusedThreads) {
+        uint4 v[kFusedUnroll];
+#pragma unroll
+        for (int u = 0; u < kFusedUnroll; ++u) {
+            const long long gu = g + u * kFusedThreads;
+            v[u] = load_group(p.x + gu, gu >= keep_from ? keep_pol : pass_pol);
+        }
+#pragma unroll
+        for (int u = 0; u < kFusedUnroll; ++u)
+            acc = amax_acc(acc, v[u]);
+    }
+    for (; g < g1; g += kFusedThreads)
+        acc = amax_acc(acc, load_group(p.x + g, g >= keep_from ? keep_pol : pass_pol));
+    if (stashed > 0) {
+        if (!wait_bounded(bar, p, kSiteStash))
+            ok_all = 0;
+        for (int j = threadIdx.x; j < stashed; j += kFusedThreads)
+            acc = amax_acc(acc, stash[j]);
+    }
+    acc = cta_max(fold_halves(acc), red);
+
+    if (threadIdx.x < 32) {
+        uint32_t m = 0;
+        const bool ok = grid_amax(p, acc, &m);
+        if (threadIdx.x == 0) {
+            grid_max = m;
+            if (!ok)
+                ok_all = 0;
+        }
+    }
+    __syncthreads();
+    const uint32_t m = grid_max;
+    if (!ok_all) {   // the status word says why
+        if (threadIdx.x == 0 && stashed > 0)
+            wait_bounded(bar, p, kSiteStash);   // no exit with copies into shared memory in flight
+        return;
+    }
+    const float s = __fdiv_rn(__uint_as_float(m << 16), qmax_of(p.q_type));
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        p.scale[0] = s;
+
+    // pass 2
+    const Divider d = make_divider(s);
+    if (d.mode == 1)
+        convert_run<true>(p, d, g0, stashed, g1, stash);
+    else
+        convert_run<false>(p, d, g0, stashed, g1, stash);
 }
 
 }  // namespace fp8q

@@ -364,6 +364,18 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
                  : "memory");
 }
 
+// As bulk_copy_g2s, with an L2 cache-eviction policy (createpolicy) for the
+// source lines.
+__device__ __forceinline__ void bulk_copy_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                                   uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // Orders this thread's earlier generic-proxy accesses to global memory before
 // its later async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global()

@@ -435,6 +435,20 @@ int fp8mm_device_status(void *stream);
 int fp8mm_debug_inject(int64_t stop_after_kblocks, int64_t wait_limit_cycles);
 
 /*
+ * Test hook for per-tensor quantisation (fp8_quantize, fp8_scaled_mm_bf16),
+ * from the next call on: mode 0 is normal operation (one cooperative launch
+ * with a grid-wide amax, falling back to two launches only when the device
+ * cannot hold the grid at once); mode 1 always takes the two-launch form (an
+ * amax kernel, then a convert kernel), so that it can be tested; mode 2
+ * makes CTA 0 of the one-launch kernel withhold its share of the grid-wide
+ * amax, so every CTA's bounded wait for it runs out: the kernel records
+ * FP8MM_ERR_TIMEOUT in the device status word and returns without writing
+ * codes or the scale. Returns FP8MM_ERR_MODE for other modes. Not for
+ * production use.
+ */
+int fp8mm_debug_quant(int mode);
+
+/*
  * Static description of a status code (never NULL; "unknown status" for a
  * code not in fp8mm_status). The codes report the operand conditions the
  * pages state for the TMA scaled_mm path, 16-byte aligned contiguous

@@ -147,6 +147,13 @@ def test_debug_inject_validates_arguments(lib):
     assert lib.fp8mm_debug_inject(-1, 0) == 0      # back to normal
 
 
+def test_debug_quant_validates_its_mode(lib):
+    assert lib.fp8mm_debug_quant(3) == -4
+    assert lib.fp8mm_debug_quant(-1) == -4
+    for mode in (1, 2, 0):                         # ends in normal operation
+        assert lib.fp8mm_debug_quant(mode) == 0
+
+
 def test_python_layer_validates_layouts():
     M, N, K = 4, 8, 32
     A = torch.zeros(M, K, dtype=torch.float8_e4m3fn)

@@ -251,3 +251,75 @@ def test_per_tensor_back_to_back_large_calls():
         q_ref, s_ref = oracle.quantize(_bits(x), 0, s % 2)
         assert np.array_equal(q.view(torch.uint8).cpu().numpy(), q_ref)
         assert _same_scales(sc.cpu().numpy(), s_ref)
+
+
+# ------------------------------------ per-tensor, one-launch partition ---
+# The one-launch per-tensor kernel gives each CTA a contiguous run of 16-byte
+# groups (8 bf16): run b is [total * b / grid, total * (b + 1) / grid) with
+# grid = min(#SMs, ceil(total / 4096)); a CTA holds the first 12288 groups of
+# its run in shared memory and streams the rest. The extreme value is placed
+# on both sides of those seams.
+
+def _seams(total: int, sms: int):
+    grid = max(1, min(sms, -(-total // 4096)))
+    out = []
+    for b in (0, grid // 2, grid - 1):
+        g0, g1 = total * b // grid, total * (b + 1) // grid
+        stash_end = g0 + min(g1 - g0, 12288)
+        out += [g0, stash_end - 1, min(stash_end, g1 - 1), g1 - 1]
+    return sorted(set(out))
+
+
+@pytest.mark.parametrize("R,C", [(8192, 8192), (3000, 1000)])
+def test_per_tensor_amax_on_run_seams(R, C):
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    base = bf16_matrix(R, C, seed=75)
+    dev = base.cuda()
+    for k, grp in enumerate(_seams(R * C // 8, sms)):
+        pos = grp * 8 + (k % 8)
+        x = dev.clone()
+        x.view(-1)[pos] = -600.0 - 4 * k          # bf16 steps are 4 apart here
+        q, s = fm.fp8_quantize(x, 0)
+        want = np.float32(600.0 + 4 * k) / np.float32(448.0)
+        assert float(s.cpu()[0]) == float(want), (grp, pos)
+        if k == 0:
+            q_ref, s_ref = oracle.quantize(_bits(x.cpu()), 0, 0)
+            assert np.array_equal(q.view(torch.uint8).cpu().numpy(), q_ref)
+
+
+def test_per_tensor_larger_than_l2():
+    _need_gpu()
+    # 256 MB of bf16: more than the shared-memory runs and the L2 hold together
+    quantize_and_compare(bf16_matrix(16384, 8192, seed=76), 0, 0)
+
+
+def test_per_tensor_grid_sizes_alternate():
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    # one-CTA, partial and full grids queued back to back: the grid barrier's
+    # counter and generation words must be left right for every grid size
+    shapes = [(64, 8), (4096, 4096), (16, 1024), (1000, 136), (8192, 1024), (1, 8)]
+    xs = [bf16_matrix(r, c, seed=90 + i, kind="wide") for i, (r, c) in enumerate(shapes)]
+    outs = [fm.fp8_quantize(x.cuda(), 0, DT[i % 2]) for i, x in enumerate(xs)]
+    torch.cuda.synchronize()
+    assert fm.fp8mm_device_status() == 0
+    for i, (x, (q, sc)) in enumerate(zip(xs, outs)):
+        q_ref, s_ref = oracle.quantize(_bits(x), 0, i % 2)
+        assert np.array_equal(q.view(torch.uint8).cpu().numpy(), q_ref), shapes[i]
+        assert _same_scales(sc.cpu().numpy(), s_ref), shapes[i]
+
+
+@pytest.mark.parametrize("R,C", [(8192, 4104), (3000, 1000), (1, 8)])
+def test_per_tensor_two_launch_form(R, C):
+    """The fallback for devices that cannot hold the one-launch grid at once
+    (an amax kernel, then a convert kernel), forced by the test hook."""
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    fm.fp8mm_debug_quant(1)
+    try:
+        quantize_and_compare(bf16_matrix(R, C, seed=77, kind="wide"), 0, 1)
+        quantize_and_compare(bf16_matrix(R, C, seed=78), 0, 0)
+    finally:
+        fm.fp8mm_debug_quant(0)

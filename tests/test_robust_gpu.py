@@ -85,3 +85,36 @@ def test_stream_k_flag_wait_runs_out_and_the_context_survives():
                                       sample=True, n_random=32)
         assert stats["violations"] == 0, stats
     assert fm.fp8mm_device_status() == 0
+
+
+def test_per_tensor_grid_wait_runs_out_and_the_context_survives():
+    """CTA 0 of the one-launch per-tensor quantisation withholds its share of
+    the grid-wide amax (test hook): every CTA's bounded wait runs out, the
+    status word says so, and the next calls are correct."""
+    _need_gpu()
+    import numpy as np
+    import oracle
+    import fp8_scaled_gemm_gb300 as fm
+    from fp8_scaled_gemm_gb300.inputs import bf16_matrix
+
+    x = bf16_matrix(4096, 4096, seed=34)
+    xd = x.cuda()
+    assert fm.fp8mm_device_status() == 0
+    fm.fp8mm_debug_inject(-1, SHORT)
+    fm.fp8mm_debug_quant(2)
+    try:
+        fm.fp8_quantize(xd, 0)
+        status = fm.fp8mm_device_status()
+    finally:
+        fm.fp8mm_debug_quant(0)
+        fm.fp8mm_debug_inject(-1, 0)
+    assert status == -7, f"expected FP8MM_ERR_TIMEOUT, got {status}"
+    assert "ran out" in fm.fp8mm_last_error()
+    assert fm.fp8mm_device_status() == 0
+    q_ref, s_ref = oracle.quantize(x.view(torch.int16).numpy().view(np.uint16), 0, 0)
+    for _ in range(2):
+        q, s = fm.fp8_quantize(xd, 0)
+        torch.cuda.synchronize()
+        assert np.array_equal(q.view(torch.uint8).cpu().numpy(), q_ref)
+        assert s.cpu().numpy().view(np.uint32)[0] == s_ref.view(np.uint32)[0]
+    assert fm.fp8mm_device_status() == 0
