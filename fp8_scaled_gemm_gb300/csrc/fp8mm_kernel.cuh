@@ -129,7 +129,7 @@ struct TileCfg {
     // the epilogue dominates: 3 stages leave room for two stage buffers per
     // epilogue warp.
     static constexpr int kStages = SWAP ? (BN >= 128 ? 6 : BN >= 64 ? 4 : BN >= 32 ? 5 : 6)
-                                        : (BN >= 256 ? 3 : 6);
+                                        : (BN >= 256 ? 3 : 5);
     static constexpr int kEpiWarps = SWAP ? 4 : (WIDE ? 16 : 8);
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     // 4 KB epilogue stages per warp (16 warps: one each, to fit the ring)
@@ -137,11 +137,14 @@ struct TileCfg {
     static constexpr int kPBytes = kTileP * kBlockK;
     static constexpr int kQBytes = BN * kBlockK;
     static constexpr int kStageBytes = kPBytes + kQBytes;
-    static constexpr int kStagingBytes = SWAP ? 0 : kEpiWarps * 4096 * kStageBufs;
+    static constexpr int kStageBufBytes = 4096;
+    static constexpr int kStagingBytes = SWAP ? 0 : kEpiWarps * kStageBufBytes * kStageBufs;
+    // per row-epilogue warp: one 64-column block's scales and biases (fp32)
+    static constexpr int kColBytes = SWAP ? 0 : kEpiWarps * 512;
     static constexpr int kTmemCols =
         (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kBarBytes;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kColBytes + kBarBytes;
     static constexpr int kChunk = BN < 32 ? BN : 32;   // TMEM columns per tcgen05.ld
     static_assert(kQBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
     static_assert(kSmemBytes <= 232448, "exceeds 227 KB of shared memory");
@@ -624,6 +627,53 @@ __device__ __forceinline__ void epilogue_rows_wide(const KernelParams &p, uint32
     }
 }
 
+// 32 accumulator values of one row to 16 words of two bf16 (F16: fp16)
+// each: y = fma(v, s, b), with s = RN(sa * sb[j]) (RW, row-wise scaling) or
+// the tensor scale sa, and b = bias[j] (HB) or +0, the same roundings as
+// the scalar form. The column scales and biases come from the warp's
+// shared-memory copy (col_sb, col_b: fp32, 16-byte aligned) as broadcast
+// reads, four columns per read, and two columns go through each packed
+// f32x2 operation.
+template <bool RW, bool HB, bool F16>
+__device__ __forceinline__ void convert_row32(const float (&v)[32], uint32_t (&w)[16], float sa,
+                                              const float *col_sb, const float *col_b)
+{
+    const uint64_t s2 = ptx::f32x2(sa, sa);
+    const uint64_t z2 = ptx::f32x2(0.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        uint64_t s01 = s2, s23 = s2, b01 = z2, b23 = z2;
+        if constexpr (RW) {
+            const float4 q = *reinterpret_cast<const float4 *>(col_sb + j);
+            s01 = ptx::mul_f32x2(s2, ptx::f32x2(q.x, q.y));
+            s23 = ptx::mul_f32x2(s2, ptx::f32x2(q.z, q.w));
+        }
+        if constexpr (HB) {
+            const float4 q = *reinterpret_cast<const float4 *>(col_b + j);
+            b01 = ptx::f32x2(q.x, q.y);
+            b23 = ptx::f32x2(q.z, q.w);
+        }
+        w[j / 2] = ptx::cvt_16x2<F16>(ptx::fma_f32x2(ptx::f32x2(v[j], v[j + 1]), s01, b01));
+        w[j / 2 + 1] = ptx::cvt_16x2<F16>(ptx::fma_f32x2(ptx::f32x2(v[j + 2], v[j + 3]), s23, b23));
+    }
+}
+
+__device__ __forceinline__ void convert_row32_any(const KernelParams &p, const float (&v)[32], uint32_t (&w)[16],
+                                                  float s, const float *col_sb, const float *col_b)
+{
+    const int k = (p.rowwise ? 4 : 0) | (p.bias != nullptr ? 2 : 0) | (p.out_type == kOutF16 ? 1 : 0);
+    switch (k) {
+    case 0: convert_row32<false, false, false>(v, w, s, col_sb, col_b); break;
+    case 1: convert_row32<false, false, true>(v, w, s, col_sb, col_b); break;
+    case 2: convert_row32<false, true, false>(v, w, s, col_sb, col_b); break;
+    case 3: convert_row32<false, true, true>(v, w, s, col_sb, col_b); break;
+    case 4: convert_row32<true, false, false>(v, w, s, col_sb, col_b); break;
+    case 5: convert_row32<true, false, true>(v, w, s, col_sb, col_b); break;
+    case 6: convert_row32<true, true, false>(v, w, s, col_sb, col_b); break;
+    default: convert_row32<true, true, true>(v, w, s, col_sb, col_b); break;
+    }
+}
+
 // Row-major epilogue of one warp's 32 accumulator rows (TMEM lanes) x BN
 // columns, 64 columns at a time, through a 4 KB shared-memory stage per
 // warp (bf16 and fp16 outputs; fp32 and e4m3 go to epilogue_rows_wide).
@@ -662,12 +712,12 @@ __device__ __forceinline__ ColPre<BN> load_col_pre(const KernelParams &p, int n0
     return c;
 }
 
-template <int BN, int NBUF, bool PRE = false>
+template <int BN, int NBUF, bool PRE = false, bool FAST_PLAIN = false>
 __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, const CUtensorMap *tmap_out,
                                                      uint32_t trow, int m_row0, int n0, int lane,
                                                      uint8_t *stage, uint32_t stage_smem, uint32_t &chunks,
                                                      float s_tensor, int item, const PartialSrc add = PartialSrc{},
-                                                     ColPre<BN> pre = ColPre<BN>{})
+                                                     ColPre<BN> pre = ColPre<BN>{}, float *colv = nullptr)
 {
     if (p.out_type == kOutF32 || p.out_type == kOutE4M3) {
         epilogue_rows_wide<BN>(p, trow, m_row0, n0, lane, s_tensor, add);
@@ -703,11 +753,24 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                 bl2[h] = (p.bias != nullptr && in) ? bias_value(p, nl) : 0.0f;
             }
         }
+        // With a shared-memory copy of the block's column values (colv: 64
+        // scales, then 64 biases), every thread reads them as broadcasts
+        // instead of taking them from the owning lane by shuffles.
+        if (colv != nullptr) {
+            __syncwarp();                       // the previous block's reads are done
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                colv[h * 32 + lane] = sbl2[h];
+                colv[64 + h * 32 + lane] = bl2[h];
+            }
+            __syncwarp();
+        }
         // Each 32-column half is converted and written to the stage on its
         // own (16 packed words live, not 32), so that the 16-warp 1-SM kernel
         // fits its registers.
         const uint32_t buf = NBUF == 1 ? 0u : (chunks & 1u);
-        uint8_t *rowp = stage + buf * 4096u + lane * 128;
+        constexpr uint32_t kBuf = 4096u;
+        uint8_t *rowp = stage + buf * kBuf + lane * 128;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             float v[32];
@@ -732,10 +795,13 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                     v[4 * g + 3] += x[g].w;
                 }
             }
+            uint32_t w[16];
+            if (colv != nullptr) {
+                convert_row32_any(p, v, w, p.rowwise ? sa : s_tensor, colv + h * 32, colv + 64 + h * 32);
+            } else {
             const float sbl = sbl2[h];
             const float bl = bl2[h];
             const bool has_bias = p.bias != nullptr;
-            uint32_t w[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
                 const float s0 = p.rowwise ? sa * __shfl_sync(kAll, sbl, j) : s_tensor;
@@ -745,6 +811,7 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                 const float y0 = fmaf(v[j], s0, b0);
                 const float y1 = fmaf(v[j + 1], s1, b1);
                 w[j / 2] = pack_out2(y0, y1, p.out_type);
+            }
             }
             if (h == 0 && p.out_tma && chunks >= NBUF) {
                 // the TMA store issued NBUF blocks ago must have read this stage
@@ -767,25 +834,60 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                ptx::tma_store_3d(tmap_out, stage_smem + buf * 4096u, nb, m_row0, item);
+                ptx::tma_store_3d(tmap_out, stage_smem + buf * kBuf, nb, m_row0, item);
                 ptx::bulk_commit_group();
             }
         } else {
+            // Rows that are not 16-byte aligned: element stores, lane l
+            // holding columns nb + 2l, nb + 2l + 1 of each row.
             __syncwarp();
             const int col = nb + 2 * lane;
+            if constexpr (!FAST_PLAIN) {
 #pragma unroll 4
-            for (int r = 0; r < 32; ++r) {
-                const int mm = m_row0 + r;
-                if (mm >= p.M)
-                    break;
-                const uint8_t *src =
-                    stage + buf * 4096u + r * 128 + ((((lane >> 2) ^ (r & 7)) & 7) * 16) + (lane & 3) * 4;
-                const uint32_t pr = *reinterpret_cast<const uint32_t *>(src);
-                unsigned short *dst = reinterpret_cast<unsigned short *>(out_row(p, mm)) + col;
-                if (col < p.N)
-                    dst[0] = static_cast<unsigned short>(pr & 0xFFFFu);
-                if (col + 1 < p.N)
-                    dst[1] = static_cast<unsigned short>(pr >> 16);
+                for (int r = 0; r < 32; ++r) {
+                    const int mm = m_row0 + r;
+                    if (mm >= p.M)
+                        break;
+                    const uint8_t *src =
+                        stage + buf * kBuf + r * 128 + ((((lane >> 2) ^ (r & 7)) & 7) * 16) + (lane & 3) * 4;
+                    const uint32_t pr = *reinterpret_cast<const uint32_t *>(src);
+                    unsigned short *dst = reinterpret_cast<unsigned short *>(out_row(p, mm)) + col;
+                    if (col < p.N)
+                        dst[0] = static_cast<unsigned short>(pr & 0xFFFFu);
+                    if (col + 1 < p.N)
+                        dst[1] = static_cast<unsigned short>(pr >> 16);
+                }
+            } else {
+                // Four rows at a time: the lane's word of row r sits at
+                // (s0 ^ 16 (r % 8)) + 128 r in the stage (the swizzle repeats
+                // every eight rows; the buffer is 1024-byte aligned, so the
+                // XOR only touches the chunk bits), and the row's output at
+                // base + r * ldo.
+                const bool in0 = col < p.N, in1 = col + 1 < p.N;
+                const int rows = min(32, p.M - m_row0);
+                unsigned short *const base = reinterpret_cast<unsigned short *>(out_row(p, m_row0)) + col;
+                const size_t ldo = static_cast<size_t>(p.ldo);
+                const uint32_t s0 = stage_smem + buf * kBuf + (((lane >> 2) & 7) * 16) + (lane & 3) * 4;
+#pragma unroll 1
+                for (int r0 = 0; r0 < rows; r0 += 4) {
+                    const uint32_t s4 = s0 ^ static_cast<uint32_t>((r0 & 4) * 16);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int r = r0 + k;
+                        if (r < rows) {
+                            uint32_t pr;
+                            asm volatile("ld.shared.u32 %0, [%1];"
+                                         : "=r"(pr)
+                                         : "r"((s4 ^ static_cast<uint32_t>(k * 16)) + r * 128)
+                                         : "memory");
+                            unsigned short *dst = base + r * ldo;
+                            if (in0)
+                                dst[0] = static_cast<unsigned short>(pr & 0xFFFFu);
+                            if (in1)
+                                dst[1] = static_cast<unsigned short>(pr >> 16);
+                        }
+                    }
+                }
             }
             __syncwarp();
         }
@@ -822,7 +924,8 @@ __global__ void __launch_bounds__(TileCfg<BN, SWAP, WIDE>::kThreads, 1)
 
     // stages[S] | epilogue stage (TILE) | barriers
     const uint32_t staging0 = sbase + S * C::kStageBytes;
-    const uint32_t bar0 = staging0 + C::kStagingBytes;
+    const uint32_t colv0 = staging0 + C::kStagingBytes;
+    const uint32_t bar0 = colv0 + C::kColBytes;
     // full[S] | empty[S] | tfull[2] | tempty[2] | done
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
@@ -965,8 +1068,8 @@ __global__ void __launch_bounds__(TileCfg<BN, SWAP, WIDE>::kThreads, 1)
         const int row = q * 32 + lane;      // row within the 128-row P tile
         const int ew = warp - 2;            // epilogue warp index: its stage buffer
         const int col0 = (ew / 4) * kWarpCols;  // this warp's first column of the tile
-        uint8_t *stage = smem + (staging0 - sbase) + ew * 4096 * C::kStageBufs;
-        const uint32_t stage_smem = staging0 + static_cast<uint32_t>(ew * 4096 * C::kStageBufs);
+        uint8_t *stage = smem + (staging0 - sbase) + ew * C::kStageBufBytes * C::kStageBufs;
+        const uint32_t stage_smem = staging0 + static_cast<uint32_t>(ew * C::kStageBufBytes * C::kStageBufs);
         uint32_t chunks = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -1004,9 +1107,12 @@ __global__ void __launch_bounds__(TileCfg<BN, SWAP, WIDE>::kThreads, 1)
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             if (p.splits == 1) {
                 if constexpr (!SWAP) {
-                    epilogue_rows_staged<kWarpCols, C::kStageBufs, true>(pb, &tmap_out, trow + col0,
-                                                    w.tp * kTileP + q * 32, w.tq * BN + col0, lane, stage,
-                                                    stage_smem, chunks, s_tensor, w.b, PartialSrc{}, pre);
+                    // the grouped plain-store loop: the 256-wide kernels, which
+                    // take the output-bound shallow-K launches
+                    epilogue_rows_staged<kWarpCols, C::kStageBufs, true, (BN >= 256)>(
+                        pb, &tmap_out, trow + col0, w.tp * kTileP + q * 32, w.tq * BN + col0, lane, stage,
+                        stage_smem, chunks, s_tensor, w.b, PartialSrc{}, pre,
+                        reinterpret_cast<float *>(smem + (colv0 - sbase)) + ew * 128);
                 } else {
                     // The last tile of the CTA: every MMA has read its stages
                     // (the accumulator is full) and no TMA load follows, so the

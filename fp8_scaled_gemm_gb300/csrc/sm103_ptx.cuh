@@ -427,5 +427,44 @@ __device__ __forceinline__ void grid_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ------------------------------------------------ packed two-lane fp32 ---
+// A pair of fp32 values in one 64-bit register (lo in the low half) and the
+// .f32x2 arithmetic on it: each lane is rounded as the scalar operation.
+
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// Both lanes to bf16 (F16: fp16), round to nearest even, lo in the low half.
+template <bool F16>
+__device__ __forceinline__ uint32_t cvt_16x2(uint64_t v)
+{
+    uint32_t r;
+    if constexpr (F16)
+        asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.f16x2.f32 %0, hi, lo;\n\t}"
+            : "=r"(r) : "l"(v));
+    else
+        asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+            : "=r"(r) : "l"(v));
+    return r;
+}
+
 }  // namespace ptx
 }  // namespace fp8mm
