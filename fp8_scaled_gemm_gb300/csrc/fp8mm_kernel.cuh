@@ -842,7 +842,7 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
             // holding columns nb + 2l, nb + 2l + 1 of each row.
             __syncwarp();
             const int col = nb + 2 * lane;
-            if constexpr (!FAST_PLAIN) {
+            if (!FAST_PLAIN || p.ldo > 0x7FFFFFFF) {
 #pragma unroll 4
                 for (int r = 0; r < 32; ++r) {
                     const int mm = m_row0 + r;
@@ -858,34 +858,36 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                         dst[1] = static_cast<unsigned short>(pr >> 16);
                 }
             } else {
-                // Four rows at a time: the lane's word of row r sits at
-                // (s0 ^ 16 (r % 8)) + 128 r in the stage (the swizzle repeats
-                // every eight rows; the buffer is 1024-byte aligned, so the
-                // XOR only touches the chunk bits), and the row's output at
-                // base + r * ldo.
+                // Four rows at a time, without branches: rows past the last
+                // valid one are clamped to it (it is written again with the
+                // same values). The lane's word of row r sits in chunk
+                // (lane / 4) ^ (r % 8) of the row (the stage's swizzle), and
+                // the row's output pitch fits 32 bits here.
                 const bool in0 = col < p.N, in1 = col + 1 < p.N;
-                const int rows = min(32, p.M - m_row0);
-                unsigned short *const base = reinterpret_cast<unsigned short *>(out_row(p, m_row0)) + col;
-                const size_t ldo = static_cast<size_t>(p.ldo);
-                const uint32_t s0 = stage_smem + buf * kBuf + (((lane >> 2) & 7) * 16) + (lane & 3) * 4;
+                const int last = min(32, p.M - m_row0) - 1;
+                uint8_t *const base = out_row(p, m_row0) + static_cast<size_t>(col) * 2;
+                const uint32_t pitch = static_cast<uint32_t>(p.ldo) * 2u;
+                const uint32_t sb = stage_smem + buf * kBuf + (lane & 3) * 4;
+                const uint32_t c = (lane >> 2) & 7;
 #pragma unroll 1
-                for (int r0 = 0; r0 < rows; r0 += 4) {
-                    const uint32_t s4 = s0 ^ static_cast<uint32_t>((r0 & 4) * 16);
+                for (int r0 = 0; r0 <= last; r0 += 4) {
+                    const uint32_t c4 = c ^ static_cast<uint32_t>(r0 & 4);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const int r = r0 + k;
-                        if (r < rows) {
-                            uint32_t pr;
-                            asm volatile("ld.shared.u32 %0, [%1];"
-                                         : "=r"(pr)
-                                         : "r"((s4 ^ static_cast<uint32_t>(k * 16)) + r * 128)
-                                         : "memory");
-                            unsigned short *dst = base + r * ldo;
-                            if (in0)
-                                dst[0] = static_cast<unsigned short>(pr & 0xFFFFu);
-                            if (in1)
-                                dst[1] = static_cast<unsigned short>(pr >> 16);
-                        }
+                        const int r = min(r0 + k, last);
+                        // (r0 + k) % 8 = (r0 & 4) + k; a clamped row keeps its own
+                        const uint32_t ck =
+                            (r == r0 + k) ? (c4 ^ static_cast<uint32_t>(k)) : (c ^ static_cast<uint32_t>(r & 7));
+                        uint32_t pr;
+                        asm volatile("ld.shared.u32 %0, [%1];"
+                                     : "=r"(pr)
+                                     : "r"(sb + static_cast<uint32_t>(r) * 128u + (ck << 4)));
+                        unsigned short *dst = reinterpret_cast<unsigned short *>(
+                            base + static_cast<size_t>(static_cast<uint32_t>(r)) * pitch);
+                        if (in0)
+                            dst[0] = static_cast<unsigned short>(pr & 0xFFFFu);
+                        if (in1)
+                            dst[1] = static_cast<unsigned short>(pr >> 16);
                     }
                 }
             }
