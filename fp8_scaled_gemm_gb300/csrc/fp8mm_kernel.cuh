@@ -881,7 +881,8 @@ __device__ __forceinline__ void epilogue_rows_staged(const KernelParams &p, cons
                         uint32_t pr;
                         asm volatile("ld.shared.u32 %0, [%1];"
                                      : "=r"(pr)
-                                     : "r"(sb + static_cast<uint32_t>(r) * 128u + (ck << 4)));
+                                     : "r"(sb + static_cast<uint32_t>(r) * 128u + (ck << 4))
+                                     : "memory");
                         unsigned short *dst = reinterpret_cast<unsigned short *>(
                             base + static_cast<size_t>(static_cast<uint32_t>(r)) * pitch);
                         if (in0)
