@@ -295,10 +295,13 @@ int fp8_scaled_bmm(const void *A, const void *B,
  * anywhere in the tensor (row) makes its scale NaN and all its codes NaN;
  * an infinity makes the scale inf, finite elements then encode as +-0.
  *
- * Asynchronous on `stream`. Row-wise is one kernel launch; per-tensor is two
- * (amax, then conversion) and uses a small per-device scratch (1024 maxima
- * and a counter) owned by the library, so per-tensor calls that overlap on
- * the GPU on different streams of one device race on it.
+ * Asynchronous on `stream`. Row-wise is one kernel launch. Per-tensor is one
+ * cooperative launch (one CTA per SM, a grid-wide amax exchange with a
+ * bounded wait that records FP8MM_ERR_TIMEOUT in the device status word if it
+ * runs out), or two launches (amax, then conversion) where the device cannot
+ * hold that grid at once. It uses a small per-device scratch owned by the
+ * library (per-CTA maxima, a call number and counters), so per-tensor calls
+ * that overlap on the GPU on different streams of one device race on it.
  */
 int fp8_quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type,
                  void *q, float *scale, void *stream);
