@@ -1096,6 +1096,13 @@ int launch_quant_rows(const fp8q::QuantParams &p, int sms, cudaStream_t stream)
 // L2 the one-launch per-tensor form asks to keep its streamed part in
 // between its passes (64 to 128 MB measured alike at 8192 x 8192).
 constexpr int64_t kFusedL2Bytes = int64_t(96) << 20;
+// Groups a CTA's run must have beyond its shared-memory head for the
+// tensor-memory part to be used (measured: 8192 x 8192 gains 2 us with it,
+// 16384 x 1024, 1509 groups beyond the head, loses 0.9 us).
+constexpr int64_t kFusedTmemMinGroups = 8192;
+// Per-tensor tensors below this size take the two launches (measured even at
+// 2 MB, and 1 us faster at 512 KB and below).
+constexpr int64_t kFusedMinBytes = int64_t(1) << 20;
 
 // Per-tensor quantisation in one cooperative launch (fp8q::quant_tensor_kernel).
 // Returns FP8MM_OK, FP8MM_ERR_CUDA, or 1 if the device cannot hold the grid
@@ -1109,7 +1116,12 @@ int launch_quant_tensor(fp8q::QuantParams p, const DeviceState &d, cudaStream_t 
     const int64_t per_cta = cdiv(p.total, grid);
     p.stash_groups = fp8q::kStashGroups;
     p.withhold = g_quant_mode.load() == 2 ? 1 : 0;
-    const int64_t streamed = std::max<int64_t>(0, per_cta - p.stash_groups);
+    // tensor memory for the next part when enough of the run is left after the
+    // shared-memory head (its allocation and four load rounds cost about
+    // what a few thousand groups of L2 re-reads save)
+    p.use_tmem = per_cta - p.stash_groups >= kFusedTmemMinGroups ? 1 : 0;
+    const int64_t on_chip = p.stash_groups + (p.use_tmem ? int64_t(fp8q::kTmemGroups) * fp8q::kFusedThreads : 0);
+    const int64_t streamed = std::max<int64_t>(0, per_cta - on_chip);
     p.keep = std::min<int64_t>(streamed, kFusedL2Bytes / 16 / grid);
     p.status = d.status;
     p.timeout_cycles = wait_limit();
@@ -1163,7 +1175,8 @@ int quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, vo
                 return cuda_fail(e, "per-tensor quantisation set-up");
             fused_ready[dev] = occ >= 1 ? 1 : -1;
         }
-        if (fused_ready[dev] == 1 && g_quant_mode.load() != 1) {
+        if (fused_ready[dev] == 1 && g_quant_mode.load() != 1 &&
+            p.total * 16 >= kFusedMinBytes) {
             const int rc = launch_quant_tensor(p, d, stream);
             if (rc <= 0)
                 return rc;

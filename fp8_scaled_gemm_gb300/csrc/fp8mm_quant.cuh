@@ -69,6 +69,7 @@ struct QuantParams {
                              // at the end of x; one-launch form: at the end of each CTA's streamed part)
     int stash_groups;        // one-launch per-tensor form: groups per CTA held in shared memory
     int withhold;            // test hook: CTA 0 of the one-launch form never publishes its amax
+    int use_tmem;            // one-launch form: hold the part after the shared-memory head in tensor memory
     int *status;             // one-launch per-tensor form: device status word
     unsigned long long timeout_cycles;   // its bound on each wait
 };
@@ -439,18 +440,25 @@ __global__ void __launch_bounds__(kThreads) quant_convert_kernel(const QuantPara
 // ------------------------------------------------ per-tensor, one launch ---
 // One CTA per SM, each owning a contiguous run of groups, all CTAs resident
 // at once (cooperative launch). Pass 1 copies the head of the run into
-// shared memory (bulk copies) and streams the rest through registers,
-// marking it evict-last in L2, and reduces amax over both. A grid-wide
-// barrier publishes the CTA maxima, so every CTA derives the same scale.
-// Pass 2 converts the streamed part, read again from L2 with its last group
-// first, then the shared-memory part. While the streamed parts fit in L2,
-// HBM sees the tensor once and the codes once: 3 bytes per element, as
-// row-wise scaling, instead of the two-launch form's 5.
+// shared memory (bulk copies, 192 KB), loads the next 256 KB through
+// registers into tensor memory, and streams the rest, marking it evict-last
+// in L2; amax is reduced over all three. A grid-wide exchange publishes the
+// CTA maxima, so every CTA derives the same scale. Pass 2 converts the L2
+// part, read again with its last group first, then the tensor-memory and
+// shared-memory parts. While the L2 parts stay in L2, HBM sees the tensor
+// once and the codes once: 3 bytes per element, as row-wise scaling,
+// instead of the two-launch form's 5; and re-reading from L2 (at most about
+// 10 TB/s here) covers only what does not fit on chip (about 65 MB of a
+// 128 MB tensor).
 constexpr int kFusedThreads = 1024;
 constexpr int kStashBytes = 192 * 1024;            // dynamic shared memory per CTA
 constexpr int kStashGroups = kStashBytes / 16;
 constexpr int kStashPiece = 32 * 1024;             // bytes per bulk copy
 constexpr int kFusedUnroll = 8;
+// Tensor memory holds the next part of each run: 512 columns x 128 lanes x
+// 4 bytes = 256 KB per SM, 16 groups per thread (64 columns of its lane).
+constexpr int kTmemCols = 512, kTmemGroups = 16;
+static_assert(kTmemGroups * 4 * (kFusedThreads / 128) == kTmemCols, "the CTA's groups fill tensor memory");
 constexpr int kSiteStash = 0x20, kSiteGridBarrier = 0x21;   // wait sites in the status word
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, const QuantParams &p, int site)
@@ -542,13 +550,13 @@ __device__ __forceinline__ bool grid_amax(const QuantParams &p, uint32_t cta_ama
 
 template <bool FAST>
 __device__ __forceinline__ void convert_run(const QuantParams &p, const Divider &d, long long g0, int stashed,
-                                            long long g1, const uint4 *stash)
+                                            long long tm_end, long long g1, const uint4 *stash, uint32_t taddr)
 {
     constexpr int U = kUnroll;
     const uint64_t pol = l2_evict_first();
     const int T = kFusedThreads;
-    // streamed part, last group first (the most recently read lines first)
-    const long long rest = g1 - (g0 + stashed);
+    // L2 part [tm_end, g1), last group first (the most recently read lines first)
+    const long long rest = g1 - tm_end;
     long long i = threadIdx.x;
     for (; i + (U - 1) * T < rest; i += U * T) {
         uint4 v[U];
@@ -561,6 +569,23 @@ __device__ __forceinline__ void convert_run(const QuantParams &p, const Divider 
     }
     for (; i < rest; i += T)
         store_group(p.q + (g1 - 1 - i), convert_group<FAST>(d, load_group(p.x + (g1 - 1 - i), pol), p.q_type), pol);
+    // tensor-memory part [g0 + stashed, tm_end): this thread's groups g0 + stashed + t + j T, j < 16,
+    // four to a 16-column load
+    const long long t0 = g0 + stashed + threadIdx.x;
+#pragma unroll 1
+    for (int jj = 0; jj < (p.use_tmem ? kTmemGroups / 4 : 0); ++jj) {
+        uint32_t r[16];
+        fp8mm::ptx::tmem_ld_16cols_u32(taddr + 16u * jj, r);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const long long g = t0 + static_cast<long long>(4 * jj + u) * T;
+            if (g < tm_end)
+                store_group(p.q + g,
+                            convert_group<FAST>(d, make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]),
+                                                p.q_type),
+                            pol);
+        }
+    }
     // shared-memory part
     for (int j = threadIdx.x; j < stashed; j += T)
         store_group(p.q + g0 + j, convert_group<FAST>(d, stash[j], p.q_type), pol);
@@ -573,9 +598,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) quant_tensor_kernel(const Qu
     __shared__ __align__(8) uint64_t stash_bar;
     __shared__ int ok_all;
     __shared__ uint32_t grid_max;
+    __shared__ uint32_t tmem_slot;
     fp8mm::ptx::grid_launch_dependents();
     fp8mm::ptx::grid_dependency_wait();
 
+    const int warp = static_cast<int>(threadIdx.x) >> 5;
     const long long g0 = p.total * blockIdx.x / gridDim.x;
     const long long g1 = p.total * (blockIdx.x + 1) / gridDim.x;
     const int stashed = static_cast<int>(min(g1 - g0, static_cast<long long>(p.stash_groups)));
@@ -585,7 +612,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1) quant_tensor_kernel(const Qu
         fp8mm::ptx::mbar_init(bar, 1);
         fp8mm::ptx::fence_mbar_init();
     }
+    if (p.use_tmem && warp == 0) {
+        fp8mm::ptx::tmem_alloc(fp8mm::ptx::smem_addr(&tmem_slot), kTmemCols);
+        fp8mm::ptx::tmem_relinquish();
+    }
+    fp8mm::ptx::tc_fence_before();
     __syncthreads();
+    fp8mm::ptx::tc_fence_after();
+    // this warp's lane quarter and its 64 columns: 16 groups per thread
+    const uint32_t taddr = tmem_slot + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
+                           static_cast<uint32_t>((warp >> 2) * (4 * kTmemGroups));
     if (threadIdx.x == 0 && stashed > 0) {
         const uint64_t first = l2_evict_first();     // these lines are not read from L2 again
         const uint32_t bytes = static_cast<uint32_t>(stashed) * 16u;
@@ -596,12 +632,33 @@ __global__ void __launch_bounds__(kFusedThreads, 1) quant_tensor_kernel(const Qu
                                            min(static_cast<uint32_t>(kStashPiece), bytes - o), bar, first);
     }
 
-    // pass 1: amax over the streamed part, then over the shared-memory part
+    // pass 1: amax over the tensor-memory part (loaded into tensor memory as
+    // it goes), the L2 part, then the shared-memory part
     const uint64_t keep_pol = l2_evict_last(), pass_pol = l2_evict_first();
-    const long long s0 = g0 + stashed;
-    const long long keep_from = max(s0, g1 - p.keep);
+    const long long t0 = g0 + stashed;
+    const long long tm_end = p.use_tmem ? min(g1, t0 + static_cast<long long>(kTmemGroups) * kFusedThreads) : t0;
     uint32_t acc = 0;
-    long long g = s0 + threadIdx.x;
+#pragma unroll 1
+    for (int jj = 0; jj < (p.use_tmem ? kTmemGroups / 4 : 0); ++jj) {
+        uint32_t r[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const long long gu = t0 + threadIdx.x + static_cast<long long>(4 * jj + u) * kFusedThreads;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (gu < tm_end)
+                v = load_group(p.x + gu, pass_pol);
+            acc = amax_acc(acc, v);
+            r[4 * u] = v.x;
+            r[4 * u + 1] = v.y;
+            r[4 * u + 2] = v.z;
+            r[4 * u + 3] = v.w;
+        }
+        fp8mm::ptx::tmem_st_16cols(taddr + 16u * jj, r);
+    }
+    if (p.use_tmem)
+        fp8mm::ptx::tmem_wait_st();
+    const long long keep_from = max(tm_end, g1 - p.keep);
+    long long g = tm_end + threadIdx.x;
     for (; g + (kFusedUnroll - 1) * kFusedThreads < g1; g += kFusedUnroll * kFusedThreads) {
         uint4 v[kFusedUnroll];
 #pragma unroll
@@ -634,21 +691,26 @@ __global__ void __launch_bounds__(kFusedThreads, 1) quant_tensor_kernel(const Qu
     }
     __syncthreads();
     const uint32_t m = grid_max;
-    if (!ok_all) {   // the status word says why
-        if (threadIdx.x == 0 && stashed > 0)
-            wait_bounded(bar, p, kSiteStash);   // no exit with copies into shared memory in flight
-        return;
+    if (ok_all) {
+        const float s = __fdiv_rn(__uint_as_float(m << 16), qmax_of(p.q_type));
+        if (blockIdx.x == 0 && threadIdx.x == 0)
+            p.scale[0] = s;
+        // pass 2
+        const Divider d = make_divider(s);
+        if (d.mode == 1)
+            convert_run<true>(p, d, g0, stashed, tm_end, g1, stash, taddr);
+        else
+            convert_run<false>(p, d, g0, stashed, tm_end, g1, stash, taddr);
+    } else if (threadIdx.x == 0 && stashed > 0) {
+        // the status word says why; no exit with copies into shared memory in flight
+        wait_bounded(bar, p, kSiteStash);
     }
-    const float s = __fdiv_rn(__uint_as_float(m << 16), qmax_of(p.q_type));
-    if (blockIdx.x == 0 && threadIdx.x == 0)
-        p.scale[0] = s;
-
-    // pass 2
-    const Divider d = make_divider(s);
-    if (d.mode == 1)
-        convert_run<true>(p, d, g0, stashed, g1, stash);
-    else
-        convert_run<false>(p, d, g0, stashed, g1, stash);
+    if (p.use_tmem) {
+        fp8mm::ptx::tc_fence_before();
+        __syncthreads();
+        if (warp == 0)
+            fp8mm::ptx::tmem_dealloc(tmem_slot, kTmemCols);
+    }
 }
 
 }  // namespace fp8q

@@ -256,8 +256,9 @@ def test_per_tensor_back_to_back_large_calls():
 # ------------------------------------ per-tensor, one-launch partition ---
 # The one-launch per-tensor kernel gives each CTA a contiguous run of 16-byte
 # groups (8 bf16): run b is [total * b / grid, total * (b + 1) / grid) with
-# grid = min(#SMs, ceil(total / 4096)); a CTA holds the first 12288 groups of
-# its run in shared memory and streams the rest. The extreme value is placed
+# grid = min(#SMs, ceil(total / 4096)). A CTA holds the first 12288 groups of
+# its run in shared memory; when at least 8192 groups are left, the next
+# 16384 go to tensor memory; it streams the rest. The extreme value is placed
 # on both sides of those seams.
 
 def _seams(total: int, sms: int):
@@ -267,6 +268,9 @@ def _seams(total: int, sms: int):
         g0, g1 = total * b // grid, total * (b + 1) // grid
         stash_end = g0 + min(g1 - g0, 12288)
         out += [g0, stash_end - 1, min(stash_end, g1 - 1), g1 - 1]
+        if g1 - stash_end >= 8192:
+            tm_end = min(g1, stash_end + 16384)
+            out += [tm_end - 1, min(tm_end, g1 - 1)]
     return sorted(set(out))
 
 
