@@ -629,6 +629,28 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
             // fixed per-launch costs. It stays available as an explicit choice.)
             if (variant == FP8MM_VARIANT_SWAP)
                 split = 1;
+            // M above 32 with few column tiles: 32-wide tiles over ceil(M / 32)
+            // row tiles put more CTAs on the SMs (two fit on an SM); the row
+            // tiles share each Bt block through L2. Clusters of 4 when that
+            // still fits one wave, else of 2 up to K = 4096. On a GB300 grid
+            // of M in {48, 64, 96, 128}, N in {2048, 4096}, K in {2048, 4096,
+            // 8192} this was the fastest measured configuration (or within
+            // 0.2 %) on every shape it covers, against up to 2.1x slower for
+            // the model above (128 x 2048 x 4096: 7.2 against 15.4 us with
+            // 128-wide tiles in clusters of 8); with N = 8192 it was not.
+            const int64_t nt = cdiv(N, fp8mm::kTileP);
+            if (M > 32 && batch == 1 && N >= 2048 && N <= 4096 && K >= 2048 && K <= 8192) {
+                const int64_t split_tiles = nt * cdiv(M, 32);
+                if (split_tiles * 4 <= int64_t(sms) * ck_ctas_per_sm(32)) {
+                    variant = FP8MM_VARIANT_SWAPK;
+                    tile_n = 32;
+                    split = 4;
+                } else if (K <= 4096 && split_tiles * 2 <= int64_t(sms) * ck_ctas_per_sm(32)) {
+                    variant = FP8MM_VARIANT_SWAPK;
+                    tile_n = 32;
+                    split = 2;
+                }
+            }
         } else if (K <= 1024 && cdiv(M, 128) * cdiv(N, 256) * batch >= sms) {
             // shallow K: the epilogue dominates; the 1-SM kernel with two
             // stage buffers per epilogue warp measured 7-15 % faster
@@ -1283,7 +1305,7 @@ std::vector<Candidate> tune_candidates(int64_t M, int64_t K)
     const int kb = static_cast<int>(cdiv(K, fp8mm::kBlockK));
     if (M <= 128) {
         for (int t : {16, 32, 64, 128}) {
-            if (t < swap_tile_for(M))
+            if (t < std::min(32, swap_tile_for(M)))   // 32-wide tiles over several row tiles are candidates too
                 continue;
             for (int s : {1, 2, 3, 4, 6, 8})
                 if (s == 1 || kb / s >= 2)

@@ -351,3 +351,21 @@ def test_e4m3_output_saturates_like_the_oracle():
     codes = out.view(torch.uint8).cpu().numpy()
     assert ((codes & 0x7F) == 0x7E).mean() > 0.2     # many saturated
     assert not ((codes & 0x7F) == 0x7F).any()        # no NaN
+
+
+# M above 32 with 16 to 32 column tiles: the automatic choice splits M into
+# 32-row tiles over clusters of 4 (or 2), ragged M included.
+@pytest.mark.parametrize("shape,choice", [
+    ((128, 2048, 4096), "swapk tile_n=32 split=4"),
+    ((128, 4096, 4096), "swapk tile_n=32 split=2"),
+    ((100, 2056, 2048), "swapk tile_n=32 split=4"),
+    ((48, 4096, 8192), "swapk tile_n=32 split=4"),
+])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_auto_row_split_skinny(shape, choice, mode):
+    _need_gpu()
+    import fp8_scaled_gemm_gb300 as fm
+    M, N, K = shape
+    assert fm.fp8mm_describe_choice(M, N, K, mode).startswith(choice)
+    stats, _, _ = run_and_compare(M, N, K, mode, seed=12, with_bias=(mode == 1))
+    _assert_ok(stats, f"{shape} mode{mode}")
