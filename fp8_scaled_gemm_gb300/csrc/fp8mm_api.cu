@@ -633,13 +633,14 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
             // row tiles put more CTAs on the SMs (two fit on an SM); the row
             // tiles share each Bt block through L2. Clusters of 4 when that
             // still fits one wave, else of 2 up to K = 4096. On a GB300 grid
-            // of M in {48, 64, 96, 128}, N in {2048, 4096}, K in {2048, 4096,
-            // 8192} this was the fastest measured configuration (or within
-            // 0.2 %) on every shape it covers, against up to 2.1x slower for
-            // the model above (128 x 2048 x 4096: 7.2 against 15.4 us with
-            // 128-wide tiles in clusters of 8); with N = 8192 it was not.
+            // of M in {48, 64, 96, 128}, N in {2048, 4096, 8192}, K in {2048,
+            // 4096, 8192} this was the fastest measured configuration (or
+            // within 0.2 %) on every shape it covers, against up to 2.1x
+            // slower for the model above (128 x 2048 x 4096: 7.2 against
+            // 15.4 us with 128-wide tiles in clusters of 8); the shapes it
+            // leaves to the model were within 3.5 % of their fastest.
             const int64_t nt = cdiv(N, fp8mm::kTileP);
-            if (M > 32 && batch == 1 && N >= 2048 && N <= 4096 && K >= 2048 && K <= 8192) {
+            if (M > 32 && batch == 1 && N >= 2048 && N <= 8192 && K >= 2048 && K <= 8192) {
                 const int64_t split_tiles = nt * cdiv(M, 32);
                 if (split_tiles * 4 <= int64_t(sms) * ck_ctas_per_sm(32)) {
                     variant = FP8MM_VARIANT_SWAPK;

@@ -360,6 +360,7 @@ def test_e4m3_output_saturates_like_the_oracle():
     ((128, 4096, 4096), "swapk tile_n=32 split=2"),
     ((100, 2056, 2048), "swapk tile_n=32 split=4"),
     ((48, 4096, 8192), "swapk tile_n=32 split=4"),
+    ((64, 8192, 2048), "swapk tile_n=32 split=2"),
 ])
 @pytest.mark.parametrize("mode", [0, 1])
 def test_auto_row_split_skinny(shape, choice, mode):
