@@ -441,8 +441,9 @@ __global__ void __launch_bounds__(kThreads) quant_convert_kernel(const QuantPara
 // One CTA per SM, each owning a contiguous run of groups, all CTAs resident
 // at once (cooperative launch). Pass 1 copies the head of the run into
 // shared memory (bulk copies, 192 KB), loads the next 256 KB through
-// registers into tensor memory, and streams the rest, marking it evict-last
-// in L2; amax is reduced over all three. A grid-wide exchange publishes the
+// registers into tensor memory (when at least 128 KB remain after the head,
+// QuantParams::use_tmem), and streams the rest, marking it evict-last in L2;
+// amax is reduced over all three. A grid-wide exchange publishes the
 // CTA maxima, so every CTA derives the same scale. Pass 2 converts the L2
 // part, read again with its last group first, then the tensor-memory and
 // shared-memory parts. While the L2 parts stay in L2, HBM sees the tensor
