@@ -638,9 +638,12 @@ Choice choose(int64_t M, int64_t N, int64_t K, int sms, int variant, int tile_n,
             // within 0.2 %) on every shape it covers, against up to 2.1x
             // slower for the model above (128 x 2048 x 4096: 7.2 against
             // 15.4 us with 128-wide tiles in clusters of 8); the shapes it
-            // leaves to the model were within 3.5 % of their fastest.
+            // leaves to the model were within 3.5 % of their fastest. At
+            // N = 1024-1536 it beat the model by 7-25 % (clusters of 8 were
+            // faster still at N = 1024 but slower at 96 x 1536 x 4096); at
+            // K = 16384 it won at 128 x 2048 and lost 4 % at 64 x 4096.
             const int64_t nt = cdiv(N, fp8mm::kTileP);
-            if (M > 32 && batch == 1 && N >= 2048 && N <= 8192 && K >= 2048 && K <= 8192) {
+            if (M > 32 && batch == 1 && N >= 1024 && N <= 8192 && K >= 2048 && K <= 8192) {
                 const int64_t split_tiles = nt * cdiv(M, 32);
                 if (split_tiles * 4 <= int64_t(sms) * ck_ctas_per_sm(32)) {
                     variant = FP8MM_VARIANT_SWAPK;

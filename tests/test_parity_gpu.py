@@ -361,6 +361,7 @@ def test_e4m3_output_saturates_like_the_oracle():
     ((100, 2056, 2048), "swapk tile_n=32 split=4"),
     ((48, 4096, 8192), "swapk tile_n=32 split=4"),
     ((64, 8192, 2048), "swapk tile_n=32 split=2"),
+    ((128, 1024, 4096), "swapk tile_n=32 split=4"),
 ])
 @pytest.mark.parametrize("mode", [0, 1])
 def test_auto_row_split_skinny(shape, choice, mode):
