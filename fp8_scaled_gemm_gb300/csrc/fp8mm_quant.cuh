@@ -518,7 +518,9 @@ __device__ __forceinline__ bool grid_amax(const QuantParams &p, uint32_t cta_ama
     uint64_t *slots = reinterpret_cast<uint64_t *>(p.partial + kSlotWords);
     // read here rather than at the kernel's start: measured faster (fewer
     // slot reads compete with the last CTAs' slot writes)
-    const unsigned int tag = fp8mm::ptx::ld_acquire_gpu_u32(gen) + 1u;
+    unsigned int tag = fp8mm::ptx::ld_acquire_gpu_u32(gen) + 1u;
+    if (tag == 0u)
+        tag = 1u;   // after 2^32 calls: zeroed slots must never match
     if (lane == 0 && !(p.withhold && blockIdx.x == 0))
         st_relaxed_gpu_u64(slots + blockIdx.x, (static_cast<uint64_t>(tag) << 32) | cta_amax);
     const int n = static_cast<int>(gridDim.x);
