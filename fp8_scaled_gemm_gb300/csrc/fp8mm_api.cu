@@ -1779,6 +1779,16 @@ const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64
     return t_describe.c_str();
 }
 
+const char *fp8mm_describe_model_choice(int64_t batch, int64_t M, int64_t N, int64_t K, int sms)
+{
+    if (M <= 0 || N <= 0 || K < 16 || batch <= 0 || sms < 2) {
+        t_describe = "no-op or invalid shape";
+        return t_describe.c_str();
+    }
+    t_describe = describe(choose(M, N, K, sms, FP8MM_VARIANT_AUTO, 0, 0, batch));
+    return t_describe.c_str();
+}
+
 const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mode)
 {
     return fp8mm_describe_bmm_choice(1, M, N, K, scale_mode);

@@ -495,6 +495,14 @@ const char *fp8mm_describe_choice(int64_t M, int64_t N, int64_t K, int scale_mod
  * (fp8mm_autotune) for e4m3 operands and bf16 output when one is held. */
 const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64_t K, int scale_mode);
 
+/* The automatic choice the time model makes for a device with `sms` SMs, in
+ * the same format: no device is needed and tuned entries are not consulted
+ * (the choice a device of that size makes before fp8mm_autotune). For tests
+ * of the dispatch on any host and for planning. Returns "no-op or invalid
+ * shape" for M, N <= 0, K < 16, batch <= 0 or sms < 2. The string is
+ * thread-local and valid until the next describe call on this thread. */
+const char *fp8mm_describe_model_choice(int64_t batch, int64_t M, int64_t N, int64_t K, int sms);
+
 #ifdef __cplusplus
 }
 #endif
