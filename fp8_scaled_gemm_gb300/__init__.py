@@ -62,6 +62,7 @@ EXPORTS = (
     "fp8_scaled_mm_layout",
     "fp8mm_reserve_workspace", "fp8mm_device_status", "fp8mm_status_string",
     "fp8mm_last_cuda_error", "fp8mm_last_error", "fp8mm_describe_choice", "fp8mm_describe_bmm_choice", "fp8mm_debug_inject", "fp8mm_debug_quant", "fp8mm_describe_model_choice",
+    "fp8mm_describe_quant_plan",
     "fp8mm_autotune", "fp8mm_autotune_clear", "fp8mm_autotune_count", "fp8mm_autotune_save",
     "fp8mm_autotune_load",
 )
@@ -134,6 +135,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fp8mm_debug_quant.restype = i32
         lib.fp8mm_describe_model_choice.argtypes = [i64, i64, i64, i64, i32]
         lib.fp8mm_describe_model_choice.restype = ctypes.c_char_p
+        lib.fp8mm_describe_quant_plan.argtypes = [i64, i64, i32, i32]
+        lib.fp8mm_describe_quant_plan.restype = ctypes.c_char_p
         lib.fp8mm_describe_choice.argtypes = [i64, i64, i64, i32]
         lib.fp8mm_describe_choice.restype = ctypes.c_char_p
         lib.fp8mm_autotune.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(Options), vp]
@@ -477,6 +480,12 @@ def fp8mm_describe_model_choice(M: int, N: int, K: int, sms: int, batch: int = 1
     """The time model's automatic choice for a device with `sms` SMs (no
     device needed, tuned entries not consulted)."""
     return load().fp8mm_describe_model_choice(int(batch), int(M), int(N), int(K), int(sms)).decode()
+
+
+def fp8mm_describe_quant_plan(R: int, C: int, scale_mode: int, sms: int) -> str:
+    """The launch plan fp8_quantize takes for bf16 [R, C] on a device with
+    `sms` SMs (no device needed)."""
+    return load().fp8mm_describe_quant_plan(int(R), int(C), int(scale_mode), int(sms)).decode()
 
 
 def fp8mm_describe_bmm_choice(batch: int, M: int, N: int, K: int, scale_mode: int = SCALE_TENSOR) -> str:

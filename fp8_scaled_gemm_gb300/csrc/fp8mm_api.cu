@@ -1134,21 +1134,42 @@ constexpr int64_t kFusedMinBytes = int64_t(1) << 20;
 // Returns FP8MM_OK, FP8MM_ERR_CUDA, or 1 if the device cannot hold the grid
 // at once (cudaErrorCooperativeLaunchTooLarge: fewer SMs available to this
 // process), for the caller to take the two-launch form instead.
+// The one-launch per-tensor plan for `total` 16-byte groups on `sms` SMs:
+// the grid (at least 64 KB of x per CTA, one CTA per SM at most), whether the
+// part after the shared-memory head goes to tensor memory (when enough of the
+// run is left: its allocation and four load rounds cost about what a few
+// thousand groups of L2 re-reads save), and the groups per CTA marked
+// evict-last in L2.
+struct QuantTensorPlan {
+    int grid;
+    int use_tmem;
+    int64_t keep;
+};
+
+QuantTensorPlan quant_tensor_plan(int64_t total, int sms)
+{
+    QuantTensorPlan q;
+    q.grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({sms, fp8q::kMaxFusedCtas, cdiv(total, 4096)})));
+    const int64_t per_cta = cdiv(total, q.grid);
+    q.use_tmem = per_cta - fp8q::kStashGroups >= kFusedTmemMinGroups ? 1 : 0;
+    const int64_t on_chip = fp8q::kStashGroups + (q.use_tmem ? int64_t(fp8q::kTmemGroups) * fp8q::kFusedThreads : 0);
+    const int64_t streamed = std::max<int64_t>(0, per_cta - on_chip);
+    q.keep = std::min<int64_t>(streamed, kFusedL2Bytes / 16 / q.grid);
+    return q;
+}
+
+// Per-tensor quantisation of `total` groups takes the one-launch form (where
+// the device can hold its grid).
+bool quant_one_launch(int64_t total) { return total * 16 >= kFusedMinBytes; }
+
 int launch_quant_tensor(fp8q::QuantParams p, const DeviceState &d, cudaStream_t stream)
 {
-    // at least 64 KB of x per CTA; one CTA per SM at most
-    const int grid = static_cast<int>(
-        std::max<int64_t>(1, std::min<int64_t>({d.sms, fp8q::kMaxFusedCtas, cdiv(p.total, 4096)})));
-    const int64_t per_cta = cdiv(p.total, grid);
+    const QuantTensorPlan plan = quant_tensor_plan(p.total, d.sms);
+    const int grid = plan.grid;
     p.stash_groups = fp8q::kStashGroups;
     p.withhold = g_quant_mode.load() == 2 ? 1 : 0;
-    // tensor memory for the next part when enough of the run is left after the
-    // shared-memory head (its allocation and four load rounds cost about
-    // what a few thousand groups of L2 re-reads save)
-    p.use_tmem = per_cta - p.stash_groups >= kFusedTmemMinGroups ? 1 : 0;
-    const int64_t on_chip = p.stash_groups + (p.use_tmem ? int64_t(fp8q::kTmemGroups) * fp8q::kFusedThreads : 0);
-    const int64_t streamed = std::max<int64_t>(0, per_cta - on_chip);
-    p.keep = std::min<int64_t>(streamed, kFusedL2Bytes / 16 / grid);
+    p.use_tmem = plan.use_tmem;
+    p.keep = plan.keep;
     p.status = d.status;
     p.timeout_cycles = wait_limit();
     cudaLaunchConfig_t cfg = {};
@@ -1171,6 +1192,25 @@ int launch_quant_tensor(fp8q::QuantParams p, const DeviceState &d, cudaStream_t 
     if (e != cudaSuccess)
         return cuda_fail(e, "per-tensor quantisation launch");
     return FP8MM_OK;
+}
+
+// Row-wise team shape for rows of g 16-byte groups (g <= 4096): `lanes` x
+// `warps` threads per row, each holding `chunks` groups of it (the smallest
+// team whose chunks cover the row; longer rows take the two-pass kernel).
+void quant_row_team(int64_t g, int *lanes, int *warps, int *chunks)
+{
+    static const struct { int64_t max_g; int l, w, c; } kTeams[] = {
+        {4, 4, 1, 1},     {8, 8, 1, 1},     {16, 16, 1, 1},    {32, 32, 1, 1},
+        {64, 32, 1, 2},   {128, 32, 1, 4},  {256, 32, 2, 4},   {512, 32, 4, 4},
+        {1024, 32, 8, 4}, {2048, 32, 8, 8}, {4096, 32, 8, 16}};
+    for (const auto &t : kTeams)
+        if (g <= t.max_g) {
+            *lanes = t.l;
+            *warps = t.w;
+            *chunks = t.c;
+            return;
+        }
+    *lanes = *warps = *chunks = 0;
 }
 
 // Enqueues the quantisation of x [R, C]; arguments already checked, R, C > 0.
@@ -1201,8 +1241,7 @@ int quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, vo
                 return cuda_fail(e, "per-tensor quantisation set-up");
             fused_ready[dev] = occ >= 1 ? 1 : -1;
         }
-        if (fused_ready[dev] == 1 && g_quant_mode.load() != 1 &&
-            p.total * 16 >= kFusedMinBytes) {
+        if (fused_ready[dev] == 1 && g_quant_mode.load() != 1 && quant_one_launch(p.total)) {
             const int rc = launch_quant_tensor(p, d, stream);
             if (rc <= 0)
                 return rc;
@@ -1231,28 +1270,23 @@ int quantize(const void *x, int64_t R, int64_t C, int scale_mode, int q_type, vo
     }
     const int64_t g = p.groups;
     const int sms = d.sms;
-    if (g <= 4)
-        return launch_quant_rows<4, 1, 1>(p, sms, stream);
-    if (g <= 8)
-        return launch_quant_rows<8, 1, 1>(p, sms, stream);
-    if (g <= 16)
-        return launch_quant_rows<16, 1, 1>(p, sms, stream);
-    if (g <= 32)
-        return launch_quant_rows<32, 1, 1>(p, sms, stream);
-    if (g <= 64)
-        return launch_quant_rows<32, 1, 2>(p, sms, stream);
-    if (g <= 128)
-        return launch_quant_rows<32, 1, 4>(p, sms, stream);
-    if (g <= 256)
-        return launch_quant_rows<32, 2, 4>(p, sms, stream);
-    if (g <= 512)
-        return launch_quant_rows<32, 4, 4>(p, sms, stream);
-    if (g <= 1024)
-        return launch_quant_rows<32, 8, 4>(p, sms, stream);
-    if (g <= 2048)
-        return launch_quant_rows<32, 8, 8>(p, sms, stream);
-    if (g <= 4096)
-        return launch_quant_rows<32, 8, 16>(p, sms, stream);
+    if (g <= 4096) {
+        int lanes = 0, warps = 0, chunks = 0;
+        quant_row_team(g, &lanes, &warps, &chunks);
+        switch (lanes * 10000 + warps * 100 + chunks) {
+        case 40101: return launch_quant_rows<4, 1, 1>(p, sms, stream);
+        case 80101: return launch_quant_rows<8, 1, 1>(p, sms, stream);
+        case 160101: return launch_quant_rows<16, 1, 1>(p, sms, stream);
+        case 320101: return launch_quant_rows<32, 1, 1>(p, sms, stream);
+        case 320102: return launch_quant_rows<32, 1, 2>(p, sms, stream);
+        case 320104: return launch_quant_rows<32, 1, 4>(p, sms, stream);
+        case 320204: return launch_quant_rows<32, 2, 4>(p, sms, stream);
+        case 320404: return launch_quant_rows<32, 4, 4>(p, sms, stream);
+        case 320804: return launch_quant_rows<32, 8, 4>(p, sms, stream);
+        case 320808: return launch_quant_rows<32, 8, 8>(p, sms, stream);
+        default: return launch_quant_rows<32, 8, 16>(p, sms, stream);
+        }
+    }
     const int grid = static_cast<int>(std::min<int64_t>(R, static_cast<int64_t>(sms) * 8));
     return launch_pdl(fp8q::quant_rows_long_kernel, grid, fp8q::kThreads, 0, stream, "quantisation launch", p);
 }
@@ -1776,6 +1810,37 @@ const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64
     }
     const Choice c = choose(M, N, K, d->sms, variant, tile_n, split, batch);
     t_describe = describe(c);
+    return t_describe.c_str();
+}
+
+const char *fp8mm_describe_quant_plan(int64_t R, int64_t C, int scale_mode, int sms)
+{
+    if (R <= 0 || C <= 0 || C % 8 != 0 || sms < 1 ||
+        (scale_mode != FP8MM_SCALE_TENSOR && scale_mode != FP8MM_SCALE_ROWWISE)) {
+        t_describe = "no-op or invalid shape";
+        return t_describe.c_str();
+    }
+    const int64_t total = R * (C / 8);
+    char buf[160];
+    if (scale_mode == FP8MM_SCALE_TENSOR) {
+        if (quant_one_launch(total)) {
+            const QuantTensorPlan q = quant_tensor_plan(total, sms);
+            snprintf(buf, sizeof buf, "tensor one-launch grid=%d tmem=%d keep=%lld", q.grid, q.use_tmem,
+                     static_cast<long long>(q.keep));
+        } else {
+            snprintf(buf, sizeof buf, "tensor two-launch");
+        }
+    } else {
+        const int64_t g = C / 8;
+        if (g > 4096)
+            snprintf(buf, sizeof buf, "rows long");
+        else {
+            int lanes = 32, warps = 1, chunks = 1;
+            quant_row_team(g, &lanes, &warps, &chunks);
+            snprintf(buf, sizeof buf, "rows team=%dx%d chunks=%d", lanes, warps, chunks);
+        }
+    }
+    t_describe = buf;
     return t_describe.c_str();
 }
 

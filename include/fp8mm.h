@@ -503,6 +503,16 @@ const char *fp8mm_describe_bmm_choice(int64_t batch, int64_t M, int64_t N, int64
  * thread-local and valid until the next describe call on this thread. */
 const char *fp8mm_describe_model_choice(int64_t batch, int64_t M, int64_t N, int64_t K, int sms);
 
+/* The launch plan fp8_quantize takes for bf16 [R, C] on a device with `sms`
+ * SMs, without a device: "rows team=<lanes>x<warps> chunks=<groups per
+ * thread>" or "rows long" (row-wise), "tensor one-launch grid=<CTAs>
+ * tmem=<0|1> keep=<groups per CTA marked evict-last>" or "tensor
+ * two-launch" (per-tensor; the one-launch form also falls back to two
+ * launches on a device that cannot hold its grid at once). Returns "no-op or
+ * invalid shape" for R, C <= 0, C % 8 != 0, sms < 1 or an unknown
+ * scale_mode. Thread-local string, valid until the next describe call. */
+const char *fp8mm_describe_quant_plan(int64_t R, int64_t C, int scale_mode, int sms);
+
 #ifdef __cplusplus
 }
 #endif

@@ -93,3 +93,55 @@ def test_grid_follows_the_sm_count():
     # a smaller device: the pair grid is its SM count (rounded to pairs)
     c = _choice(8192, 8192, 8192, sms=132)
     assert c.startswith("pair ") and "grid=132" in c, c
+
+
+# ------------------------------------------------------------ quantiser ---
+
+def _qplan(R, C, mode, sms=SMS):
+    return fm.fp8mm_describe_quant_plan(R, C, mode, sms)
+
+
+@pytest.mark.parametrize("C,team", [(8, "4x1 chunks=1"), (64, "8x1 chunks=1"), (128, "16x1 chunks=1"),
+                                    (256, "32x1 chunks=1"), (512, "32x1 chunks=2"), (1024, "32x1 chunks=4"),
+                                    (2048, "32x2 chunks=4"), (4096, "32x4 chunks=4"), (8192, "32x8 chunks=4"),
+                                    (16384, "32x8 chunks=8"), (32768, "32x8 chunks=16")])
+def test_row_wise_team_covers_the_row(C, team):
+    """The smallest measured team whose chunks cover the row (C / 8 groups of
+    8 bf16): lanes x warps threads x chunks groups >= C / 8."""
+    plan = _qplan(1000, C, 1)
+    assert plan == f"rows team={team}", plan
+    lanes, rest = team.split("x")
+    warps, chunks = rest.split(" chunks=")
+    assert int(lanes) * int(warps) * int(chunks) >= C // 8
+
+
+def test_row_wise_long_rows_take_the_two_pass_kernel():
+    assert _qplan(10, 32776, 1) == "rows long"
+
+
+@pytest.mark.parametrize("R,C,plan", [
+    (16, 4096, "tensor two-launch"),                 # 128 KB: under 1 MB
+    (64, 4096, "tensor two-launch"),                 # 512 KB
+    (128, 4096, "tensor one-launch grid=16 tmem=0 keep=0"),    # 1 MB: 64 KB per CTA
+    (16384, 1024, "tensor one-launch grid=152 tmem=0 keep=1510"),
+])
+def test_per_tensor_form(R, C, plan):
+    assert _qplan(R, C, 0) == plan
+
+
+@pytest.mark.parametrize("R,C", [(8192, 8192), (16384, 8192), (4096, 14336)])
+def test_per_tensor_large_tensors_hold_a_part_in_tensor_memory(R, C):
+    plan = _qplan(R, C, 0)
+    assert plan.startswith("tensor one-launch grid=152 tmem=1 "), plan
+    total = R * C // 8
+    per_cta = -(-total // 152)
+    keep = int(plan.split("keep=")[1])
+    # the rest after 12288 groups in shared memory and 16384 in tensor memory,
+    # capped at 96 MB of L2 over the grid
+    assert keep == min(max(0, per_cta - 12288 - 16384), (96 << 20) // 16 // 152)
+
+
+def test_quant_plan_rejects_bad_arguments():
+    for args in [(0, 8, 0), (8, 0, 0), (8, 12, 0), (8, 8, 2)]:
+        assert _qplan(*args) == "no-op or invalid shape"
+    assert _qplan(8, 8, 0, sms=0) == "no-op or invalid shape"
