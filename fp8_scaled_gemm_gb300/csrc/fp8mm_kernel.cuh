@@ -682,13 +682,18 @@ __device__ __forceinline__ void convert_row32_any(const KernelParams &p, const f
 // 128-byte swizzle, so the eight threads of a quarter-warp hit distinct
 // banks). The block then leaves as one TMA tensor store of 32 rows x 64
 // columns (out-of-range rows and columns are clipped by the hardware), or,
-// when the output rows are not 16-byte aligned, as coalesced 4-byte row
-// segments. `chunks` counts the blocks this warp has staged so far; before
-// the stage is rewritten, the TMA store of the previous block must have read
-// it (that wait comes after the next block's TMEM loads and arithmetic).
+// when the output rows are not 16-byte aligned, row by row as element
+// stores, lane l writing columns 2l and 2l + 1 (FAST_PLAIN: four rows at a
+// time without branches). `chunks` counts the blocks this warp has staged so
+// far; before the stage is rewritten, the TMA store of the previous block
+// must have read it (that wait comes after the next block's TMEM loads and
+// arithmetic). With a per-warp shared-memory copy of the block's column
+// values (colv), the conversion reads them as broadcasts (convert_row32);
+// without one, from the owning lanes by shuffles.
 //
 // With add.count > 0 (stream-K owner), the fp32 partials that add describes
 // are added to the accumulator first, in piece order.
+
 // A warp's column scales and biases for one tile, loaded before the
 // accumulator wait (lane l holds columns n0 + 32 i + l).
 template <int BN>
