@@ -96,16 +96,26 @@ def peaks():
 GEMM_KERNEL_SOURCES = ("fp8mm_kernel.cuh", "fp8mm_kernel_pair.cuh", "fp8mm_kernel_ck.cuh", "sm103_ptx.cuh")
 
 
+def source_code_only(text: str) -> str:
+    """C/C++ source without its comments and blank lines, each line stripped
+    of surrounding white space: what the compiler sees, for hashing."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).strip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_src_sha() -> str:
-    """Hash of the GEMM kernels' CUDA sources; a stored ncu traffic figure is
-    used only while this hash and the launch configuration both match."""
+    """Hash of the GEMM kernels' CUDA sources (comments and white space
+    aside); a stored ncu traffic figure is used only while this hash and the
+    launch configuration both match."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "fp8_scaled_gemm_gb300", "csrc")
     for f in GEMM_KERNEL_SOURCES:
         h.update(f.encode())
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            h.update(source_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -112,3 +112,10 @@ def test_skinny_shapes_are_the_memory_bound_benchmark_shapes():
         # below the ridge point of the measured peaks (fp8 ~ 3846 TFLOP/s / 6747 GB/s)
         assert flops / nbytes < 3846e12 / (pk_hbm * 1e9)
     assert bench.parse_args([]).no_skinny is False
+
+
+def test_kernel_source_hash_ignores_comments_and_white_space():
+    code = "int f(int x)\n{\n    return x + 1;   // one more\n}\n"
+    commented = "/* a block\n   comment */\nint f(int x)\n{\n\n        return x + 1;\n}\n"
+    assert bench.source_code_only(code) == bench.source_code_only(commented)
+    assert bench.source_code_only(code) != bench.source_code_only(code.replace("+ 1", "+ 2"))
