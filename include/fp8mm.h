@@ -298,8 +298,9 @@ int fp8_scaled_bmm(const void *A, const void *B,
  * Asynchronous on `stream`. Row-wise is one kernel launch. Per-tensor is one
  * cooperative launch (one CTA per SM, a grid-wide amax exchange with a
  * bounded wait that records FP8MM_ERR_TIMEOUT in the device status word if it
- * runs out), or two launches (amax, then conversion) where the device cannot
- * hold that grid at once. It uses a small per-device scratch owned by the
+ * runs out), or two launches (amax, then conversion) for tensors under 1 MB
+ * and where the device cannot hold that grid at once
+ * (fp8mm_describe_quant_plan reports which). It uses a small per-device scratch owned by the
  * library (per-CTA maxima, a call number and counters), so per-tensor calls
  * that overlap on the GPU on different streams of one device race on it.
  */
